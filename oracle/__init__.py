@@ -1,0 +1,133 @@
+"""fp64 CPU oracle for the attention forward pass (TEST INFRASTRUCTURE ONLY).
+
+Only the test suite, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU
+baseline / reference arm may import this package. The CUDA library never
+imports, links or calls it, and it shares no code with the CUDA path: the two
+meet only through the seeded input generator, which holds none of the
+method's arithmetic.
+
+The arithmetic lives in ``attn_ref.cpp`` (plain C++17, fp64, std::thread).
+This module compiles it with g++ and wraps it with ctypes.
+
+Parity pins: every function here is checked in ``tests/test_oracle_pins.py``
+against closed forms, invariances, exhaustive decoder checks and an
+explicit-softmax formulation built from scipy routines.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_ref.cpp")
+_LIB = os.path.join(_HERE, "_build", "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+DTYPE_CODES = {"fp16": 0, "bf16": 1}
+
+
+def build(force: bool = False) -> str:
+    """Compiles attn_ref.cpp into a shared library (g++, -O2, no fast-math)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["g++", "-std=c++17", "-O2", "-fno-fast-math", "-ffp-contract=off",
+           "-fPIC", "-shared", "-pthread", _SRC, "-o", tmp]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            u16p = ctypes.POINTER(ctypes.c_uint16)
+            f64p = ctypes.POINTER(ctypes.c_double)
+            i64 = ctypes.c_int64
+            lib.oracle_threads.argtypes = [ctypes.c_int]
+            lib.oracle_threads.restype = ctypes.c_int
+            lib.oracle_decode.argtypes = [u16p, ctypes.c_int, i64, f64p]
+            lib.oracle_decode.restype = None
+            lib.oracle_attn_fwd.argtypes = [u16p, u16p, u16p, ctypes.c_int, i64, i64, i64, i64,
+                                            ctypes.c_int, ctypes.c_float, f64p, f64p, ctypes.c_int]
+            lib.oracle_attn_fwd.restype = ctypes.c_int
+            lib.oracle_attn_rows.argtypes = [u16p, u16p, u16p, ctypes.c_int, i64, i64, i64, i64,
+                                             ctypes.c_int, ctypes.c_float, ctypes.POINTER(i64), i64,
+                                             f64p, f64p, ctypes.c_int]
+            lib.oracle_attn_rows.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _u16(a: np.ndarray):
+    a = np.ascontiguousarray(a, dtype=np.uint16)
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16))
+
+
+def threads(requested: int = 0) -> int:
+    """Worker threads the oracle uses for ``requested`` (0 = every core)."""
+    return _load().oracle_threads(requested)
+
+
+def decode(bits: np.ndarray, dtype: str) -> np.ndarray:
+    """Exact decode of stored 16-bit values (``fp16`` or ``bf16``) to float64."""
+    bits, p = _u16(bits)
+    out = np.empty(bits.shape, dtype=np.float64)
+    _load().oracle_decode(p, DTYPE_CODES[dtype], bits.size,
+                          out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
+    return out
+
+
+def attn_fwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, dtype: str, causal: bool,
+             scale: float, nthreads: int = 0):
+    """Full forward on [B, H, N, d] stored 16-bit inputs.
+
+    Returns (O float64 [B, H, N, d], LSE float64 [B, H, N]). ``scale`` is taken
+    as the float32 value the CUDA library receives.
+    """
+    assert q.shape == k.shape == v.shape and q.ndim == 4
+    B, H, N, d = q.shape
+    q, qp = _u16(q)
+    k, kp = _u16(k)
+    v, vp = _u16(v)
+    o = np.empty((B, H, N, d), dtype=np.float64)
+    lse = np.empty((B, H, N), dtype=np.float64)
+    rc = _load().oracle_attn_fwd(qp, kp, vp, DTYPE_CODES[dtype], B, H, N, d, int(bool(causal)),
+                                 float(np.float32(scale)),
+                                 o.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+                                 lse.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_attn_fwd rejected its arguments")
+    return o, lse
+
+
+def attn_rows(q: np.ndarray, k: np.ndarray, v: np.ndarray, dtype: str, causal: bool,
+              scale: float, rows: np.ndarray, nthreads: int = 0):
+    """Selected rows of the forward. ``rows`` are flat indices bh * N + i.
+
+    Returns (O float64 [R, d], LSE float64 [R]).
+    """
+    assert q.shape == k.shape == v.shape and q.ndim == 4
+    B, H, N, d = q.shape
+    q, qp = _u16(q)
+    k, kp = _u16(k)
+    v, vp = _u16(v)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    o = np.empty((rows.size, d), dtype=np.float64)
+    lse = np.empty((rows.size,), dtype=np.float64)
+    rc = _load().oracle_attn_rows(qp, kp, vp, DTYPE_CODES[dtype], B, H, N, d, int(bool(causal)),
+                                  float(np.float32(scale)),
+                                  rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), rows.size,
+                                  o.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+                                  lse.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_attn_rows rejected its arguments")
+    return o, lse

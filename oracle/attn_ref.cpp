@@ -1,0 +1,209 @@
+// Attention forward oracle: plain, slow, fp64 CPU reference.
+//
+// TEST INFRASTRUCTURE ONLY. Nothing on the product path may call, link or
+// load this file: only the test suite, the smoke check and the benchmark's
+// CPU-baseline leg use it. It shares no code, header or constant with the
+// CUDA library.
+//
+// What it computes (the plain definition that the fused, tiled kernel reaches
+// up to rounding order):
+//   for every batch b, head h and query row i
+//     s_j    = scale * sum_t q_i[t] * k_j[t]        for j in J(i)
+//     J(i)   = {0 .. N-1}, or {0 .. i} when causal (query i sees keys 0..i)
+//     m      = max_j s_j
+//     l      = sum_j exp(s_j - m)
+//     O_i    = sum_j exp(s_j - m) * v_j / l
+//     LSE_i  = m + ln(l)
+// Sources:
+//   - "TCA 51%, MFU below 8%" (zhihu), section on Flash Attention 2's online
+//     softmax: attention is softmax of the scaled scores applied to V, and the
+//     fused method only avoids materialising the score matrix.
+//   - "TMA + Warp Specialization" (CUDA book ch. 17), section 17.5: the
+//     consumer's per-tile steps (S = Q K^T, softmax, O += P V, final O / l).
+//   The causal mask and the per-row logsumexp are not on those pages; they are
+//   taken as the method's output specification (query i attends keys 0..i;
+//   LSE in natural-log units).
+//
+// Inputs are the stored 16-bit values (IEEE binary16 or bfloat16 bit
+// patterns), decoded exactly to double. Nothing is rounded back to 16 bits:
+// O and LSE are returned in double.
+//
+// Parity pins (see tests/test_oracle_pins.py): closed forms for Q = 0
+// (column mean / prefix mean of V, LSE = ln N / ln(i+1)), one-hot selection,
+// V = const, linearity, permutation and shift invariances, exhaustive decoder
+// checks against numpy/torch, and agreement with an explicit-softmax
+// formulation built from scipy routines at N <= 64.
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <thread>
+#include <vector>
+
+namespace {
+
+// IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
+double decode_binary16(uint16_t h) {
+  const int sign = h >> 15;
+  const int expo = (h >> 10) & 0x1F;
+  const int frac = h & 0x3FF;
+  double v;
+  if (expo == 0) {
+    v = std::ldexp(static_cast<double>(frac), -24);  // subnormal: frac * 2^-24
+  } else if (expo == 31) {
+    v = frac ? NAN : INFINITY;
+  } else {
+    // (1 + frac / 2^10) * 2^(expo - 15) = (2^10 + frac) * 2^(expo - 25)
+    v = std::ldexp(static_cast<double>(frac | 0x400), expo - 25);
+  }
+  return sign ? -v : v;
+}
+
+// bfloat16: the upper half of an IEEE binary32 (8 exponent bits, bias 127,
+// 7 fraction bits).
+double decode_bfloat16(uint16_t b) {
+  const int sign = b >> 15;
+  const int expo = (b >> 7) & 0xFF;
+  const int frac = b & 0x7F;
+  double v;
+  if (expo == 0) {
+    v = std::ldexp(static_cast<double>(frac), -133);  // frac * 2^-126 / 2^7
+  } else if (expo == 255) {
+    v = frac ? NAN : INFINITY;
+  } else {
+    // (1 + frac / 2^7) * 2^(expo - 127) = (2^7 + frac) * 2^(expo - 134)
+    v = std::ldexp(static_cast<double>(frac | 0x80), expo - 134);
+  }
+  return sign ? -v : v;
+}
+
+double decode(uint16_t x, int dtype) {
+  return dtype == 0 ? decode_binary16(x) : decode_bfloat16(x);
+}
+
+void decode_block(const uint16_t* src, int64_t n, int dtype, double* dst) {
+  for (int64_t t = 0; t < n; ++t) dst[t] = decode(src[t], dtype);
+}
+
+// One query row against the keys 0..nkeys-1 of one (batch, head).
+// K and V are the decoded [N][d] matrices of that head.
+void attend_row(const double* qi, const double* K, const double* V,
+                int64_t d, int64_t nkeys, double scale,
+                std::vector<double>& s, double* out_o, double* out_lse) {
+  double m = -INFINITY;
+  for (int64_t j = 0; j < nkeys; ++j) {
+    double dot = 0.0;
+    for (int64_t t = 0; t < d; ++t) dot += qi[t] * K[j * d + t];
+    s[j] = scale * dot;
+    m = std::max(m, s[j]);
+  }
+  double l = 0.0;
+  for (int64_t j = 0; j < nkeys; ++j) {
+    s[j] = std::exp(s[j] - m);
+    l += s[j];
+  }
+  for (int64_t t = 0; t < d; ++t) out_o[t] = 0.0;
+  for (int64_t j = 0; j < nkeys; ++j) {
+    const double w = s[j];
+    for (int64_t t = 0; t < d; ++t) out_o[t] += w * V[j * d + t];
+  }
+  for (int64_t t = 0; t < d; ++t) out_o[t] /= l;
+  *out_lse = m + std::log(l);
+}
+
+int pick_threads(int requested) {
+  if (requested > 0) return requested;
+  const unsigned hc = std::thread::hardware_concurrency();
+  return hc ? static_cast<int>(hc) : 1;
+}
+
+// Runs f(worker, count) on `nthreads` threads.
+template <class F>
+void run_parallel(int nthreads, F f) {
+  std::vector<std::thread> pool;
+  for (int w = 1; w < nthreads; ++w) pool.emplace_back(f, w, nthreads);
+  f(0, nthreads);
+  for (auto& t : pool) t.join();
+}
+
+}  // namespace
+
+extern "C" {
+
+// Number of worker threads the oracle uses for `requested` (0 = all cores).
+int oracle_threads(int requested) { return pick_threads(requested); }
+
+// Decodes n stored 16-bit values (dtype 0 = binary16, 1 = bfloat16).
+void oracle_decode(const uint16_t* x, int dtype, int64_t n, double* out) {
+  decode_block(x, n, dtype, out);
+}
+
+// Full forward: q, k, v are [B][H][N][d] stored 16-bit values; o is
+// [B][H][N][d] double, lse is [B][H][N] double. Returns 0, or -1 on bad
+// arguments.
+int oracle_attn_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                    int dtype, int64_t B, int64_t H, int64_t N, int64_t d,
+                    int causal, float scale, double* o, double* lse,
+                    int nthreads) {
+  if (!q || !k || !v || !o || !lse || B <= 0 || H <= 0 || N <= 0 || d <= 0 ||
+      (dtype != 0 && dtype != 1))
+    return -1;
+  const int64_t BH = B * H;
+  const double sc = static_cast<double>(scale);
+  const int T = std::min<int64_t>(pick_threads(nthreads), BH);
+  run_parallel(T, [&](int w, int nt) {
+    std::vector<double> K(N * d), V(N * d), qi(d), s(N);
+    for (int64_t bh = w; bh < BH; bh += nt) {
+      const int64_t base = bh * N * d;
+      decode_block(k + base, N * d, dtype, K.data());
+      decode_block(v + base, N * d, dtype, V.data());
+      for (int64_t i = 0; i < N; ++i) {
+        decode_block(q + base + i * d, d, dtype, qi.data());
+        const int64_t nkeys = causal ? i + 1 : N;
+        attend_row(qi.data(), K.data(), V.data(), d, nkeys, sc, s,
+                   o + base + i * d, lse + bh * N + i);
+      }
+    }
+  });
+  return 0;
+}
+
+// Selected rows only. rows[r] is a flat row index bh * N + i. Outputs are
+// o[r][d] and lse[r]. Rows are split into contiguous chunks, one per thread;
+// a thread re-decodes K and V whenever its (batch, head) changes, so callers
+// should group rows by head.
+int oracle_attn_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                     int dtype, int64_t B, int64_t H, int64_t N, int64_t d,
+                     int causal, float scale, const int64_t* rows,
+                     int64_t nrows, double* o, double* lse, int nthreads) {
+  if (!q || !k || !v || !rows || !o || !lse || B <= 0 || H <= 0 || N <= 0 ||
+      d <= 0 || nrows < 0 || (dtype != 0 && dtype != 1))
+    return -1;
+  const int64_t BH = B * H;
+  for (int64_t r = 0; r < nrows; ++r)
+    if (rows[r] < 0 || rows[r] >= BH * N) return -1;
+  const double sc = static_cast<double>(scale);
+  const int T = static_cast<int>(
+      std::max<int64_t>(1, std::min<int64_t>(pick_threads(nthreads), nrows)));
+  run_parallel(T, [&](int w, int nt) {
+    const int64_t lo = nrows * w / nt, hi = nrows * (w + 1) / nt;
+    std::vector<double> K(N * d), V(N * d), qi(d), s(N);
+    int64_t cur = -1;
+    for (int64_t r = lo; r < hi; ++r) {
+      const int64_t bh = rows[r] / N, i = rows[r] % N;
+      const int64_t base = bh * N * d;
+      if (bh != cur) {
+        decode_block(k + base, N * d, dtype, K.data());
+        decode_block(v + base, N * d, dtype, V.data());
+        cur = bh;
+      }
+      decode_block(q + base + i * d, d, dtype, qi.data());
+      const int64_t nkeys = causal ? i + 1 : N;
+      attend_row(qi.data(), K.data(), V.data(), d, nkeys, sc, s, o + r * d,
+                 lse + r);
+    }
+  });
+  return 0;
+}
+
+}  // extern "C"

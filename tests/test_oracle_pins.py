@@ -1,0 +1,218 @@
+"""Pins for the fp64 oracle: closed forms, invariances and library routines.
+
+None of these re-types the oracle's formula. Each check comes from a fact the
+mathematics fixes independently of the oracle's code:
+  * exhaustive decode of every 16-bit pattern against numpy / the IEEE layout;
+  * Q = 0 makes every score 0, so O is the (prefix) mean of V and
+    LSE = ln(#keys) (closed form);
+  * one-hot scores select a single V row with a computable residual weight;
+  * V = const gives O = const (rows of P sum to 1);
+  * O is linear in V; non-causal O is invariant under a joint permutation of
+    K and V rows; adding a constant vector u to every key shifts each score
+    of row i by scale * q_i . u, so O is unchanged and LSE shifts by it;
+  * agreement with an explicit-softmax formulation built from numpy's matmul
+    and scipy.special.softmax / logsumexp on small problems.
+A mistake such as a dropped max-subtraction, a wrong mask index, a transposed
+operand, a missing scale or a wrong log base fails at least one of them.
+"""
+import numpy as np
+import pytest
+import scipy.special as sps
+
+from attention_forward_flashattention_gb300 import inputs as I
+
+
+def _rand_bits(rng, shape, dtype, mult=1.0):
+    return I.to_bits(rng.standard_normal(shape) * mult, dtype)
+
+
+# ---------------------------------------------------------------- decoding
+
+def test_decode_fp16_exhaustive(oracle_mod):
+    bits = np.arange(65536, dtype=np.uint16)
+    got = oracle_mod.decode(bits, "fp16")
+    want = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+
+
+def test_decode_bf16_exhaustive(oracle_mod):
+    bits = np.arange(65536, dtype=np.uint16)
+    got = oracle_mod.decode(bits, "bf16")
+    with np.errstate(invalid="ignore"):
+        want = (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+
+
+# ---------------------------------------------------------------- closed forms
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("N,d", [(1, 64), (37, 64), (128, 128)])
+def test_q_zero_gives_column_mean(oracle_mod, dtype, N, d):
+    rng = np.random.default_rng(11)
+    q = np.zeros((1, 2, N, d), dtype=np.uint16)          # +0.0 in both formats
+    k = _rand_bits(rng, (1, 2, N, d), dtype)
+    v = _rand_bits(rng, (1, 2, N, d), dtype)
+    o, lse = oracle_mod.attn_fwd(q, k, v, dtype, False, 0.125)
+    vd = oracle_mod.decode(v, dtype)
+    mean = vd.mean(axis=2, keepdims=True)
+    np.testing.assert_allclose(o, np.broadcast_to(mean, o.shape), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, np.full(lse.shape, np.log(N)), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_q_zero_causal_gives_prefix_mean(oracle_mod, dtype):
+    rng = np.random.default_rng(12)
+    N, d = 200, 64
+    q = np.zeros((2, 1, N, d), dtype=np.uint16)
+    k = _rand_bits(rng, (2, 1, N, d), dtype)
+    v = _rand_bits(rng, (2, 1, N, d), dtype)
+    o, lse = oracle_mod.attn_fwd(q, k, v, dtype, True, 0.3)
+    vd = oracle_mod.decode(v, dtype)
+    counts = np.arange(1, N + 1, dtype=np.float64)[None, None, :, None]
+    prefix = np.cumsum(vd, axis=2) / counts
+    np.testing.assert_allclose(o, prefix, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, np.broadcast_to(np.log(counts[..., 0]), lse.shape), rtol=0, atol=1e-12)
+    # row 0 sees key 0 only: O_0 = v_0 exactly
+    assert np.array_equal(o[:, :, 0, :], vd[:, :, 0, :])
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_one_hot_scores_select_one_row(oracle_mod, dtype):
+    # k_j = e_j, q_i = 16 e_{pi(i)}, scale 1: s_ij = 16 [j == pi(i)].
+    N, d = 48, 64
+    rng = np.random.default_rng(13)
+    perm = rng.permutation(N)
+    qf = np.zeros((1, 1, N, d))
+    qf[0, 0, np.arange(N), perm] = 16.0
+    kf = np.zeros((1, 1, N, d))
+    kf[0, 0, np.arange(N), np.arange(N)] = 1.0
+    v = _rand_bits(rng, (1, 1, N, d), dtype)
+    o, lse = oracle_mod.attn_fwd(I.to_bits(qf, dtype), I.to_bits(kf, dtype), v, dtype, False, 1.0)
+    vd = oracle_mod.decode(v, dtype)[0, 0]
+    e16 = np.exp(16.0)
+    want = (e16 * vd[perm] + (vd.sum(axis=0)[None, :] - vd[perm])) / (e16 + N - 1)
+    np.testing.assert_allclose(o[0, 0], want, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse[0, 0], np.full(N, np.log(e16 + N - 1)), rtol=0, atol=1e-12)
+    # and the selected row dominates: |O_i - v_pi(i)| <= (N-1) e^-16 max|v| * 2
+    assert np.max(np.abs(o[0, 0] - vd[perm])) <= 2 * (N - 1) * np.exp(-16.0) * np.max(np.abs(vd)) + 1e-15
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_constant_v_rows_sum_to_one(oracle_mod, causal):
+    rng = np.random.default_rng(14)
+    N, d = 96, 64
+    q = _rand_bits(rng, (1, 2, N, d), "fp16", 2.0)
+    k = _rand_bits(rng, (1, 2, N, d), "fp16")
+    cols = rng.standard_normal(d)
+    v = I.to_bits(np.broadcast_to(cols, (1, 2, N, d)), "fp16")
+    o, _ = oracle_mod.attn_fwd(q, k, v, "fp16", causal, 0.125)
+    c = oracle_mod.decode(v, "fp16")[0, 0, 0]
+    np.testing.assert_allclose(o, np.broadcast_to(c, o.shape), rtol=0, atol=1e-13)
+
+
+# ---------------------------------------------------------------- invariances
+
+def test_linear_in_v(oracle_mod):
+    rng = np.random.default_rng(15)
+    N, d = 80, 128
+    q = _rand_bits(rng, (1, 1, N, d), "fp16")
+    k = _rand_bits(rng, (1, 1, N, d), "fp16")
+    vf = oracle_mod.decode(_rand_bits(rng, (1, 1, N, d), "fp16"), "fp16")
+    o1, l1 = oracle_mod.attn_fwd(q, k, I.to_bits(vf, "fp16"), "fp16", True, 0.09)
+    o2, l2 = oracle_mod.attn_fwd(q, k, I.to_bits(4.0 * vf, "fp16"), "fp16", True, 0.09)
+    np.testing.assert_allclose(o2, 4.0 * o1, rtol=1e-14, atol=1e-14)
+    assert np.array_equal(l1, l2)
+
+
+def test_joint_permutation_of_keys(oracle_mod):
+    rng = np.random.default_rng(16)
+    N, d = 70, 64
+    q = _rand_bits(rng, (1, 1, N, d), "bf16")
+    k = _rand_bits(rng, (1, 1, N, d), "bf16")
+    v = _rand_bits(rng, (1, 1, N, d), "bf16")
+    perm = rng.permutation(N)
+    o1, l1 = oracle_mod.attn_fwd(q, k, v, "bf16", False, 0.125)
+    o2, l2 = oracle_mod.attn_fwd(q, k[:, :, perm], v[:, :, perm], "bf16", False, 0.125)
+    np.testing.assert_allclose(o2, o1, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l2, l1, rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_key_shift_moves_lse_only(oracle_mod, causal):
+    # Small integers keep K + u exact in fp16; then s'_ij = s_ij + scale q_i.u.
+    rng = np.random.default_rng(17)
+    N, d = 64, 64
+    qf = rng.integers(-3, 4, size=(1, 1, N, d)).astype(np.float64) * 0.25
+    kf = rng.integers(-3, 4, size=(1, 1, N, d)).astype(np.float64)
+    u = rng.integers(-2, 3, size=d).astype(np.float64)
+    vf = rng.standard_normal((1, 1, N, d))
+    scale = 0.125
+    q, k, k2, v = (I.to_bits(x, "fp16") for x in (qf, kf, kf + u, vf))
+    o1, l1 = oracle_mod.attn_fwd(q, k, v, "fp16", causal, scale)
+    o2, l2 = oracle_mod.attn_fwd(q, k2, v, "fp16", causal, scale)
+    np.testing.assert_allclose(o2, o1, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l2, l1 + scale * (qf[0, 0] @ u)[None, None, :], rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- library formulation
+
+def _explicit(qd, kd, vd, causal, scale):
+    """Materialised scores -> scipy softmax -> P @ V, and scipy logsumexp."""
+    s = scale * np.matmul(qd, np.swapaxes(kd, -1, -2))
+    if causal:
+        n = s.shape[-1]
+        s = np.where(np.tril(np.ones((n, n), dtype=bool)), s, -np.inf)
+    p = sps.softmax(s, axis=-1)
+    return np.matmul(p, vd), sps.logsumexp(s, axis=-1)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,N,d", [(1, 1, 1, 64), (1, 2, 7, 64), (2, 1, 33, 128), (1, 2, 64, 128)])
+def test_matches_explicit_softmax(oracle_mod, dtype, causal, B, H, N, d):
+    rng = np.random.default_rng(N * 131 + d)
+    q = _rand_bits(rng, (B, H, N, d), dtype, 3.0)
+    k = _rand_bits(rng, (B, H, N, d), dtype)
+    v = _rand_bits(rng, (B, H, N, d), dtype)
+    scale = float(np.float32(1.0 / np.sqrt(d)))
+    o, lse = oracle_mod.attn_fwd(q, k, v, dtype, causal, scale)
+    want_o, want_lse = _explicit(*(oracle_mod.decode(x, dtype) for x in (q, k, v)), causal, scale)
+    np.testing.assert_allclose(o, want_o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, want_lse, rtol=0, atol=1e-12)
+
+
+def test_scale_is_taken_as_float32(oracle_mod):
+    rng = np.random.default_rng(18)
+    q = _rand_bits(rng, (1, 1, 16, 64), "fp16", 4.0)
+    k = _rand_bits(rng, (1, 1, 16, 64), "fp16")
+    v = _rand_bits(rng, (1, 1, 16, 64), "fp16")
+    _, lse = oracle_mod.attn_fwd(q, k, v, "fp16", False, 0.1)
+    qd, kd, vd = (oracle_mod.decode(x, "fp16") for x in (q, k, v))
+    _, l32 = _explicit(qd, kd, vd, False, float(np.float32(0.1)))
+    np.testing.assert_allclose(lse, l32, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- row sampler
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_rows_equal_full(oracle_mod, causal):
+    rng = np.random.default_rng(19)
+    B, H, N, d = 2, 3, 96, 64
+    q = _rand_bits(rng, (B, H, N, d), "bf16")
+    k = _rand_bits(rng, (B, H, N, d), "bf16")
+    v = _rand_bits(rng, (B, H, N, d), "bf16")
+    o, lse = oracle_mod.attn_fwd(q, k, v, "bf16", causal, 0.125, nthreads=3)
+    rows = np.sort(rng.choice(B * H * N, size=50, replace=False))
+    ro, rl = oracle_mod.attn_rows(q, k, v, "bf16", causal, 0.125, rows, nthreads=4)
+    assert np.array_equal(ro, o.reshape(-1, d)[rows])
+    assert np.array_equal(rl, lse.reshape(-1)[rows])
+
+
+def test_rejects_bad_arguments(oracle_mod):
+    q = np.zeros((1, 1, 4, 64), dtype=np.uint16)
+    with pytest.raises(ValueError):
+        oracle_mod.attn_rows(q, q, q, "fp16", False, 1.0, np.array([4]))
