@@ -1,1 +1,156 @@
-"""GB300-native fused attention forward (placeholder until the binding lands)."""
+"""GB300-native (sm_103a) fused attention forward.
+
+A thin ctypes binding over the C ABI in ``include/fa.h``. Every step of the
+computation runs in the CUDA library ``_build/libfa_sm103.so``; this module
+only marshals arguments (torch tensors -> device pointers, streams -> handles).
+There is no fallback: if the library is missing or cannot be loaded, calls
+raise.
+
+    import torch
+    from attention_forward_flashattention_gb300 import attention_forward
+    o, lse = attention_forward(q, k, v, causal=True)   # q, k, v: [B, H, N, d] fp16/bf16 on cuda
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+import threading
+
+from . import build as _build
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_CUDA = 3
+FA_ERR_ARCH = 4
+FA_ERR_TIMEOUT = 5
+FA_DTYPE_FP16 = 0
+FA_DTYPE_BF16 = 1
+
+HEADER = os.path.join(_build.ROOT, "include", "fa.h")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+        self.status = status
+
+
+def header_functions() -> list[str]:
+    """Names of the entry points that include/fa.h declares."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:fa_status|const char\s*\*|int)\s+(fa_\w+)\s*\(", text, flags=re.M)
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Loads libfa_sm103.so (built in-tree by build.build()). Raises if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or _build.lib_path()
+        if not os.path.exists(p):
+            raise RuntimeError(f"CUDA library not built: {p} (run __graft_entry__.build())")
+        lib = ctypes.CDLL(p)
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+        lib.fa_fwd.restype = i
+        lib.fa_check.argtypes = [vp]
+        lib.fa_check.restype = i
+        ip = ctypes.POINTER(ctypes.c_int)
+        lib.fa_query_launch.argtypes = [i, i, i, i, i, ip, ip, ip, ip]
+        lib.fa_query_launch.restype = i
+        lib.fa_sm_clock_probe.argtypes = [vp, ctypes.c_longlong, vp]
+        lib.fa_sm_clock_probe.restype = i
+        lib.fa_status_string.argtypes = [i]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        lib.fa_version.argtypes = []
+        lib.fa_version.restype = i
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().fa_status_string(int(status)).decode()
+
+
+# ------------------------------------------------------------ raw C ABI
+
+def fa_fwd(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, d: int,
+           causal: bool, scale: float, dtype: int, stream: int = 0) -> int:
+    """Same arguments as the C function (device pointers as ints); returns the status."""
+    return load_library().fa_fwd(q, k, v, o, lse, B, H, N, d, int(bool(causal)), float(scale),
+                                 int(dtype), stream)
+
+
+def fa_check(stream: int = 0) -> int:
+    return load_library().fa_check(stream)
+
+
+def fa_query_launch(B: int, H: int, N: int, d: int, causal: bool = False) -> dict:
+    g, t, s, u = (ctypes.c_int(0) for _ in range(4))
+    rc = load_library().fa_query_launch(B, H, N, d, int(bool(causal)), ctypes.byref(g),
+                                        ctypes.byref(t), ctypes.byref(s), ctypes.byref(u))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_query_launch")
+    return {"grid": g.value, "threads": t.value, "smem_bytes": s.value, "units": u.value}
+
+
+def fa_sm_clock_probe(out_ptr: int, cycles: int, stream: int = 0) -> int:
+    return load_library().fa_sm_clock_probe(out_ptr, int(cycles), stream)
+
+
+def fa_version() -> int:
+    return load_library().fa_version()
+
+
+# ------------------------------------------------------------ torch helpers
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float16:
+        return FA_DTYPE_FP16
+    if t.dtype == torch.bfloat16:
+        return FA_DTYPE_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (fp16 or bf16)")
+
+
+def _stream_handle(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def attention_forward_into(q, k, v, o, lse, causal: bool = False, scale: float | None = None,
+                           stream=None) -> None:
+    """Enqueues fa_fwd on torch tensors (contiguous [B, H, N, d] on one GPU)."""
+    B, H, N, d = q.shape
+    for t in (q, k, v, o):
+        if tuple(t.shape) != (B, H, N, d) or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("q, k, v, o must be contiguous [B, H, N, d] CUDA tensors")
+    if tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous [B, H, N] float32 CUDA tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    rc = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                B, H, N, d, causal, scale, _dtype_code(q), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd")
+
+
+def attention_forward(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
+    """Returns (O [B, H, N, d] in q's dtype, LSE [B, H, N] float32)."""
+    import torch
+    B, H, N, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    attention_forward_into(q, k, v, o, lse, causal, scale, stream)
+    return o, lse

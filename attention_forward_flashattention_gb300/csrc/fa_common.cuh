@@ -1,0 +1,165 @@
+// Device-side building blocks shared by the attention kernel and the PTX
+// self-test kernels: shared-memory tile layout, bounded mbarrier waits,
+// swizzled row stores, and the two tcgen05.mma sequences (S = Q K^T and
+// O += P V).
+//
+// Operand layout (the fix of the SW128 pitfall in "Flash Attention CUDA
+// Kernel: 56 to 986 TFLOPS on B300, G4", V14 "pitfall two"): every 16-bit
+// tile of 128 rows is held as panels of 128 rows x 128 bytes (64 elements);
+// a d = 128 tile is two panels 16 KB apart. TMA writes each panel with
+// 128-byte swizzling, which is the tcgen05 K-major SW128 canonical layout:
+// 8-row x 128-byte atoms, stride 1024 bytes between 8-row groups. A K step of
+// 16 elements advances the descriptor start by 32 bytes inside a panel and
+// jumps to the next panel every 64 elements.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace fa {
+
+// Rows of a Q / K / V / O tile and keys of a KV tile.
+constexpr int kTileRows = 128;
+// One swizzle panel: 128 rows x 128 bytes.
+constexpr int kPanelBytes = 128 * 128;
+// A wait that makes no progress for this long is treated as a deadlock.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// Status word bits (ORed into the device status word by a failed wait).
+enum StatusBits : uint32_t {
+  kStatusProducer = 1u,
+  kStatusMma = 2u,
+  kStatusSoftmax = 4u,
+  kStatusEpilogue = 8u,
+  kStatusDrain = 16u,
+  kStatusSelftest = 32u,
+};
+
+struct AbortCtx {
+  volatile uint32_t* flag;  // shared memory: set once any role gives up
+  uint32_t* status;         // global memory: the device status word
+};
+
+// Waits for phase `parity` of `bar`. Returns false if the CTA is aborting, or
+// after kWaitLimitNs without progress (then it raises the abort flag and
+// records `code` in the status word).
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const AbortCtx& ab,
+                                             uint32_t code, uint64_t limit_ns = kWaitLimitNs) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((it & 15u) == 0u) {
+      if (*ab.flag) return false;
+      if (ptx::globaltimer_ns() - t0 > limit_ns) {
+        *ab.flag = 1u;
+        atomicOr(ab.status, code);
+        return false;
+      }
+    }
+  }
+}
+
+// Same, ignoring the abort flag: used to drain work already in flight
+// (TMA loads, MMAs) before a CTA exits.
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, const AbortCtx& ab,
+                                           uint32_t code) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((it & 15u) == 15u && ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+      *ab.flag = 1u;
+      atomicOr(ab.status, code);
+      return false;
+    }
+  }
+}
+
+// Warp-uniform variant: every lane polls; the warp proceeds only if all
+// lanes saw the phase complete.
+__device__ __forceinline__ bool wait_bounded_warp(uint32_t bar, uint32_t parity,
+                                                  const AbortCtx& ab, uint32_t code) {
+  const bool ok = wait_bounded(bar, parity, ab, code);
+  return __all_sync(0xffffffffu, ok) != 0;
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  uint32_t u;
+  if constexpr (BF16) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    __builtin_memcpy(&u, &h, 4);
+  } else {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    __builtin_memcpy(&u, &h, 4);
+  }
+  return u;
+}
+
+// Writes row r (64 packed 16-bit pairs = 128 elements) of a two-panel SW128
+// tile: elements 0-63 go to panel 0, 64-127 to panel 1; 16-byte chunk q of a
+// row lands at chunk q ^ (r % 8). Eight consecutive rows cover all 32 banks.
+__device__ __forceinline__ void store_row128_sw128(uint32_t tile, int r, const uint32_t (&pk)[64]) {
+  const uint32_t row = tile + static_cast<uint32_t>(r) * 128u;
+  const uint32_t x = static_cast<uint32_t>(r & 7);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      ptx::st_shared_v4(row + h * kPanelBytes + ((static_cast<uint32_t>(q) ^ x) << 4),
+                        pk[32 * h + 4 * q], pk[32 * h + 4 * q + 1], pk[32 * h + 4 * q + 2],
+                        pk[32 * h + 4 * q + 3]);
+    }
+  }
+}
+
+// Writes 32 consecutive elements (16 packed pairs) starting at column
+// `col0` (a multiple of 32) of row r of an SW128 tile.
+__device__ __forceinline__ void store_row32_sw128(uint32_t tile, int r, int col0,
+                                                  const uint32_t (&pk)[16]) {
+  const uint32_t row = tile + static_cast<uint32_t>(col0 >> 6) * kPanelBytes +
+                       static_cast<uint32_t>(r) * 128u;
+  const uint32_t x = static_cast<uint32_t>(r & 7);
+  const uint32_t q0 = static_cast<uint32_t>((col0 & 63) >> 3);
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    ptx::st_shared_v4(row + (((q0 + t) ^ x) << 4), pk[4 * t], pk[4 * t + 1], pk[4 * t + 2],
+                      pk[4 * t + 3]);
+  }
+}
+
+// S[tmem: 128 lanes x 128 cols] = Q[128 x D] * K[128 x D]^T, both K-major.
+template <int D, bool BF16>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sQ, uint32_t sK) {
+  constexpr uint32_t id = ptx::idesc_f16(BF16, false, 128, 128);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = static_cast<uint32_t>((kk >> 2) * kPanelBytes + (kk & 3) * 32);
+    ptx::umma_f16_ss(d_tmem, ptx::sdesc_sw128(sQ + off, 16, 1024),
+                     ptx::sdesc_sw128(sK + off, 16, 1024), id, kk > 0 ? 1u : 0u);
+  }
+}
+
+// O[tmem: 128 lanes x D cols] (+)= P[128 x 128] * V[128 x D]. P is K-major
+// (two panels of 64 keys); V is stored as loaded, [key][d], i.e. MN-major for
+// the B operand: 8-key groups 1024 bytes apart (SBO), 64-column panels
+// 16 KB apart (LBO); a K step of 16 keys advances 2048 bytes.
+template <int D, bool BF16>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t sP, uint32_t sV, bool accumulate,
+                                         uint32_t lbo = kPanelBytes, uint32_t sbo = 1024) {
+  constexpr uint32_t id = ptx::idesc_f16(BF16, true, 128, D);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t aoff = static_cast<uint32_t>((kk >> 2) * kPanelBytes + (kk & 3) * 32);
+    const uint32_t boff = static_cast<uint32_t>(kk * 2048);
+    ptx::umma_f16_ss(d_tmem, ptx::sdesc_sw128(sP + aoff, 16, 1024),
+                     ptx::sdesc_sw128(sV + boff, lbo, sbo), id,
+                     (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+}  // namespace fa

@@ -1,0 +1,235 @@
+// C ABI of the attention forward library (declared in include/fa.h):
+// argument checks, per-device state, TMA descriptor encoding and launch.
+//
+// TMA descriptors follow the host-side construction of "TMA + Warp
+// Specialization" (CUDA book ch. 17, section 17.3): cuTensorMapEncodeTiled on
+// the host, passed by value as __grid_constant__ kernel parameters. Unlike
+// that chapter's single {d, Bc} box, each tile here is fetched as 64-element
+// (128-byte) wide panels, the layout fix of the B300 walkthrough (V14, second
+// pitfall), so that what TMA writes is the tcgen05 K-major SW128 layout.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_kernel.cuh"
+
+namespace fa {
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;
+  bool arch_ok = false;
+  int sm_count = 0;
+  uint32_t* status = nullptr;  // one word, allocated on first use, kept until exit
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+EncodeTiledFn g_encode = nullptr;
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  return g_encode;
+}
+
+// Device facts for the current device; allocates its status word on first use.
+fa_status current_device(int* dev_out, DeviceState** st_out, bool need_status) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FA_ERR_CUDA;
+    st.arch_ok = (major == 10 && minor == 3);
+    st.sm_count = sms;
+    st.ready = true;
+  }
+  if (!st.arch_ok) return FA_ERR_ARCH;
+  if (need_status && st.status == nullptr) {
+    uint32_t* p = nullptr;
+    if (cudaMalloc(&p, 256) != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaMemset(p, 0, 256) != cudaSuccess) {
+      cudaFree(p);
+      return FA_ERR_CUDA;
+    }
+    st.status = p;
+  }
+  *dev_out = dev;
+  *st_out = &st;
+  return FA_OK;
+}
+
+// [BH][N][d] 16-bit tensor as a 3-D map {d, N, BH}; box = one 64-element x
+// 128-row panel, 128-byte swizzle. Rows past N read as zero and are not
+// written by stores.
+bool encode_qkvo(CUtensorMap* m, const void* ptr, bool bf16, int d, int N, long long BH) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2u,
+                                 static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2u};
+  const cuuint32_t box[3] = {64u, 128u, 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+             const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Size checks shared by fa_fwd and fa_query_launch.
+fa_status check_sizes(int B, int H, int N, int d) {
+  if (B <= 0 || H <= 0 || N <= 0) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long BH = static_cast<long long>(B) * H;
+  if (BH > 0x7FFFFFFFLL) return FA_ERR_UNSUPPORTED;
+  // unit count BH * ceil(N / 256) and row index bh * N + i stay in int range
+  const long long units = BH * ((static_cast<long long>(N) + 255) / 256);
+  if (units > 0x7FFFFFFFLL) return FA_ERR_UNSUPPORTED;
+  if (N > (1 << 30)) return FA_ERR_UNSUPPORTED;  // tile row coordinates stay in int range
+  return FA_OK;
+}
+
+__global__ void clock_probe_kernel(uint64_t* out, long long cycles) {
+  if (threadIdx.x != 0) return;
+  const uint64_t g0 = ptx::globaltimer_ns();
+  const long long c0 = clock64();
+  long long c = c0;
+  while (c - c0 < cycles) c = clock64();
+  const uint64_t g1 = ptx::globaltimer_ns();
+  out[0] = static_cast<uint64_t>(c - c0);
+  out[1] = g1 - g0;
+}
+
+}  // namespace
+
+int fwd_smem_bytes(int d) { return d == 64 ? Layout<64>::kSmemBytes : Layout<128>::kSmemBytes; }
+
+}  // namespace fa
+
+extern "C" {
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, int d, int causal, float scale, fa_dtype dtype, void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!fa::aligned16(q) || !fa::aligned16(k) || !fa::aligned16(v) || !fa::aligned16(o) ||
+      !fa::aligned16(lse))
+    return FA_ERR_INVALID_ARG;
+  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
+  const fa_status sz = fa::check_sizes(B, H, N, d);
+  if (sz != FA_OK) return sz;
+
+  int dev = 0;
+  fa::DeviceState* st = nullptr;
+  const fa_status ds = fa::current_device(&dev, &st, true);
+  if (ds != FA_OK) return ds;
+
+  const bool bf16 = dtype == FA_DTYPE_BF16;
+  const long long BH = static_cast<long long>(B) * H;
+  CUtensorMap maps[4];
+  if (!fa::encode_qkvo(&maps[0], q, bf16, d, N, BH) || !fa::encode_qkvo(&maps[1], k, bf16, d, N, BH) ||
+      !fa::encode_qkvo(&maps[2], v, bf16, d, N, BH) || !fa::encode_qkvo(&maps[3], o, bf16, d, N, BH))
+    return FA_ERR_CUDA;
+
+  fa::FwdArgs a{};
+  a.lse = lse;
+  a.status = st->status;
+  a.N = N;
+  a.BH = static_cast<int>(BH);
+  a.n_mblk = (N + 255) / 256;
+  a.n_units = static_cast<int>(BH * a.n_mblk);
+  a.n_kv = (N + 127) / 128;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  const int grid = a.n_units < st->sm_count ? a.n_units : st->sm_count;
+
+  (void)cudaGetLastError();  // do not report an earlier, unrelated error as ours
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = (d == 64) ? fa::launch_fwd_d64(bf16, causal != 0, maps, a, grid, s)
+                                  : fa::launch_fwd_d128(bf16, causal != 0, maps, a, grid, s);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_check(void* stream) {
+  int dev = 0;
+  fa::DeviceState* st = nullptr;
+  const fa_status ds = fa::current_device(&dev, &st, false);
+  if (ds != FA_OK) return ds;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  if (st->status == nullptr) return FA_OK;  // nothing launched on this device yet
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, st->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (word == 0) return FA_OK;
+  if (cudaMemset(st->status, 0, sizeof(word)) != cudaSuccess) return FA_ERR_CUDA;
+  return FA_ERR_TIMEOUT;
+}
+
+fa_status fa_query_launch(int B, int H, int N, int d, int causal, int* grid, int* threads,
+                          int* smem_bytes, int* units) {
+  (void)causal;
+  const fa_status sz = fa::check_sizes(B, H, N, d);
+  if (sz != FA_OK) return sz;
+  int dev = 0;
+  fa::DeviceState* st = nullptr;
+  const fa_status ds = fa::current_device(&dev, &st, false);
+  if (ds != FA_OK) return ds;
+  const long long n_units = static_cast<long long>(B) * H * ((N + 255) / 256);
+  if (grid) *grid = static_cast<int>(n_units < st->sm_count ? n_units : st->sm_count);
+  if (threads) *threads = fa::kFwdThreads;
+  if (smem_bytes) *smem_bytes = fa::fwd_smem_bytes(d);
+  if (units) *units = static_cast<int>(n_units);
+  return FA_OK;
+}
+
+fa_status fa_sm_clock_probe(uint64_t* out, long long cycles, void* stream) {
+  if (!out || cycles <= 0 || cycles > 8000000000LL) return FA_ERR_INVALID_ARG;
+  int dev = 0;
+  fa::DeviceState* st = nullptr;
+  const fa_status ds = fa::current_device(&dev, &st, false);
+  if (ds != FA_OK) return ds;
+  (void)cudaGetLastError();
+  fa::clock_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(out, cycles);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_ARCH: return "FA_ERR_ARCH";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+  }
+  return "FA_ERR_UNKNOWN";
+}
+
+int fa_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,386 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused attention forward on GB300.
+
+One step = one fa_fwd launch over the whole workload (all B*H*N query rows),
+inputs resident in HBM. Default workload: non-causal MHA, B=4 H=16 N=4096
+d=128, fp16 in / fp16 out, fp32 accumulate, scale 1/sqrt(128).
+
+Metric: attention forward TFLOPS = 4 B H N^2 d / time (halved for causal),
+also reported as a percentage of 2.25 PFLOP/s dense fp16.
+
+Prints ONE JSON line (rank 0). Reference arm (--impl reference): the fp64 CPU
+oracle timed on this host's cores on a bounded sample of the same workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from attention_forward_flashattention_gb300 import inputs as I  # noqa: E402
+
+DEFAULT_WORKLOAD = "mha_b4_h16_n4096_d128_fp16"
+METRIC = "attention fwd TFLOPS (4BHN²d, causal halved) and % of 2.25 PF dense fp16"
+NOMINAL_DENSE_FP16_TFLOPS = 2250.0
+FALLBACK_PEAK_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 256 << 20
+SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+REASON_NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=I.WORKLOAD_ORDER)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--soak-s", type=float, default=1.5,
+                   help="untimed loaded seconds before the timed steps (clock samples)")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------ helpers
+
+def measured_peaks() -> dict:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except OSError:
+        return {}
+
+
+def kernel_source_sha256() -> str:
+    from attention_forward_flashattention_gb300 import build as fabuild
+    h = hashlib.sha256()
+    for name in sorted(fabuild.HEADERS + fabuild.LIB_UNITS):
+        with open(os.path.join(fabuild.CSRC, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "fa_fwd_traffic.txt")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    kv = {}
+    for ln in lines:
+        if ":" in ln and not ln.lstrip().startswith("#"):
+            k, v = ln.split(":", 1)
+            kv.setdefault(k.strip(), []).append(v.strip())
+    if kv.get("kernel_source_sha256", [None])[0] != kernel_source_sha256():
+        return None
+    for wl, b in zip(kv.get("workload", []), kv.get("dram_bytes_per_launch", [])):
+        if wl == workload:
+            return int(float(b))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms while running."""
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        self.t0 = self.t1 = None
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            sel = []
+        fd, self.path = tempfile.mkstemp(prefix="fa_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", *sel, f"--query-gpu={SMI_FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        with open(self.path) as f:
+            for ln in f:
+                parts = [x.strip() for x in ln.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(REASON_NAMES, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def oracle_sample_rows(w, nrows: int, seed: int) -> np.ndarray:
+    """Rows of the workload for the CPU oracle: a few heads, rows spread over N."""
+    rng = np.random.default_rng(seed)
+    heads = sorted(set(rng.integers(0, w.B * w.H, size=4).tolist()))
+    per = max(1, nrows // len(heads))
+    rows = [h * w.N + int(i) for h in heads for i in rng.integers(0, w.N, size=per)]
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def sample_flops(w, rows: np.ndarray) -> float:
+    """Metric FLOPs attributable to these rows: the workload's metric FLOPs per
+    row (4 N d, halved for causal) times the number of rows."""
+    return w.flops / (w.B * w.H * w.N) * len(rows)
+
+
+def time_oracle(w, q, k, v, target_s: float, seed: int):
+    """Times the oracle on a row sample sized to about target_s seconds."""
+    import oracle
+    cores = oracle.threads(0)
+    calib = oracle_sample_rows(w, 2 * cores, seed)
+    t = time.perf_counter()
+    oracle.attn_rows(q, k, v, w.dtype, w.causal, w.scale, calib)
+    dt = max(time.perf_counter() - t, 1e-3)
+    n = int(min(max(len(calib) * target_s / dt, len(calib)), 200000))
+    rows = oracle_sample_rows(w, n, seed + 1)
+    t = time.perf_counter()
+    oracle.attn_rows(q, k, v, w.dtype, w.causal, w.scale, rows)
+    dt = time.perf_counter() - t
+    return sample_flops(w, rows) / dt / 1e12, dt, len(rows), cores
+
+
+# ------------------------------------------------------------ arms
+
+def run_reference(args, rank: int, world: int):
+    if rank != 0:
+        return
+    w = I.WORKLOADS[args.workload]
+    q, k, v = I.qkv_bits(w)
+    import oracle
+    oracle.build()
+    step_target = 2.0
+    vals, secs, nrows, cores = [], [], 0, oracle.threads(0)
+    for s in range(args.warmup + args.steps):
+        tf, dt, n, cores = time_oracle(w, q, k, v, step_target, seed=w.seed * 7 + s)
+        if s >= args.warmup:
+            vals.append(tf)
+            secs.append(dt)
+            nrows += n
+    value = statistics.mean(vals)
+    ms = statistics.mean(secs) * 1e3
+    sample = (f"{nrows // max(1, args.steps)} query rows per step (grouped over 4 heads) of "
+              f"{w.name}; TFLOPS = rows x (metric FLOPs per row) / wall time")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded SplitMix64 + Box-Muller, N(0,1))",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w) -> dict:
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "dtype": w.dtype,
+            "causal": w.causal, "scale": w.scale, "q_mult": w.q_mult,
+            "global_batch": w.B, "seq_len": w.N}
+
+
+def run_ours(args, rank: int, world: int, local_rank: int):
+    import torch
+    import torch.distributed as dist
+
+    import attention_forward_flashattention_gb300 as fa
+    from attention_forward_flashattention_gb300 import build as fabuild
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    fabuild.build()
+    fa.load_library()
+    w = I.WORKLOADS[args.workload]
+    qb, kb, vb = I.qkv_bits(w)
+    tdt = torch.float16 if w.dtype == "fp16" else torch.bfloat16
+    host = [torch.from_numpy(x.view(np.int16)).view(tdt).pin_memory() for x in (qb, kb, vb)]
+    q, k, v = (h.to(dev) for h in host)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = int(stream.cuda_stream)
+    launch = fa.fa_query_launch(w.B, w.H, w.N, w.d, w.causal)
+
+    def step():
+        fa.attention_forward_into(q, k, v, o, lse, w.causal, w.scale, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    rc = fa.fa_check(sh)
+    if rc != fa.FA_OK:
+        raise RuntimeError("warm-up failed: " + fa.status_string(rc))
+
+    sampler = ClockSampler(local_rank)
+    t_end = time.perf_counter() + args.soak_s
+    while time.perf_counter() < t_end:   # untimed load so clock samples exist
+        for _ in range(20):
+            step()
+        torch.cuda.synchronize(dev)
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()                    # evict L2 between steps (outside the events)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    rc = fa.fa_check(sh)
+    if rc != fa.FA_OK:
+        raise RuntimeError("timed steps failed: " + fa.status_string(rc))
+    times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(times_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    per_gpu_tflops = w.flops / (ms_per_step * 1e-3) / 1e12
+    value = per_gpu_tflops * world
+
+    # SM clock from clock64 (one CTA spinning 2e8 cycles right after the load)
+    probe = torch.zeros(2, dtype=torch.int64, device=dev)
+    clk64_mhz = None
+    if fa.fa_sm_clock_probe(probe.data_ptr(), 200_000_000, sh) == fa.FA_OK:
+        torch.cuda.synchronize(dev)
+        c, ns = probe.tolist()
+        clk64_mhz = 1e3 * c / ns if ns > 0 else None
+
+    # end to end through the public API: pinned host in, pinned host out
+    e2e = None
+    if not args.no_e2e:
+        oh = torch.empty(o.shape, dtype=tdt).pin_memory()
+        lh = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            qd, kd, vd = (h.to(dev, non_blocking=True) for h in host)
+            fa.attention_forward_into(qd, kd, vd, o, lse, w.causal, w.scale, stream)
+            oh.copy_(o, non_blocking=True)
+            lh.copy_(lse, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        n_e2e = max(3, min(args.steps, 10))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1) / n_e2e
+        if world > 1:
+            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        elem = w.B * w.H * w.N * w.d
+        e2e = {"value": w.flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": 3 * elem * 2,
+               "d2h_bytes_per_step": elem * 2 + w.B * w.H * w.N * 4}
+
+    if rank != 0:
+        return
+    peaks = measured_peaks()
+    if "bf16_tflops" in peaks:
+        peak, peak_src = float(peaks["bf16_tflops"]), "measured bf16 burst (fp16 same nominal rate)"
+    else:
+        peak, peak_src = FALLBACK_PEAK_TFLOPS, "fallback"
+    cpu = None
+    if not args.no_cpu_baseline:
+        tf, dt, n, cores = time_oracle(w, qb, kb, vb, target_s=12.0, seed=w.seed * 13)
+        cpu = {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+               "sample": f"{n} query rows (grouped over 4 heads) of {w.name}, {dt:.1f} s wall; "
+                         f"TFLOPS = rows x (metric FLOPs per row) / wall time"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded SplitMix64 + Box-Muller, N(0,1)), resident in HBM",
+        "config": {**workload_config(w), "parallelism": f"replicas x{world}",
+                   "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)",
+                   "grid": launch["grid"], "threads": launch["threads"],
+                   "smem_bytes": launch["smem_bytes"], "units": launch["units"]},
+        "pct_of_2250_tflops": 100.0 * per_gpu_tflops / NOMINAL_DENSE_FP16_TFLOPS,
+        "roofline": {"bound": "tensor", "achieved": per_gpu_tflops, "peak": peak,
+                     "unit": "TFLOP/s", "frac": per_gpu_tflops / peak,
+                     "traffic": recorded_traffic(w.name), "peak_source": peak_src,
+                     "kernel": "fa_fwd_kernel"},
+        "clocks": {**clocks, "clk64_mhz": clk64_mhz, "window": "soak + timed steps"},
+        "gpu_launches": args.steps,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "step_ms_min": min(times_ms), "step_ms_median": statistics.median(times_ms),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,111 @@
+/*
+ * fa.h - C ABI of the GB300 (sm_103a) fused attention forward library.
+ *
+ * The operation (per batch b and head h, for every query row i):
+ *
+ *     O[b,h,i,:] = sum_{j in J(i)} softmax_j(scale * q_i . k_j) * v_j
+ *     LSE[b,h,i] = ln sum_{j in J(i)} exp(scale * q_i . k_j)
+ *
+ * with J(i) = {0..N-1}, or {0..i} when causal. It is the flash-attention
+ * forward pass: scores are produced tile by tile with an online softmax, so
+ * the N x N score matrix never reaches HBM. Sources:
+ *   - "TCA 51%, MFU below 8%" (zhihu), section on Flash Attention 2 and the
+ *     online softmax (O is softmax(QK^T) V accumulated block by block);
+ *   - "TMA + Warp Specialization" (CUDA book ch. 17), sections 17.3-17.5
+ *     (TMA descriptors, producer / consumer loop, final O / row_sum);
+ *   - "Flash Attention CUDA Kernel: 56 to 986 TFLOPS on B300, G4" (hjcheng0602
+ *     blog), versions V14-V16 (TMA + tcgen05 with accumulators in TMEM).
+ *   The causal mask and the logsumexp output are part of this library's
+ *   specification; the pages do not define them.
+ *
+ * All entry points are plain C: pointers and sizes, no framework types.
+ */
+#ifndef FA_SM103_H
+#define FA_SM103_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fa_status {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* null / misaligned pointer, bad size, bad scale or dtype */
+  FA_ERR_UNSUPPORTED = 2, /* head dim not 64 or 128, or sizes beyond the 32-bit limits */
+  FA_ERR_CUDA = 3,        /* a CUDA runtime / driver call failed (launch, attribute, encode) */
+  FA_ERR_ARCH = 4,        /* the current device is not compute capability 10.3 */
+  FA_ERR_TIMEOUT = 5      /* a kernel wait ran past its limit (reported by fa_check) */
+} fa_status;
+
+typedef enum fa_dtype {
+  FA_DTYPE_FP16 = 0, /* IEEE binary16 */
+  FA_DTYPE_BF16 = 1  /* bfloat16 */
+} fa_dtype;
+
+/*
+ * fa_fwd - enqueue one fused attention forward on `stream`.
+ *
+ * q, k, v : device pointers, contiguous [B][H][N][d] of `dtype` (16-bit
+ *           elements, row i of head (b,h) at ((b*H + h)*N + i)*d).
+ *           Caller-owned, read only. 16-byte aligned.
+ * o       : device pointer, contiguous [B][H][N][d] of `dtype`, written.
+ *           Rounded to nearest even from the fp32 result. 16-byte aligned.
+ * lse     : device pointer, contiguous [B][H][N] float32, written: the
+ *           natural-log logsumexp of the scaled scores of each row.
+ * B, H, N : batch, heads, sequence length (queries = keys = N), each >= 1,
+ *           N <= 2^30, B*H*ceil(N/256) <= 2^31-1. Any N is accepted: the last
+ *           key tile is masked and rows past N are neither read nor written.
+ * d       : head dimension, 64 or 128.
+ * causal  : 0 = full attention, nonzero = query i attends keys 0..i.
+ * scale   : score scale (usually 1/sqrt(d)); finite and > 0.
+ * dtype   : FA_DTYPE_FP16 or FA_DTYPE_BF16 (both inputs and O).
+ * stream  : cudaStream_t to enqueue on (NULL = legacy default stream).
+ *
+ * Asynchronous: returns after the launch is enqueued; O and LSE are valid
+ * once the stream reaches that point. Arguments are checked before anything
+ * is enqueued; on any error nothing is launched and nothing is written.
+ * The first call on a device allocates a small device status word for that
+ * device (kept until process exit); later calls allocate nothing.
+ * A kernel whose internal waits run past their limit stops early and records
+ * the failure in that status word: call fa_check to read it.
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int H, int N, int d, int causal, float scale,
+                 fa_dtype dtype, void* stream);
+
+/*
+ * fa_check - synchronise `stream`, then read and clear the current device's
+ * status word. Returns FA_OK, FA_ERR_TIMEOUT if a launch since the last check
+ * stopped on a wait limit, or FA_ERR_CUDA if the stream reports an error.
+ */
+fa_status fa_check(void* stream);
+
+/*
+ * fa_query_launch - launch shape fa_fwd would use on the current device for
+ * these sizes: grid (persistent CTAs), threads per CTA, dynamic shared memory
+ * bytes, and the number of 256-row work units. Any output pointer may be
+ * NULL. Host memory only; enqueues nothing.
+ */
+fa_status fa_query_launch(int B, int H, int N, int d, int causal, int* grid, int* threads,
+                          int* smem_bytes, int* units);
+
+/*
+ * fa_sm_clock_probe - measure the SM clock: one CTA spins for `cycles`
+ * clock64 ticks and writes out[0] = clock64 ticks elapsed and
+ * out[1] = %globaltimer nanoseconds elapsed (MHz = 1000 * out[0] / out[1]).
+ * out: device pointer to 2 uint64. Enqueued on `stream`.
+ */
+fa_status fa_sm_clock_probe(uint64_t* out, long long cycles, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* fa_status_string(fa_status s);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_SM103_H */

@@ -1,0 +1,89 @@
+"""The C ABI library builds, loads and exports what include/fa.h declares, and
+rejects bad arguments before touching a GPU (runs without one)."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import attention_forward_flashattention_gb300 as fa
+from attention_forward_flashattention_gb300 import build as fabuild
+
+GOOD = 0x100000  # 16-byte aligned stand-in pointer: never dereferenced by the checks
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fabuild.build()
+    return fa.load_library()
+
+
+def test_header_declares_expected_entry_points():
+    names = fa.header_functions()
+    assert names == ["fa_fwd", "fa_check", "fa_query_launch", "fa_sm_clock_probe",
+                     "fa_status_string", "fa_version"]
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in fa.header_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_selftest_library_exports():
+    _, st = fabuild.build()
+    slib = ctypes.CDLL(st)
+    for name in ("fa_selftest_gemm_qk", "fa_selftest_gemm_pv", "fa_selftest_wait_timeout"):
+        assert hasattr(slib, name)
+
+
+def test_status_strings(lib):
+    assert fa.status_string(fa.FA_OK) == "FA_OK"
+    assert fa.status_string(fa.FA_ERR_TIMEOUT) == "FA_ERR_TIMEOUT"
+    assert fa.status_string(99) == "FA_ERR_UNKNOWN"
+    assert fa.fa_version() == 100
+
+
+def _call(q=GOOD, k=GOOD, v=GOOD, o=GOOD, lse=GOOD, B=1, H=1, N=128, d=128, causal=0,
+          scale=0.125, dtype=fa.FA_DTYPE_FP16):
+    return fa.fa_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, 0)
+
+
+@pytest.mark.parametrize("kw", [dict(q=0), dict(k=0), dict(v=0), dict(o=0), dict(lse=0)])
+def test_null_pointers_rejected(lib, kw):
+    assert _call(**kw) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [dict(q=GOOD + 2), dict(v=GOOD + 8), dict(o=GOOD + 4),
+                                dict(lse=GOOD + 4)])
+def test_misaligned_pointers_rejected(lib, kw):
+    assert _call(**kw) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.125, float("nan"), float("inf")])
+def test_bad_scale_rejected(lib, scale):
+    assert _call(scale=scale) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(H=0), dict(N=0), dict(N=-5), dict(dtype=2),
+                                dict(dtype=-1)])
+def test_bad_sizes_and_dtype_rejected(lib, kw):
+    assert _call(**kw) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [dict(d=96), dict(d=256), dict(d=32), dict(N=(1 << 30) + 1),
+                                dict(B=1 << 16, H=1 << 16)])
+def test_unsupported_shapes(lib, kw):
+    assert _call(**kw) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_no_device_is_an_error_not_a_fallback(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    # valid arguments on a machine without a GPU must fail, never compute on the CPU
+    assert _call() in (fa.FA_ERR_CUDA, fa.FA_ERR_ARCH)
+
+
+def test_missing_library_raises(tmp_path):
+    with pytest.raises(RuntimeError):
+        fa.load_library(str(tmp_path / "libfa_sm103.so"))

@@ -1,0 +1,161 @@
+"""Parity of the CUDA attention forward with the fp64 oracle.
+
+* small problems (several tiles, ragged tails, both head dims, dtypes and
+  masks): every element against the full oracle;
+* the five named workloads at full size, launched exactly as the benchmark
+  launches them: sampled rows (tile edges of the first, middle and last
+  heads + random rows) against the oracle, plus properties of every row;
+* closed forms run on the GPU (Q = 0 gives the column / prefix mean of V);
+* determinism and the status word.
+"""
+import functools
+
+import numpy as np
+import pytest
+
+import attention_forward_flashattention_gb300 as fa
+from attention_forward_flashattention_gb300 import inputs as I
+
+from parity_util import bits_to_f64, compare, half_ulp, run_fa, sample_rows, to_bits, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built(oracle_mod):
+    import torch
+    torch.cuda.init()
+    fa.build.build()
+    fa.load_library()
+
+
+@functools.lru_cache(maxsize=2)
+def _inputs(name):
+    return I.qkv_bits(I.WORKLOADS[name])
+
+
+def _check(res, what):
+    assert res["ok"], f"{what}: {res}"
+
+
+# ------------------------------------------------------------ small, every element
+
+SMALL = [
+    # B, H, N, d, dtype, causal
+    (1, 2, 256, 64, "fp16", False),
+    (1, 2, 256, 128, "fp16", True),
+    (2, 3, 1000, 128, "bf16", False),
+    (2, 3, 1000, 64, "bf16", True),
+    (1, 1, 1, 64, "fp16", False),
+    (1, 1, 1, 128, "bf16", True),
+    (1, 4, 17, 128, "fp16", True),
+    (3, 1, 128, 64, "fp16", True),
+    (1, 2, 129, 128, "bf16", False),
+    (1, 1, 384, 128, "fp16", True),
+    (1, 1, 640, 64, "bf16", False),
+    (2, 2, 520, 128, "fp16", True),
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,dtype,causal", SMALL)
+def test_small_every_element(oracle_mod, B, H, N, d, dtype, causal):
+    w = I.custom("small", B, H, N, d, dtype, causal, seed_index=100 + N + d)
+    q, k, v = I.qkv_bits(w)
+    o, lse = run_fa(q, k, v, dtype, causal, w.scale)
+    o_ref, l_ref = oracle_mod.attn_fwd(q, k, v, dtype, causal, w.scale)
+    _check(compare(o, lse, o_ref, l_ref, dtype), f"B{B} H{H} N{N} d{d} {dtype} causal={causal}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_sharpened_scores_rescale_path(oracle_mod, d, dtype):
+    # Q x 3 makes the running max jump by more than 2^8 between tiles.
+    w = I.custom("sharp", 1, 2, 1024, d, dtype, True, seed_index=7, q_mult=3.0)
+    q, k, v = I.qkv_bits(w)
+    o, lse = run_fa(q, k, v, dtype, True, w.scale)
+    o_ref, l_ref = oracle_mod.attn_fwd(q, k, v, dtype, True, w.scale)
+    _check(compare(o, lse, o_ref, l_ref, dtype), f"sharp d{d} {dtype}")
+
+
+# ------------------------------------------------------------ closed forms on the GPU
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_q_zero_gives_mean_of_v(causal, d):
+    rng = np.random.default_rng(5 + d)
+    N = 640
+    q = np.zeros((1, 2, N, d), dtype=np.uint16)
+    k = I.to_bits(rng.standard_normal((1, 2, N, d)), "fp16")
+    v = I.to_bits(rng.standard_normal((1, 2, N, d)), "fp16")
+    o, lse = run_fa(q, k, v, "fp16", causal, 1.0 / np.sqrt(d))
+    vd = bits_to_f64(v, "fp16")
+    cnt = np.arange(1, N + 1, dtype=np.float64)[None, None, :, None]
+    want = np.cumsum(vd, axis=2) / cnt if causal else np.broadcast_to(vd.mean(axis=2, keepdims=True), vd.shape)
+    want_lse = np.log(cnt[..., 0]) if causal else np.full((1, 2, N), np.log(N))
+    got = bits_to_f64(o, "fp16")
+    assert np.all(np.abs(got - want) <= 2e-3 + half_ulp(want, "fp16"))
+    np.testing.assert_allclose(lse, np.broadcast_to(want_lse, lse.shape), rtol=0, atol=1e-4)
+    if causal:
+        assert np.array_equal(o[:, :, 0, :], v[:, :, 0, :])   # row 0 = v_0 exactly
+
+
+# ------------------------------------------------------------ named workloads, full size
+
+@pytest.mark.parametrize("name", I.WORKLOAD_ORDER)
+def test_named_workload(oracle_mod, name):
+    w = I.WORKLOADS[name]
+    q, k, v = _inputs(name)
+    o, lse = run_fa(q, k, v, w.dtype, w.causal, w.scale)
+    if w.B * w.H * w.N <= 4096:
+        o_ref, l_ref = oracle_mod.attn_fwd(q, k, v, w.dtype, w.causal, w.scale)
+        _check(compare(o, lse, o_ref, l_ref, w.dtype), name)
+    else:
+        rows = sample_rows(w.B, w.H, w.N, 192, seed=w.seed)
+        o_ref, l_ref = oracle_mod.attn_rows(q, k, v, w.dtype, w.causal, w.scale, rows)
+        _check(compare(o.reshape(-1, w.d)[rows], lse.reshape(-1)[rows], o_ref, l_ref, w.dtype),
+               name + " (sampled rows)")
+    # every row: finite, and O is a convex combination of V rows, so each
+    # element lies within its column's range over the head's keys
+    vd = bits_to_f64(v, w.dtype).reshape(w.B * w.H, w.N, w.d)
+    od = bits_to_f64(o, w.dtype).reshape(w.B * w.H, w.N, w.d)
+    assert np.all(np.isfinite(od)) and np.all(np.isfinite(lse))
+    lo, hi = vd.min(axis=1, keepdims=True), vd.max(axis=1, keepdims=True)
+    slack = 1e-3 + half_ulp(od, w.dtype)
+    assert np.all(od >= lo - slack) and np.all(od <= hi + slack)
+
+
+def test_deterministic_and_status_clean():
+    name = "causal_b4_h16_n4096_d128_bf16"
+    w = I.WORKLOADS[name]
+    q, k, v = _inputs(name)
+    o1, l1 = run_fa(q, k, v, w.dtype, w.causal, w.scale)
+    o2, l2 = run_fa(q, k, v, w.dtype, w.causal, w.scale)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    assert fa.fa_check(0) == fa.FA_OK
+
+
+def test_runs_on_a_side_stream(oracle_mod):
+    import torch
+    w = I.custom("stream", 1, 3, 300, 64, "fp16", False, seed_index=31)
+    q, k, v = I.qkv_bits(w)
+    s = torch.cuda.Stream()
+    o, lse = run_fa(q, k, v, "fp16", False, w.scale, stream=s)
+    o_ref, l_ref = oracle_mod.attn_fwd(q, k, v, "fp16", False, w.scale)
+    _check(compare(o, lse, o_ref, l_ref, "fp16"), "side stream")
+
+
+def test_rejects_unsupported_head_dim_on_gpu():
+    import torch
+    x = torch.zeros((1, 1, 128, 96), dtype=torch.float16, device="cuda:0")
+    lse = torch.zeros((1, 1, 128), dtype=torch.float32, device="cuda:0")
+    with pytest.raises(fa.FaError) as e:
+        fa.attention_forward_into(x, x, x, x.clone(), lse)
+    assert e.value.status == fa.FA_ERR_UNSUPPORTED
+
+
+def test_query_launch_is_persistent():
+    info = fa.fa_query_launch(4, 16, 4096, 128)
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert info["units"] == 4 * 16 * 16 and info["grid"] == min(sms, info["units"])
+    assert info["threads"] == 320 and info["smem_bytes"] <= 232448
