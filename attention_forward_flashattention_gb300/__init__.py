@@ -61,6 +61,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
         lib.fa_fwd.restype = i
+        lib.fa_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+        lib.fa_fwd_noalloc.restype = i
         lib.fa_check.argtypes = [vp]
         lib.fa_check.restype = i
         ip = ctypes.POINTER(ctypes.c_int)
@@ -88,6 +90,13 @@ def fa_fwd(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, d: 
     """Same arguments as the C function (device pointers as ints); returns the status."""
     return load_library().fa_fwd(q, k, v, o, lse, B, H, N, d, int(bool(causal)), float(scale),
                                  int(dtype), stream)
+
+
+def fa_fwd_noalloc(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, d: int,
+                   causal: bool, scale: float, dtype: int, stream: int = 0) -> int:
+    """The allocation-free variant of fa_fwd (same arguments); returns the status."""
+    return load_library().fa_fwd_noalloc(q, k, v, o, lse, B, H, N, d, int(bool(causal)),
+                                         float(scale), int(dtype), stream)
 
 
 def fa_check(stream: int = 0) -> int:

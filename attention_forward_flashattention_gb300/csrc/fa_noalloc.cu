@@ -1,0 +1,155 @@
+// fa_fwd_noalloc: the attention forward for callers that cannot allocate
+// device memory. See include/fa.h for the contract.
+//
+// fa_fwd keeps its status word (the scratch its kernel writes when a bounded
+// wait gives up) in device memory it allocates on its first call on a device.
+// This entry point runs the same kernel with that scratch taken from a
+// statically sized device array of this library instead, so no call ever
+// allocates: no cudaMalloc, no cudaFree, no allocating library routine.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_kernel.cuh"
+
+namespace {
+
+// Scratch of the allocation-free entry point: word 0 is the status word of
+// the launch in flight. Every device that loads this library holds these
+// 256 bytes until the process exits; all calls share them.
+constexpr int kNoAllocScratchWords = 64;
+constexpr int kStatusWordsPerLaunch = 1;  // independent of B, H, N, d
+static_assert(kStatusWordsPerLaunch <= kNoAllocScratchWords, "scratch maximum");
+static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocScratchWords];
+
+constexpr int kMaxDevices = 64;
+
+struct NoAllocDevice {
+  bool ready = false;
+  bool arch_ok = false;
+  int sm_count = 0;
+  uint32_t* scratch = nullptr;  // device address of g_noalloc_scratch
+};
+
+std::mutex g_mu;
+NoAllocDevice g_dev[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Same tensor-map layout as fa_fwd: {d, N, B*H}, 64 x 128 x 1 boxes, SW128.
+bool encode(CUtensorMap* m, const void* ptr, bool bf16, int d, int N, long long BH) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2u,
+                                 static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2u};
+  const cuuint32_t box[3] = {64u, 128u, 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+             const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Per-device set-up, done by the first call on each device with that device
+// current: architecture check and the device address of the scratch array
+// (the array's name is only a host-side stand-in in host code).
+fa_status device_setup(NoAllocDevice** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  NoAllocDevice& st = g_dev[dev];
+  if (!st.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FA_ERR_CUDA;
+    st.arch_ok = (major == 10 && minor == 3);
+    st.sm_count = sms;
+    if (st.arch_ok) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+        return FA_ERR_CUDA;
+      st.scratch = static_cast<uint32_t*>(p);
+    }
+    st.ready = true;
+  }
+  if (!st.arch_ok) return FA_ERR_ARCH;
+  *out = &st;
+  return FA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" fa_status fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o,
+                                    float* lse, int B, int H, int N, int d, int causal,
+                                    float scale, fa_dtype dtype, void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_INVALID_ARG;
+  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || N <= 0) return FA_ERR_INVALID_ARG;
+  // Sizes: the scratch need is one status word whatever the problem, so the
+  // limits are the kernel's own (the same as fa_fwd's).
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long BH = static_cast<long long>(B) * H;
+  const long long units = BH * ((static_cast<long long>(N) + 255) / 256);
+  if (BH > 0x7FFFFFFFLL || units > 0x7FFFFFFFLL || N > (1 << 30)) return FA_ERR_UNSUPPORTED;
+
+  NoAllocDevice* st = nullptr;
+  const fa_status ds = device_setup(&st);
+  if (ds != FA_OK) return ds;
+
+  const bool bf16 = dtype == FA_DTYPE_BF16;
+  CUtensorMap maps[4];
+  if (!encode(&maps[0], q, bf16, d, N, BH) || !encode(&maps[1], k, bf16, d, N, BH) ||
+      !encode(&maps[2], v, bf16, d, N, BH) || !encode(&maps[3], o, bf16, d, N, BH))
+    return FA_ERR_CUDA;
+
+  fa::FwdArgs a{};
+  a.lse = lse;
+  a.status = st->scratch;
+  a.N = N;
+  a.BH = static_cast<int>(BH);
+  a.n_mblk = (N + 255) / 256;
+  a.n_units = static_cast<int>(units);
+  a.n_kv = (N + 127) / 128;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  const int grid = a.n_units < st->sm_count ? a.n_units : st->sm_count;
+
+  (void)cudaGetLastError();
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The scratch keeps the previous call's contents: the status word must start
+  // at zero for this launch.
+  if (cudaMemsetAsync(st->scratch, 0, kStatusWordsPerLaunch * sizeof(uint32_t), s) != cudaSuccess)
+    return FA_ERR_CUDA;
+  const cudaError_t e = (d == 64) ? fa::launch_fwd_d64(bf16, causal != 0, maps, a, grid, s)
+                                  : fa::launch_fwd_d128(bf16, causal != 0, maps, a, grid, s);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}

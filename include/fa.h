@@ -75,6 +75,33 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  fa_dtype dtype, void* stream);
 
 /*
+ * fa_fwd_noalloc - fa_fwd for callers that cannot allocate device memory.
+ * (A library convenience: the pages have no counterpart.)
+ *
+ * Some callers own all of the GPU's memory through their own allocator (for
+ * example a serving process that carves HBM into a pool at start-up), or must
+ * not call cudaMalloc / cudaFree at all once running (both can synchronise the
+ * device). fa_fwd allocates a small status word on its first call on a
+ * device; this entry point never allocates: it takes the same arguments and
+ * runs the same kernel, with its scratch (one status word per launch) in a
+ * fixed 256-byte array inside this library that every device loading the
+ * library holds until process exit. The scratch need does not grow with the
+ * problem, so the size limits are fa_fwd's: larger sizes return
+ * FA_ERR_UNSUPPORTED, bad arguments FA_ERR_INVALID_ARG, as fa_fwd.
+ *
+ * The first call on each device (with that device current) looks up the
+ * array's device address with cudaGetSymbolAddress; make that first call
+ * before any stream capture. Each call clears the status word on `stream`
+ * before its launch (an asynchronous memset, not an allocation). All calls
+ * share the one array, so calls that overlap on the GPU (different streams
+ * without ordering between them) race on it. A launch whose bounded waits
+ * gave up leaves O / LSE incomplete; its status is not reported by fa_check.
+ */
+fa_status fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int B, int H, int N, int d, int causal, float scale,
+                         fa_dtype dtype, void* stream);
+
+/*
  * fa_check - synchronise `stream`, then read and clear the current device's
  * status word. Returns FA_OK, FA_ERR_TIMEOUT if a launch since the last check
  * stopped on a wait limit, or FA_ERR_CUDA if the stream reports an error.

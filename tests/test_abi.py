@@ -19,8 +19,8 @@ def lib():
 
 def test_header_declares_expected_entry_points():
     names = fa.header_functions()
-    assert names == ["fa_fwd", "fa_check", "fa_query_launch", "fa_sm_clock_probe",
-                     "fa_status_string", "fa_version"]
+    assert names == ["fa_fwd", "fa_fwd_noalloc", "fa_check", "fa_query_launch",
+                     "fa_sm_clock_probe", "fa_status_string", "fa_version"]
 
 
 def test_library_exports_every_declared_symbol(lib):
