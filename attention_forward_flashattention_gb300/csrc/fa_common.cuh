@@ -132,16 +132,41 @@ __device__ __forceinline__ void store_row32_sw128(uint32_t tile, int r, int col0
   }
 }
 
-// S[tmem: 128 lanes x 128 cols] = Q[128 x D] * K[128 x D]^T, both K-major.
+// Shared-memory descriptor of a K-major SW128 tile (8-row groups 1024 B apart).
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t saddr) {
+  return ptx::sdesc_sw128(saddr, 16, 1024);
+}
+// Shared-memory descriptor of V as an MN-major B operand: 8-key groups 1024 B
+// apart (SBO), 64-column panels 16 KB apart (LBO).
+__device__ __forceinline__ uint64_t desc_v(uint32_t saddr) {
+  return ptx::sdesc_sw128(saddr, kPanelBytes, 1024);
+}
+// A descriptor advanced by `bytes` (the start address field holds addr >> 4;
+// shared addresses stay below 2^18, so the field never carries).
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) {
+  return desc + static_cast<uint64_t>(bytes >> 4);
+}
+
+// S[tmem: 128 lanes x 128 cols] = Q[128 x D] * K[128 x D]^T, both K-major,
+// from precomputed base descriptors (a K step of 16 is +32 B inside a panel,
+// the next panel every 4 steps).
 template <int D, bool BF16>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sQ, uint32_t sK) {
+__device__ __forceinline__ void issue_qk_desc(uint32_t d_tmem, uint64_t dq, uint64_t dk) {
   constexpr uint32_t id = ptx::idesc_f16(BF16, false, 128, 128);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = static_cast<uint32_t>((kk >> 2) * kPanelBytes + (kk & 3) * 32);
-    ptx::umma_f16_ss(d_tmem, ptx::sdesc_sw128(sQ + off, 16, 1024),
-                     ptx::sdesc_sw128(sK + off, 16, 1024), id, kk > 0 ? 1u : 0u);
+    ptx::umma_f16_ss(d_tmem, dq, dk, id, kk > 0 ? 1u : 0u);
+    // next K step: +32 B inside a panel, or on to the next panel
+    const uint32_t step = ((kk & 3) == 3) ? static_cast<uint32_t>(kPanelBytes - 96) : 32u;
+    dq = desc_add(dq, step);
+    dk = desc_add(dk, step);
+    asm volatile("" : "+l"(dq), "+l"(dk));  // advance in place: two live descriptors
   }
+}
+
+template <int D, bool BF16>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sQ, uint32_t sK) {
+  issue_qk_desc<D, BF16>(d_tmem, desc_kmajor(sQ), desc_kmajor(sK));
 }
 
 // O[tmem: 128 lanes x D cols] (+)= P[128 x 128] * V[128 x D]. P is K-major
@@ -152,7 +177,7 @@ template <int D, bool BF16>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t sP, uint32_t sV, bool accumulate,
                                          uint32_t lbo = kPanelBytes, uint32_t sbo = 1024) {
   constexpr uint32_t id = ptx::idesc_f16(BF16, true, 128, D);
-#pragma unroll
+#pragma unroll 1
   for (int kk = 0; kk < 8; ++kk) {
     const uint32_t aoff = static_cast<uint32_t>((kk >> 2) * kPanelBytes + (kk & 3) * 32);
     const uint32_t boff = static_cast<uint32_t>(kk * 2048);
@@ -160,6 +185,26 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t sP, uint32_t 
                      ptx::sdesc_sw128(sV + boff, lbo, sbo), id,
                      (accumulate || kk > 0) ? 1u : 0u);
   }
+}
+
+// O[tmem] (+)= P[tmem] * V[smem]: the P operand comes from tensor memory
+// (128 lanes x 64 columns holding 128 packed 16-bit keys), V as in issue_pv.
+template <int D, bool BF16>
+__device__ __forceinline__ void issue_pv_ts_desc(uint32_t d_tmem, uint32_t p_tmem, uint64_t dv,
+                                                 bool accumulate) {
+  constexpr uint32_t id = ptx::idesc_f16(BF16, true, 128, D);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    ptx::umma_f16_ts(d_tmem, p_tmem + 8u * kk, dv, id, (accumulate || kk > 0) ? 1u : 0u);
+    dv = desc_add(dv, 2048u);
+    asm volatile("" : "+l"(dv));
+  }
+}
+
+template <int D, bool BF16>
+__device__ __forceinline__ void issue_pv_ts(uint32_t d_tmem, uint32_t p_tmem, uint32_t sV,
+                                            bool accumulate) {
+  issue_pv_ts_desc<D, BF16>(d_tmem, p_tmem, desc_v(sV), accumulate);
 }
 
 }  // namespace fa

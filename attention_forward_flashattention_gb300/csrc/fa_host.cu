@@ -152,12 +152,13 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 
   const bool bf16 = dtype == FA_DTYPE_BF16;
   const long long BH = static_cast<long long>(B) * H;
-  CUtensorMap maps[4];
+  CUtensorMap maps[3];
   if (!fa::encode_qkvo(&maps[0], q, bf16, d, N, BH) || !fa::encode_qkvo(&maps[1], k, bf16, d, N, BH) ||
-      !fa::encode_qkvo(&maps[2], v, bf16, d, N, BH) || !fa::encode_qkvo(&maps[3], o, bf16, d, N, BH))
+      !fa::encode_qkvo(&maps[2], v, bf16, d, N, BH))
     return FA_ERR_CUDA;
 
   fa::FwdArgs a{};
+  a.o = o;
   a.lse = lse;
   a.status = st->status;
   a.N = N;

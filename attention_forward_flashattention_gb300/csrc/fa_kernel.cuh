@@ -1,26 +1,36 @@
-// Fused attention forward for sm_103a: TMA loads, tcgen05.mma with S and O
-// accumulators in TMEM, online softmax in registers, TMA-store epilogue.
+// Fused attention forward for sm_103a: TMA loads, tcgen05.mma with S, P and O
+// in TMEM, online softmax in registers, direct epilogue from TMEM.
 //
 // Work unit: 256 query rows of one (batch, head), split into two 128-row
 // Q tiles that share every K / V tile (ping-pong: while the softmax of one
 // tile runs, the tensor core works on the other). A persistent grid of one
 // CTA per SM walks the units.
 //
-// Warp roles (10 warps, 320 threads):
-//   warp 0      TMA producer: Q tiles, then K_j, V_j into a ring of stages
-//               (the producer loop of "TMA + Warp Specialization", 17.4).
-//   warp 1      TMEM owner and single-thread MMA issuer (tcgen05.mma is
-//               issued by one thread, "TCA 51%, MFU below 8%", B200 section).
-//   warps 2-5   softmax for Q tile 0 (one thread per row = TMEM lane, as in
-//               the B300 walkthrough, V14 item d).
-//   warps 6-9   softmax for Q tile 1.
-// A softmax warpgroup is four consecutive warps, so its warps cover the four
-// TMEM lane quarters (warp w reaches lanes 32*(w%4)..+31).
+// Warp roles (16 warps = 4 warpgroups, 512 threads):
+//   WG0  warp 0: TMA producer: Q tiles, then K_j, V_j into a ring of stages
+//                (the producer loop of "TMA + Warp Specialization", 17.4).
+//        warp 1: TMEM owner and single-thread MMA issuer (tcgen05.mma is
+//                issued by one thread, "TCA 51%, MFU below 8%", B200 section).
+//        warps 2-3 idle.
+//   WG1  softmax of Q tile 0, one thread per row = TMEM lane (the B300
+//        walkthrough, V14 item d);
+//   WG2  softmax of Q tile 1;
+//   WG3  epilogue of both tiles: O / l from TMEM straight to global memory.
+// Each warpgroup's four warps cover the four TMEM lane quarters (warp w
+// reaches lanes 32*(w%4)..+31). Registers are rebalanced with setmaxnreg
+// (the register reallocation of "TMA + Warp Specialization", 17.4-17.5):
+// 64 for WG0, 192 for each softmax WG, 64 for the epilogue, which sums to the
+// 128 x 4 the CTA is launched with.
 //
-// The MMA thread issues S0 = Q0 K_0^T, S1 = Q1 K_0^T, then per KV tile j, in order,
-//   O0 += P0 V_j, S0 = Q0 K_{j+1}^T, O1 += P1 V_j, S1 = Q1 K_{j+1}^T
-// Tensor-core ops of one thread execute in issue order, so S_i(j+1) may reuse
-// the S_i columns right after the PV that consumed P_i(j).
+// TMEM (512 columns): S0 0-127, S1 128-255, O0 256.., O1 256+D..; P_i is
+// written by the softmax over the first 64 columns of S_i (two 16-bit values
+// per column) and read from there by the O += P V MMA (A operand in TMEM).
+//
+// MMA order: S0 = Q0 K_0^T, S1 = Q1 K_0^T, then per KV tile j
+//   O0 += P0 V_j, S0 = Q0 K_{j+1}^T, O1 += P1 V_j, S1 = Q1 K_{j+1}^T.
+// Tensor-core ops of one thread execute in issue order, so S_i(j+1) may
+// overwrite the S_i / P_i columns right after the PV that consumed P_i(j),
+// and the commit that signals S_i(j+1) also implies O_i holds PV_i(j).
 //
 // Online softmax in base 2 (c = scale * log2 e): m_new = max(m_ref, c * max s);
 // the reference max m_ref is only moved (and O, l rescaled by
@@ -37,6 +47,7 @@
 namespace fa {
 
 struct FwdArgs {
+  void* o;           // [BH][N][D] 16-bit output
   float* lse;        // [BH][N] fp32, natural-log logsumexp
   uint32_t* status;  // device status word (timeouts)
   int N;             // sequence length
@@ -47,37 +58,42 @@ struct FwdArgs {
   float scale_log2;  // scale * log2(e)
 };
 
+constexpr int kFwdThreads = 512;
+// setmaxnreg split per thread: WG0, each softmax WG, epilogue WG (sum 512 = 4 x 128).
+constexpr uint32_t kRegsWG0 = 64, kRegsSoftmax = 192, kRegsEpilogue = 64;
+static_assert(kRegsWG0 + 2 * kRegsSoftmax + kRegsEpilogue == 4 * (65536 / kFwdThreads),
+              "register split must equal the launch allocation");
+
 template <int D>
 struct Layout {
   static constexpr int kPanels = D / 64;                   // 128-byte panels per row
-  static constexpr int kTileBytes = kPanels * kPanelBytes;  // a Q, K, V or O tile
-  static constexpr int kPBytes = 2 * kPanelBytes;           // P tile: 128 x 128 16-bit
-  static constexpr int kStages = (D == 128) ? 3 : 6;        // K / V ring slots
+  static constexpr int kTileBytes = kPanels * kPanelBytes;  // a Q, K or V tile
+  static constexpr int kStages = (D == 128) ? 4 : 8;        // K / V ring slots
   static constexpr int kOffQ = 0;                           // Q0, Q1
-  static constexpr int kOffP = 2 * kTileBytes;              // P0, P1 (also O staging)
-  static constexpr int kOffKV = kOffP + 2 * kPBytes;        // ring
-  static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
-  static constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers + alignment slack
+  static constexpr int kOffKV = 2 * kTileBytes;             // ring
+  static constexpr int kOffStats = kOffKV + kStages * kTileBytes;  // [2 units][2 tiles][128] l
+  static constexpr int kOffBar = kOffStats + 2 * 2 * 128 * 4;
+  static constexpr int kSmemBytes = kOffBar + 512 + 1024;  // barriers + alignment slack
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColS = 0;    // S_i at columns i*128
+  static constexpr uint32_t kColS = 0;    // S_i (and P_i) at columns i*128
   static constexpr uint32_t kColO = 256;  // O_i at columns 256 + i*D
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
 // Barrier slots (8 bytes each) in the barrier block.
 enum BarSlot : int {
-  kBarQFull = 0,    // [2] TMA: Q_i landed
-  kBarQEmpty = 2,   // MMA: all S MMAs of the unit done (Q tiles reusable)
-  kBarSFull = 3,    // [2] MMA: S_i ready in TMEM
-  kBarPFull = 5,    // [2] 128 softmax threads: P_i in smem, O_i rescaled
-  kBarPVDone = 7,   // [2] MMA: O_i += P_i V done (P_i, O_i reusable)
-  kBarEpiFull = 9,  // [2] 128 softmax threads: O_i staged in smem
-  kBarEpiFree = 11, // [2] store thread: staged O_i read by the TMA store
-  kBarDrain = 13,   // MMA: every tcgen05 op of the CTA completed
-  kBarKVFull = 14,  // [stages] TMA: ring slot loaded
+  kBarQFull = 0,      // [2] TMA: Q_i landed
+  kBarQEmpty = 2,     // MMA: all S MMAs of the unit done (Q tiles reusable)
+  kBarSFull = 3,      // [2] MMA: S_i ready in TMEM (and O_i holds every earlier PV)
+  kBarPFull = 5,      // [2] 128 softmax threads: P_i in TMEM, O_i rescaled
+  kBarOFull = 7,      // [2] MMA: the unit's last O_i += P_i V done
+  kBarOFree = 9,      // [2] 128 epilogue threads: O_i read, may be overwritten
+  kBarStatsFull = 11, // [2] 128 softmax threads: row sums l of tile i in smem
+  kBarDrain = 13,     // MMA: every tcgen05 op of the CTA completed
+  kBarKVFull = 14,    // [stages] TMA: ring slot loaded; then [stages] ring slot free
 };
-constexpr int kSlotTmem = 224;   // byte offset of the TMEM base address
-constexpr int kSlotAbort = 228;  // byte offset of the abort flag
+constexpr int kSlotTmem = 480;   // byte offset of the TMEM base address
+constexpr int kSlotAbort = 484;  // byte offset of the abort flag
 
 // Walks this CTA's units: round k takes unit k*G + c; for causal problems odd
 // rounds go in reverse CTA order so per-CTA work evens out over the
@@ -170,87 +186,106 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tm_q, const CUt
   }
 }
 
+// The whole MMA warp runs this loop (waits are warp-wide and every value is
+// warp-uniform); one lane issues the tcgen05 instructions. Descriptors are
+// built once and advanced by constant offsets, so one MMA costs a few
+// instructions to issue, well under the ~64 cycles a 128x128x16 MMA keeps the
+// tensor core busy.
 template <int D, bool BF16, bool CAUSAL>
 __device__ __forceinline__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t bars,
-                                         uint32_t tmem, const AbortCtx& ab) {
+                                         uint32_t tmem, const AbortCtx& ab, int lane) {
   using L = Layout<D>;
   constexpr int S = L::kStages;
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
-  const uint32_t sQ[2] = {sbase + L::kOffQ, sbase + L::kOffQ + L::kTileBytes};
-  const uint32_t sP[2] = {sbase + L::kOffP, sbase + L::kOffP + L::kPBytes};
+  const bool leader = lane == 0;
+  const uint64_t dQ[2] = {desc_kmajor(sbase + L::kOffQ),
+                          desc_kmajor(sbase + L::kOffQ + L::kTileBytes)};
+  const uint64_t dK0 = desc_kmajor(sbase + L::kOffKV);  // ring slot s: + s * kTileBytes
+  const uint64_t dV0 = desc_v(sbase + L::kOffKV);
   const uint32_t tS[2] = {tmem + L::kColS, tmem + L::kColS + 128};
   const uint32_t tO[2] = {tmem + L::kColO, tmem + L::kColO + D};
-  auto slot = [&](uint32_t idx) { return sbase + L::kOffKV + (idx % S) * L::kTileBytes; };
+  auto slot_off = [](uint32_t idx) { return (idx % S) * static_cast<uint32_t>(L::kTileBytes); };
+  auto kv_wait = [&](uint32_t idx) {
+    return wait_bounded_warp(bar(kBarKVFull + idx % S), (idx / S) & 1u, ab, kStatusMma);
+  };
   uint32_t ring = 0, units = 0, pcnt[2] = {0u, 0u};
   int round = 0, bh = 0, mblk = 0;
   bool ok = true;
   while (ok && next_unit<CAUSAL>(round, a, bh, mblk)) {
     const int nkv = unit_kv_tiles<CAUSAL>(a, mblk);
-    ok = wait_bounded(bar(kBarQFull + 0), units & 1u, ab, kStatusMma) &&
-         wait_bounded(bar(kBarQFull + 1), units & 1u, ab, kStatusMma);
+    ok = wait_bounded_warp(bar(kBarQFull + 0), units & 1u, ab, kStatusMma) &&
+         wait_bounded_warp(bar(kBarQFull + 1), units & 1u, ab, kStatusMma);
     if (!ok) break;
-    ++units;
     // S_i(0) = Q_i K_0^T
     const uint32_t k0 = ring++;
-    if (!(ok = wait_bounded(bar(kBarKVFull + k0 % S), (k0 / S) & 1u, ab, kStatusMma))) break;
+    if (!(ok = kv_wait(k0))) break;
     ptx::tc_fence_after();
-    issue_qk<D, BF16>(tS[0], sQ[0], slot(k0));
-    ptx::umma_commit(bar(kBarSFull + 0));
-    issue_qk<D, BF16>(tS[1], sQ[1], slot(k0));
-    ptx::umma_commit(bar(kBarSFull + 1));
-    ptx::umma_commit(bar(kBarKVFull + S + k0 % S));
-    if (nkv == 1) ptx::umma_commit(bar(kBarQEmpty));
+    if (leader) {
+      const uint64_t dk = desc_add(dK0, slot_off(k0));
+      issue_qk_desc<D, BF16>(tS[0], dQ[0], dk);
+      ptx::umma_commit(bar(kBarSFull + 0));
+      issue_qk_desc<D, BF16>(tS[1], dQ[1], dk);
+      ptx::umma_commit(bar(kBarSFull + 1));
+      ptx::umma_commit(bar(kBarKVFull + S + k0 % S));
+      if (nkv == 1) ptx::umma_commit(bar(kBarQEmpty));
+    }
+    __syncwarp();
     for (int j = 0; j < nkv; ++j) {
       const uint32_t vj = ring++;
-      if (!(ok = wait_bounded(bar(kBarKVFull + vj % S), (vj / S) & 1u, ab, kStatusMma))) break;
+      if (!(ok = kv_wait(vj))) break;
       const bool more = j + 1 < nkv;
-      const uint32_t kn = more ? ring : 0u;
-      // Q tile 0: O0 += P0 V_j, then S0 = Q0 K_{j+1}^T
-      if (!(ok = wait_bounded(bar(kBarPFull + 0), (pcnt[0]++) & 1u, ab, kStatusMma))) break;
-      ptx::tc_fence_after();
-      issue_pv<D, BF16>(tO[0], sP[0], slot(vj), j > 0);
-      ptx::umma_commit(bar(kBarPVDone + 0));
-      if (more) {
-        ++ring;
-        if (!(ok = wait_bounded(bar(kBarKVFull + kn % S), (kn / S) & 1u, ab, kStatusMma))) break;
+      const uint32_t kn = ring;
+      const uint64_t dv = desc_add(dV0, slot_off(vj));
+      const uint64_t dk = desc_add(dK0, slot_off(kn));
+      for (int i = 0; i < 2; ++i) {
+        // O_i += P_i V_j (P_i read from TMEM), then S_i = Q_i K_{j+1}^T
+        if (!(ok = wait_bounded_warp(bar(kBarPFull + i), (pcnt[i]++) & 1u, ab, kStatusMma))) break;
+        if (j == 0 && units > 0 &&
+            !(ok = wait_bounded_warp(bar(kBarOFree + i), (units - 1) & 1u, ab, kStatusMma)))
+          break;
+        if (more && i == 0 && !(ok = kv_wait(kn))) break;
         ptx::tc_fence_after();
-        issue_qk<D, BF16>(tS[0], sQ[0], slot(kn));
-        ptx::umma_commit(bar(kBarSFull + 0));
+        if (leader) {
+          issue_pv_ts_desc<D, BF16>(tO[i], tS[i], dv, j > 0);
+          if (i == 1) ptx::umma_commit(bar(kBarKVFull + S + vj % S));
+          if (!more) {
+            ptx::umma_commit(bar(kBarOFull + i));
+          } else {
+            issue_qk_desc<D, BF16>(tS[i], dQ[i], dk);
+            ptx::umma_commit(bar(kBarSFull + i));
+            if (i == 1) {
+              ptx::umma_commit(bar(kBarKVFull + S + kn % S));
+              if (j + 2 == nkv) ptx::umma_commit(bar(kBarQEmpty));
+            }
+          }
+        }
+        __syncwarp();
       }
-      // Q tile 1: O1 += P1 V_j, then S1 = Q1 K_{j+1}^T
-      if (!(ok = wait_bounded(bar(kBarPFull + 1), (pcnt[1]++) & 1u, ab, kStatusMma))) break;
-      ptx::tc_fence_after();
-      issue_pv<D, BF16>(tO[1], sP[1], slot(vj), j > 0);
-      ptx::umma_commit(bar(kBarPVDone + 1));
-      ptx::umma_commit(bar(kBarKVFull + S + vj % S));
-      if (more) {
-        issue_qk<D, BF16>(tS[1], sQ[1], slot(kn));
-        ptx::umma_commit(bar(kBarSFull + 1));
-        ptx::umma_commit(bar(kBarKVFull + S + kn % S));
-        if (j + 2 == nkv) ptx::umma_commit(bar(kBarQEmpty));
-      }
+      if (!ok) break;
+      if (more) ++ring;
     }
+    ++units;
   }
-  // Every tcgen05 op this thread issued must finish before TMEM is freed.
-  ptx::umma_commit(bar(kBarDrain));
+  // Every tcgen05 op this warp issued must finish before TMEM is freed.
+  if (leader) ptx::umma_commit(bar(kBarDrain));
+  __syncwarp();
   wait_drain(bar(kBarDrain), 0u, ab, kStatusDrain);
 }
 
 template <int D, bool BF16, bool CAUSAL>
-__device__ __forceinline__ void softmax_role(const CUtensorMap* tm_o, const FwdArgs& a,
-                                             uint32_t sbase, uint32_t bars, uint32_t tmem,
-                                             const AbortCtx& ab, int warp, int lane) {
+__device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t bars, uint32_t tmem,
+                                             float* stats, const AbortCtx& ab, int warp,
+                                             int lane) {
   using L = Layout<D>;
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
-  const int wg = (warp - 2) >> 2;           // which Q tile
+  const int wg = (warp >> 2) - 1;           // which Q tile
   const int r = (warp & 3) * 32 + lane;     // row in the tile = TMEM lane
   const uint32_t tl = ptx::tmem_lane_base(tmem, warp);
-  const uint32_t tS = tl + L::kColS + 128u * wg;
+  const uint32_t tS = tl + L::kColS + 128u * wg;  // S_i; P_i over its first 64 columns
   const uint32_t tO = tl + L::kColO + static_cast<uint32_t>(D) * wg;
-  const uint32_t sP = sbase + L::kOffP + L::kPBytes * wg;  // P tile, then O staging
-  const bool store_thread = (warp == 2 + 4 * wg) && lane == 0;
   const float cl2 = a.scale_log2;
-  uint32_t scnt = 0, pvcnt = 0, units = 0;
+  const float2 c2 = make_float2(cl2, cl2);
+  uint32_t scnt = 0, units = 0;
   int round = 0, bh = 0, mblk = 0;
   bool ok = true;
   while (ok && next_unit<CAUSAL>(round, a, bh, mblk)) {
@@ -282,11 +317,11 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap* tm_o, const FwdA
       }
       float mx[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-      for (int c = 4; c < 128; c += 4) {
-        mx[0] = fmaxf(mx[0], s[c]);
-        mx[1] = fmaxf(mx[1], s[c + 1]);
-        mx[2] = fmaxf(mx[2], s[c + 2]);
-        mx[3] = fmaxf(mx[3], s[c + 3]);
+      for (int c = 4; c < 128; c += 8) {
+        mx[0] = ptx::fmax3(mx[0], s[c], s[c + 1]);
+        mx[1] = ptx::fmax3(mx[1], s[c + 2], s[c + 3]);
+        mx[2] = ptx::fmax3(mx[2], s[c + 4], s[c + 5]);
+        mx[3] = ptx::fmax3(mx[3], s[c + 6], s[c + 7]);
       }
       const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * cl2;
       const float m_new = fmaxf(m_ref, m_tile);
@@ -297,108 +332,132 @@ __device__ __forceinline__ void softmax_role(const CUtensorMap* tm_o, const FwdA
         alpha = ptx::ex2(m_ref - m_new);
         m_ref = m_new;
       }
-      const float neg = -m_ref;
-      uint32_t pk[64];
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
-      float lr[4] = {0.f, 0.f, 0.f, 0.f};
+      const float2 neg2 = make_float2(-m_ref, -m_ref);
+      uint32_t pk[2][32];
+      float2 ls[4], lr[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) ls[t] = lr[t] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        const float p0 = ptx::ex2(fmaf(s[2 * c], cl2, neg));
-        const float p1 = ptx::ex2(fmaf(s[2 * c + 1], cl2, neg));
-        pk[c] = pack2<BF16>(p0, p1);
-        ls[c & 3] += p0 + p1;
+        const float2 t = ptx::ffma2(make_float2(s[2 * c], s[2 * c + 1]), c2, neg2);
+        const float p0 = ptx::ex2(t.x), p1 = ptx::ex2(t.y);
+        const uint32_t w = pack2<BF16>(p0, p1);
+        pk[c >> 5][c & 31] = w;
+        ls[c & 3] = ptx::fadd2(ls[c & 3], make_float2(p0, p1));
         if constexpr (BF16) {
           // bf16 P carries 8 significant bits: O is normalised by the sum of
           // the rounded weights the PV product actually uses (a row dominated
           // by one key then returns that V row exactly), while the LSE keeps
           // the unrounded sum.
-          lr[c & 3] += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xFFFF0000u);
+          lr[c & 3] = ptx::fadd2(lr[c & 3], make_float2(__uint_as_float(w << 16),
+                                                        __uint_as_float(w & 0xFFFF0000u)));
         }
       }
-      const float lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      const float lsum_p = BF16 ? (lr[0] + lr[1]) + (lr[2] + lr[3]) : lsum;
-      if (j > 0) {
-        // O_i must hold PV(j-1) before it is rescaled, and P_i must be free.
-        if (!(ok = wait_bounded_warp(bar(kBarPVDone + wg), (pvcnt++) & 1u, ab, kStatusSoftmax)))
-          break;
-        ptx::tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+      // P_i into TMEM over the S_i columns this thread has already read.
+      ptx::tmem_st32(tS, pk[0]);
+      ptx::tmem_st32(tS + 32u, pk[1]);
+      const float2 s01 = ptx::fadd2(ptx::fadd2(ls[0], ls[1]), ptx::fadd2(ls[2], ls[3]));
+      const float lsum = s01.x + s01.y;
+      float lsum_p = lsum;
+      if constexpr (BF16) {
+        const float2 r01 = ptx::fadd2(ptx::fadd2(lr[0], lr[1]), ptx::fadd2(lr[2], lr[3]));
+        lsum_p = r01.x + r01.y;
+      }
+      // Rescale O_i (it holds PV_i(j-1): the S_i(j) commit came after it).
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            ptx::tmem_ld32(tO + 32u * c, o);
-            ptx::tmem_ld_wait(o);
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          ptx::tmem_ld32(tO + 32u * c, o);
+          ptx::tmem_ld_wait(o);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            ptx::tmem_st32(tO + 32u * c, o);
+          for (int e = 0; e < 32; e += 2) {
+            const float2 v =
+                ptx::fmul2(make_float2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2);
+            o[e] = __float_as_uint(v.x);
+            o[e + 1] = __float_as_uint(v.y);
           }
-          ptx::tmem_st_wait();
+          ptx::tmem_st32(tO + 32u * c, o);
         }
-      } else if (units > 0) {
-        // P_i doubles as the previous unit's O staging: wait for its store.
-        if (!(ok = wait_bounded_warp(bar(kBarEpiFree + wg), (units - 1) & 1u, ab, kStatusSoftmax)))
-          break;
       }
-      l = l * alpha + lsum_p;
-      l_exp = l_exp * alpha + lsum;
-      store_row128_sw128(sP, r, pk);
-      ptx::fence_proxy_async_smem();
+      ptx::tmem_st_wait();
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(kBarPFull + wg));
+      l = l * alpha + lsum_p;
+      l_exp = l_exp * alpha + lsum;
     }
     if (!ok) break;
-    // Epilogue: O_i / l -> 16-bit -> staging (SW128) -> TMA store; LSE.
-    if (!(ok = wait_bounded_warp(bar(kBarPVDone + wg), (pvcnt++) & 1u, ab, kStatusSoftmax))) break;
-    ptx::tc_fence_after();
-    const float inv_l = 1.f / l;
-#pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t o[32];
-      ptx::tmem_ld32(tO + 32u * c, o);
-      ptx::tmem_ld_wait(o);
-      uint32_t pk[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e)
-        pk[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
-      store_row32_sw128(sP, r, 32 * c, pk);
-    }
     if (grow < a.N)
       a.lse[static_cast<size_t>(bh) * a.N + grow] = (m_ref + log2f(l_exp)) * 0.69314718055994531f;
-    ptx::fence_proxy_async_smem();
-    ptx::tc_fence_before();
-    ptx::mbar_arrive(bar(kBarEpiFull + wg));
-    if (store_thread) {
-      if (wait_bounded(bar(kBarEpiFull + wg), units & 1u, ab, kStatusEpilogue)) {
-        if (tile_row0 < a.N) {  // a tile wholly past N (odd tile count) has nothing to store
-          for (int p = 0; p < L::kPanels; ++p)
-            ptx::tma_store_3d(tm_o, sP + p * kPanelBytes, 64 * p, tile_row0, bh);
-          ptx::bulk_commit();
-          ptx::bulk_wait_read_all();
-        }
-        ptx::mbar_arrive(bar(kBarEpiFree + wg));
-      } else {
-        ok = false;
-      }
-    }
-    __syncwarp();
+    stats[(units & 1u) * 256u + wg * 128 + r] = l;
+    ptx::mbar_arrive(bar(kBarStatsFull + wg));
     ++units;
   }
-  if (store_thread) ptx::bulk_wait_all();
 }
 
 template <int D, bool BF16, bool CAUSAL>
-__global__ void __launch_bounds__(320, 1)
+__device__ __forceinline__ void epilogue_role(const FwdArgs& a, uint32_t bars, uint32_t tmem,
+                                              const float* stats, const AbortCtx& ab, int warp,
+                                              int lane) {
+  using L = Layout<D>;
+  auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
+  const int r = (warp & 3) * 32 + lane;
+  const uint32_t tl = ptx::tmem_lane_base(tmem, warp);
+  uint16_t* out = static_cast<uint16_t*>(a.o);
+  uint32_t units = 0;
+  int round = 0, bh = 0, mblk = 0;
+  bool ok = true;
+  while (ok && next_unit<CAUSAL>(round, a, bh, mblk)) {
+    for (int i = 0; i < 2 && ok; ++i) {
+      ok = wait_bounded_warp(bar(kBarOFull + i), units & 1u, ab, kStatusEpilogue) &&
+           wait_bounded_warp(bar(kBarStatsFull + i), units & 1u, ab, kStatusEpilogue);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const float inv_l = 1.f / stats[(units & 1u) * 256u + i * 128 + r];
+      const float2 il2 = make_float2(inv_l, inv_l);
+      const int grow = mblk * 256 + 128 * i + r;
+      uint4* orow = reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * a.N + grow) * D);
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        ptx::tmem_ld32(tl + L::kColO + static_cast<uint32_t>(D) * i + 32u * c, o);
+        ptx::tmem_ld_wait(o);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float2 v = ptx::fmul2(
+              make_float2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), il2);
+          pk[e] = pack2<BF16>(v.x, v.y);
+        }
+        if (grow < a.N) {
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            __stcs(orow + 4 * c + t,
+                   make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]));
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(kBarOFree + i));
+    }
+    ++units;
+  }
+}
+
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                  const FwdArgs a) {
+                  const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
   using L = Layout<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t* sgen = smem_raw + (sbase - raw);
   const uint32_t bars = sbase + L::kOffBar;
+  float* stats = reinterpret_cast<float*>(sgen + L::kOffStats);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + L::kOffBar + kSlotTmem);
-  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(sgen + L::kOffBar + kSlotAbort);
+  volatile uint32_t* abort_flag =
+      reinterpret_cast<volatile uint32_t*>(sgen + L::kOffBar + kSlotAbort);
   const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
   const AbortCtx ab{abort_flag, a.status};
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
@@ -408,9 +467,9 @@ __global__ void __launch_bounds__(320, 1)
       ptx::mbar_init(bar(kBarQFull + i), 1);
       ptx::mbar_init(bar(kBarSFull + i), 1);
       ptx::mbar_init(bar(kBarPFull + i), 128);
-      ptx::mbar_init(bar(kBarPVDone + i), 1);
-      ptx::mbar_init(bar(kBarEpiFull + i), 128);
-      ptx::mbar_init(bar(kBarEpiFree + i), 1);
+      ptx::mbar_init(bar(kBarOFull + i), 1);
+      ptx::mbar_init(bar(kBarOFree + i), 128);
+      ptx::mbar_init(bar(kBarStatsFull + i), 128);
     }
     ptx::mbar_init(bar(kBarQEmpty), 1);
     ptx::mbar_init(bar(kBarDrain), 1);
@@ -430,12 +489,20 @@ __global__ void __launch_bounds__(320, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    if (lane == 0) producer_role<D, BF16, CAUSAL>(&tm_q, &tm_k, &tm_v, a, sbase, bars, ab);
-  } else if (warp == 1) {
-    if (lane == 0) mma_role<D, BF16, CAUSAL>(a, sbase, bars, tmem, ab);
+  const int wgrp = warp >> 2;
+  if (wgrp == 0) {
+    ptx::setmaxnreg_dec<kRegsWG0>();
+    if (warp == 0) {
+      if (lane == 0) producer_role<D, BF16, CAUSAL>(&tm_q, &tm_k, &tm_v, a, sbase, bars, ab);
+    } else if (warp == 1) {
+      mma_role<D, BF16, CAUSAL>(a, sbase, bars, tmem, ab, lane);
+    }
+  } else if (wgrp < 3) {
+    ptx::setmaxnreg_inc<kRegsSoftmax>();
+    softmax_role<D, BF16, CAUSAL>(a, bars, tmem, stats, ab, warp, lane);
   } else {
-    softmax_role<D, BF16, CAUSAL>(&tm_o, a, sbase, bars, tmem, ab, warp, lane);
+    ptx::setmaxnreg_dec<kRegsEpilogue>();
+    epilogue_role<D, BF16, CAUSAL>(a, bars, tmem, stats, ab, warp, lane);
   }
   __syncwarp();
   ptx::tc_fence_before();
@@ -445,11 +512,11 @@ __global__ void __launch_bounds__(320, 1)
 }
 
 // Host-side launch of one instance (defined in the per-head-dim files).
+// maps: Q, K, V tensor maps.
 cudaError_t launch_fwd_d64(bool bf16, bool causal, const CUtensorMap* maps, const FwdArgs& a,
                            int grid, cudaStream_t stream);
 cudaError_t launch_fwd_d128(bool bf16, bool causal, const CUtensorMap* maps, const FwdArgs& a,
                             int grid, cudaStream_t stream);
 int fwd_smem_bytes(int d);
-constexpr int kFwdThreads = 320;
 
 }  // namespace fa

@@ -127,12 +127,13 @@ extern "C" fa_status fa_fwd_noalloc(const void* q, const void* k, const void* v,
   if (ds != FA_OK) return ds;
 
   const bool bf16 = dtype == FA_DTYPE_BF16;
-  CUtensorMap maps[4];
+  CUtensorMap maps[3];
   if (!encode(&maps[0], q, bf16, d, N, BH) || !encode(&maps[1], k, bf16, d, N, BH) ||
-      !encode(&maps[2], v, bf16, d, N, BH) || !encode(&maps[3], o, bf16, d, N, BH))
+      !encode(&maps[2], v, bf16, d, N, BH))
     return FA_ERR_CUDA;
 
   fa::FwdArgs a{};
+  a.o = o;
   a.lse = lse;
   a.status = st->scratch;
   a.N = N;

@@ -144,6 +144,19 @@ __device__ __forceinline__ void umma_f16_ss(uint32_t d_tmem, uint64_t adesc, uin
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem desc], kind::f16. A is M lanes x K 16-bit
+// elements packed two per 32-bit column (element 2c in the low half of
+// column c), so a K step of 16 elements advances A by 8 columns.
+__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // The mbarrier receives one arrival when all tcgen05 operations this thread
 // issued before the commit have completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -224,6 +237,59 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, bool b_mn_major, int
 }
 
 // ----------------------------------------------------------------- math
+
+// Register reallocation for the executing warpgroup (all its warps execute it).
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Packed fp32 pair arithmetic (two IEEE fp32 lanes per instruction, each
+// lane rounded exactly as the scalar instruction).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  uint64_t r;
+  asm("{\n\t.reg .b64 xa, xb, xc;\n\t"
+      "mov.b64 xa, {%1, %2};\n\tmov.b64 xb, {%3, %4};\n\tmov.b64 xc, {%5, %6};\n\t"
+      "fma.rn.f32x2 %0, xa, xb, xc;\n\t}"
+      : "=l"(r)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  float2 o;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+  return o;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  uint64_t r;
+  asm("{\n\t.reg .b64 xa, xb;\n\t"
+      "mov.b64 xa, {%1, %2};\n\tmov.b64 xb, {%3, %4};\n\t"
+      "add.f32x2 %0, xa, xb;\n\t}"
+      : "=l"(r)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  float2 o;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+  return o;
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  uint64_t r;
+  asm("{\n\t.reg .b64 xa, xb;\n\t"
+      "mov.b64 xa, {%1, %2};\n\tmov.b64 xb, {%3, %4};\n\t"
+      "mul.f32x2 %0, xa, xb;\n\t}"
+      : "=l"(r)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  float2 o;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+  return o;
+}
 
 // 2^x on the MUFU unit (approximate, flushes denormals; 2^-inf = 0).
 __device__ __forceinline__ float ex2(float x) {

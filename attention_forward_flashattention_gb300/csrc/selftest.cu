@@ -14,6 +14,9 @@
 //                         `variant` swaps the two byte offsets of the B
 //                         descriptor (both stay inside the B tile), so one run
 //                         shows which assignment the hardware expects.
+//   fa_selftest_gemm_ts : as gemm_pv, but A is stored by the threads into TMEM
+//                         with tcgen05.st (packed pairs) and the MMA reads it
+//                         from there (the P-in-TMEM path).
 //   fa_selftest_wait_timeout : a wait on a barrier nothing completes, with a
 //                         short limit; checks that the bounded wait gives up,
 //                         records its status bit and lets the kernel exit.
@@ -197,6 +200,67 @@ __global__ void __launch_bounds__(128, 1)
   if (warp == 0) ptx::tmem_dealloc(tmem, 128);
 }
 
+// C[128][N] = A[128][128] * B[128][N] with A stored by the threads into TMEM
+// (tcgen05.st, packed pairs, columns 128..191) and multiplied from there.
+template <int N, bool BF16>
+__global__ void __launch_bounds__(128, 1)
+    gemm_ts_kernel(const uint16_t* a, const __grid_constant__ CUtensorMap tb, float* c,
+                   uint32_t* status) {
+  extern __shared__ __align__(1024) uint8_t raw[];
+  const Smem s = carve(raw);
+  const AbortCtx ab{s.abort_flag, status};
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(s.bars, 1);
+    ptx::mbar_init(s.bars + 8, 1);
+    *s.abort_flag = 0u;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc(ptx::smem_u32(s.tmem_slot), 256);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *s.tmem_slot;
+  {
+    const int r = threadIdx.x;
+    uint32_t pk[2][32];
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(a + r * 128);
+    for (int i = 0; i < 64; ++i) pk[i >> 5][i & 31] = src[i];
+    const uint32_t t = ptx::tmem_lane_base(tmem, warp) + 128u;
+    ptx::tmem_st32(t, pk[0]);
+    ptx::tmem_st32(t + 32u, pk[1]);
+    ptx::tmem_st_wait();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  constexpr int kPanels = N / 64;
+  bool ok = true;
+  if (threadIdx.x == 0) {
+    ptx::mbar_arrive_expect_tx(s.bars, kPanels * kPanelBytes);
+    for (int p = 0; p < kPanels; ++p)
+      ptx::tma_load_3d(s.base + 2 * kPanelBytes + p * kPanelBytes, &tb, s.bars, 64 * p, 0, 0);
+    ok = wait_bounded(s.bars, 0, ab, kStatusSelftest);
+    if (ok) {
+      ptx::tc_fence_after();
+      issue_pv_ts<N, BF16>(tmem, tmem + 128u, s.base + 2 * kPanelBytes, false);
+    }
+    ptx::umma_commit(s.bars + 8);
+    if (!ok) wait_drain(s.bars, 0, ab, kStatusDrain);
+  }
+  __syncwarp();
+  const bool done = wait_bounded_warp(s.bars + 8, 0, ab, kStatusSelftest);
+  ptx::tc_fence_after();
+  if (done && !*s.abort_flag) read_back(tmem, c, N);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 0) ptx::tmem_dealloc(tmem, 256);
+}
+
 // One warp waits on a barrier that never completes, with a 20 ms limit.
 __global__ void wait_timeout_kernel(uint32_t* status, uint32_t* out) {
   __shared__ __align__(8) uint64_t bar;
@@ -255,6 +319,25 @@ int fa_selftest_gemm_pv(const void* a, const void* b, float* c, int N, int bf16,
   };
   if (N == 64) return bf16 ? launch(fa::gemm_pv_kernel<64, true>) : launch(fa::gemm_pv_kernel<64, false>);
   return bf16 ? launch(fa::gemm_pv_kernel<128, true>) : launch(fa::gemm_pv_kernel<128, false>);
+}
+
+int fa_selftest_gemm_ts(const void* a, const void* b, float* c, int N, int bf16,
+                        uint32_t* status, void* stream) {
+  if (!a || !b || !c || !status || (N != 64 && N != 128)) return 1;
+  CUtensorMap tb;
+  if (!fa::encode_2d(&tb, b, bf16 != 0, N, 128)) return 3;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  (void)cudaGetLastError();
+  const uint16_t* a16 = static_cast<const uint16_t*>(a);
+  auto launch = [&](auto kern) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, fa::kSmemBytes) !=
+        cudaSuccess)
+      return 3;
+    kern<<<1, 128, fa::kSmemBytes, st>>>(a16, tb, c, status);
+    return cudaGetLastError() == cudaSuccess ? 0 : 3;
+  };
+  if (N == 64) return bf16 ? launch(fa::gemm_ts_kernel<64, true>) : launch(fa::gemm_ts_kernel<64, false>);
+  return bf16 ? launch(fa::gemm_ts_kernel<128, true>) : launch(fa::gemm_ts_kernel<128, false>);
 }
 
 // out[0] = 1 if the wait completed (it must not), 0 if it gave up.

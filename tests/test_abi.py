@@ -32,7 +32,8 @@ def test_library_exports_every_declared_symbol(lib):
 def test_selftest_library_exports():
     _, st = fabuild.build()
     slib = ctypes.CDLL(st)
-    for name in ("fa_selftest_gemm_qk", "fa_selftest_gemm_pv", "fa_selftest_wait_timeout"):
+    for name in ("fa_selftest_gemm_qk", "fa_selftest_gemm_pv", "fa_selftest_gemm_ts",
+                 "fa_selftest_wait_timeout"):
         assert hasattr(slib, name)
 
 

@@ -158,4 +158,4 @@ def test_query_launch_is_persistent():
     import torch
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert info["units"] == 4 * 16 * 16 and info["grid"] == min(sms, info["units"])
-    assert info["threads"] == 320 and info["smem_bytes"] <= 232448
+    assert info["threads"] == 512 and info["smem_bytes"] <= 232448

@@ -22,6 +22,7 @@ def slib():
     vp, i = ctypes.c_void_p, ctypes.c_int
     lib.fa_selftest_gemm_qk.argtypes = [vp, vp, vp, i, i, vp, vp]
     lib.fa_selftest_gemm_pv.argtypes = [vp, vp, vp, i, i, i, vp, vp]
+    lib.fa_selftest_gemm_ts.argtypes = [vp, vp, vp, i, i, vp, vp]
     lib.fa_selftest_wait_timeout.argtypes = [vp, vp, vp]
     return lib
 
@@ -69,6 +70,24 @@ def test_gemm_pv_mn_major_b(slib, N, dtype):
         got = c.cpu().numpy()
         results[variant] = bool(np.allclose(got, ref, rtol=1e-5, atol=1e-4))
     assert results[0], f"MN-major B descriptor mismatch (LBO/SBO swapped variant matches: {results[1]})"
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("N", [64, 128])
+def test_gemm_ts_a_from_tmem(slib, N, dtype):
+    import torch
+    rng = np.random.default_rng(3 * N + (dtype == "bf16"))
+    a = I.to_bits(rng.random((128, 128)), dtype)             # P-like, stored into TMEM
+    b = I.to_bits(rng.standard_normal((128, N)), dtype)      # V-like, [key][d]
+    ref = bits_to_f64(a, dtype) @ bits_to_f64(b, dtype)
+    da, db = to_device(a, dtype), to_device(b, dtype)
+    c = torch.full((128, N), float("nan"), dtype=torch.float32, device="cuda:0")
+    st = _status()
+    rc = slib.fa_selftest_gemm_ts(da.data_ptr(), db.data_ptr(), c.data_ptr(), N,
+                                  int(dtype == "bf16"), st.data_ptr(), None)
+    torch.cuda.synchronize()
+    assert rc == 0 and int(st[0]) == 0
+    np.testing.assert_allclose(c.cpu().numpy(), ref, rtol=1e-5, atol=1e-4)
 
 
 def test_bounded_wait_gives_up_and_reports(slib):
