@@ -47,15 +47,37 @@ struct AbortCtx {
 // Waits for phase `parity` of `bar`. Returns false if the CTA is aborting, or
 // after kWaitLimitNs without progress (then it raises the abort flag and
 // records `code` in the status word).
+// Each try_wait suspends the thread for at most this long (it wakes as soon as
+// the phase completes); between attempts the abort flag and the limit are
+// checked.
+constexpr uint32_t kSleepHintNs = 100000u;
+
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const AbortCtx& ab,
                                              uint32_t code, uint64_t limit_ns = kWaitLimitNs) {
+  if (ptx::mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (;;) {
+    if (ptx::mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+    if (*ab.flag) return false;
+    if (ptx::globaltimer_ns() - t0 > limit_ns) {
+      *ab.flag = 1u;
+      atomicOr(ab.status, code);
+      return false;
+    }
+  }
+}
+
+// Spinning variant for the single-thread roles (TMA producer, MMA issuer):
+// one poller costs little, and a test of a completed phase returns fastest.
+__device__ __forceinline__ bool wait_spin(uint32_t bar, uint32_t parity, const AbortCtx& ab,
+                                          uint32_t code) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
-    if ((it & 15u) == 0u) {
+    if ((it & 63u) == 0u) {
       if (*ab.flag) return false;
-      if (ptx::globaltimer_ns() - t0 > limit_ns) {
+      if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
         *ab.flag = 1u;
         atomicOr(ab.status, code);
         return false;
@@ -69,9 +91,9 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
 __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, const AbortCtx& ab,
                                            uint32_t code) {
   const uint64_t t0 = ptx::globaltimer_ns();
-  for (uint32_t it = 0;; ++it) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if ((it & 15u) == 15u && ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+  for (;;) {
+    if (ptx::mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+    if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
       *ab.flag = 1u;
       atomicOr(ab.status, code);
       return false;

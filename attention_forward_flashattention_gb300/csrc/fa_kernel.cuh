@@ -19,7 +19,7 @@
 // Each warpgroup's four warps cover the four TMEM lane quarters (warp w
 // reaches lanes 32*(w%4)..+31). Registers are rebalanced with setmaxnreg
 // (the register reallocation of "TMA + Warp Specialization", 17.4-17.5):
-// 64 for WG0, 192 for each softmax WG, 64 for the epilogue, which sums to the
+// 72 for WG0, 192 for each softmax WG, 56 for the epilogue, which sums to the
 // 128 x 4 the CTA is launched with.
 //
 // TMEM (512 columns): S0 0-127, S1 128-255, O0 256.., O1 256+D..; P_i is
@@ -60,7 +60,7 @@ struct FwdArgs {
 
 constexpr int kFwdThreads = 512;
 // setmaxnreg split per thread: WG0, each softmax WG, epilogue WG (sum 512 = 4 x 128).
-constexpr uint32_t kRegsWG0 = 64, kRegsSoftmax = 192, kRegsEpilogue = 64;
+constexpr uint32_t kRegsWG0 = 72, kRegsSoftmax = 192, kRegsEpilogue = 56;
 static_assert(kRegsWG0 + 2 * kRegsSoftmax + kRegsEpilogue == 4 * (65536 / kFwdThreads),
               "register split must equal the launch allocation");
 
@@ -146,7 +146,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tm_q, const CUt
   bool ok = true;
   while (ok && next_unit<CAUSAL>(round, a, bh, mblk)) {
     const int nkv = unit_kv_tiles<CAUSAL>(a, mblk);
-    if (!wait_bounded(bar(kBarQEmpty), (units & 1u) ^ 1u, ab, kStatusProducer)) {
+    if (!wait_spin(bar(kBarQEmpty), (units & 1u) ^ 1u, ab, kStatusProducer)) {
       ok = false;
       break;
     }
@@ -160,7 +160,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tm_q, const CUt
     for (int j = 0; j < nkv && ok; ++j) {
       for (int t = 0; t < 2; ++t) {
         const uint32_t s = ring % S, ph = (ring / S) & 1u;
-        if (!wait_bounded(bar(kBarKVFull + S + s), ph ^ 1u, ab, kStatusProducer)) {
+        if (!wait_spin(bar(kBarKVFull + S + s), ph ^ 1u, ab, kStatusProducer)) {
           ok = false;
           break;
         }
@@ -186,18 +186,17 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tm_q, const CUt
   }
 }
 
-// The whole MMA warp runs this loop (waits are warp-wide and every value is
-// warp-uniform); one lane issues the tcgen05 instructions. Descriptors are
-// built once and advanced by constant offsets, so one MMA costs a few
-// instructions to issue, well under the ~64 cycles a 128x128x16 MMA keeps the
-// tensor core busy.
+// One thread issues every tcgen05 instruction. An MMA of 128x128x16 keeps the
+// tensor core busy ~64 cycles while its issue costs ~50, so the loop keeps
+// everything else minimal: descriptors are built once and advanced in place,
+// waits are single-thread try_waits, and each step commits only what a
+// waiter needs.
 template <int D, bool BF16, bool CAUSAL>
 __device__ __forceinline__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t bars,
-                                         uint32_t tmem, const AbortCtx& ab, int lane) {
+                                         uint32_t tmem, const AbortCtx& ab) {
   using L = Layout<D>;
   constexpr int S = L::kStages;
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
-  const bool leader = lane == 0;
   const uint64_t dQ[2] = {desc_kmajor(sbase + L::kOffQ),
                           desc_kmajor(sbase + L::kOffQ + L::kTileBytes)};
   const uint64_t dK0 = desc_kmajor(sbase + L::kOffKV);  // ring slot s: + s * kTileBytes
@@ -206,21 +205,21 @@ __device__ __forceinline__ void mma_role(const FwdArgs& a, uint32_t sbase, uint3
   const uint32_t tO[2] = {tmem + L::kColO, tmem + L::kColO + D};
   auto slot_off = [](uint32_t idx) { return (idx % S) * static_cast<uint32_t>(L::kTileBytes); };
   auto kv_wait = [&](uint32_t idx) {
-    return wait_bounded_warp(bar(kBarKVFull + idx % S), (idx / S) & 1u, ab, kStatusMma);
+    return wait_spin(bar(kBarKVFull + idx % S), (idx / S) & 1u, ab, kStatusMma);
   };
   uint32_t ring = 0, units = 0, pcnt[2] = {0u, 0u};
   int round = 0, bh = 0, mblk = 0;
   bool ok = true;
   while (ok && next_unit<CAUSAL>(round, a, bh, mblk)) {
     const int nkv = unit_kv_tiles<CAUSAL>(a, mblk);
-    ok = wait_bounded_warp(bar(kBarQFull + 0), units & 1u, ab, kStatusMma) &&
-         wait_bounded_warp(bar(kBarQFull + 1), units & 1u, ab, kStatusMma);
+    ok = wait_spin(bar(kBarQFull + 0), units & 1u, ab, kStatusMma) &&
+         wait_spin(bar(kBarQFull + 1), units & 1u, ab, kStatusMma);
     if (!ok) break;
     // S_i(0) = Q_i K_0^T
     const uint32_t k0 = ring++;
     if (!(ok = kv_wait(k0))) break;
     ptx::tc_fence_after();
-    if (leader) {
+    {
       const uint64_t dk = desc_add(dK0, slot_off(k0));
       issue_qk_desc<D, BF16>(tS[0], dQ[0], dk);
       ptx::umma_commit(bar(kBarSFull + 0));
@@ -229,7 +228,10 @@ __device__ __forceinline__ void mma_role(const FwdArgs& a, uint32_t sbase, uint3
       ptx::umma_commit(bar(kBarKVFull + S + k0 % S));
       if (nkv == 1) ptx::umma_commit(bar(kBarQEmpty));
     }
-    __syncwarp();
+    // Slot releases of a step are committed after the next step's first PV is
+    // queued, so the path from "P ready" to the tensor core stays short.
+    uint32_t rel_v = 0, rel_k = 0;
+    bool rel_pending = false;
     for (int j = 0; j < nkv; ++j) {
       const uint32_t vj = ring++;
       if (!(ok = kv_wait(vj))) break;
@@ -239,36 +241,44 @@ __device__ __forceinline__ void mma_role(const FwdArgs& a, uint32_t sbase, uint3
       const uint64_t dk = desc_add(dK0, slot_off(kn));
       for (int i = 0; i < 2; ++i) {
         // O_i += P_i V_j (P_i read from TMEM), then S_i = Q_i K_{j+1}^T
-        if (!(ok = wait_bounded_warp(bar(kBarPFull + i), (pcnt[i]++) & 1u, ab, kStatusMma))) break;
+        if (!(ok = wait_spin(bar(kBarPFull + i), (pcnt[i]++) & 1u, ab, kStatusMma))) break;
         if (j == 0 && units > 0 &&
-            !(ok = wait_bounded_warp(bar(kBarOFree + i), (units - 1) & 1u, ab, kStatusMma)))
+            !(ok = wait_spin(bar(kBarOFree + i), (units - 1) & 1u, ab, kStatusMma)))
           break;
-        if (more && i == 0 && !(ok = kv_wait(kn))) break;
         ptx::tc_fence_after();
-        if (leader) {
-          issue_pv_ts_desc<D, BF16>(tO[i], tS[i], dv, j > 0);
-          if (i == 1) ptx::umma_commit(bar(kBarKVFull + S + vj % S));
-          if (!more) {
-            ptx::umma_commit(bar(kBarOFull + i));
-          } else {
-            issue_qk_desc<D, BF16>(tS[i], dQ[i], dk);
-            ptx::umma_commit(bar(kBarSFull + i));
-            if (i == 1) {
-              ptx::umma_commit(bar(kBarKVFull + S + kn % S));
-              if (j + 2 == nkv) ptx::umma_commit(bar(kBarQEmpty));
-            }
-          }
+        issue_pv_ts_desc<D, BF16>(tO[i], tS[i], dv, j > 0);
+        if (i == 0 && rel_pending) {
+          ptx::umma_commit(bar(kBarKVFull + S + rel_v % S));
+          ptx::umma_commit(bar(kBarKVFull + S + rel_k % S));
+          rel_pending = false;
         }
-        __syncwarp();
+        if (!more) {
+          if (i == 1) ptx::umma_commit(bar(kBarKVFull + S + vj % S));
+          ptx::umma_commit(bar(kBarOFull + i));
+          continue;
+        }
+        if (i == 0 && !(ok = kv_wait(kn))) break;
+        issue_qk_desc<D, BF16>(tS[i], dQ[i], dk);
+        ptx::umma_commit(bar(kBarSFull + i));
+        if (i == 1) {
+          // V_j and K_{j+1} are both consumed once S1(j+1) completes
+          rel_v = vj;
+          rel_k = kn;
+          rel_pending = true;
+          if (j + 2 == nkv) ptx::umma_commit(bar(kBarQEmpty));
+        }
       }
       if (!ok) break;
       if (more) ++ring;
     }
+    if (rel_pending) {  // (only when the unit ended early on an abort)
+      ptx::umma_commit(bar(kBarKVFull + S + rel_v % S));
+      ptx::umma_commit(bar(kBarKVFull + S + rel_k % S));
+    }
     ++units;
   }
-  // Every tcgen05 op this warp issued must finish before TMEM is freed.
-  if (leader) ptx::umma_commit(bar(kBarDrain));
-  __syncwarp();
+  // Every tcgen05 op this thread issued must finish before TMEM is freed.
+  ptx::umma_commit(bar(kBarDrain));
   wait_drain(bar(kBarDrain), 0u, ab, kStatusDrain);
 }
 
@@ -495,7 +505,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (warp == 0) {
       if (lane == 0) producer_role<D, BF16, CAUSAL>(&tm_q, &tm_k, &tm_v, a, sbase, bars, ab);
     } else if (warp == 1) {
-      mma_role<D, BF16, CAUSAL>(a, sbase, bars, tmem, ab, lane);
+      if (lane == 0) mma_role<D, BF16, CAUSAL>(a, sbase, bars, tmem, ab);
     }
   } else if (wgrp < 3) {
     ptx::setmaxnreg_inc<kRegsSoftmax>();

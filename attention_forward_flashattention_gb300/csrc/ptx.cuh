@@ -59,6 +59,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
+// Same test, but a thread whose phase is not complete yet is suspended in
+// hardware until it completes or about `hint_ns` nanoseconds pass, instead of
+// spinning (spinning waiters compete with the threads doing the work).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred P1;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 P1, [%1], %2, %3;\n\t"
+      "selp.b32 %0, 1, 0, P1;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
 // ----------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
