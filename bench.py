@@ -149,6 +149,25 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Largest `value` over all ranks (the slowest rank sets a job's time)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_rank: float, total_ms_max: float, steps: int, world: int) -> float:
+    """Whole-job TFLOPS: every rank processes its own copy of the workload
+    (weak scaling), so the job does world x flops per step in the slowest
+    rank's time."""
+    ms_per_step = total_ms_max / steps
+    return world * flops_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
 def oracle_sample_rows(w, nrows: int, seed: int) -> np.ndarray:
     """Rows of the workload for the CPU oracle: a few heads, rows spread over N."""
     rng = np.random.default_rng(seed)
@@ -278,14 +297,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     if rc != fa.FA_OK:
         raise RuntimeError("timed steps failed: " + fa.status_string(rc))
     times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = sum(times_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(times_ms), world, dev)
     ms_per_step = total_ms / args.steps
-    per_gpu_tflops = w.flops / (ms_per_step * 1e-3) / 1e12
-    value = per_gpu_tflops * world
+    value = job_throughput(w.flops, total_ms, args.steps, world)
+    per_gpu_tflops = value / world
 
     # SM clock from clock64 (one CTA spinning 2e8 cycles right after the load)
     probe = torch.zeros(2, dtype=torch.int64, device=dev)
@@ -316,11 +331,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize(dev)
-        e2e_ms = e0.elapsed_time(e1) / n_e2e
-        if world > 1:
-            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, world, dev)
         elem = w.B * w.H * w.N * w.d
         e2e = {"value": w.flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": 3 * elem * 2,
