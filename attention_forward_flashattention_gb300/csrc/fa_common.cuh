@@ -101,6 +101,31 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, const 
   }
 }
 
+// Cluster-scope variant for barriers that receive arrivals or transaction
+// bytes from the peer CTA of a pair (sleeping, or spinning for the
+// single-thread roles).
+template <bool kSleep>
+__device__ __forceinline__ bool wait_cluster(uint32_t bar, uint32_t parity, const AbortCtx& ab,
+                                             uint32_t code) {
+  auto test = [&] {
+    return kSleep ? ptx::mbar_try_wait_cluster(bar, parity, kSleepHintNs)
+                  : ptx::mbar_test_cluster(bar, parity);
+  };
+  if (test()) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (test()) return true;
+    if (kSleep || (it & 63u) == 0u) {
+      if (*ab.flag) return false;
+      if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+        *ab.flag = 1u;
+        atomicOr(ab.status, code);
+        return false;
+      }
+    }
+  }
+}
+
 // Warp-uniform variant: every lane polls; the warp proceeds only if all
 // lanes saw the phase complete.
 __device__ __forceinline__ bool wait_bounded_warp(uint32_t bar, uint32_t parity,
@@ -227,6 +252,36 @@ template <int D, bool BF16>
 __device__ __forceinline__ void issue_pv_ts(uint32_t d_tmem, uint32_t p_tmem, uint32_t sV,
                                             bool accumulate) {
   issue_pv_ts_desc<D, BF16>(d_tmem, p_tmem, desc_v(sV), accumulate);
+}
+
+// Pair MMAs for head dimension 128 (M = 256: 128 query rows in each CTA).
+// S = Q K^T: each CTA holds its 128 Q rows (two 16 KB panels) and 64 of the
+// 128 keys (two 8 KB panels of 64 rows); the pair's S has all 128 keys.
+template <bool BF16>
+__device__ __forceinline__ void issue_qk_pair(uint32_t d_tmem, uint64_t dq, uint64_t dk) {
+  constexpr uint32_t id = ptx::idesc_f16(BF16, false, 256, 128);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    ptx::umma_f16_ss_pair(d_tmem, dq, dk, id, kk > 0 ? 1u : 0u);
+    const bool next_panel = (kk & 3) == 3;
+    dq = desc_add(dq, next_panel ? static_cast<uint32_t>(kPanelBytes - 96) : 32u);
+    dk = desc_add(dk, next_panel ? static_cast<uint32_t>(kPanelBytes / 2 - 96) : 32u);
+    asm volatile("" : "+l"(dq), "+l"(dk));
+  }
+}
+
+// O += P V: P (each CTA's 128 rows) from TMEM; each CTA holds 64 of the 128
+// columns of V (one 128-key x 64-column panel, MN-major).
+template <bool BF16>
+__device__ __forceinline__ void issue_pv_ts_pair(uint32_t d_tmem, uint32_t p_tmem, uint64_t dv,
+                                                 bool accumulate) {
+  constexpr uint32_t id = ptx::idesc_f16(BF16, true, 256, 128);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    ptx::umma_f16_ts_pair(d_tmem, p_tmem + 8u * kk, dv, id, (accumulate || kk > 0) ? 1u : 0u);
+    dv = desc_add(dv, 2048u);
+    asm volatile("" : "+l"(dv));
+  }
 }
 
 }  // namespace fa

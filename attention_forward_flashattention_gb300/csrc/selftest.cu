@@ -17,6 +17,10 @@
 //   fa_selftest_gemm_ts : as gemm_pv, but A is stored by the threads into TMEM
 //                         with tcgen05.st (packed pairs) and the MMA reads it
 //                         from there (the P-in-TMEM path).
+//   fa_selftest_gemm_qk_pair / _pv_pair : the same two products on a CTA pair
+//                         (cta_group::2, M = 256): each CTA loads half of the
+//                         B operand, the even CTA issues the MMAs, each CTA
+//                         reads back its own 128 rows.
 //   fa_selftest_wait_timeout : a wait on a barrier nothing completes, with a
 //                         short limit; checks that the bounded wait gives up,
 //                         records its status bit and lets the kernel exit.
@@ -48,14 +52,14 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// rows x cols 16-bit row-major matrix, box = 64 columns x 128 rows, SW128.
-bool encode_2d(CUtensorMap* m, const void* ptr, bool bf16, int cols, int rows) {
+// rows x cols 16-bit row-major matrix, box = 64 columns x box_rows rows, SW128.
+bool encode_2d(CUtensorMap* m, const void* ptr, bool bf16, int cols, int rows, int box_rows = 128) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows), 1u};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2u,
                                  static_cast<cuuint64_t>(cols) * rows * 2u};
-  const cuuint32_t box[3] = {64u, 128u, 1u};
+  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
              const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -261,6 +265,138 @@ __global__ void __launch_bounds__(128, 1)
   if (warp == 0) ptx::tmem_dealloc(tmem, 256);
 }
 
+// Pair (cta_group::2) version of gemm_qk for K = 128: C[256][128] = A * B^T.
+// CTA r loads A rows 128r..+128 and B rows (keys) 64r..+64, counting the bytes
+// on the even CTA's barrier; the even CTA issues M = 256 MMAs; each CTA reads
+// back its own 128 rows of C.
+template <bool BF16>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
+    gemm_qk_pair_kernel(const __grid_constant__ CUtensorMap ta,
+                        const __grid_constant__ CUtensorMap tb, float* c, uint32_t* status,
+                        int variant) {
+  extern __shared__ __align__(1024) uint8_t raw[];
+  const Smem s = carve(raw);  // A at +0 (32 KB), B at +32 KB (16 KB)
+  const AbortCtx ab{s.abort_flag, status};
+  const int warp = threadIdx.x >> 5;
+  const uint32_t rank = ptx::cluster_ctarank();
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(s.bars, 1);
+    ptx::mbar_init(s.bars + 8, 1);
+    *s.abort_flag = 0u;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc_pair(ptx::smem_u32(s.tmem_slot), 128);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  ptx::cluster_sync();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *s.tmem_slot;
+  const uint32_t lead_load = ptx::mapa_shared(s.bars, 0);
+  if (threadIdx.x == 0) {
+    if (rank == 0) ptx::mbar_arrive_expect_tx(s.bars, 2 * (2 * kPanelBytes + kPanelBytes));
+    for (int p = 0; p < 2; ++p) {
+      ptx::tma_load_3d_pair(s.base + p * kPanelBytes, &ta, lead_load, 64 * p, 128 * rank, 0);
+      ptx::tma_load_3d_pair(s.base + 2 * kPanelBytes + p * (kPanelBytes / 2), &tb, lead_load,
+                            64 * p, 64 * rank, 0);
+    }
+    if (rank == 0) {
+      const bool ok = wait_cluster<false>(s.bars, 0, ab, kStatusSelftest);
+      if (ok) {
+        ptx::tc_fence_after();
+        issue_qk_pair<BF16>(tmem, desc_kmajor(s.base), desc_kmajor(s.base + 2 * kPanelBytes));
+      }
+      if (variant == 2) {
+        ptx::umma_commit_pair(s.bars + 8, 2);  // the peer, multicast
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                s.bars + 8)
+            : "memory");                       // this CTA
+      } else {
+        ptx::umma_commit_pair(s.bars + 8, 3);
+      }
+    }
+  }
+  __syncwarp();
+  const bool done = wait_cluster<true>(s.bars + 8, 0, ab, kStatusSelftest);
+  const bool all_done = __all_sync(0xffffffffu, done) != 0;
+  if (variant == 1) {  // read back 1 ms later
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (ptx::globaltimer_ns() - t0 < 1000000ull) {
+    }
+  }
+  ptx::tc_fence_after();
+  if (all_done && !*s.abort_flag) read_back(tmem, c + rank * 128 * 128, 128);
+  ptx::tc_fence_before();
+  ptx::cluster_sync();
+  ptx::tc_fence_after();
+  if (warp == 0) ptx::tmem_dealloc_pair(tmem, 128);
+}
+
+// Pair version of the P V product: C[256][128] = P[256][128] * V[128][128] with
+// each CTA storing its 128 rows of P into its TMEM (columns 128..191), loading
+// its 64 columns of V, and signalling "P ready" on the even CTA's barrier.
+template <bool BF16>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
+    gemm_pv_pair_kernel(const uint16_t* a, const __grid_constant__ CUtensorMap tv, float* c,
+                        uint32_t* status) {
+  extern __shared__ __align__(1024) uint8_t raw[];
+  const Smem s = carve(raw);  // V half at +0 (16 KB)
+  const AbortCtx ab{s.abort_flag, status};
+  const int warp = threadIdx.x >> 5;
+  const uint32_t rank = ptx::cluster_ctarank();
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(s.bars, 1);         // V loaded (both halves)
+    ptx::mbar_init(s.bars + 8, 256);   // P stored (both CTAs)
+    ptx::mbar_init(s.bars + 16, 1);    // MMA done
+    *s.abort_flag = 0u;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc_pair(ptx::smem_u32(s.tmem_slot), 256);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  ptx::cluster_sync();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *s.tmem_slot;
+  {
+    const int r = threadIdx.x;
+    uint32_t pk[2][32];
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(a + (128 * rank + r) * 128);
+    for (int i = 0; i < 64; ++i) pk[i >> 5][i & 31] = src[i];
+    const uint32_t t = ptx::tmem_lane_base(tmem, warp) + 128u;
+    ptx::tmem_st32(t, pk[0]);
+    ptx::tmem_st32(t + 32u, pk[1]);
+    ptx::tmem_st_wait();
+    ptx::tc_fence_before();
+    ptx::mbar_arrive_cluster(ptx::mapa_shared(s.bars + 8, 0));
+  }
+  if (threadIdx.x == 0) {
+    if (rank == 0) ptx::mbar_arrive_expect_tx(s.bars, 2 * kPanelBytes);
+    ptx::tma_load_3d_pair(s.base, &tv, ptx::mapa_shared(s.bars, 0), 64 * rank, 0, 0);
+    if (rank == 0) {
+      const bool ok = wait_cluster<false>(s.bars, 0, ab, kStatusSelftest) &&
+                      wait_cluster<false>(s.bars + 8, 0, ab, kStatusSelftest);
+      if (ok) {
+        ptx::tc_fence_after();
+        issue_pv_ts_pair<BF16>(tmem, tmem + 128u, desc_v(s.base), false);
+      }
+      ptx::umma_commit_pair(s.bars + 16, 3);
+    }
+  }
+  __syncwarp();
+  const bool done = wait_cluster<true>(s.bars + 16, 0, ab, kStatusSelftest);
+  const bool all_done = __all_sync(0xffffffffu, done) != 0;
+  ptx::tc_fence_after();
+  if (all_done && !*s.abort_flag) read_back(tmem, c + rank * 128 * 128, 128);
+  ptx::tc_fence_before();
+  ptx::cluster_sync();
+  ptx::tc_fence_after();
+  if (warp == 0) ptx::tmem_dealloc_pair(tmem, 256);
+}
+
 // One warp waits on a barrier that never completes, with a 20 ms limit.
 __global__ void wait_timeout_kernel(uint32_t* status, uint32_t* out) {
   __shared__ __align__(8) uint64_t bar;
@@ -338,6 +474,44 @@ int fa_selftest_gemm_ts(const void* a, const void* b, float* c, int N, int bf16,
   };
   if (N == 64) return bf16 ? launch(fa::gemm_ts_kernel<64, true>) : launch(fa::gemm_ts_kernel<64, false>);
   return bf16 ? launch(fa::gemm_ts_kernel<128, true>) : launch(fa::gemm_ts_kernel<128, false>);
+}
+
+// C[256][128] = A[256][128] * B[128][128]^T on a CTA pair (cta_group::2).
+int fa_selftest_gemm_qk_pair(const void* a, const void* b, float* c, int bf16, int variant,
+                             uint32_t* status, void* stream) {
+  if (!a || !b || !c || !status) return 1;
+  CUtensorMap ta, tb;
+  if (!fa::encode_2d(&ta, a, bf16 != 0, 128, 256) || !fa::encode_2d(&tb, b, bf16 != 0, 128, 128, 64))
+    return 3;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  (void)cudaGetLastError();
+  auto launch = [&](auto kern) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, fa::kSmemBytes) !=
+        cudaSuccess)
+      return 3;
+    kern<<<2, 128, fa::kSmemBytes, st>>>(ta, tb, c, status, variant);
+    return cudaGetLastError() == cudaSuccess ? 0 : 3;
+  };
+  return bf16 ? launch(fa::gemm_qk_pair_kernel<true>) : launch(fa::gemm_qk_pair_kernel<false>);
+}
+
+// C[256][128] = P[256][128] * V[128][128] on a CTA pair, P from TMEM.
+int fa_selftest_gemm_pv_pair(const void* p, const void* v, float* c, int bf16, uint32_t* status,
+                             void* stream) {
+  if (!p || !v || !c || !status) return 1;
+  CUtensorMap tv;
+  if (!fa::encode_2d(&tv, v, bf16 != 0, 128, 128)) return 3;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  (void)cudaGetLastError();
+  const uint16_t* p16 = static_cast<const uint16_t*>(p);
+  auto launch = [&](auto kern) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, fa::kSmemBytes) !=
+        cudaSuccess)
+      return 3;
+    kern<<<2, 128, fa::kSmemBytes, st>>>(p16, tv, c, status);
+    return cudaGetLastError() == cudaSuccess ? 0 : 3;
+  };
+  return bf16 ? launch(fa::gemm_pv_pair_kernel<true>) : launch(fa::gemm_pv_pair_kernel<false>);
 }
 
 // out[0] = 1 if the wait completed (it must not), 0 if it gave up.

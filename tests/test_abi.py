@@ -33,7 +33,7 @@ def test_selftest_library_exports():
     _, st = fabuild.build()
     slib = ctypes.CDLL(st)
     for name in ("fa_selftest_gemm_qk", "fa_selftest_gemm_pv", "fa_selftest_gemm_ts",
-                 "fa_selftest_wait_timeout"):
+                 "fa_selftest_gemm_qk_pair", "fa_selftest_gemm_pv_pair", "fa_selftest_wait_timeout"):
         assert hasattr(slib, name)
 
 

@@ -23,6 +23,8 @@ def slib():
     lib.fa_selftest_gemm_qk.argtypes = [vp, vp, vp, i, i, vp, vp]
     lib.fa_selftest_gemm_pv.argtypes = [vp, vp, vp, i, i, i, vp, vp]
     lib.fa_selftest_gemm_ts.argtypes = [vp, vp, vp, i, i, vp, vp]
+    lib.fa_selftest_gemm_qk_pair.argtypes = [vp, vp, vp, i, i, vp, vp]
+    lib.fa_selftest_gemm_pv_pair.argtypes = [vp, vp, vp, i, vp, vp]
     lib.fa_selftest_wait_timeout.argtypes = [vp, vp, vp]
     return lib
 
@@ -87,6 +89,40 @@ def test_gemm_ts_a_from_tmem(slib, N, dtype):
                                   int(dtype == "bf16"), st.data_ptr(), None)
     torch.cuda.synchronize()
     assert rc == 0 and int(st[0]) == 0
+    np.testing.assert_allclose(c.cpu().numpy(), ref, rtol=1e-5, atol=1e-4)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_gemm_qk_on_cta_pair(slib, dtype):
+    import torch
+    rng = np.random.default_rng(11 + (dtype == "bf16"))
+    a = I.to_bits(rng.standard_normal((256, 128)), dtype)   # Q-like, 128 rows per CTA
+    b = I.to_bits(rng.standard_normal((128, 128)), dtype)   # K-like, 64 keys per CTA
+    c = torch.full((256, 128), float("nan"), dtype=torch.float32, device="cuda:0")
+    st = _status()
+    da, db = to_device(a, dtype), to_device(b, dtype)   # keep both alive across the launch
+    rc = slib.fa_selftest_gemm_qk_pair(da.data_ptr(), db.data_ptr(), c.data_ptr(),
+                                       int(dtype == "bf16"), 0, st.data_ptr(), None)
+    torch.cuda.synchronize()
+    assert rc == 0 and int(st[0]) == 0
+    ref = bits_to_f64(a, dtype) @ bits_to_f64(b, dtype).T
+    np.testing.assert_allclose(c.cpu().numpy(), ref, rtol=1e-5, atol=1e-4)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_gemm_pv_on_cta_pair(slib, dtype):
+    import torch
+    rng = np.random.default_rng(21 + (dtype == "bf16"))
+    p = I.to_bits(rng.random((256, 128)), dtype)              # P-like, from TMEM
+    v = I.to_bits(rng.standard_normal((128, 128)), dtype)     # V-like, 64 columns per CTA
+    c = torch.full((256, 128), float("nan"), dtype=torch.float32, device="cuda:0")
+    st = _status()
+    dp, dv = to_device(p, dtype), to_device(v, dtype)   # keep both alive across the launch
+    rc = slib.fa_selftest_gemm_pv_pair(dp.data_ptr(), dv.data_ptr(), c.data_ptr(),
+                                       int(dtype == "bf16"), st.data_ptr(), None)
+    torch.cuda.synchronize()
+    assert rc == 0 and int(st[0]) == 0
+    ref = bits_to_f64(p, dtype) @ bits_to_f64(v, dtype)
     np.testing.assert_allclose(c.cpu().numpy(), ref, rtol=1e-5, atol=1e-4)
 
 
