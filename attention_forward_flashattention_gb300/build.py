@@ -24,7 +24,7 @@ LIB_NAME = "libfa_sm103.so"
 SELFTEST_NAME = "libfa_selftest.so"
 LIB_UNITS = ["fa_host.cu", "fa_fwd_d64.cu", "fa_fwd_d128.cu", "fa_noalloc.cu"]
 SELFTEST_UNITS = ["selftest.cu"]
-HEADERS = ["ptx.cuh", "fa_common.cuh", "fa_kernel.cuh"]
+HEADERS = ["ptx.cuh", "fa_common.cuh", "fa_kernel.cuh", "fa_launch.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

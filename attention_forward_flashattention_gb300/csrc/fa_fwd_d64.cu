@@ -1,29 +1,16 @@
 // Instances of the attention forward kernel for head dimension 64
 // (fp16 / bf16, full / causal) and their launch.
-#include "fa_kernel.cuh"
+#include "fa_launch.cuh"
 
 namespace fa {
-namespace {
 
-template <bool BF16, bool CAUSAL>
-cudaError_t launch_one(const CUtensorMap* m, const FwdArgs& a, int grid, cudaStream_t st) {
-  constexpr int kSmem = Layout<64>::kSmemBytes;
-  auto kern = fa_fwd_kernel<64, BF16, CAUSAL>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-  if (e != cudaSuccess) return e;
-  kern<<<grid, kFwdThreads, kSmem, st>>>(m[0], m[1], m[2], a);
-  return cudaGetLastError();
+int fwd_grid_d64(int n_units, int sm_count) {
+  return launch_detail::fwd_grid(n_units, sm_count);
 }
-
-}  // namespace
 
 cudaError_t launch_fwd_d64(bool bf16, bool causal, const CUtensorMap* maps, const FwdArgs& a,
                            int grid, cudaStream_t stream) {
-  if (bf16)
-    return causal ? launch_one<true, true>(maps, a, grid, stream)
-                  : launch_one<true, false>(maps, a, grid, stream);
-  return causal ? launch_one<false, true>(maps, a, grid, stream)
-                : launch_one<false, false>(maps, a, grid, stream);
+  return launch_detail::launch_fwd<64>(bf16, causal, maps, a, grid, stream);
 }
 
 }  // namespace fa

@@ -83,16 +83,17 @@ fa_status current_device(int* dev_out, DeviceState** st_out, bool need_status) {
 }
 
 // [BH][N][d] 16-bit tensor as a 3-D map {d, N, BH}; box = one 64-element x
-// 128-row panel, 128-byte swizzle. Rows past N read as zero and are not
+// box_rows panel, 128-byte swizzle. Rows past N read as zero and are not
 // written by stores.
-bool encode_qkvo(CUtensorMap* m, const void* ptr, bool bf16, int d, int N, long long BH) {
+bool encode_qkvo(CUtensorMap* m, const void* ptr, bool bf16, int d, int N, long long BH,
+                 int box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                               static_cast<cuuint64_t>(BH)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2u,
                                  static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2u};
-  const cuuint32_t box[3] = {64u, 128u, 1u};
+  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
              const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -128,7 +129,32 @@ __global__ void clock_probe_kernel(uint64_t* out, long long cycles) {
 
 }  // namespace
 
-int fwd_smem_bytes(int d) { return d == 64 ? Layout<64>::kSmemBytes : Layout<128>::kSmemBytes; }
+int fwd_smem_bytes(int d) {
+  return d == 64 ? Layout<64>::kSmemBytes : Layout<128>::kSmemBytes;
+}
+
+bool encode_fwd_maps(CUtensorMap* maps, const void* q, const void* k, const void* v, bool bf16,
+                     int d, int N, long long BH) {
+  return encode_qkvo(&maps[0], q, bf16, d, N, BH, 128) &&
+         encode_qkvo(&maps[1], k, bf16, d, N, BH, fwd_k_box_rows(d)) &&
+         encode_qkvo(&maps[2], v, bf16, d, N, BH, 128);
+}
+
+void plan_fwd(int d, int N, long long BH, int sm_count, FwdArgs* a, int* grid) {
+  const int rows = fwd_unit_rows(d);
+  a->N = N;
+  a->BH = static_cast<int>(BH);
+  a->n_mblk = (N + rows - 1) / rows;
+  a->n_units = static_cast<int>(BH * a->n_mblk);
+  a->n_kv = (N + 127) / 128;
+  *grid = d == 64 ? fwd_grid_d64(a->n_units, sm_count) : fwd_grid_d128(a->n_units, sm_count);
+}
+
+cudaError_t launch_fwd(int d, bool bf16, bool causal, const CUtensorMap* maps, const FwdArgs& a,
+                       int grid, cudaStream_t stream) {
+  return d == 64 ? launch_fwd_d64(bf16, causal, maps, a, grid, stream)
+                 : launch_fwd_d128(bf16, causal, maps, a, grid, stream);
+}
 
 }  // namespace fa
 
@@ -153,26 +179,19 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   const bool bf16 = dtype == FA_DTYPE_BF16;
   const long long BH = static_cast<long long>(B) * H;
   CUtensorMap maps[3];
-  if (!fa::encode_qkvo(&maps[0], q, bf16, d, N, BH) || !fa::encode_qkvo(&maps[1], k, bf16, d, N, BH) ||
-      !fa::encode_qkvo(&maps[2], v, bf16, d, N, BH))
-    return FA_ERR_CUDA;
+  if (!fa::encode_fwd_maps(maps, q, k, v, bf16, d, N, BH)) return FA_ERR_CUDA;
 
   fa::FwdArgs a{};
   a.o = o;
   a.lse = lse;
   a.status = st->status;
-  a.N = N;
-  a.BH = static_cast<int>(BH);
-  a.n_mblk = (N + 255) / 256;
-  a.n_units = static_cast<int>(BH * a.n_mblk);
-  a.n_kv = (N + 127) / 128;
   a.scale_log2 = scale * 1.4426950408889634f;
-  const int grid = a.n_units < st->sm_count ? a.n_units : st->sm_count;
+  int grid = 0;
+  fa::plan_fwd(d, N, BH, st->sm_count, &a, &grid);
 
   (void)cudaGetLastError();  // do not report an earlier, unrelated error as ours
-  const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const cudaError_t e = (d == 64) ? fa::launch_fwd_d64(bf16, causal != 0, maps, a, grid, s)
-                                  : fa::launch_fwd_d128(bf16, causal != 0, maps, a, grid, s);
+  const cudaError_t e =
+      fa::launch_fwd(d, bf16, causal != 0, maps, a, grid, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -200,11 +219,13 @@ fa_status fa_query_launch(int B, int H, int N, int d, int causal, int* grid, int
   fa::DeviceState* st = nullptr;
   const fa_status ds = fa::current_device(&dev, &st, false);
   if (ds != FA_OK) return ds;
-  const long long n_units = static_cast<long long>(B) * H * ((N + 255) / 256);
-  if (grid) *grid = static_cast<int>(n_units < st->sm_count ? n_units : st->sm_count);
+  fa::FwdArgs a{};
+  int g = 0;
+  fa::plan_fwd(d, N, static_cast<long long>(B) * H, st->sm_count, &a, &g);
+  if (grid) *grid = g;
   if (threads) *threads = fa::kFwdThreads;
   if (smem_bytes) *smem_bytes = fa::fwd_smem_bytes(d);
-  if (units) *units = static_cast<int>(n_units);
+  if (units) *units = a.n_units;
   return FA_OK;
 }
 

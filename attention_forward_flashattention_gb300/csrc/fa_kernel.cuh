@@ -71,8 +71,8 @@ struct Layout {
   static constexpr int kStages = (D == 128) ? 4 : 8;        // K / V ring slots
   static constexpr int kOffQ = 0;                           // Q0, Q1
   static constexpr int kOffKV = 2 * kTileBytes;             // ring
-  static constexpr int kOffStats = kOffKV + kStages * kTileBytes;  // [2 units][2 tiles][128] l
-  static constexpr int kOffBar = kOffStats + 2 * 2 * 128 * 4;
+  static constexpr int kOffStats = kOffKV + kStages * kTileBytes;  // [2 tiles][128] row sums l
+  static constexpr int kOffBar = kOffStats + 2 * 128 * 4;
   static constexpr int kSmemBytes = kOffBar + 512 + 1024;  // barriers + alignment slack
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0;    // S_i (and P_i) at columns i*128
@@ -90,7 +90,8 @@ enum BarSlot : int {
   kBarOFree = 9,      // [2] 128 epilogue threads: O_i read, may be overwritten
   kBarStatsFull = 11, // [2] 128 softmax threads: row sums l of tile i in smem
   kBarDrain = 13,     // MMA: every tcgen05 op of the CTA completed
-  kBarKVFull = 14,    // [stages] TMA: ring slot loaded; then [stages] ring slot free
+  kBarStatsFree = 14, // [2] 128 epilogue threads: row sums of tile i read
+  kBarKVFull = 16,    // [stages] TMA: ring slot loaded; then [stages] ring slot free
 };
 constexpr int kSlotTmem = 480;   // byte offset of the TMEM base address
 constexpr int kSlotAbort = 484;  // byte offset of the abort flag
@@ -400,7 +401,14 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t bars, ui
     if (!ok) break;
     if (grow < a.N)
       a.lse[static_cast<size_t>(bh) * a.N + grow] = (m_ref + log2f(l_exp)) * 0.69314718055994531f;
-    stats[(units & 1u) * 256u + wg * 128 + r] = l;
+    // One slot per row, and at most one unit ahead of the epilogue: the
+    // previous unit's sum must have been read (with a single KV tile per unit
+    // this role could otherwise finish two units before the epilogue reads
+    // the first, and the epilogue's parity wait would miss a phase).
+    if (units > 0 &&
+        !(ok = wait_bounded_warp(bar(kBarStatsFree + wg), (units - 1) & 1u, ab, kStatusSoftmax)))
+      break;
+    stats[wg * 128 + r] = l;
     ptx::mbar_arrive(bar(kBarStatsFull + wg));
     ++units;
   }
@@ -424,7 +432,8 @@ __device__ __forceinline__ void epilogue_role(const FwdArgs& a, uint32_t bars, u
            wait_bounded_warp(bar(kBarStatsFull + i), units & 1u, ab, kStatusEpilogue);
       if (!ok) break;
       ptx::tc_fence_after();
-      const float inv_l = 1.f / stats[(units & 1u) * 256u + i * 128 + r];
+      const float inv_l = 1.f / stats[i * 128 + r];
+      ptx::mbar_arrive(bar(kBarStatsFree + i));
       const float2 il2 = make_float2(inv_l, inv_l);
       const int grow = mblk * 256 + 128 * i + r;
       uint4* orow = reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * a.N + grow) * D);
@@ -480,6 +489,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       ptx::mbar_init(bar(kBarOFull + i), 1);
       ptx::mbar_init(bar(kBarOFree + i), 128);
       ptx::mbar_init(bar(kBarStatsFull + i), 128);
+      ptx::mbar_init(bar(kBarStatsFree + i), 128);
     }
     ptx::mbar_init(bar(kBarQEmpty), 1);
     ptx::mbar_init(bar(kBarDrain), 1);
@@ -521,12 +531,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (warp == 1) ptx::tmem_dealloc(tmem, L::kTmemCols);
 }
 
-// Host-side launch of one instance (defined in the per-head-dim files).
+// Host side (defined in the per-head-dimension files and fa_host.cu).
+// Rows of Q per unit, and of K per TMA box.
+constexpr int fwd_unit_rows(int) { return 256; }
+constexpr int fwd_k_box_rows(int) { return 128; }
+// Persistent grid for n_units units on the current device.
+int fwd_grid_d64(int n_units, int sm_count);
+int fwd_grid_d128(int n_units, int sm_count);
 // maps: Q, K, V tensor maps.
 cudaError_t launch_fwd_d64(bool bf16, bool causal, const CUtensorMap* maps, const FwdArgs& a,
                            int grid, cudaStream_t stream);
 cudaError_t launch_fwd_d128(bool bf16, bool causal, const CUtensorMap* maps, const FwdArgs& a,
                             int grid, cudaStream_t stream);
 int fwd_smem_bytes(int d);
+// Q, K, V tensor maps of a call (fa_host.cu).
+bool encode_fwd_maps(CUtensorMap* maps, const void* q, const void* k, const void* v, bool bf16,
+                     int d, int N, long long BH);
+// Unit counts of a call into `a` (N, BH, n_mblk, n_units, n_kv) and its grid.
+void plan_fwd(int d, int N, long long BH, int sm_count, FwdArgs* a, int* grid);
+cudaError_t launch_fwd(int d, bool bf16, bool causal, const CUtensorMap* maps, const FwdArgs& a,
+                       int grid, cudaStream_t stream);
 
 }  // namespace fa

@@ -38,41 +38,6 @@ struct NoAllocDevice {
 std::mutex g_mu;
 NoAllocDevice g_dev[kMaxDevices];
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static std::once_flag once;
-  static EncodeTiledFn fn = nullptr;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
-
-// Same tensor-map layout as fa_fwd: {d, N, B*H}, 64 x 128 x 1 boxes, SW128.
-bool encode(CUtensorMap* m, const void* ptr, bool bf16, int d, int N, long long BH) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
-                              static_cast<cuuint64_t>(BH)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2u,
-                                 static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2u};
-  const cuuint32_t box[3] = {64u, 128u, 1u};
-  const cuuint32_t estr[3] = {1u, 1u, 1u};
-  return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
-             const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // Per-device set-up, done by the first call on each device with that device
 // current: architecture check and the device address of the scratch array
 // (the array's name is only a host-side stand-in in host code).
@@ -127,22 +92,16 @@ extern "C" fa_status fa_fwd_noalloc(const void* q, const void* k, const void* v,
   if (ds != FA_OK) return ds;
 
   const bool bf16 = dtype == FA_DTYPE_BF16;
-  CUtensorMap maps[3];
-  if (!encode(&maps[0], q, bf16, d, N, BH) || !encode(&maps[1], k, bf16, d, N, BH) ||
-      !encode(&maps[2], v, bf16, d, N, BH))
-    return FA_ERR_CUDA;
+  CUtensorMap maps[3];  // same tensor maps, unit plan and kernels as fa_fwd
+  if (!fa::encode_fwd_maps(maps, q, k, v, bf16, d, N, BH)) return FA_ERR_CUDA;
 
   fa::FwdArgs a{};
   a.o = o;
   a.lse = lse;
   a.status = st->scratch;
-  a.N = N;
-  a.BH = static_cast<int>(BH);
-  a.n_mblk = (N + 255) / 256;
-  a.n_units = static_cast<int>(units);
-  a.n_kv = (N + 127) / 128;
   a.scale_log2 = scale * 1.4426950408889634f;
-  const int grid = a.n_units < st->sm_count ? a.n_units : st->sm_count;
+  int grid = 0;
+  fa::plan_fwd(d, N, BH, st->sm_count, &a, &grid);
 
   (void)cudaGetLastError();
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -150,7 +109,6 @@ extern "C" fa_status fa_fwd_noalloc(const void* q, const void* k, const void* v,
   // at zero for this launch.
   if (cudaMemsetAsync(st->scratch, 0, kStatusWordsPerLaunch * sizeof(uint32_t), s) != cudaSuccess)
     return FA_ERR_CUDA;
-  const cudaError_t e = (d == 64) ? fa::launch_fwd_d64(bf16, causal != 0, maps, a, grid, s)
-                                  : fa::launch_fwd_d128(bf16, causal != 0, maps, a, grid, s);
+  const cudaError_t e = fa::launch_fwd(d, bf16, causal != 0, maps, a, grid, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

@@ -111,8 +111,8 @@ fa_status fa_check(void* stream);
 /*
  * fa_query_launch - launch shape fa_fwd would use on the current device for
  * these sizes: grid (persistent CTAs), threads per CTA, dynamic shared memory
- * bytes, and the number of 256-row work units. Any output pointer may be
- * NULL. Host memory only; enqueues nothing.
+ * bytes per CTA, and the number of 256-row work units. Any output pointer may
+ * be NULL. Host memory only; enqueues nothing.
  */
 fa_status fa_query_launch(int B, int H, int N, int d, int causal, int* grid, int* threads,
                           int* smem_bytes, int* units);

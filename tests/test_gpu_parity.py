@@ -54,6 +54,15 @@ SMALL = [
     (1, 1, 384, 128, "fp16", True),
     (1, 1, 640, 64, "bf16", False),
     (2, 2, 520, 128, "fp16", True),
+    # second Q tile of a unit past N, several units per CTA, ragged tails
+    (1, 1, 300, 128, "fp16", False),
+    (1, 3, 1100, 128, "bf16", True),
+    (1, 96, 700, 128, "bf16", True),
+    (2, 40, 513, 128, "fp16", False),
+    # one KV tile per unit and more units than CTAs: a CTA's softmax and
+    # epilogue hand row sums over unit after unit
+    (1, 400, 100, 64, "fp16", False),
+    (2, 200, 128, 128, "bf16", True),
 ]
 
 
@@ -154,8 +163,10 @@ def test_rejects_unsupported_head_dim_on_gpu():
 
 
 def test_query_launch_is_persistent():
-    info = fa.fa_query_launch(4, 16, 4096, 128)
     import torch
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert info["units"] == 4 * 16 * 16 and info["grid"] == min(sms, info["units"])
-    assert info["threads"] == 512 and info["smem_bytes"] <= 232448
+    for (B, H, N, d) in ((4, 16, 4096, 128), (2, 32, 8192, 64), (1, 1, 300, 128)):
+        info = fa.fa_query_launch(B, H, N, d)
+        assert info["units"] == B * H * ((N + 255) // 256)
+        assert info["grid"] == min(sms, info["units"])
+        assert info["threads"] == 512 and info["smem_bytes"] <= 232448
