@@ -35,6 +35,11 @@ _lock = threading.Lock()
 _lib = None
 
 
+class FaStrides(ctypes.Structure):
+    """fa_strides: element strides of a [B][H][N][d] view (d stride 1)."""
+    _fields_ = [("b", ctypes.c_longlong), ("h", ctypes.c_longlong), ("n", ctypes.c_longlong)]
+
+
 class FaError(RuntimeError):
     def __init__(self, status: int, what: str):
         super().__init__(f"{what}: {status_string(status)} ({status})")
@@ -61,6 +66,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
         lib.fa_fwd.restype = i
+        if hasattr(lib, "fa_fwd_strided"):
+            lib.fa_fwd_strided.argtypes = [vp, vp, vp, vp, vp, i, i, i, i,
+                                           ctypes.POINTER(FaStrides), i, f, i, vp]
+            lib.fa_fwd_strided.restype = i
         lib.fa_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
         lib.fa_fwd_noalloc.restype = i
         lib.fa_check.argtypes = [vp]
@@ -90,6 +99,17 @@ def fa_fwd(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, d: 
     """Same arguments as the C function (device pointers as ints); returns the status."""
     return load_library().fa_fwd(q, k, v, o, lse, B, H, N, d, int(bool(causal)), float(scale),
                                  int(dtype), stream)
+
+
+def fa_fwd_strided(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, d: int,
+                   strides, causal: bool, scale: float, dtype: int, stream: int = 0) -> int:
+    """fa_fwd on strided [B][H][N][d] views; strides: 4 (b, h, n) element-stride
+    triples for q, k, v, o (None passes a null pointer). Returns the status."""
+    arr = None
+    if strides is not None:
+        arr = (FaStrides * 4)(*[FaStrides(*map(int, s)) for s in strides])
+    return load_library().fa_fwd_strided(q, k, v, o, lse, B, H, N, d, arr, int(bool(causal)),
+                                         float(scale), int(dtype), stream)
 
 
 def fa_fwd_noalloc(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, d: int,
@@ -140,19 +160,30 @@ def _stream_handle(stream) -> int:
 
 def attention_forward_into(q, k, v, o, lse, causal: bool = False, scale: float | None = None,
                            stream=None) -> None:
-    """Enqueues fa_fwd on torch tensors (contiguous [B, H, N, d] on one GPU)."""
+    """Enqueues the forward on torch tensors: q, k, v, o are [B, H, N, d] CUDA
+    views with unit stride along d (any other strides that are multiples of 8
+    elements, e.g. a [B, N, H, d] tensor passed as .transpose(1, 2)); lse is a
+    contiguous [B, H, N] float32 tensor."""
     B, H, N, d = q.shape
     for t in (q, k, v, o):
-        if tuple(t.shape) != (B, H, N, d) or not t.is_contiguous() or not t.is_cuda:
-            raise ValueError("q, k, v, o must be contiguous [B, H, N, d] CUDA tensors")
+        if tuple(t.shape) != (B, H, N, d) or t.stride(-1) != 1 or not t.is_cuda:
+            raise ValueError("q, k, v, o must be [B, H, N, d] CUDA tensors with unit d stride")
     if tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous [B, H, N] float32 CUDA tensor")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    rc = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                B, H, N, d, causal, scale, _dtype_code(q), _stream_handle(stream))
+    if all(t.is_contiguous() for t in (q, k, v, o)):
+        rc = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                    B, H, N, d, causal, scale, _dtype_code(q), _stream_handle(stream))
+        what = "fa_fwd"
+    else:
+        strides = [t.stride()[:3] for t in (q, k, v, o)]
+        rc = fa_fwd_strided(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                            lse.data_ptr(), B, H, N, d, strides, causal, scale, _dtype_code(q),
+                            _stream_handle(stream))
+        what = "fa_fwd_strided"
     if rc != FA_OK:
-        raise FaError(rc, "fa_fwd")
+        raise FaError(rc, what)
 
 
 def attention_forward(q, k, v, causal: bool = False, scale: float | None = None, stream=None):

@@ -82,20 +82,21 @@ fa_status current_device(int* dev_out, DeviceState** st_out, bool need_status) {
   return FA_OK;
 }
 
-// [BH][N][d] 16-bit tensor as a 3-D map {d, N, BH}; box = one 64-element x
-// box_rows panel, 128-byte swizzle. Rows past N read as zero and are not
-// written by stores.
-bool encode_qkvo(CUtensorMap* m, const void* ptr, bool bf16, int d, int N, long long BH,
-                 int box_rows) {
+// One [B][H][N][d] 16-bit tensor with element strides `st` (d stride 1) as a
+// 4-D map {d, N, H, B}; box = one 64-element x box_rows panel of one (b, h),
+// 128-byte swizzle. Rows past N read as zero.
+bool encode_qkv(CUtensorMap* m, const void* ptr, const fa_strides& st, bool bf16, int B, int H,
+                int N, int d, int box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
-                              static_cast<cuuint64_t>(BH)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2u,
-                                 static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2u};
-  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
-  const cuuint32_t estr[3] = {1u, 1u, 1u};
-  return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.n) * 2u,
+                                 static_cast<cuuint64_t>(st.h) * 2u,
+                                 static_cast<cuuint64_t>(st.b) * 2u};
+  const cuuint32_t box[4] = {64u, static_cast<cuuint32_t>(box_rows), 1u, 1u};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
              const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -133,16 +134,39 @@ int fwd_smem_bytes(int d) {
   return d == 64 ? Layout<64>::kSmemBytes : Layout<128>::kSmemBytes;
 }
 
-bool encode_fwd_maps(CUtensorMap* maps, const void* q, const void* k, const void* v, bool bf16,
-                     int d, int N, long long BH) {
-  return encode_qkvo(&maps[0], q, bf16, d, N, BH, 128) &&
-         encode_qkvo(&maps[1], k, bf16, d, N, BH, fwd_k_box_rows(d)) &&
-         encode_qkvo(&maps[2], v, bf16, d, N, BH, 128);
+fa_strides contiguous_strides(int H, int N, int d) {
+  fa_strides s;
+  s.n = d;
+  s.h = static_cast<long long>(N) * d;
+  s.b = s.h * H;
+  return s;
 }
 
-void plan_fwd(int d, int N, long long BH, int sm_count, FwdArgs* a, int* grid) {
+fa_status check_strides(const fa_strides* s, int d) {
+  // Multiples of 8 elements (16 bytes: TMA rows and 16-byte output stores),
+  // rows at least d apart; byte strides inside the tensor-map range.
+  for (int t = 0; t < 4; ++t) {
+    for (const long long v : {s[t].b, s[t].h, s[t].n})
+      if (v <= 0 || (v & 7) != 0) return FA_ERR_INVALID_ARG;
+    if (s[t].n < d) return FA_ERR_INVALID_ARG;
+  }
+  for (int t = 0; t < 4; ++t)
+    for (const long long v : {s[t].b, s[t].h, s[t].n})
+      if (v >= (1LL << 38)) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+bool encode_fwd_maps(CUtensorMap* maps, const void* q, const void* k, const void* v,
+                     const fa_strides* s, bool bf16, int B, int H, int N, int d) {
+  return encode_qkv(&maps[0], q, s[0], bf16, B, H, N, d, 128) &&
+         encode_qkv(&maps[1], k, s[1], bf16, B, H, N, d, fwd_k_box_rows(d)) &&
+         encode_qkv(&maps[2], v, s[2], bf16, B, H, N, d, 128);
+}
+
+void plan_fwd(int d, int N, int H, long long BH, int sm_count, FwdArgs* a, int* grid) {
   const int rows = fwd_unit_rows(d);
   a->N = N;
+  a->H = H;
   a->BH = static_cast<int>(BH);
   a->n_mblk = (N + rows - 1) / rows;
   a->n_units = static_cast<int>(BH * a->n_mblk);
@@ -160,9 +184,13 @@ cudaError_t launch_fwd(int d, bool bf16, bool causal, const CUtensorMap* maps, c
 
 extern "C" {
 
-fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                 int N, int d, int causal, float scale, fa_dtype dtype, void* stream) {
-  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+namespace {
+
+// fa_fwd and fa_fwd_strided: checks, tensor maps, plan, launch.
+fa_status fwd_call(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                   int N, int d, const fa_strides* s, int causal, float scale, fa_dtype dtype,
+                   void* stream) {
+  if (!q || !k || !v || !o || !lse || !s) return FA_ERR_INVALID_ARG;
   if (!fa::aligned16(q) || !fa::aligned16(k) || !fa::aligned16(v) || !fa::aligned16(o) ||
       !fa::aligned16(lse))
     return FA_ERR_INVALID_ARG;
@@ -170,6 +198,8 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
   const fa_status sz = fa::check_sizes(B, H, N, d);
   if (sz != FA_OK) return sz;
+  const fa_status ss = fa::check_strides(s, d);
+  if (ss != FA_OK) return ss;
 
   int dev = 0;
   fa::DeviceState* st = nullptr;
@@ -179,20 +209,40 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   const bool bf16 = dtype == FA_DTYPE_BF16;
   const long long BH = static_cast<long long>(B) * H;
   CUtensorMap maps[3];
-  if (!fa::encode_fwd_maps(maps, q, k, v, bf16, d, N, BH)) return FA_ERR_CUDA;
+  if (!fa::encode_fwd_maps(maps, q, k, v, s, bf16, B, H, N, d)) return FA_ERR_CUDA;
 
   fa::FwdArgs a{};
   a.o = o;
+  a.o_sb = s[3].b;
+  a.o_sh = s[3].h;
+  a.o_sn = s[3].n;
   a.lse = lse;
   a.status = st->status;
   a.scale_log2 = scale * 1.4426950408889634f;
   int grid = 0;
-  fa::plan_fwd(d, N, BH, st->sm_count, &a, &grid);
+  fa::plan_fwd(d, N, H, BH, st->sm_count, &a, &grid);
 
   (void)cudaGetLastError();  // do not report an earlier, unrelated error as ours
   const cudaError_t e =
       fa::launch_fwd(d, bf16, causal != 0, maps, a, grid, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, int d, int causal, float scale, fa_dtype dtype, void* stream) {
+  if (B <= 0 || H <= 0 || N <= 0) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const fa_strides c = fa::contiguous_strides(H, N, d);
+  const fa_strides s[4] = {c, c, c, c};
+  return fwd_call(q, k, v, o, lse, B, H, N, d, s, causal, scale, dtype, stream);
+}
+
+fa_status fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                         int H, int N, int d, const fa_strides* strides, int causal, float scale,
+                         fa_dtype dtype, void* stream) {
+  return fwd_call(q, k, v, o, lse, B, H, N, d, strides, causal, scale, dtype, stream);
 }
 
 fa_status fa_check(void* stream) {
@@ -221,7 +271,7 @@ fa_status fa_query_launch(int B, int H, int N, int d, int causal, int* grid, int
   if (ds != FA_OK) return ds;
   fa::FwdArgs a{};
   int g = 0;
-  fa::plan_fwd(d, N, static_cast<long long>(B) * H, st->sm_count, &a, &g);
+  fa::plan_fwd(d, N, H, static_cast<long long>(B) * H, st->sm_count, &a, &g);
   if (grid) *grid = g;
   if (threads) *threads = fa::kFwdThreads;
   if (smem_bytes) *smem_bytes = fa::fwd_smem_bytes(d);

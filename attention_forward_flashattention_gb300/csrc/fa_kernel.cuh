@@ -42,15 +42,18 @@
 
 #include <cuda.h>
 
+#include "fa.h"
 #include "fa_common.cuh"
 
 namespace fa {
 
 struct FwdArgs {
-  void* o;           // [BH][N][D] 16-bit output
+  void* o;           // 16-bit output: row (b, h, n) at o + b*o_sb + h*o_sh + n*o_sn elements
   float* lse;        // [BH][N] fp32, natural-log logsumexp
   uint32_t* status;  // device status word (timeouts)
+  long long o_sb, o_sh, o_sn;  // output strides in elements (multiples of 8)
   int N;             // sequence length
+  int H;             // heads
   int BH;            // batch * heads
   int n_mblk;        // 256-row units per head: ceil(N / 256)
   int n_units;       // BH * n_mblk
@@ -151,11 +154,12 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tm_q, const CUt
       ok = false;
       break;
     }
+    const int hh = bh % a.H, bb = bh / a.H;  // tensor-map coordinates {d, n, h, b}
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_arrive_expect_tx(bar(kBarQFull + i), L::kTileBytes);
       for (int p = 0; p < L::kPanels; ++p)
-        ptx::tma_load_3d(sbase + L::kOffQ + i * L::kTileBytes + p * kPanelBytes, tm_q,
-                         bar(kBarQFull + i), 64 * p, mblk * 256 + 128 * i, bh);
+        ptx::tma_load_4d(sbase + L::kOffQ + i * L::kTileBytes + p * kPanelBytes, tm_q,
+                         bar(kBarQFull + i), 64 * p, mblk * 256 + 128 * i, hh, bb);
     }
     ++units;
     for (int j = 0; j < nkv && ok; ++j) {
@@ -168,8 +172,8 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tm_q, const CUt
         ptx::mbar_arrive_expect_tx(bar(kBarKVFull + s), L::kTileBytes);
         const CUtensorMap* tm = t ? tm_v : tm_k;
         for (int p = 0; p < L::kPanels; ++p)
-          ptx::tma_load_3d(sbase + L::kOffKV + s * L::kTileBytes + p * kPanelBytes, tm,
-                           bar(kBarKVFull + s), 64 * p, 128 * j, bh);
+          ptx::tma_load_4d(sbase + L::kOffKV + s * L::kTileBytes + p * kPanelBytes, tm,
+                           bar(kBarKVFull + s), 64 * p, 128 * j, hh, bb);
         ++ring;
       }
     }
@@ -436,7 +440,8 @@ __device__ __forceinline__ void epilogue_role(const FwdArgs& a, uint32_t bars, u
       ptx::mbar_arrive(bar(kBarStatsFree + i));
       const float2 il2 = make_float2(inv_l, inv_l);
       const int grow = mblk * 256 + 128 * i + r;
-      uint4* orow = reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * a.N + grow) * D);
+      const long long hh = bh % a.H, bb = bh / a.H;
+      uint4* orow = reinterpret_cast<uint4*>(out + bb * a.o_sb + hh * a.o_sh + grow * a.o_sn);
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -544,11 +549,15 @@ cudaError_t launch_fwd_d64(bool bf16, bool causal, const CUtensorMap* maps, cons
 cudaError_t launch_fwd_d128(bool bf16, bool causal, const CUtensorMap* maps, const FwdArgs& a,
                             int grid, cudaStream_t stream);
 int fwd_smem_bytes(int d);
-// Q, K, V tensor maps of a call (fa_host.cu).
-bool encode_fwd_maps(CUtensorMap* maps, const void* q, const void* k, const void* v, bool bf16,
-                     int d, int N, long long BH);
-// Unit counts of a call into `a` (N, BH, n_mblk, n_units, n_kv) and its grid.
-void plan_fwd(int d, int N, long long BH, int sm_count, FwdArgs* a, int* grid);
+// Element strides of a contiguous [B][H][N][d] tensor, and the checks on a
+// call's strides (fa_host.cu).
+fa_strides contiguous_strides(int H, int N, int d);
+fa_status check_strides(const fa_strides* s /* q, k, v, o */, int d);
+// Q, K, V tensor maps of a call (s: q, k, v strides).
+bool encode_fwd_maps(CUtensorMap* maps, const void* q, const void* k, const void* v,
+                     const fa_strides* s, bool bf16, int B, int H, int N, int d);
+// Unit counts of a call into `a` (N, H, BH, n_mblk, n_units, n_kv) and its grid.
+void plan_fwd(int d, int N, int H, long long BH, int sm_count, FwdArgs* a, int* grid);
 cudaError_t launch_fwd(int d, bool bf16, bool causal, const CUtensorMap* maps, const FwdArgs& a,
                        int grid, cudaStream_t stream);
 

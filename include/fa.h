@@ -43,6 +43,14 @@ typedef enum fa_dtype {
   FA_DTYPE_BF16 = 1  /* bfloat16 */
 } fa_dtype;
 
+/* Element strides of one tensor viewed as [B][H][N][d] (the d stride is 1):
+ * element (b, h, n, t) is at base + b*b_stride + h*h_stride + n*n_stride + t. */
+typedef struct fa_strides {
+  long long b; /* batch stride */
+  long long h; /* head stride */
+  long long n; /* row (sequence position) stride */
+} fa_strides;
+
 /*
  * fa_fwd - enqueue one fused attention forward on `stream`.
  *
@@ -73,6 +81,30 @@ typedef enum fa_dtype {
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                  int B, int H, int N, int d, int causal, float scale,
                  fa_dtype dtype, void* stream);
+
+/*
+ * fa_fwd_strided - fa_fwd on tensors in any [B][H][N][d] view with unit d
+ * stride: e.g. the [B][N][H][d] layout of a fused projection output
+ * (strides {N*H*d, d, H*d}), or rows padded to a longer pitch. This is the
+ * layout extension of the seq-major tensor maps of the B300 walkthrough
+ * (V14, TMA descriptor section); the pages use contiguous tensors only.
+ *
+ * strides : host pointer to 4 fa_strides, for q, k, v and o in that order,
+ *           in elements. Every stride must be a positive multiple of 8
+ *           elements (16 bytes: tensor-map rows and 16-byte output stores)
+ *           and every n stride at least d (else FA_ERR_INVALID_ARG); strides
+ *           of 2^38 elements or more return FA_ERR_UNSUPPORTED. Read during
+ *           the call only.
+ * o       : written rows must not overlap one another or q, k, v (not
+ *           checked; overlapping outputs give undefined results).
+ * lse     : contiguous [B][H][N] float32, as in fa_fwd.
+ * Everything else (arguments, errors, asynchrony, status word) is as in
+ * fa_fwd; a bad stride returns FA_ERR_INVALID_ARG before anything is
+ * enqueued.
+ */
+fa_status fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int B, int H, int N, int d, const fa_strides* strides, int causal,
+                         float scale, fa_dtype dtype, void* stream);
 
 /*
  * fa_fwd_noalloc - fa_fwd for callers that cannot allocate device memory.

@@ -19,7 +19,7 @@ def lib():
 
 def test_header_declares_expected_entry_points():
     names = fa.header_functions()
-    assert names == ["fa_fwd", "fa_fwd_noalloc", "fa_check", "fa_query_launch",
+    assert names == ["fa_fwd", "fa_fwd_strided", "fa_fwd_noalloc", "fa_check", "fa_query_launch",
                      "fa_sm_clock_probe", "fa_status_string", "fa_version"]
 
 
@@ -88,3 +88,48 @@ def test_no_device_is_an_error_not_a_fallback(lib):
 def test_missing_library_raises(tmp_path):
     with pytest.raises(RuntimeError):
         fa.load_library(str(tmp_path / "libfa_sm103.so"))
+
+
+def _strided(strides, d=128, N=128, **kw):
+    args = dict(q=GOOD, k=GOOD, v=GOOD, o=GOOD, lse=GOOD, B=1, H=2, N=N, d=d)
+    args.update(kw)
+    return fa.fa_fwd_strided(args["q"], args["k"], args["v"], args["o"], args["lse"], args["B"],
+                             args["H"], args["N"], args["d"], strides, 0, 0.125,
+                             fa.FA_DTYPE_FP16, 0)
+
+
+CONTIG = (2 * 128 * 128, 128 * 128, 128)   # [B][H][N][d], H=2, N=128, d=128
+BNHD = (128 * 2 * 128, 128, 2 * 128)       # [B][N][H][d]
+
+
+def test_strided_null_strides_rejected(lib):
+    assert _strided(None) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("bad", [(CONTIG[0], CONTIG[1], 130), (CONTIG[0], 4, 128),
+                                 (0, CONTIG[1], 128), (CONTIG[0], -128, 128),
+                                 (CONTIG[0], CONTIG[1], 64)])
+@pytest.mark.parametrize("which", [0, 1, 2, 3])
+def test_strided_bad_strides_rejected(lib, bad, which):
+    s = [CONTIG] * 4
+    s[which] = bad
+    assert _strided(s) == fa.FA_ERR_INVALID_ARG
+
+
+def test_strided_huge_strides_unsupported(lib):
+    assert _strided([CONTIG, CONTIG, (1 << 38, CONTIG[1], 128), CONTIG]) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_strided_checks_sizes_and_pointers_first(lib):
+    assert _strided([BNHD] * 4, d=96) == fa.FA_ERR_UNSUPPORTED
+    assert _strided([BNHD] * 4, q=0) == fa.FA_ERR_INVALID_ARG
+    assert _strided([BNHD] * 4, o=GOOD + 8) == fa.FA_ERR_INVALID_ARG
+
+
+def test_strided_valid_layouts_reach_the_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    # valid strides pass every check; without a GPU the call must then fail, never fall back
+    assert _strided([BNHD, CONTIG, (2 * 136 * 128, 136 * 128, 136), BNHD]) in (fa.FA_ERR_CUDA,
+                                                                           fa.FA_ERR_ARCH)

@@ -170,3 +170,70 @@ def test_query_launch_is_persistent():
         assert info["units"] == B * H * ((N + 255) // 256)
         assert info["grid"] == min(sms, info["units"])
         assert info["threads"] == 512 and info["smem_bytes"] <= 232448
+
+
+# ------------------------------------------------------------ strided views (fa_fwd_strided)
+
+def _in_layout(t, layout: str, pad_value=None):
+    """A [B, H, N, d] view of `t`'s values stored in `layout`:
+    bnhd = [B, N, H, d] storage; pad = rows at a pitch of d + 8 elements."""
+    import torch
+    B, H, N, d = t.shape
+    if layout == "bhnd":
+        return t.contiguous()
+    if layout == "bnhd":
+        store = torch.empty((B, N, H, d), dtype=t.dtype, device=t.device)
+        store.copy_(t.permute(0, 2, 1, 3))
+        return store.transpose(1, 2)
+    if layout == "pad":
+        store = torch.full((B, H, N, d + 8), float("nan") if pad_value is None else pad_value,
+                           dtype=t.dtype, device=t.device)
+        store[..., :d].copy_(t)
+        return store[..., :d]
+    raise ValueError(layout)
+
+
+STRIDED = [
+    # B, H, N, d, dtype, causal, layouts of q, k, v, o
+    (2, 3, 700, 128, "fp16", False, ("bnhd", "bnhd", "bnhd", "bnhd")),
+    (1, 4, 513, 64, "bf16", True, ("bnhd", "bnhd", "bnhd", "bnhd")),
+    (2, 2, 300, 128, "bf16", True, ("pad", "pad", "pad", "pad")),
+    (1, 3, 1000, 64, "fp16", False, ("bnhd", "bhnd", "pad", "pad")),
+    (3, 2, 129, 128, "fp16", True, ("bhnd", "bnhd", "bhnd", "bnhd")),
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,dtype,causal,layouts", STRIDED)
+def test_strided_views_every_element(oracle_mod, B, H, N, d, dtype, causal, layouts):
+    import torch
+    w = I.custom("strided", B, H, N, d, dtype, causal, seed_index=300 + N + d)
+    q, k, v = I.qkv_bits(w)
+    qd, kd, vd = (_in_layout(to_device(x, dtype), lay) for x, lay in zip((q, k, v), layouts[:3]))
+    sentinel = 7.0
+    o = _in_layout(torch.full((B, H, N, d), float("nan"), dtype=qd.dtype, device="cuda:0"),
+                   layouts[3], pad_value=sentinel)
+    lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device="cuda:0")
+    assert any(not t.is_contiguous() for t in (qd, kd, vd, o))
+    fa.attention_forward_into(qd, kd, vd, o, lse, causal=causal, scale=w.scale)
+    torch.cuda.synchronize()
+    assert fa.fa_check(0) == fa.FA_OK
+    o_ref, l_ref = oracle_mod.attn_fwd(q, k, v, dtype, causal, w.scale)
+    _check(compare(to_bits(o.contiguous()), lse.cpu().numpy(), o_ref, l_ref, dtype),
+           f"strided {layouts}")
+    if layouts[3] == "pad":  # the 8 padding elements of every output row are untouched
+        store = o.as_strided((B, H, N, d + 8), o.stride())
+        assert bool(torch.all(store[..., d:] == sentinel))
+
+
+def test_strided_matches_contiguous_bitwise():
+    import torch
+    name = "mha_b4_h16_n4096_d128_fp16"
+    w = I.WORKLOADS[name]
+    q, k, v = _inputs(name)
+    o1, l1 = run_fa(q, k, v, w.dtype, w.causal, w.scale)
+    qd, kd, vd = (_in_layout(to_device(x, w.dtype), "bnhd") for x in (q, k, v))
+    o = _in_layout(torch.empty((w.B, w.H, w.N, w.d), dtype=qd.dtype, device="cuda:0"), "bnhd")
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device="cuda:0")
+    fa.attention_forward_into(qd, kd, vd, o, lse, causal=w.causal, scale=w.scale)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_bits(o.contiguous()), o1) and np.array_equal(lse.cpu().numpy(), l1)
