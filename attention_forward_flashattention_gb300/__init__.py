@@ -70,6 +70,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             lib.fa_fwd_strided.argtypes = [vp, vp, vp, vp, vp, i, i, i, i,
                                            ctypes.POINTER(FaStrides), i, f, i, vp]
             lib.fa_fwd_strided.restype = i
+        if hasattr(lib, "fa_fwd_fp8"):
+            lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, f, i, f, vp]
+            lib.fa_fwd_fp8.restype = i
         lib.fa_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
         lib.fa_fwd_noalloc.restype = i
         lib.fa_check.argtypes = [vp]
@@ -110,6 +113,14 @@ def fa_fwd_strided(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: 
         arr = (FaStrides * 4)(*[FaStrides(*map(int, s)) for s in strides])
     return load_library().fa_fwd_strided(q, k, v, o, lse, B, H, N, d, arr, int(bool(causal)),
                                          float(scale), int(dtype), stream)
+
+
+def fa_fwd_fp8(q: int, k: int, vt: int, o: int, lse: int, B: int, H: int, N: int, d: int,
+               ldv: int, q_scale: float, k_scales: int, v_scale: float, causal: bool,
+               scale: float, stream: int = 0) -> int:
+    """Same arguments as the C function (device pointers as ints); returns the status."""
+    return load_library().fa_fwd_fp8(q, k, vt, o, lse, B, H, N, d, ldv, float(q_scale), k_scales,
+                                     float(v_scale), int(bool(causal)), float(scale), stream)
 
 
 def fa_fwd_noalloc(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, d: int,
@@ -193,4 +204,45 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     attention_forward_into(q, k, v, o, lse, causal, scale, stream)
+    return o, lse
+
+
+def attention_forward_fp8_into(q8, k8, vt8, o, lse, q_scale: float, k_scales, v_scale: float,
+                               causal: bool = False, scale: float | None = None,
+                               stream=None) -> None:
+    """Enqueues fa_fwd_fp8: q8, k8 [B, H, N, 128] and vt8 [B, H, 128, ldv] (V
+    transposed) contiguous CUDA tensors of e4m3 codes (uint8 or float8_e4m3fn),
+    k_scales a contiguous float32 [B, H, ceil(N / 128)] CUDA tensor, o a
+    contiguous bfloat16 [B, H, N, 128] tensor, lse a contiguous float32
+    [B, H, N] tensor."""
+    import torch
+    B, H, N, d = q8.shape
+    ldv = vt8.shape[-1]
+    ok = (tuple(k8.shape) == (B, H, N, d) and tuple(vt8.shape) == (B, H, d, ldv)
+          and tuple(o.shape) == (B, H, N, d) and o.dtype == torch.bfloat16
+          and tuple(lse.shape) == (B, H, N) and lse.dtype == torch.float32
+          and tuple(k_scales.shape) == (B, H, (N + 127) // 128)
+          and k_scales.dtype == torch.float32
+          and all(t.element_size() == 1 for t in (q8, k8, vt8))
+          and all(t.is_cuda and t.is_contiguous() for t in (q8, k8, vt8, o, lse, k_scales)))
+    if not ok:
+        raise ValueError("fa_fwd_fp8: bad shapes, dtypes or layouts")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    rc = fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), vt8.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                    B, H, N, d, ldv, q_scale, k_scales.data_ptr(), v_scale, causal, scale,
+                    _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_fp8")
+
+
+def attention_forward_fp8(q8, k8, vt8, q_scale: float, k_scales, v_scale: float,
+                          causal: bool = False, scale: float | None = None, stream=None):
+    """Returns (O bfloat16 [B, H, N, 128], LSE float32 [B, H, N]) of the 8-bit forward."""
+    import torch
+    B, H, N, d = q8.shape
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    attention_forward_fp8_into(q8, k8, vt8, o, lse, q_scale, k_scales, v_scale, causal, scale,
+                               stream)
     return o, lse

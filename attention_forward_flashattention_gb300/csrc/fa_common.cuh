@@ -254,6 +254,32 @@ __device__ __forceinline__ void issue_pv_ts(uint32_t d_tmem, uint32_t p_tmem, ui
   issue_pv_ts_desc<D, BF16>(d_tmem, p_tmem, desc_v(sV), accumulate);
 }
 
+// 8-bit (e4m3) products for head dimension 128: a 128-element row is one
+// 128-byte SW128 panel, and one MMA covers K = 32 (+32 bytes per step).
+// S[tmem] = Q[128 x 128] K[128 x 128]^T, both K-major in shared memory.
+__device__ __forceinline__ void issue_qk_fp8(uint32_t d_tmem, uint64_t dq, uint64_t dk) {
+  constexpr uint32_t id = ptx::idesc_f8(128, 128);
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    ptx::umma_f8_ss(d_tmem, dq, dk, id, kk > 0 ? 1u : 0u);
+    dq = desc_add(dq, 32u);
+    dk = desc_add(dk, 32u);
+    asm volatile("" : "+l"(dq), "+l"(dk));
+  }
+}
+// O[tmem] (+)= P[tmem: 128 lanes x 32 columns, four keys per column] V with V
+// given transposed, V^T[128 columns of O][128 keys], K-major in shared memory.
+__device__ __forceinline__ void issue_pv_fp8(uint32_t d_tmem, uint32_t p_tmem, uint64_t dvt,
+                                             bool accumulate) {
+  constexpr uint32_t id = ptx::idesc_f8(128, 128);
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    ptx::umma_f8_ts(d_tmem, p_tmem + 8u * kk, dvt, id, (accumulate || kk > 0) ? 1u : 0u);
+    dvt = desc_add(dvt, 32u);
+    asm volatile("" : "+l"(dvt));
+  }
+}
+
 // Pair MMAs for head dimension 128 (M = 256: 128 query rows in each CTA).
 // S = Q K^T: each CTA holds its 128 Q rows (two 16 KB panels) and 64 of the
 // 128 keys (two 8 KB panels of 64 rows); the pair's S has all 128 keys.

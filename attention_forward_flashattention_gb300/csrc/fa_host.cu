@@ -102,6 +102,20 @@ bool encode_qkv(CUtensorMap* m, const void* ptr, const fa_strides& st, bool bf16
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A 4-D byte tensor (e4m3 codes) {dims[0] (contiguous), dims[1], dims[2],
+// dims[3]} with byte strides for dims 1..3; box = 128 x 128 x 1 x 1 bytes,
+// 128-byte swizzle. Elements past dims[0] / dims[1] read as zero.
+bool encode_bytes4(CUtensorMap* m, const void* ptr, const cuuint64_t (&dims)[4],
+                   const cuuint64_t (&strides)[3]) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint32_t box[4] = {128u, 128u, 1u, 1u};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Size checks shared by fa_fwd and fa_query_launch.
@@ -243,6 +257,57 @@ fa_status fa_fwd_strided(const void* q, const void* k, const void* v, void* o, f
                          int H, int N, int d, const fa_strides* strides, int causal, float scale,
                          fa_dtype dtype, void* stream) {
   return fwd_call(q, k, v, o, lse, B, H, N, d, strides, causal, scale, dtype, stream);
+}
+
+fa_status fa_fwd_fp8(const void* q, const void* k, const void* vt, void* o, float* lse, int B,
+                     int H, int N, int d, int ldv, float q_scale, const float* k_scales,
+                     float v_scale, int causal, float scale, void* stream) {
+  if (!q || !k || !vt || !o || !lse || !k_scales) return FA_ERR_INVALID_ARG;
+  if (!fa::aligned16(q) || !fa::aligned16(k) || !fa::aligned16(vt) || !fa::aligned16(o) ||
+      !fa::aligned16(lse) || (reinterpret_cast<uintptr_t>(k_scales) & 3u) != 0)
+    return FA_ERR_INVALID_ARG;
+  for (const float x : {scale, q_scale, v_scale})
+    if (!(std::isfinite(x) && x > 0.f)) return FA_ERR_INVALID_ARG;
+  const fa_status sz = fa::check_sizes(B, H, N, d);
+  if (sz != FA_OK) return sz;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (ldv < N || (ldv & 15) != 0) return FA_ERR_INVALID_ARG;
+
+  int dev = 0;
+  fa::DeviceState* st = nullptr;
+  const fa_status ds = fa::current_device(&dev, &st, true);
+  if (ds != FA_OK) return ds;
+
+  const cuuint64_t n = static_cast<cuuint64_t>(N), h = static_cast<cuuint64_t>(H),
+                   b = static_cast<cuuint64_t>(B), lv = static_cast<cuuint64_t>(ldv);
+  CUtensorMap maps[3];
+  const cuuint64_t qk_dims[4] = {128u, n, h, b};
+  const cuuint64_t qk_strides[3] = {128u, 128u * n, 128u * n * h};
+  const cuuint64_t vt_dims[4] = {n, 128u, h, b};
+  const cuuint64_t vt_strides[3] = {lv, 128u * lv, 128u * lv * h};
+  if (!fa::encode_bytes4(&maps[0], q, qk_dims, qk_strides) ||
+      !fa::encode_bytes4(&maps[1], k, qk_dims, qk_strides) ||
+      !fa::encode_bytes4(&maps[2], vt, vt_dims, vt_strides))
+    return FA_ERR_CUDA;
+
+  fa::FwdArgs a{};
+  const fa_strides c = fa::contiguous_strides(H, N, d);
+  a.o = o;
+  a.o_sb = c.b;
+  a.o_sh = c.h;
+  a.o_sn = c.n;
+  a.lse = lse;
+  a.status = st->status;
+  a.scale_log2 = scale * q_scale * 1.4426950408889634f;
+  a.k_scales = k_scales;
+  a.v_scale = v_scale;
+  int grid = 0;
+  fa::plan_fwd(d, N, H, static_cast<long long>(B) * H, st->sm_count, &a, &grid);
+
+  (void)cudaGetLastError();
+  const cudaError_t e =
+      fa::launch_fwd_fp8(causal != 0, maps, a, grid, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 fa_status fa_check(void* stream) {

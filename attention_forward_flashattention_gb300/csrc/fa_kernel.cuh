@@ -58,7 +58,9 @@ struct FwdArgs {
   int n_mblk;        // 256-row units per head: ceil(N / 256)
   int n_units;       // BH * n_mblk
   int n_kv;          // 128-key tiles per head: ceil(N / 128)
-  float scale_log2;  // scale * log2(e)
+  float scale_log2;  // scale * log2(e) (8-bit inputs: times the Q scale)
+  const float* k_scales;  // 8-bit inputs: [BH][n_kv] scale of each 128-key block of K
+  float v_scale;          // 8-bit inputs: scale of V
 };
 
 constexpr int kFwdThreads = 512;
@@ -67,11 +69,13 @@ constexpr uint32_t kRegsWG0 = 72, kRegsSoftmax = 192, kRegsEpilogue = 56;
 static_assert(kRegsWG0 + 2 * kRegsSoftmax + kRegsEpilogue == 4 * (65536 / kFwdThreads),
               "register split must equal the launch allocation");
 
-template <int D>
+// FP8: e4m3 Q, K and V^T (d = 128 only): a 128-element row is one panel.
+template <int D, bool FP8 = false>
 struct Layout {
-  static constexpr int kPanels = D / 64;                   // 128-byte panels per row
-  static constexpr int kTileBytes = kPanels * kPanelBytes;  // a Q, K or V tile
-  static constexpr int kStages = (D == 128) ? 4 : 8;        // K / V ring slots
+  static_assert(!FP8 || D == 128, "the 8-bit kernel is laid out for head dimension 128");
+  static constexpr int kPanels = FP8 ? 1 : D / 64;         // 128-byte panels per row
+  static constexpr int kTileBytes = kPanels * kPanelBytes;  // a Q, K or V (V^T) tile
+  static constexpr int kStages = (D == 128 && !FP8) ? 4 : 8;  // K / V ring slots
   static constexpr int kOffQ = 0;                           // Q0, Q1
   static constexpr int kOffKV = 2 * kTileBytes;             // ring
   static constexpr int kOffStats = kOffKV + kStages * kTileBytes;  // [2 tiles][128] row sums l
@@ -135,11 +139,11 @@ __device__ __forceinline__ int unit_kv_tiles(const FwdArgs& a, int mblk) {
   return CAUSAL ? min(2 * mblk + 2, a.n_kv) : a.n_kv;
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool FP8>
 __device__ __forceinline__ void producer_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                               const CUtensorMap* tm_v, const FwdArgs& a,
                                               uint32_t sbase, uint32_t bars, const AbortCtx& ab) {
-  using L = Layout<D>;
+  using L = Layout<D, FP8>;
   constexpr int S = L::kStages;
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
   ptx::prefetch_tmap(tm_q);
@@ -170,10 +174,16 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tm_q, const CUt
           break;
         }
         ptx::mbar_arrive_expect_tx(bar(kBarKVFull + s), L::kTileBytes);
-        const CUtensorMap* tm = t ? tm_v : tm_k;
-        for (int p = 0; p < L::kPanels; ++p)
-          ptx::tma_load_4d(sbase + L::kOffKV + s * L::kTileBytes + p * kPanelBytes, tm,
-                           bar(kBarKVFull + s), 64 * p, 128 * j, hh, bb);
+        const uint32_t dst = sbase + L::kOffKV + s * L::kTileBytes;
+        if (FP8 && t) {
+          // V^T {keys, d, h, b}: keys 128j.. of all d rows, one 128-byte panel
+          ptx::tma_load_4d(dst, tm_v, bar(kBarKVFull + s), 128 * j, 0, hh, bb);
+        } else {
+          const CUtensorMap* tm = t ? tm_v : tm_k;
+          for (int p = 0; p < L::kPanels; ++p)
+            ptx::tma_load_4d(dst + p * kPanelBytes, tm, bar(kBarKVFull + s), 64 * p, 128 * j, hh,
+                             bb);
+        }
         ++ring;
       }
     }
@@ -196,18 +206,23 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tm_q, const CUt
 // everything else minimal: descriptors are built once and advanced in place,
 // waits are single-thread try_waits, and each step commits only what a
 // waiter needs.
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool FP8>
 __device__ __forceinline__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t bars,
                                          uint32_t tmem, const AbortCtx& ab) {
-  using L = Layout<D>;
+  using L = Layout<D, FP8>;
   constexpr int S = L::kStages;
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
   const uint64_t dQ[2] = {desc_kmajor(sbase + L::kOffQ),
                           desc_kmajor(sbase + L::kOffQ + L::kTileBytes)};
   const uint64_t dK0 = desc_kmajor(sbase + L::kOffKV);  // ring slot s: + s * kTileBytes
-  const uint64_t dV0 = desc_v(sbase + L::kOffKV);
+  // V as stored ([key][d], MN-major B operand), or V^T for 8-bit (K-major)
+  const uint64_t dV0 = FP8 ? desc_kmajor(sbase + L::kOffKV) : desc_v(sbase + L::kOffKV);
   const uint32_t tS[2] = {tmem + L::kColS, tmem + L::kColS + 128};
   const uint32_t tO[2] = {tmem + L::kColO, tmem + L::kColO + D};
+  auto qk = [&](int i, uint64_t dk) {
+    if constexpr (FP8) issue_qk_fp8(tS[i], dQ[i], dk);
+    else issue_qk_desc<D, BF16>(tS[i], dQ[i], dk);
+  };
   auto slot_off = [](uint32_t idx) { return (idx % S) * static_cast<uint32_t>(L::kTileBytes); };
   auto kv_wait = [&](uint32_t idx) {
     return wait_spin(bar(kBarKVFull + idx % S), (idx / S) & 1u, ab, kStatusMma);
@@ -226,9 +241,9 @@ __device__ __forceinline__ void mma_role(const FwdArgs& a, uint32_t sbase, uint3
     ptx::tc_fence_after();
     {
       const uint64_t dk = desc_add(dK0, slot_off(k0));
-      issue_qk_desc<D, BF16>(tS[0], dQ[0], dk);
+      qk(0, dk);
       ptx::umma_commit(bar(kBarSFull + 0));
-      issue_qk_desc<D, BF16>(tS[1], dQ[1], dk);
+      qk(1, dk);
       ptx::umma_commit(bar(kBarSFull + 1));
       ptx::umma_commit(bar(kBarKVFull + S + k0 % S));
       if (nkv == 1) ptx::umma_commit(bar(kBarQEmpty));
@@ -251,7 +266,8 @@ __device__ __forceinline__ void mma_role(const FwdArgs& a, uint32_t sbase, uint3
             !(ok = wait_spin(bar(kBarOFree + i), (units - 1) & 1u, ab, kStatusMma)))
           break;
         ptx::tc_fence_after();
-        issue_pv_ts_desc<D, BF16>(tO[i], tS[i], dv, j > 0);
+        if constexpr (FP8) issue_pv_fp8(tO[i], tS[i], dv, j > 0);
+        else issue_pv_ts_desc<D, BF16>(tO[i], tS[i], dv, j > 0);
         if (i == 0 && rel_pending) {
           ptx::umma_commit(bar(kBarKVFull + S + rel_v % S));
           ptx::umma_commit(bar(kBarKVFull + S + rel_k % S));
@@ -263,7 +279,7 @@ __device__ __forceinline__ void mma_role(const FwdArgs& a, uint32_t sbase, uint3
           continue;
         }
         if (i == 0 && !(ok = kv_wait(kn))) break;
-        issue_qk_desc<D, BF16>(tS[i], dQ[i], dk);
+        qk(i, dk);
         ptx::umma_commit(bar(kBarSFull + i));
         if (i == 1) {
           // V_j and K_{j+1} are both consumed once S1(j+1) completes
@@ -287,11 +303,11 @@ __device__ __forceinline__ void mma_role(const FwdArgs& a, uint32_t sbase, uint3
   wait_drain(bar(kBarDrain), 0u, ab, kStatusDrain);
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool FP8>
 __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t bars, uint32_t tmem,
                                              float* stats, const AbortCtx& ab, int warp,
                                              int lane) {
-  using L = Layout<D>;
+  using L = Layout<D, FP8>;
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
   const int wg = (warp >> 2) - 1;           // which Q tile
   const int r = (warp & 3) * 32 + lane;     // row in the tile = TMEM lane
@@ -299,7 +315,6 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t bars, ui
   const uint32_t tS = tl + L::kColS + 128u * wg;  // S_i; P_i over its first 64 columns
   const uint32_t tO = tl + L::kColO + static_cast<uint32_t>(D) * wg;
   const float cl2 = a.scale_log2;
-  const float2 c2 = make_float2(cl2, cl2);
   uint32_t scnt = 0, units = 0;
   int round = 0, bh = 0, mblk = 0;
   bool ok = true;
@@ -313,6 +328,10 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t bars, ui
     for (int j = 0; j < nkv; ++j) {
       if (!(ok = wait_bounded_warp(bar(kBarSFull + wg), (scnt++) & 1u, ab, kStatusSoftmax))) break;
       ptx::tc_fence_after();
+      // base-2 score scale of this tile (8-bit inputs: times its K block's scale)
+      float cj = cl2;
+      if constexpr (FP8) cj = cl2 * __ldg(a.k_scales + static_cast<size_t>(bh) * a.n_kv + j);
+      const float2 c2j = make_float2(cj, cj);
       uint32_t sr[4][32];
 #pragma unroll
       for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + 32u * c, sr[c]);
@@ -338,7 +357,7 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t bars, ui
         mx[2] = ptx::fmax3(mx[2], s[c + 4], s[c + 5]);
         mx[3] = ptx::fmax3(mx[3], s[c + 6], s[c + 7]);
       }
-      const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * cl2;
+      const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * cj;
       const float m_new = fmaxf(m_ref, m_tile);
       float alpha = 1.f;
       if (j == 0) {
@@ -348,33 +367,50 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t bars, ui
         m_ref = m_new;
       }
       const float2 neg2 = make_float2(-m_ref, -m_ref);
-      uint32_t pk[2][32];
       float2 ls[4], lr[4];
 #pragma unroll
       for (int t = 0; t < 4; ++t) ls[t] = lr[t] = make_float2(0.f, 0.f);
+      if constexpr (FP8) {
+        // P as e4m3, four keys per TMEM column over the first 32 S_i columns
+        // (O is normalised by the unrounded sum).
+        uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float2 t = ptx::ffma2(make_float2(s[2 * c], s[2 * c + 1]), c2, neg2);
-        const float p0 = ptx::ex2(t.x), p1 = ptx::ex2(t.y);
-        const uint32_t w = pack2<BF16>(p0, p1);
-        pk[c >> 5][c & 31] = w;
-        ls[c & 3] = ptx::fadd2(ls[c & 3], make_float2(p0, p1));
-        if constexpr (BF16) {
-          // bf16 P carries 8 significant bits: O is normalised by the sum of
-          // the rounded weights the PV product actually uses (a row dominated
-          // by one key then returns that V row exactly), while the LSE keeps
-          // the unrounded sum.
-          lr[c & 3] = ptx::fadd2(lr[c & 3], make_float2(__uint_as_float(w << 16),
-                                                        __uint_as_float(w & 0xFFFF0000u)));
+        for (int c = 0; c < 32; ++c) {
+          const float2 t0 = ptx::ffma2(make_float2(s[4 * c], s[4 * c + 1]), c2j, neg2);
+          const float2 t1 = ptx::ffma2(make_float2(s[4 * c + 2], s[4 * c + 3]), c2j, neg2);
+          const float p0 = ptx::ex2(t0.x), p1 = ptx::ex2(t0.y);
+          const float p2 = ptx::ex2(t1.x), p3 = ptx::ex2(t1.y);
+          pk[c] = ptx::pack4_e4m3(p0, p1, p2, p3);
+          ls[(2 * c) & 3] = ptx::fadd2(ls[(2 * c) & 3], make_float2(p0, p1));
+          ls[(2 * c + 1) & 3] = ptx::fadd2(ls[(2 * c + 1) & 3], make_float2(p2, p3));
         }
+        ptx::tmem_st32(tS, pk);
+      } else {
+        uint32_t pk[2][32];
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const float2 t = ptx::ffma2(make_float2(s[2 * c], s[2 * c + 1]), c2j, neg2);
+          const float p0 = ptx::ex2(t.x), p1 = ptx::ex2(t.y);
+          const uint32_t w = pack2<BF16>(p0, p1);
+          pk[c >> 5][c & 31] = w;
+          ls[c & 3] = ptx::fadd2(ls[c & 3], make_float2(p0, p1));
+          if constexpr (BF16) {
+            // bf16 P carries 8 significant bits: O is normalised by the sum of
+            // the rounded weights the PV product actually uses (a row dominated
+            // by one key then returns that V row exactly), while the LSE keeps
+            // the unrounded sum.
+            lr[c & 3] = ptx::fadd2(lr[c & 3], make_float2(__uint_as_float(w << 16),
+                                                          __uint_as_float(w & 0xFFFF0000u)));
+          }
+        }
+        // P_i into TMEM over the S_i columns this thread has already read.
+        ptx::tmem_st32(tS, pk[0]);
+        ptx::tmem_st32(tS + 32u, pk[1]);
       }
-      // P_i into TMEM over the S_i columns this thread has already read.
-      ptx::tmem_st32(tS, pk[0]);
-      ptx::tmem_st32(tS + 32u, pk[1]);
       const float2 s01 = ptx::fadd2(ptx::fadd2(ls[0], ls[1]), ptx::fadd2(ls[2], ls[3]));
       const float lsum = s01.x + s01.y;
       float lsum_p = lsum;
-      if constexpr (BF16) {
+      if constexpr (BF16 && !FP8) {
         const float2 r01 = ptx::fadd2(ptx::fadd2(lr[0], lr[1]), ptx::fadd2(lr[2], lr[3]));
         lsum_p = r01.x + r01.y;
       }
@@ -418,11 +454,11 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t bars, ui
   }
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool FP8>
 __device__ __forceinline__ void epilogue_role(const FwdArgs& a, uint32_t bars, uint32_t tmem,
                                               const float* stats, const AbortCtx& ab, int warp,
                                               int lane) {
-  using L = Layout<D>;
+  using L = Layout<D, FP8>;
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
   const int r = (warp & 3) * 32 + lane;
   const uint32_t tl = ptx::tmem_lane_base(tmem, warp);
@@ -436,7 +472,7 @@ __device__ __forceinline__ void epilogue_role(const FwdArgs& a, uint32_t bars, u
            wait_bounded_warp(bar(kBarStatsFull + i), units & 1u, ab, kStatusEpilogue);
       if (!ok) break;
       ptx::tc_fence_after();
-      const float inv_l = 1.f / stats[i * 128 + r];
+      const float inv_l = (FP8 ? a.v_scale : 1.f) / stats[i * 128 + r];
       ptx::mbar_arrive(bar(kBarStatsFree + i));
       const float2 il2 = make_float2(inv_l, inv_l);
       const int grow = mblk * 256 + 128 * i + r;
@@ -468,11 +504,12 @@ __device__ __forceinline__ void epilogue_role(const FwdArgs& a, uint32_t bars, u
   }
 }
 
-template <int D, bool BF16, bool CAUSAL>
+// FP8: e4m3 Q, K, V^T (d = 128), bf16 O (instantiate with BF16 = true).
+template <int D, bool BF16, bool CAUSAL, bool FP8 = false>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
-  using L = Layout<D>;
+  using L = Layout<D, FP8>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -518,16 +555,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (wgrp == 0) {
     ptx::setmaxnreg_dec<kRegsWG0>();
     if (warp == 0) {
-      if (lane == 0) producer_role<D, BF16, CAUSAL>(&tm_q, &tm_k, &tm_v, a, sbase, bars, ab);
+      if (lane == 0) producer_role<D, BF16, CAUSAL, FP8>(&tm_q, &tm_k, &tm_v, a, sbase, bars, ab);
     } else if (warp == 1) {
-      if (lane == 0) mma_role<D, BF16, CAUSAL>(a, sbase, bars, tmem, ab);
+      if (lane == 0) mma_role<D, BF16, CAUSAL, FP8>(a, sbase, bars, tmem, ab);
     }
   } else if (wgrp < 3) {
     ptx::setmaxnreg_inc<kRegsSoftmax>();
-    softmax_role<D, BF16, CAUSAL>(a, bars, tmem, stats, ab, warp, lane);
+    softmax_role<D, BF16, CAUSAL, FP8>(a, bars, tmem, stats, ab, warp, lane);
   } else {
     ptx::setmaxnreg_dec<kRegsEpilogue>();
-    epilogue_role<D, BF16, CAUSAL>(a, bars, tmem, stats, ab, warp, lane);
+    epilogue_role<D, BF16, CAUSAL, FP8>(a, bars, tmem, stats, ab, warp, lane);
   }
   __syncwarp();
   ptx::tc_fence_before();
@@ -560,5 +597,10 @@ bool encode_fwd_maps(CUtensorMap* maps, const void* q, const void* k, const void
 void plan_fwd(int d, int N, int H, long long BH, int sm_count, FwdArgs* a, int* grid);
 cudaError_t launch_fwd(int d, bool bf16, bool causal, const CUtensorMap* maps, const FwdArgs& a,
                        int grid, cudaStream_t stream);
+// 8-bit inputs (fa_fwd_fp8.cu): maps = Q, K ({128 bytes, N, H, B}) and V^T
+// ({keys, 128, H, B}), all e4m3 bytes.
+cudaError_t launch_fwd_fp8(bool causal, const CUtensorMap* maps, const FwdArgs& a, int grid,
+                           cudaStream_t stream);
+int fwd_smem_bytes_fp8();
 
 }  // namespace fa

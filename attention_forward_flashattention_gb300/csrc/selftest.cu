@@ -397,6 +397,125 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
   if (warp == 0) ptx::tmem_dealloc_pair(tmem, 256);
 }
 
+// rows x cols byte matrix (e4m3 codes), box = 128 x 128 bytes, SW128.
+bool encode_2d_u8(CUtensorMap* m, const void* ptr, int cols, int rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows), 1u};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols),
+                                 static_cast<cuuint64_t>(cols) * rows};
+  const cuuint32_t box[3] = {128u, 128u, 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// e4m3: C[128][128] = A[128][128] * B[128][128]^T (fp32), A and B fetched by
+// TMA as one 128-byte SW128 panel each (the S = Q K^T path of the 8-bit kernel).
+__global__ void __launch_bounds__(128, 1)
+    gemm_qk_fp8_kernel(const __grid_constant__ CUtensorMap ta,
+                       const __grid_constant__ CUtensorMap tb, float* c, uint32_t* status) {
+  extern __shared__ __align__(1024) uint8_t raw[];
+  const Smem s = carve(raw);
+  const AbortCtx ab{s.abort_flag, status};
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(s.bars, 1);
+    ptx::mbar_init(s.bars + 8, 1);
+    *s.abort_flag = 0u;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc(ptx::smem_u32(s.tmem_slot), 128);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *s.tmem_slot;
+  if (threadIdx.x == 0) {
+    ptx::mbar_arrive_expect_tx(s.bars, 2 * kPanelBytes);
+    ptx::tma_load_3d(s.base, &ta, s.bars, 0, 0, 0);
+    ptx::tma_load_3d(s.base + 2 * kPanelBytes, &tb, s.bars, 0, 0, 0);
+    const bool ok = wait_bounded(s.bars, 0, ab, kStatusSelftest);
+    if (ok) {
+      ptx::tc_fence_after();
+      issue_qk_fp8(tmem, desc_kmajor(s.base), desc_kmajor(s.base + 2 * kPanelBytes));
+    }
+    ptx::umma_commit(s.bars + 8);
+    if (!ok) wait_drain(s.bars, 0, ab, kStatusDrain);
+  }
+  __syncwarp();
+  const bool done = wait_bounded_warp(s.bars + 8, 0, ab, kStatusSelftest);
+  ptx::tc_fence_after();
+  if (done && !*s.abort_flag) read_back(tmem, c, 128);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 0) ptx::tmem_dealloc(tmem, 128);
+}
+
+// e4m3: C[128][128] = A[128][128] * Bt[128][128]^T with A (four codes per
+// 32-bit word, row r = 32 words) stored by the threads into TMEM columns
+// 128..159 and read from there, Bt fetched by TMA (the P V^T path).
+__global__ void __launch_bounds__(128, 1)
+    gemm_ts_fp8_kernel(const uint32_t* a, const __grid_constant__ CUtensorMap tb, float* c,
+                       uint32_t* status) {
+  extern __shared__ __align__(1024) uint8_t raw[];
+  const Smem s = carve(raw);
+  const AbortCtx ab{s.abort_flag, status};
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(s.bars, 1);
+    ptx::mbar_init(s.bars + 8, 1);
+    *s.abort_flag = 0u;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc(ptx::smem_u32(s.tmem_slot), 256);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *s.tmem_slot;
+  {
+    uint32_t pk[32];
+    for (int i = 0; i < 32; ++i) pk[i] = a[threadIdx.x * 32 + i];
+    ptx::tmem_st32(ptx::tmem_lane_base(tmem, warp) + 128u, pk);
+    ptx::tmem_st_wait();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (threadIdx.x == 0) {
+    ptx::mbar_arrive_expect_tx(s.bars, kPanelBytes);
+    ptx::tma_load_3d(s.base + 2 * kPanelBytes, &tb, s.bars, 0, 0, 0);
+    const bool ok = wait_bounded(s.bars, 0, ab, kStatusSelftest);
+    if (ok) {
+      ptx::tc_fence_after();
+      issue_pv_fp8(tmem, tmem + 128u, desc_kmajor(s.base + 2 * kPanelBytes), false);
+    }
+    ptx::umma_commit(s.bars + 8);
+    if (!ok) wait_drain(s.bars, 0, ab, kStatusDrain);
+  }
+  __syncwarp();
+  const bool done = wait_bounded_warp(s.bars + 8, 0, ab, kStatusSelftest);
+  ptx::tc_fence_after();
+  if (done && !*s.abort_flag) read_back(tmem, c, 128);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 0) ptx::tmem_dealloc(tmem, 256);
+}
+
+// out[i] = pack4_e4m3(in[4i], in[4i+1], in[4i+2], in[4i+3]).
+__global__ void pack_e4m3_kernel(const float* in, uint32_t* out, int n_words) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n_words) out[i] = ptx::pack4_e4m3(in[4 * i], in[4 * i + 1], in[4 * i + 2], in[4 * i + 3]);
+}
+
 // One warp waits on a barrier that never completes, with a 20 ms limit.
 __global__ void wait_timeout_kernel(uint32_t* status, uint32_t* out) {
   __shared__ __align__(8) uint64_t bar;
@@ -519,6 +638,50 @@ int fa_selftest_wait_timeout(uint32_t* status, uint32_t* out, void* stream) {
   if (!status || !out) return 1;
   (void)cudaGetLastError();
   fa::wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status, out);
+  return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
+
+}  // extern "C"
+
+extern "C" {
+
+// e4m3 C[128][128] = A[128][128] * B[128][128]^T (row-major byte matrices).
+int fa_selftest_gemm_qk_fp8(const void* a, const void* b, float* c, uint32_t* status,
+                            void* stream) {
+  if (!a || !b || !c || !status) return 1;
+  CUtensorMap ta, tb;
+  if (!fa::encode_2d_u8(&ta, a, 128, 128) || !fa::encode_2d_u8(&tb, b, 128, 128)) return 3;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  (void)cudaGetLastError();
+  if (cudaFuncSetAttribute(fa::gemm_qk_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           fa::kSmemBytes) != cudaSuccess)
+    return 3;
+  fa::gemm_qk_fp8_kernel<<<1, 128, fa::kSmemBytes, st>>>(ta, tb, c, status);
+  return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
+
+// e4m3 C[128][128] = A[128][128] * Bt[128][128]^T with A taken from TMEM.
+int fa_selftest_gemm_ts_fp8(const void* a, const void* bt, float* c, uint32_t* status,
+                            void* stream) {
+  if (!a || !bt || !c || !status) return 1;
+  CUtensorMap tb;
+  if (!fa::encode_2d_u8(&tb, bt, 128, 128)) return 3;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  (void)cudaGetLastError();
+  if (cudaFuncSetAttribute(fa::gemm_ts_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           fa::kSmemBytes) != cudaSuccess)
+    return 3;
+  fa::gemm_ts_fp8_kernel<<<1, 128, fa::kSmemBytes, st>>>(static_cast<const uint32_t*>(a), tb, c,
+                                                          status);
+  return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
+
+// Packs n_words groups of four floats into e4m3 codes with the kernel's packer.
+int fa_selftest_pack_e4m3(const float* in, uint32_t* out, int n_words, void* stream) {
+  if (!in || !out || n_words <= 0) return 1;
+  (void)cudaGetLastError();
+  fa::pack_e4m3_kernel<<<(n_words + 127) / 128, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+      in, out, n_words);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 

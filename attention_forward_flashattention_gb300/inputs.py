@@ -17,6 +17,14 @@ Generator (counter based, so any slice can be produced independently):
 
 Streams: tensor t in {Q: 0, K: 1, V: 2} of a workload with seed index c uses
 seed (1000 + c) * 4 + t.
+
+8-bit (e4m3) inputs for the FP8 forward: the same normals, divided by a
+float32 scale (the largest magnitude / 448: per tensor for Q and V, per
+128-key block of each head for K) and rounded to the nearest e4m3 value (ties
+to an even code, magnitudes above 448 saturating). V is stored transposed,
+[B][H][d][ldv] with ldv = N rounded up to 16 and zero padding. Format: OCP
+8-bit floating point, E4M3 "fn" variant (bias 7, 3 fraction bits, no
+infinities, S.1111.111 = NaN, largest finite 448).
 """
 from __future__ import annotations
 
@@ -144,3 +152,91 @@ def custom(name: str, B: int, H: int, N: int, d: int, dtype: str, causal: bool,
            seed_index: int, q_mult: float = 1.0) -> Workload:
     """A workload outside the five named ones (edge cases in tests)."""
     return Workload(name, B, H, N, d, dtype, causal, seed_index, q_mult)
+
+
+# ------------------------------------------------------------ 8-bit (e4m3) inputs
+
+E4M3_MAX = 448.0
+
+
+def e4m3_values() -> np.ndarray:
+    """Value of each of the 256 e4m3 codes (float64; NaN for S.1111.111)."""
+    c = np.arange(256)
+    e, m = (c >> 3) & 0xF, c & 7
+    v = np.where(e == 0, m * 2.0 ** -9, (8 + m) * np.exp2(e - 10.0))
+    v = np.where(c & 0x80, -v, v)
+    v[(e == 15) & (m == 7)] = np.nan
+    return v
+
+
+def to_e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """float64 -> e4m3 codes: nearest value, ties to the even code, |x| > 448 -> 448;
+    the sign bit follows x (a negative value that rounds to zero gives -0)."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    # spacing of e4m3 values around a: 2^(e - 3) in the binade [2^e, 2^(e+1)),
+    # 2^-9 below 2^-6 (subnormals); numpy's round is round-half-to-even, and
+    # a / spacing is exact, so r is the correctly rounded value
+    _, ex = np.frexp(a)                       # a = f 2^ex, f in [0.5, 1)
+    e = np.maximum(ex - 1, -6)
+    r = np.minimum(np.round(np.ldexp(a, 3 - e)), 16.0)   # 8..16 (normal) or 0..8 (subnormal)
+    # r == 16 carried into the next binade; below 2^-6 r counts 2^-9 steps
+    e = np.where(r == 16.0, e + 1, e)
+    r = np.where(r == 16.0, 8.0, r)
+    normal = r >= 8.0
+    code = np.where(normal, ((e + 7) << 3) + (r.astype(np.int64) - 8), r.astype(np.int64))
+    code = np.minimum(code, 0x7E).astype(np.uint8)
+    return np.where(np.signbit(x), code | np.uint8(0x80), code).astype(np.uint8)
+
+
+@dataclass(frozen=True)
+class Fp8Inputs:
+    """e4m3 codes and scales of one workload (values = scale * code value)."""
+    q: np.ndarray         # uint8 [B, H, N, d]
+    k: np.ndarray         # uint8 [B, H, N, d]
+    vt: np.ndarray        # uint8 [B, H, d, ldv], V transposed, zero padded
+    q_scale: float        # float32 value
+    k_scales: np.ndarray  # float32 [B, H, ceil(N / 128)]
+    v_scale: float        # float32 value
+
+    @property
+    def ldv(self) -> int:
+        return int(self.vt.shape[-1])
+
+
+def _scale_for(amax: float) -> float:
+    return float(np.float32(amax / E4M3_MAX)) if amax > 0 else 1.0
+
+
+def fp8_inputs(w: Workload) -> Fp8Inputs:
+    """e4m3 inputs of ``w`` from the same normals as its 16-bit inputs."""
+    B, H, N, d = w.B, w.H, w.N, w.d
+    n = B * H * N * d
+    zq = normal(w.seed * 4 + 0, n).reshape(B, H, N, d) * w.q_mult
+    zk = normal(w.seed * 4 + 1, n).reshape(B, H, N, d)
+    zv = normal(w.seed * 4 + 2, n).reshape(B, H, N, d)
+    q_scale = _scale_for(float(np.abs(zq).max()))
+    v_scale = _scale_for(float(np.abs(zv).max()))
+    q8 = to_e4m3_bits(zq / q_scale)
+    nt = (N + 127) // 128
+    k_scales = np.empty((B, H, nt), dtype=np.float32)
+    k8 = np.empty((B, H, N, d), dtype=np.uint8)
+    for t in range(nt):
+        blk = zk[:, :, 128 * t:128 * (t + 1), :]
+        sc = np.array([[_scale_for(float(np.abs(blk[b, h]).max())) for h in range(H)]
+                       for b in range(B)], dtype=np.float32)
+        k_scales[:, :, t] = sc
+        k8[:, :, 128 * t:128 * (t + 1), :] = to_e4m3_bits(blk / sc[:, :, None, None].astype(np.float64))
+    ldv = (N + 15) // 16 * 16
+    vt = np.zeros((B, H, d, ldv), dtype=np.uint8)
+    vt[:, :, :, :N] = to_e4m3_bits(zv / v_scale).transpose(0, 1, 3, 2)
+    return Fp8Inputs(q8, k8, vt, q_scale, k_scales, v_scale)
+
+
+# 8-bit workloads (e4m3 Q, K, V; bf16 O): the shape of the headline 16-bit one.
+FP8_WORKLOADS = {
+    w.name: w for w in [
+        Workload("mha_b4_h16_n4096_d128_e4m3", 4, 16, 4096, 128, "e4m3", False, 2),
+        Workload("causal_b4_h16_n4096_d128_e4m3", 4, 16, 4096, 128, "e4m3", True, 3),
+    ]
+}

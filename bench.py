@@ -49,7 +49,8 @@ def parse_args():
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
-    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=I.WORKLOAD_ORDER)
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                   choices=I.WORKLOAD_ORDER + list(I.FP8_WORKLOADS))
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -183,18 +184,36 @@ def sample_flops(w, rows: np.ndarray) -> float:
     return w.flops / (w.B * w.H * w.N) * len(rows)
 
 
-def time_oracle(w, q, k, v, target_s: float, seed: int):
+def get_workload(name: str):
+    return I.WORKLOADS[name] if name in I.WORKLOADS else I.FP8_WORKLOADS[name]
+
+
+def workload_inputs(w):
+    """Host inputs of w: (q, k, v) 16-bit values, or an I.Fp8Inputs for e4m3."""
+    return I.fp8_inputs(w) if w.dtype == "e4m3" else I.qkv_bits(w)
+
+
+def oracle_rows(w, x, rows):
+    import oracle
+    if w.dtype == "e4m3":
+        return oracle.attn_fp8(x.q, x.k, x.vt, x.q_scale, x.k_scales, x.v_scale, w.causal,
+                               w.scale, rows=rows)
+    q, k, v = x
+    return oracle.attn_rows(q, k, v, w.dtype, w.causal, w.scale, rows)
+
+
+def time_oracle(w, x, target_s: float, seed: int):
     """Times the oracle on a row sample sized to about target_s seconds."""
     import oracle
     cores = oracle.threads(0)
     calib = oracle_sample_rows(w, 2 * cores, seed)
     t = time.perf_counter()
-    oracle.attn_rows(q, k, v, w.dtype, w.causal, w.scale, calib)
+    oracle_rows(w, x, calib)
     dt = max(time.perf_counter() - t, 1e-3)
     n = int(min(max(len(calib) * target_s / dt, len(calib)), 200000))
     rows = oracle_sample_rows(w, n, seed + 1)
     t = time.perf_counter()
-    oracle.attn_rows(q, k, v, w.dtype, w.causal, w.scale, rows)
+    oracle_rows(w, x, rows)
     dt = time.perf_counter() - t
     return sample_flops(w, rows) / dt / 1e12, dt, len(rows), cores
 
@@ -204,14 +223,14 @@ def time_oracle(w, q, k, v, target_s: float, seed: int):
 def run_reference(args, rank: int, world: int):
     if rank != 0:
         return
-    w = I.WORKLOADS[args.workload]
-    q, k, v = I.qkv_bits(w)
+    w = get_workload(args.workload)
+    x = workload_inputs(w)
     import oracle
     oracle.build()
     step_target = 2.0
     vals, secs, nrows, cores = [], [], 0, oracle.threads(0)
     for s in range(args.warmup + args.steps):
-        tf, dt, n, cores = time_oracle(w, q, k, v, step_target, seed=w.seed * 7 + s)
+        tf, dt, n, cores = time_oracle(w, x, step_target, seed=w.seed * 7 + s)
         if s >= args.warmup:
             vals.append(tf)
             secs.append(dt)
@@ -251,20 +270,34 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     dev = torch.device("cuda", local_rank)
     fabuild.build()
     fa.load_library()
-    w = I.WORKLOADS[args.workload]
-    qb, kb, vb = I.qkv_bits(w)
-    tdt = torch.float16 if w.dtype == "fp16" else torch.bfloat16
-    host = [torch.from_numpy(x.view(np.int16)).view(tdt).pin_memory() for x in (qb, kb, vb)]
-    q, k, v = (h.to(dev) for h in host)
-    o = torch.empty_like(q)
+    w = get_workload(args.workload)
+    fp8 = w.dtype == "e4m3"
+    x = workload_inputs(w)
+    if fp8:
+        # e4m3 codes (Q, K, V^T) and the per-block K scales; bf16 output
+        tdt = torch.bfloat16
+        host = [torch.from_numpy(np.ascontiguousarray(t)).pin_memory() for t in (x.q, x.k, x.vt)]
+        host.append(torch.from_numpy(np.ascontiguousarray(x.k_scales)).pin_memory())
+    else:
+        tdt = torch.float16 if w.dtype == "fp16" else torch.bfloat16
+        host = [torch.from_numpy(t.view(np.int16)).view(tdt).pin_memory() for t in x]
+    dev_in = [h.to(dev) for h in host]
+    o = torch.empty((w.B, w.H, w.N, w.d), dtype=tdt, device=dev)
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
     sh = int(stream.cuda_stream)
     launch = fa.fa_query_launch(w.B, w.H, w.N, w.d, w.causal)
 
+    def run(ins):
+        if fp8:
+            fa.attention_forward_fp8_into(ins[0], ins[1], ins[2], o, lse, x.q_scale, ins[3],
+                                          x.v_scale, w.causal, w.scale, stream)
+        else:
+            fa.attention_forward_into(ins[0], ins[1], ins[2], o, lse, w.causal, w.scale, stream)
+
     def step():
-        fa.attention_forward_into(q, k, v, o, lse, w.causal, w.scale, stream)
+        run(dev_in)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -317,8 +350,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         lh = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
 
         def e2e_step():
-            qd, kd, vd = (h.to(dev, non_blocking=True) for h in host)
-            fa.attention_forward_into(qd, kd, vd, o, lse, w.causal, w.scale, stream)
+            run([h.to(dev, non_blocking=True) for h in host])
             oh.copy_(o, non_blocking=True)
             lh.copy_(lse, non_blocking=True)
 
@@ -334,7 +366,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, world, dev)
         elem = w.B * w.H * w.N * w.d
         e2e = {"value": w.flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
-               "ms_per_step": e2e_ms, "h2d_bytes_per_step": 3 * elem * 2,
+               "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in host),
                "d2h_bytes_per_step": elem * 2 + w.B * w.H * w.N * 4}
 
     if rank != 0:
@@ -344,9 +377,11 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         peak, peak_src = float(peaks["bf16_tflops"]), "measured bf16 burst (fp16 same nominal rate)"
     else:
         peak, peak_src = FALLBACK_PEAK_TFLOPS, "fallback"
+    if fp8:   # e4m3 dense rate is twice the 16-bit one (4.5 vs 2.25 PFLOP/s nominal)
+        peak, peak_src = 2.0 * peak, peak_src + " x 2 (e4m3 / bf16 nominal dense ratio)"
     cpu = None
     if not args.no_cpu_baseline:
-        tf, dt, n, cores = time_oracle(w, qb, kb, vb, target_s=12.0, seed=w.seed * 13)
+        tf, dt, n, cores = time_oracle(w, x, target_s=12.0, seed=w.seed * 13)
         cpu = {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
                "sample": f"{n} query rows (grouped over 4 heads) of {w.name}, {dt:.1f} s wall; "
                          f"TFLOPS = rows x (metric FLOPs per row) / wall time"}
@@ -358,7 +393,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "config": {**workload_config(w), "parallelism": f"replicas x{world}",
                    "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)",
                    "grid": launch["grid"], "threads": launch["threads"],
-                   "smem_bytes": launch["smem_bytes"], "units": launch["units"]},
+                   "smem_bytes": None if fp8 else launch["smem_bytes"],
+                   "units": launch["units"]},
         "pct_of_2250_tflops": 100.0 * per_gpu_tflops / NOMINAL_DENSE_FP16_TFLOPS,
         "roofline": {"bound": "tensor", "achieved": per_gpu_tflops, "peak": peak,
                      "unit": "TFLOP/s", "frac": per_gpu_tflops / peak,

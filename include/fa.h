@@ -107,6 +107,40 @@ fa_status fa_fwd_strided(const void* q, const void* k, const void* v, void* o, f
                          float scale, fa_dtype dtype, void* stream);
 
 /*
+ * fa_fwd_fp8 - the forward on 8-bit inputs: FP8 E4M3 (OCP 8-bit floating
+ * point, "fn" variant: bias 7, 3 fraction bits, no infinities, largest finite
+ * 448), after the FP8 path of "TMA + Warp Specialization" (section 17.7):
+ * one scale per 128-key block of K, the softmax weights P rounded to 8 bits
+ * before the P V product, fp32 accumulation.
+ *
+ * q, k     : device, contiguous [B][H][N][128] e4m3 codes (one byte each).
+ * vt       : device, V transposed: [B][H][128][ldv] e4m3 codes, byte
+ *            (b, h, t, n) holding V[b][h][n][t]; bytes n >= N of a row are
+ *            not read.
+ * ldv      : row length of vt in bytes: ldv >= N and a multiple of 16.
+ * k_scales : device float32 [B][H][ceil(N / 128)]: the scale of each 128-key
+ *            block of K (finite and > 0; not checked, it is device memory).
+ * q_scale, v_scale : scales of Q and V, finite and > 0.
+ *            The values are q = q_scale * q8, k_n = k_scales[b][h][n/128] *
+ *            k8_n and v = v_scale * v8.
+ * o        : device, contiguous [B][H][N][128] bfloat16, written.
+ * lse      : as fa_fwd (natural-log logsumexp of the scaled scores).
+ * d        : must be 128 (else FA_ERR_UNSUPPORTED).
+ * All pointers 16-byte aligned (k_scales 4-byte aligned). Other arguments,
+ * errors, asynchrony and the status word are as in fa_fwd.
+ *
+ * Precision: each weight p of a row (largest weight in [1, 256] on the
+ * kernel's scale) is rounded to e4m3, O is normalised by the unrounded sum;
+ * per element |O - O_exact| <= sum_j (2^-4 p_j + 2^-10) |v_j| / sum_j p_j with
+ * p_j = exp(s_j - max s) (plus fp32 and bf16 output rounding). The LSE is
+ * computed from the unrounded weights.
+ */
+fa_status fa_fwd_fp8(const void* q, const void* k, const void* vt, void* o, float* lse,
+                     int B, int H, int N, int d, int ldv, float q_scale,
+                     const float* k_scales, float v_scale, int causal, float scale,
+                     void* stream);
+
+/*
  * fa_fwd_noalloc - fa_fwd for callers that cannot allocate device memory.
  * (A library convenience: the pages have no counterpart.)
  *

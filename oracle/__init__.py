@@ -63,6 +63,15 @@ def _load():
                                              ctypes.c_int, ctypes.c_float, ctypes.POINTER(i64), i64,
                                              f64p, f64p, ctypes.c_int]
             lib.oracle_attn_rows.restype = ctypes.c_int
+            u8p = ctypes.POINTER(ctypes.c_uint8)
+            f32p = ctypes.POINTER(ctypes.c_float)
+            lib.oracle_attn_fp8.argtypes = [u8p, u8p, u8p, i64, i64, i64, i64, i64, ctypes.c_float,
+                                            f32p, ctypes.c_float, ctypes.c_int, ctypes.c_float,
+                                            ctypes.POINTER(i64), i64, f64p, f64p, f64p,
+                                            ctypes.c_int]
+            lib.oracle_attn_fp8.restype = ctypes.c_int
+            lib.oracle_decode_e4m3.argtypes = [u8p, i64, f64p]
+            lib.oracle_decode_e4m3.restype = None
             _lib = lib
     return _lib
 
@@ -131,3 +140,54 @@ def attn_rows(q: np.ndarray, k: np.ndarray, v: np.ndarray, dtype: str, causal: b
     if rc != 0:
         raise ValueError("oracle_attn_rows rejected its arguments")
     return o, lse
+
+
+def _u8(a: np.ndarray):
+    a = np.ascontiguousarray(a, dtype=np.uint8)
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8))
+
+
+def decode_e4m3(codes: np.ndarray) -> np.ndarray:
+    """Exact decode of e4m3 codes (OCP FP8 E4M3, "fn" variant) to float64."""
+    codes, p = _u8(codes)
+    out = np.empty(codes.shape, dtype=np.float64)
+    _load().oracle_decode_e4m3(p, codes.size, out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
+    return out
+
+
+def attn_fp8(q8: np.ndarray, k8: np.ndarray, vt8: np.ndarray, q_scale: float,
+             k_scales: np.ndarray, v_scale: float, causal: bool, scale: float,
+             rows: np.ndarray | None = None, nthreads: int = 0):
+    """8-bit forward on e4m3 codes: q8, k8 [B, H, N, d], vt8 [B, H, d, ldv] (V
+    transposed), k_scales float32 [B, H, ceil(N / 128)] (one per 128-key block).
+
+    Returns (O float64 [R, d], LSE float64 [R], bound float64 [R, d]) for the
+    flat rows ``rows`` (bh * N + i), or every row in order when ``rows`` is None;
+    ``bound`` bounds |O' - O| for any kernel that rounds the softmax weights to
+    e4m3 before the P V product (see attend_row_bound in attn_ref.cpp).
+    """
+    B, H, N, d = q8.shape
+    ldv = vt8.shape[-1]
+    assert k8.shape == q8.shape and vt8.shape == (B, H, d, ldv)
+    assert k_scales.shape == (B, H, (N + 127) // 128)
+    q8, qp = _u8(q8)
+    k8, kp = _u8(k8)
+    vt8, vp = _u8(vt8)
+    ks = np.ascontiguousarray(k_scales, dtype=np.float32)
+    if rows is None:
+        nr, rp = B * H * N, None
+    else:
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        nr, rp = rows.size, rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+    o = np.empty((nr, d), dtype=np.float64)
+    lse = np.empty((nr,), dtype=np.float64)
+    bound = np.empty((nr, d), dtype=np.float64)
+    f64 = ctypes.POINTER(ctypes.c_double)
+    rc = _load().oracle_attn_fp8(qp, kp, vp, B, H, N, d, ldv, float(np.float32(q_scale)),
+                                 ks.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
+                                 float(np.float32(v_scale)), int(bool(causal)),
+                                 float(np.float32(scale)), rp, nr, o.ctypes.data_as(f64),
+                                 lse.ctypes.data_as(f64), bound.ctypes.data_as(f64), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_attn_fp8 rejected its arguments")
+    return o, lse, bound

@@ -111,6 +111,47 @@ void attend_row(const double* qi, const double* K, const double* V,
   *out_lse = m + std::log(l);
 }
 
+// OCP 8-bit floating point E4M3 ("fn" variant): 1 sign bit, 4 exponent bits
+// (bias 7), 3 fraction bits; no infinities; S.1111.111 is NaN; largest
+// finite value 0x7E = 448; subnormals frac * 2^-9.
+double decode_e4m3(uint8_t c) {
+  const int sign = c >> 7;
+  const int expo = (c >> 3) & 0xF;
+  const int frac = c & 0x7;
+  double v;
+  if (expo == 0xF && frac == 0x7) {
+    v = NAN;
+  } else if (expo == 0) {
+    v = std::ldexp(static_cast<double>(frac), -9);
+  } else {
+    // (1 + frac / 8) * 2^(expo - 7) = (8 + frac) * 2^(expo - 10)
+    v = std::ldexp(static_cast<double>(frac | 0x8), expo - 10);
+  }
+  return sign ? -v : v;
+}
+
+// The 8-bit variant of attend_row: same definition, plus a bound on how far a
+// kernel that rounds every softmax weight p to e4m3 before the P V product
+// (and normalises by the sum of the unrounded weights) can land from O.
+// Rounding p in [2^-6, 448] moves it by at most 2^-4 p (3 fraction bits),
+// below 2^-6 by at most 2^-10 (subnormal spacing 2^-9), on the kernel's own
+// weight scale, whose largest weight lies in [1, 2^8]; so on the scale where
+// the largest weight is 1 each weight moves by at most 2^-4 p_j + 2^-10, and
+//   |O_t - O'_t| <= sum_j (2^-4 p_j + 2^-10) |v_jt| / sum_j p_j.
+void attend_row_bound(const double* qi, const double* K, const double* V,
+                      int64_t d, int64_t nkeys, double scale, std::vector<double>& s,
+                      double* out_o, double* out_lse, double* out_bound) {
+  attend_row(qi, K, V, d, nkeys, scale, s, out_o, out_lse);  // s now holds p_j
+  double l = 0.0;
+  for (int64_t j = 0; j < nkeys; ++j) l += s[j];
+  for (int64_t t = 0; t < d; ++t) out_bound[t] = 0.0;
+  for (int64_t j = 0; j < nkeys; ++j) {
+    const double w = 0.0625 * s[j] + 1.0 / 1024.0;
+    for (int64_t t = 0; t < d; ++t) out_bound[t] += w * std::fabs(V[j * d + t]);
+  }
+  for (int64_t t = 0; t < d; ++t) out_bound[t] /= l;
+}
+
 int pick_threads(int requested) {
   if (requested > 0) return requested;
   const unsigned hc = std::thread::hardware_concurrency();
@@ -204,6 +245,62 @@ int oracle_attn_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
     }
   });
   return 0;
+}
+
+// 8-bit forward. q8, k8: [B][H][N][d] e4m3 codes; vt8: [B][H][d][ldv] e4m3
+// codes of V transposed (column n of row t is V[n][t]); the values are
+//   q = q_scale * q8,  k_n = k_scales[b][h][n / 128] * k8_n,  v = v_scale * v8.
+// rows: flat row indices bh * N + i (nrows of them), or all rows in order
+// when rows is null. Outputs per row: o[r][d], lse[r] and bound[r][d], the
+// e4m3-weight bound of attend_row_bound. Returns 0, or -1 on bad arguments.
+int oracle_attn_fp8(const uint8_t* q8, const uint8_t* k8, const uint8_t* vt8, int64_t B,
+                    int64_t H, int64_t N, int64_t d, int64_t ldv, float q_scale,
+                    const float* k_scales, float v_scale, int causal, float scale,
+                    const int64_t* rows, int64_t nrows, double* o, double* lse,
+                    double* bound, int nthreads) {
+  const int64_t BH = B * H;
+  if (!q8 || !k8 || !vt8 || !k_scales || !o || !lse || !bound || B <= 0 || H <= 0 ||
+      N <= 0 || d <= 0 || ldv < N)
+    return -1;
+  if (!rows) nrows = BH * N;
+  if (nrows < 0) return -1;
+  if (rows)
+    for (int64_t r = 0; r < nrows; ++r)
+      if (rows[r] < 0 || rows[r] >= BH * N) return -1;
+  const int64_t ntiles = (N + 127) / 128;
+  const double sc = static_cast<double>(scale);
+  const int T = static_cast<int>(
+      std::max<int64_t>(1, std::min<int64_t>(pick_threads(nthreads), nrows)));
+  run_parallel(T, [&](int w, int nt) {
+    const int64_t lo = nrows * w / nt, hi = nrows * (w + 1) / nt;
+    std::vector<double> K(N * d), V(N * d), qi(d), s(N);
+    int64_t cur = -1;
+    for (int64_t r = lo; r < hi; ++r) {
+      const int64_t row = rows ? rows[r] : r;
+      const int64_t bh = row / N, i = row % N;
+      if (bh != cur) {
+        for (int64_t n = 0; n < N; ++n) {
+          const double ks = static_cast<double>(k_scales[bh * ntiles + n / 128]);
+          for (int64_t t = 0; t < d; ++t) {
+            K[n * d + t] = ks * decode_e4m3(k8[(bh * N + n) * d + t]);
+            V[n * d + t] = static_cast<double>(v_scale) * decode_e4m3(vt8[(bh * d + t) * ldv + n]);
+          }
+        }
+        cur = bh;
+      }
+      for (int64_t t = 0; t < d; ++t)
+        qi[t] = static_cast<double>(q_scale) * decode_e4m3(q8[(bh * N + i) * d + t]);
+      const int64_t nkeys = causal ? i + 1 : N;
+      attend_row_bound(qi.data(), K.data(), V.data(), d, nkeys, sc, s, o + r * d, lse + r,
+                       bound + r * d);
+    }
+  });
+  return 0;
+}
+
+// Decodes n e4m3 codes.
+void oracle_decode_e4m3(const uint8_t* x, int64_t n, double* out) {
+  for (int64_t t = 0; t < n; ++t) out[t] = decode_e4m3(x[t]);
 }
 
 }  // extern "C"

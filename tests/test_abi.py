@@ -19,7 +19,8 @@ def lib():
 
 def test_header_declares_expected_entry_points():
     names = fa.header_functions()
-    assert names == ["fa_fwd", "fa_fwd_strided", "fa_fwd_noalloc", "fa_check", "fa_query_launch",
+    assert names == ["fa_fwd", "fa_fwd_strided", "fa_fwd_fp8", "fa_fwd_noalloc", "fa_check",
+                     "fa_query_launch",
                      "fa_sm_clock_probe", "fa_status_string", "fa_version"]
 
 
@@ -33,7 +34,8 @@ def test_selftest_library_exports():
     _, st = fabuild.build()
     slib = ctypes.CDLL(st)
     for name in ("fa_selftest_gemm_qk", "fa_selftest_gemm_pv", "fa_selftest_gemm_ts",
-                 "fa_selftest_gemm_qk_pair", "fa_selftest_gemm_pv_pair", "fa_selftest_wait_timeout"):
+                 "fa_selftest_gemm_qk_pair", "fa_selftest_gemm_pv_pair", "fa_selftest_wait_timeout",
+                 "fa_selftest_gemm_qk_fp8", "fa_selftest_gemm_ts_fp8", "fa_selftest_pack_e4m3"):
         assert hasattr(slib, name)
 
 
@@ -133,3 +135,32 @@ def test_strided_valid_layouts_reach_the_device(lib):
     # valid strides pass every check; without a GPU the call must then fail, never fall back
     assert _strided([BNHD, CONTIG, (2 * 136 * 128, 136 * 128, 136), BNHD]) in (fa.FA_ERR_CUDA,
                                                                            fa.FA_ERR_ARCH)
+
+
+def _fp8(**kw):
+    a = dict(q=GOOD, k=GOOD, vt=GOOD, o=GOOD, lse=GOOD, B=1, H=2, N=300, d=128, ldv=304,
+             q_scale=0.01, k_scales=GOOD, v_scale=0.01, causal=0, scale=0.088)
+    a.update(kw)
+    return fa.fa_fwd_fp8(a["q"], a["k"], a["vt"], a["o"], a["lse"], a["B"], a["H"], a["N"],
+                         a["d"], a["ldv"], a["q_scale"], a["k_scales"], a["v_scale"], a["causal"],
+                         a["scale"], 0)
+
+
+@pytest.mark.parametrize("kw", [dict(q=0), dict(vt=0), dict(k_scales=0), dict(vt=GOOD + 8),
+                                dict(k_scales=GOOD + 2), dict(ldv=296), dict(ldv=300),
+                                dict(q_scale=0.0), dict(v_scale=float("nan")),
+                                dict(scale=-1.0), dict(N=0)])
+def test_fp8_bad_arguments_rejected(lib, kw):
+    assert _fp8(**kw) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [dict(d=64), dict(d=96)])
+def test_fp8_head_dim_must_be_128(lib, kw):
+    assert _fp8(**kw) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_fp8_valid_arguments_reach_the_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _fp8() in (fa.FA_ERR_CUDA, fa.FA_ERR_ARCH)

@@ -81,3 +81,49 @@ def test_workload_flops(name):
     w = I.WORKLOADS[name]
     f = 4.0 * w.B * w.H * w.N ** 2 * w.d
     assert w.flops == (f / 2 if w.causal else f)
+
+
+def test_e4m3_values_match_torch():
+    torch = pytest.importorskip("torch")
+    want = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = I.e4m3_values()
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    assert np.array_equal(got[~np.isnan(got)], want[~np.isnan(want)])
+
+
+def test_e4m3_rounding_matches_torch_and_saturates():
+    torch = pytest.importorskip("torch")
+    x = np.random.default_rng(3).standard_normal(200000) * 60.0
+    ties = np.array([1.0625, 1.1875, -1.0625, 2.0 ** -10, 3 * 2.0 ** -10, 464.0, 1e6, -1e6])
+    # float32 values: torch rounds from float32 (a float64 is first rounded to
+    # float32 there), the encoder rounds once from the exact value
+    x = np.concatenate([x, ties]).astype(np.float32).astype(np.float64)
+    got = I.to_e4m3_bits(x)
+    want = torch.from_numpy(np.clip(x, -448.0, 448.0).astype(np.float32)).to(
+        torch.float8_e4m3fn).view(torch.uint8)
+    assert np.array_equal(got, want.numpy())
+    assert list(I.e4m3_values()[I.to_e4m3_bits(np.array([1.0625, 1.1875, 464.0, -1e6]))]) == \
+        [1.0, 1.25, 448.0, -448.0]
+
+
+def test_fp8_inputs_scales_and_layout():
+    w = I.custom("fp8in", 1, 2, 300, 128, "e4m3", False, 21)
+    f = I.fp8_inputs(w)
+    assert f.q.dtype == np.uint8 and f.vt.shape == (1, 2, 128, 304)
+    assert f.k_scales.shape == (1, 2, 3) and f.k_scales.dtype == np.float32
+    assert np.all(f.vt[..., 300:] == 0)
+    vals = I.e4m3_values()
+    # every K block's largest code is the largest finite value (scale = amax / 448)
+    for t in range(3):
+        assert np.abs(vals[f.k[:, :, 128 * t:128 * (t + 1)]]).max() == 448.0
+    # decoded Q approximates the normals within half an e4m3 spacing (relative 2^-4)
+    zq = I.normal(w.seed * 4, 1 * 2 * 300 * 128).reshape(1, 2, 300, 128)
+    approx = vals[f.q] * f.q_scale
+    assert np.all(np.abs(approx - zq) <= np.abs(zq) * 2.0 ** -4 + 2.0 ** -10 * f.q_scale + 1e-12)
+
+
+def test_e4m3_rounding_is_single_rounding_from_float64():
+    # just below / above a tie between two e4m3 values: no detour through float32
+    below, above = np.nextafter(0.59375, 0.0), np.nextafter(1.5625, 2.0)
+    vals = I.e4m3_values()[I.to_e4m3_bits(np.array([below, 0.59375, above, 1.5625]))]
+    assert list(vals) == [0.5625, 0.625, 1.625, 1.5]

@@ -216,3 +216,83 @@ def test_rejects_bad_arguments(oracle_mod):
     q = np.zeros((1, 1, 4, 64), dtype=np.uint16)
     with pytest.raises(ValueError):
         oracle_mod.attn_rows(q, q, q, "fp16", False, 1.0, np.array([4]))
+
+
+# ---------------------------------------------------------------- 8-bit (e4m3) oracle
+
+def test_decode_e4m3_exhaustive_against_torch(oracle_mod):
+    torch = pytest.importorskip("torch")
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle_mod.decode_e4m3(codes)
+    want = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan) and nan.sum() == 2   # S.1111.111 only
+    assert np.array_equal(got[~nan], want[~nan])
+
+
+def test_decode_e4m3_format_constants(oracle_mod):
+    # OCP FP8 E4M3: 1.0 = 0x38, largest 448 = 0x7E, smallest normal 2^-6 = 0x08,
+    # smallest subnormal 2^-9 = 0x01, sign in bit 7
+    got = oracle_mod.decode_e4m3(np.array([0x38, 0x7E, 0x08, 0x01, 0xB8, 0x00, 0x80], np.uint8))
+    assert list(got) == [1.0, 448.0, 2.0 ** -6, 2.0 ** -9, -1.0, 0.0, -0.0]
+
+
+def _fp8_problem(seed, B, H, N, d=128, q_mult=1.0):
+    w = I.custom("fp8pin", B, H, N, d, "e4m3", False, seed, q_mult)
+    return w, I.fp8_inputs(w)
+
+
+def _decoded(oracle_mod, f):
+    B, H, N, d = f.q.shape
+    q = oracle_mod.decode_e4m3(f.q) * np.float64(f.q_scale)
+    ks = np.repeat(f.k_scales.astype(np.float64), 128, axis=2)[:, :, :N, None]
+    k = oracle_mod.decode_e4m3(f.k) * ks
+    v = oracle_mod.decode_e4m3(f.vt[..., :N]).transpose(0, 1, 3, 2) * np.float64(f.v_scale)
+    return q, k, v
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_oracle_matches_explicit_softmax(oracle_mod, causal):
+    w, f = _fp8_problem(11, 1, 2, 300)
+    o, lse, _ = oracle_mod.attn_fp8(f.q, f.k, f.vt, f.q_scale, f.k_scales, f.v_scale, causal,
+                                    w.scale)
+    q, k, v = _decoded(oracle_mod, f)
+    s = np.einsum("bhid,bhjd->bhij", q, k) * np.float64(np.float32(w.scale))
+    if causal:
+        s = np.where(np.tril(np.ones((w.N, w.N), bool)), s, -np.inf)
+    p = sps.softmax(s, axis=-1)
+    want_o = np.einsum("bhij,bhjd->bhid", p, v).reshape(-1, w.d)
+    want_l = sps.logsumexp(s, axis=-1).reshape(-1)
+    np.testing.assert_allclose(o, want_o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, want_l, rtol=0, atol=1e-12)
+
+
+def test_fp8_oracle_rows_equal_full(oracle_mod):
+    w, f = _fp8_problem(12, 2, 1, 200)
+    o, lse, b = oracle_mod.attn_fp8(f.q, f.k, f.vt, f.q_scale, f.k_scales, f.v_scale, True,
+                                    w.scale)
+    rows = np.array([0, 5, 199, 200, 333, 399])
+    o2, l2, b2 = oracle_mod.attn_fp8(f.q, f.k, f.vt, f.q_scale, f.k_scales, f.v_scale, True,
+                                     w.scale, rows=rows)
+    assert np.array_equal(o[rows], o2) and np.array_equal(lse[rows], l2)
+    assert np.array_equal(b[rows], b2)
+
+
+@pytest.mark.parametrize("shift", [0.0, 2.5, 8.0])
+@pytest.mark.parametrize("q_mult", [1.0, 3.0])
+def test_fp8_bound_covers_rounded_weights(oracle_mod, shift, q_mult):
+    # Simulate what the bound is about: weights on a scale whose largest value
+    # is 2^shift (shift in [0, 8]), each rounded to the nearest e4m3 value,
+    # O normalised by the unrounded sum. The bound must hold for every element
+    # and be far from vacuous.
+    w, f = _fp8_problem(13, 1, 2, 256, q_mult=q_mult)
+    o, lse, bound = oracle_mod.attn_fp8(f.q, f.k, f.vt, f.q_scale, f.k_scales, f.v_scale,
+                                        False, w.scale)
+    q, k, v = _decoded(oracle_mod, f)
+    s = np.einsum("bhid,bhjd->bhij", q, k) * np.float64(np.float32(w.scale))
+    p = np.exp(s - s.max(axis=-1, keepdims=True)) * 2.0 ** shift
+    p_rounded = oracle_mod.decode_e4m3(I.to_e4m3_bits(p))
+    o_q = np.einsum("bhij,bhjd->bhid", p_rounded, v) / p.sum(axis=-1)[..., None]
+    err = np.abs(o_q.reshape(-1, w.d) - o)
+    assert np.all(err <= bound + 1e-12)
+    assert float(bound.max()) < 0.5 and float(err.max()) > 0.0
