@@ -70,6 +70,10 @@ def _load():
                                             ctypes.POINTER(i64), i64, f64p, f64p, f64p,
                                             ctypes.c_int]
             lib.oracle_attn_fp8.restype = ctypes.c_int
+            lib.oracle_attn_bwd.argtypes = [u16p, u16p, u16p, u16p, ctypes.c_int, i64, i64, i64,
+                                            i64, ctypes.c_int, ctypes.c_float,
+                                            ctypes.POINTER(i64), i64] + [f64p] * 6 + [ctypes.c_int]
+            lib.oracle_attn_bwd.restype = ctypes.c_int
             lib.oracle_decode_e4m3.argtypes = [u8p, i64, f64p]
             lib.oracle_decode_e4m3.restype = None
             _lib = lib
@@ -191,3 +195,32 @@ def attn_fp8(q8: np.ndarray, k8: np.ndarray, vt8: np.ndarray, q_scale: float,
     if rc != 0:
         raise ValueError("oracle_attn_fp8 rejected its arguments")
     return o, lse, bound
+
+
+def attn_bwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, dout: np.ndarray, dtype: str,
+             causal: bool, scale: float, heads=None, nthreads: int = 0):
+    """Backward of the forward on [B, H, N, d] stored 16-bit inputs, for the
+    flat heads ``heads`` (bh indices; all heads when None), from the
+    definition (see bwd_head in attn_ref.cpp).
+
+    Returns a dict of float64 [nheads, N, d] arrays: dq, dk, dv and the
+    magnitude sums mag_dq, mag_dk, mag_dv.
+    """
+    assert q.shape == k.shape == v.shape == dout.shape and q.ndim == 4
+    B, H, N, d = q.shape
+    heads = np.arange(B * H) if heads is None else np.asarray(heads)
+    heads = np.ascontiguousarray(heads, dtype=np.int64)
+    q, qp = _u16(q)
+    k, kp = _u16(k)
+    v, vp = _u16(v)
+    dout, dp = _u16(dout)
+    names = ("dq", "dk", "dv", "mag_dq", "mag_dk", "mag_dv")
+    out = {n: np.empty((heads.size, N, d), dtype=np.float64) for n in names}
+    f64 = ctypes.POINTER(ctypes.c_double)
+    rc = _load().oracle_attn_bwd(qp, kp, vp, dp, DTYPE_CODES[dtype], B, H, N, d,
+                                 int(bool(causal)), float(np.float32(scale)),
+                                 heads.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), heads.size,
+                                 *[out[n].ctypes.data_as(f64) for n in names], nthreads)
+    if rc != 0:
+        raise ValueError("oracle_attn_bwd rejected its arguments")
+    return out

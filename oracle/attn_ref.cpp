@@ -303,4 +303,100 @@ void oracle_decode_e4m3(const uint8_t* x, int64_t n, double* out) {
   for (int64_t t = 0; t < n; ++t) out[t] = decode_e4m3(x[t]);
 }
 
+// Backward pass of one (batch, head), from the definition. With
+//   P_ij = exp(s_ij - LSE_i) (the softmax weights, j in J(i)),
+//   O_i = sum_j P_ij v_j and a loss whose gradient at O is dO:
+//   dV_j  = sum_i P_ij dO_i
+//   dP_ij = dO_i . v_j
+//   dS_ij = P_ij (dP_ij - D_i),   D_i = sum_j P_ij dP_ij = dO_i . O_i
+//   dQ_i  = scale * sum_j dS_ij k_j
+//   dK_j  = scale * sum_i dS_ij q_i
+// (the chain rule through s = scale q.k and the softmax Jacobian
+// diag(P) - P P^T; sources: the Flash Attention 2 discussion of
+// "TCA 51%, MFU below 8%" names the recomputation of P from the saved
+// logsumexp, which is why the forward emits the LSE).
+// Besides the gradients, mag_* hold the sums of the magnitudes of the terms
+// of each element (sum_i |P_ij dO_it| for dV, scale * sum_j |dS_ij k_jt| for
+// dQ, scale * sum_i |dS_ij q_it| for dK) and mag_ds_* the same with |dS_ij|
+// replaced by P_ij (|dP_ij| + |D_i|): the scale of the rounding errors a
+// 16-bit P and dS introduce.
+void bwd_head(const double* Q, const double* K, const double* V, const double* dO,
+              int64_t N, int64_t d, bool causal, double scale, double* dq, double* dk,
+              double* dv, double* mq, double* mk, double* mv) {
+  std::vector<double> s(N), P(N * N, 0.0), dS(N * N, 0.0), DS(N * N, 0.0), o(d);
+  for (int64_t i = 0; i < N; ++i) {
+    const int64_t nk = causal ? i + 1 : N;
+    double m = -INFINITY;
+    for (int64_t j = 0; j < nk; ++j) {
+      double dot = 0.0;
+      for (int64_t t = 0; t < d; ++t) dot += Q[i * d + t] * K[j * d + t];
+      s[j] = scale * dot;
+      m = std::max(m, s[j]);
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j < nk; ++j) l += std::exp(s[j] - m);
+    const double lse = m + std::log(l);
+    for (int64_t t = 0; t < d; ++t) o[t] = 0.0;
+    for (int64_t j = 0; j < nk; ++j) {
+      P[i * N + j] = std::exp(s[j] - lse);
+      for (int64_t t = 0; t < d; ++t) o[t] += P[i * N + j] * V[j * d + t];
+    }
+    double Di = 0.0;
+    for (int64_t t = 0; t < d; ++t) Di += dO[i * d + t] * o[t];
+    for (int64_t j = 0; j < nk; ++j) {
+      double dp = 0.0;
+      for (int64_t t = 0; t < d; ++t) dp += dO[i * d + t] * V[j * d + t];
+      dS[i * N + j] = P[i * N + j] * (dp - Di);
+      DS[i * N + j] = P[i * N + j] * (std::fabs(dp) + std::fabs(Di));
+    }
+  }
+  for (int64_t x = 0; x < N * d; ++x) dq[x] = dk[x] = dv[x] = mq[x] = mk[x] = mv[x] = 0.0;
+  for (int64_t i = 0; i < N; ++i) {
+    const int64_t nk = causal ? i + 1 : N;
+    for (int64_t j = 0; j < nk; ++j) {
+      const double p = P[i * N + j], ds = dS[i * N + j], ads = DS[i * N + j];
+      for (int64_t t = 0; t < d; ++t) {
+        dv[j * d + t] += p * dO[i * d + t];
+        mv[j * d + t] += std::fabs(p * dO[i * d + t]);
+        dq[i * d + t] += scale * ds * K[j * d + t];
+        mq[i * d + t] += scale * ads * std::fabs(K[j * d + t]);
+        dk[j * d + t] += scale * ds * Q[i * d + t];
+        mk[j * d + t] += scale * ads * std::fabs(Q[i * d + t]);
+      }
+    }
+  }
+}
+
+// Backward for the heads listed in `heads` (flat bh indices): q, k, v, dout
+// are [B][H][N][d] stored 16-bit values; outputs are [nheads][N][d] double
+// (gradients and magnitude sums, see bwd_head). Returns 0, or -1 on bad
+// arguments.
+int oracle_attn_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* dout,
+                    int dtype, int64_t B, int64_t H, int64_t N, int64_t d, int causal,
+                    float scale, const int64_t* heads, int64_t nheads, double* dq, double* dk,
+                    double* dv, double* mq, double* mk, double* mv, int nthreads) {
+  if (!q || !k || !v || !dout || !heads || !dq || !dk || !dv || !mq || !mk || !mv || B <= 0 ||
+      H <= 0 || N <= 0 || d <= 0 || nheads < 0 || (dtype != 0 && dtype != 1))
+    return -1;
+  for (int64_t r = 0; r < nheads; ++r)
+    if (heads[r] < 0 || heads[r] >= B * H) return -1;
+  const double sc = static_cast<double>(scale);
+  const int T = static_cast<int>(
+      std::max<int64_t>(1, std::min<int64_t>(pick_threads(nthreads), nheads)));
+  run_parallel(T, [&](int w, int nt) {
+    std::vector<double> Q(N * d), K(N * d), V(N * d), dO(N * d);
+    for (int64_t r = w; r < nheads; r += nt) {
+      const int64_t base = heads[r] * N * d;
+      decode_block(q + base, N * d, dtype, Q.data());
+      decode_block(k + base, N * d, dtype, K.data());
+      decode_block(v + base, N * d, dtype, V.data());
+      decode_block(dout + base, N * d, dtype, dO.data());
+      const int64_t off = r * N * d;
+      bwd_head(Q.data(), K.data(), V.data(), dO.data(), N, d, causal != 0, sc, dq + off,
+               dk + off, dv + off, mq + off, mk + off, mv + off);
+    }
+  });
+  return 0;
+}
+
 }  // extern "C"
