@@ -316,14 +316,16 @@ void oracle_decode_e4m3(const uint8_t* x, int64_t n, double* out) {
 // "TCA 51%, MFU below 8%" names the recomputation of P from the saved
 // logsumexp, which is why the forward emits the LSE).
 // Besides the gradients, mag_* hold the sums of the magnitudes of the terms
-// of each element (sum_i |P_ij dO_it| for dV, scale * sum_j |dS_ij k_jt| for
-// dQ, scale * sum_i |dS_ij q_it| for dK) and mag_ds_* the same with |dS_ij|
-// replaced by P_ij (|dP_ij| + |D_i|): the scale of the rounding errors a
-// 16-bit P and dS introduce.
+// of each element: sum_i |P_ij dO_it| for dV; for dQ and dK the sums
+// scale * sum_j A_ij |k_jt| and scale * sum_i A_ij |q_it| with
+//   A_ij = P_ij (sum_t |dO_it v_jt| + sum_t |dO_it| sum_j' P_ij' |v_j't|),
+// the magnitudes of the terms of dP_ij and of D_i (through the terms of O_i).
+// Rounding P, dS or O to a 16-bit format perturbs an element by a multiple
+// of the unit roundoff times these sums, even where dP_ij - D_i cancels.
 void bwd_head(const double* Q, const double* K, const double* V, const double* dO,
               int64_t N, int64_t d, bool causal, double scale, double* dq, double* dk,
               double* dv, double* mq, double* mk, double* mv) {
-  std::vector<double> s(N), P(N * N, 0.0), dS(N * N, 0.0), DS(N * N, 0.0), o(d);
+  std::vector<double> s(N), P(N * N, 0.0), dS(N * N, 0.0), DS(N * N, 0.0), o(d), ao(d);
   for (int64_t i = 0; i < N; ++i) {
     const int64_t nk = causal ? i + 1 : N;
     double m = -INFINITY;
@@ -336,18 +338,28 @@ void bwd_head(const double* Q, const double* K, const double* V, const double* d
     double l = 0.0;
     for (int64_t j = 0; j < nk; ++j) l += std::exp(s[j] - m);
     const double lse = m + std::log(l);
-    for (int64_t t = 0; t < d; ++t) o[t] = 0.0;
+    for (int64_t t = 0; t < d; ++t) o[t] = ao[t] = 0.0;
     for (int64_t j = 0; j < nk; ++j) {
       P[i * N + j] = std::exp(s[j] - lse);
-      for (int64_t t = 0; t < d; ++t) o[t] += P[i * N + j] * V[j * d + t];
+      for (int64_t t = 0; t < d; ++t) {
+        o[t] += P[i * N + j] * V[j * d + t];
+        ao[t] += P[i * N + j] * std::fabs(V[j * d + t]);
+      }
     }
-    double Di = 0.0;
-    for (int64_t t = 0; t < d; ++t) Di += dO[i * d + t] * o[t];
+    // D_i = dO_i . O_i; its term magnitude sums |dO_it| over the terms of O_it
+    double Di = 0.0, aDi = 0.0;
+    for (int64_t t = 0; t < d; ++t) {
+      Di += dO[i * d + t] * o[t];
+      aDi += std::fabs(dO[i * d + t]) * ao[t];
+    }
     for (int64_t j = 0; j < nk; ++j) {
-      double dp = 0.0;
-      for (int64_t t = 0; t < d; ++t) dp += dO[i * d + t] * V[j * d + t];
+      double dp = 0.0, adp = 0.0;
+      for (int64_t t = 0; t < d; ++t) {
+        dp += dO[i * d + t] * V[j * d + t];
+        adp += std::fabs(dO[i * d + t] * V[j * d + t]);
+      }
       dS[i * N + j] = P[i * N + j] * (dp - Di);
-      DS[i * N + j] = P[i * N + j] * (std::fabs(dp) + std::fabs(Di));
+      DS[i * N + j] = P[i * N + j] * (adp + aDi);
     }
   }
   for (int64_t x = 0; x < N * d; ++x) dq[x] = dk[x] = dv[x] = mq[x] = mk[x] = mv[x] = 0.0;
