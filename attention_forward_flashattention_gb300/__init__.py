@@ -73,6 +73,11 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         if hasattr(lib, "fa_fwd_fp8"):
             lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, f, i, f, vp]
             lib.fa_fwd_fp8.restype = i
+        if hasattr(lib, "fa_bwd"):
+            lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+            lib.fa_bwd.restype = i
+            lib.fa_bwd_workspace_size.argtypes = [i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
+            lib.fa_bwd_workspace_size.restype = i
         lib.fa_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
         lib.fa_fwd_noalloc.restype = i
         lib.fa_check.argtypes = [vp]
@@ -121,6 +126,22 @@ def fa_fwd_fp8(q: int, k: int, vt: int, o: int, lse: int, B: int, H: int, N: int
     """Same arguments as the C function (device pointers as ints); returns the status."""
     return load_library().fa_fwd_fp8(q, k, vt, o, lse, B, H, N, d, ldv, float(q_scale), k_scales,
                                      float(v_scale), int(bool(causal)), float(scale), stream)
+
+
+def fa_bwd(q: int, k: int, v: int, o: int, dout: int, lse: int, dq: int, dk: int, dv: int,
+           workspace: int, B: int, H: int, N: int, d: int, causal: bool, scale: float,
+           dtype: int, stream: int = 0) -> int:
+    """Same arguments as the C function (device pointers as ints); returns the status."""
+    return load_library().fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, B, H, N, d,
+                                 int(bool(causal)), float(scale), int(dtype), stream)
+
+
+def fa_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    n = ctypes.c_size_t(0)
+    rc = load_library().fa_bwd_workspace_size(B, H, N, d, ctypes.byref(n))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd_workspace_size")
+    return int(n.value)
 
 
 def fa_fwd_noalloc(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, d: int,
@@ -246,3 +267,29 @@ def attention_forward_fp8(q8, k8, vt8, q_scale: float, k_scales, v_scale: float,
     attention_forward_fp8_into(q8, k8, vt8, o, lse, q_scale, k_scales, v_scale, causal, scale,
                                stream)
     return o, lse
+
+
+def attention_backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,
+                       stream=None):
+    """Gradients (dq, dk, dv) of the forward at q, k, v for the output
+    gradient dout; o and lse are the forward's outputs. All [B, H, N, d]
+    contiguous CUDA tensors of one dtype (fp16 / bf16), lse [B, H, N] float32."""
+    import torch
+    B, H, N, d = q.shape
+    for t in (k, v, o, dout):
+        if tuple(t.shape) != (B, H, N, d) or t.dtype != q.dtype:
+            raise ValueError("q, k, v, o, dout must share shape [B, H, N, d] and dtype")
+    for t in (q, k, v, o, dout, lse):
+        if not (t.is_cuda and t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    ws = torch.empty(fa_bwd_workspace_size(B, H, N, d) // 4, dtype=torch.float32,
+                     device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    rc = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws.data_ptr(),
+                B, H, N, d, causal, scale, _dtype_code(q), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd")
+    return dq, dk, dv

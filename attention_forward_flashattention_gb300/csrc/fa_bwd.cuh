@@ -1,0 +1,575 @@
+// Fused attention backward for sm_103a: dQ, dK, dV of the forward, with the
+// softmax weights recomputed from the forward's row logsumexp (the reason the
+// forward emits it: "TCA 51%, MFU below 8%", Flash Attention 2 section).
+//
+// With P_ij = exp(scale q_i.k_j - LSE_i), D_i = dO_i . O_i:
+//   dV_j = sum_i P_ij dO_i            dP_ij = dO_i . v_j
+//   dS_ij = P_ij (dP_ij - D_i)        dQ_i = scale sum_j dS_ij k_j
+//   dK_j = scale sum_i dS_ij q_i
+//
+// Three launches, no atomics, deterministic:
+//   1. bwd_prep_kernel: D_i and LSE_i * log2(e) into a workspace padded to
+//      128-row tiles (padding rows: D = 0, lse2 = +inf, so their weights are 0).
+//   2. bwd_dkdv_kernel: one unit = one 128-key tile of one head; it loops over
+//      the 128-row query tiles that see it. Per query tile i (TMEM, lane = key):
+//        S^T = K Q_i^T, dP^T = V dO_i^T           (both operands in smem)
+//        P^T = 2^(c S^T - lse2_i)  -> 16 bit over the S^T columns
+//        dV += P^T dO_i                           (A = P^T from TMEM)
+//        dS^T = P^T (dP^T - D_i)   -> 16 bit over the dP^T columns
+//        dK += dS^T Q_i                           (A = dS^T from TMEM)
+//      dK and dV accumulate in TMEM; the epilogue scales dK and stores both.
+//   3. bwd_dq_kernel: one unit = one 128-row query tile; it loops over the key
+//      tiles it sees. Per key tile j (lane = query row):
+//        S = Q K_j^T, dP = dO V_j^T
+//        P = 2^(c S - lse2), dS = P (dP - D)  -> 16 bit over the S columns
+//        dQ += dS K_j                             (A = dS from TMEM)
+//
+// Roles (12 warps): warp 0 TMA producer (lane 0), warp 1 TMEM owner and MMA
+// issuer (lane 0), warpgroup 1 the element-wise softmax gradient (one thread
+// per TMEM lane), warpgroup 2 the epilogue. Every wait is bounded as in the
+// forward (abort flag, status bits, drain before TMEM is freed).
+#pragma once
+
+#include <cuda.h>
+
+#include "fa.h"
+#include "fa_common.cuh"
+
+namespace fa {
+
+struct BwdArgs {
+  void* dq;               // [BH][N][D] outputs, 16-bit
+  void* dk;
+  void* dv;
+  const float* lse2;      // workspace [BH][n_t * 128]: LSE * log2(e), +inf past N
+  const float* delta;     // workspace [BH][n_t * 128]: D = dO . O, 0 past N
+  uint32_t* status;
+  int N;
+  int H;
+  int BH;
+  int n_t;                // 128-row tiles per head: ceil(N / 128)
+  int n_units;            // BH * n_t
+  float scale_log2;       // scale * log2(e)
+  float scale;
+};
+
+constexpr int kBwdThreads = 384;
+// setmaxnreg split: the 384-thread launch gives 168 registers per thread
+// (65536 / 384, rounded down to a multiple of 8); the three warpgroups move
+// to 64 / 256 / 184, which sum to the same 3 x 168.
+constexpr uint32_t kBwdRegsLaunch = 168;
+constexpr uint32_t kBwdRegsWG0 = 64, kBwdRegsElem = 256, kBwdRegsEpi = 184;
+static_assert(kBwdRegsWG0 + kBwdRegsElem + kBwdRegsEpi == 3 * kBwdRegsLaunch, "register split");
+static_assert(kBwdRegsLaunch == (65536 / kBwdThreads) / 8 * 8, "launch allocation");
+
+template <int D>
+struct BwdLayout {
+  static constexpr int kPanels = D / 64;
+  static constexpr int kTileBytes = kPanels * kPanelBytes;  // a 128-row tile of Q, K, V, dO
+  static constexpr int kStages = (D == 128) ? 2 : 4;       // ring slots (two tiles + vectors each)
+  static constexpr int kVecBytes = 2 * 128 * 4;            // lse2 and D of one query tile
+  static constexpr int kStageBytes = 2 * kTileBytes + kVecBytes;
+  static constexpr int kOffFix = 0;                         // two fixed tiles (K, V or Q, dO)
+  static constexpr int kOffRing = 2 * kTileBytes;
+  static constexpr int kOffBar = kOffRing + kStages * kStageBytes;
+  static constexpr int kSmemBytes = kOffBar + 512 + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kStageBytes % 1024 == 0, "stages keep tiles 1024-byte aligned");
+  // TMEM columns: two 128-column fp32 scratch tiles, then the accumulators.
+  static constexpr uint32_t kColA = 0;    // S^T (dkdv) / S (dq); 16-bit P^T / dS over its first 64
+  static constexpr uint32_t kColB = 128;  // dP^T (dkdv) / dP (dq); dS^T over its first 64 (dkdv)
+  static constexpr uint32_t kColAcc0 = 256;      // dV (dkdv) / dQ (dq)
+  static constexpr uint32_t kColAcc1 = 256 + D;  // dK (dkdv)
+};
+
+enum BwdBar : int {
+  kBbFixFull = 0,    // the unit's two fixed tiles landed
+  kBbFixEmpty = 1,   // MMA: the unit's last use of the fixed tiles done
+  kBbAFull = 2,      // MMA: scratch A (S^T / S) ready
+  kBbBFull = 3,      // MMA: scratch B (dP^T / dP) ready
+  kBbPFull = 4,      // element-wise (4 warps): P^T in TMEM (dkdv only)
+  kBbDsFull = 5,     // element-wise (4 warps): dS^T / dS in TMEM
+  kBbAccFull = 6,    // MMA: the unit's accumulators final
+  kBbAccFree = 7,    // epilogue (4 warps): accumulators read
+  kBbDrain = 8,      // MMA: all tcgen05 ops done
+  kBbRing = 9,       // [stages] full, then [stages] empty
+};
+constexpr int kBwdSlotTmem = 480;
+constexpr int kBwdSlotAbort = 484;
+
+// D_i and LSE_i * log2(e) into the tile-padded workspace. One thread per
+// padded row (grid covers BH * n_t * 128 rows).
+template <int D, bool BF16>
+__global__ void bwd_prep_kernel(const void* o, const void* dout, const float* lse, float* lse2,
+                                float* delta, int N, int n_t, long long rows) {
+  const long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (g >= rows) return;
+  const long long bh = g / (static_cast<long long>(n_t) * 128);
+  const int i = static_cast<int>(g - bh * n_t * 128);
+  if (i >= N) {
+    lse2[g] = INFINITY;
+    delta[g] = 0.f;
+    return;
+  }
+  const size_t row = static_cast<size_t>(bh) * N + i;
+  const uint4* po = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(o) + row * D);
+  const uint4* pd = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(dout) + row * D);
+  float acc = 0.f;
+#pragma unroll 4
+  for (int c = 0; c < D / 8; ++c) {
+    const uint4 a = po[c], b = pd[c];
+    const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float a0, a1, b0, b1;
+      if constexpr (BF16) {
+        a0 = __uint_as_float(wa[e] << 16);
+        a1 = __uint_as_float(wa[e] & 0xFFFF0000u);
+        b0 = __uint_as_float(wb[e] << 16);
+        b1 = __uint_as_float(wb[e] & 0xFFFF0000u);
+      } else {
+        const __half2 ha = *reinterpret_cast<const __half2*>(&wa[e]);
+        const __half2 hb = *reinterpret_cast<const __half2*>(&wb[e]);
+        const float2 fa = __half22float2(ha), fb = __half22float2(hb);
+        a0 = fa.x;
+        a1 = fa.y;
+        b0 = fb.x;
+        b1 = fb.y;
+      }
+      acc = fmaf(a0, b0, acc);
+      acc = fmaf(a1, b1, acc);
+    }
+  }
+  delta[g] = acc;
+  lse2[g] = lse[row] * 1.4426950408889634f;
+}
+
+// Unit order: causal problems longest first, odd rounds reversed (as the
+// forward); otherwise head-major. A dkdv unit of key tile t sees the query
+// tiles t.. n_t-1 (causal), a dq unit of query tile t the key tiles 0..t.
+template <bool CAUSAL, bool KEYS>
+__device__ __forceinline__ bool bwd_next_unit(int& round, const BwdArgs& a, int& bh, int& t) {
+  const int G = static_cast<int>(gridDim.x);
+  for (;;) {
+    const long long base = static_cast<long long>(round) * G;
+    if (base >= a.n_units) return false;
+    int c = static_cast<int>(blockIdx.x);
+    if (CAUSAL && (round & 1)) c = G - 1 - c;
+    const long long u = base + c;
+    ++round;
+    if (u >= a.n_units) continue;
+    if (CAUSAL) {
+      const int lvl = static_cast<int>(u / a.BH);
+      bh = static_cast<int>(u - static_cast<long long>(lvl) * a.BH);
+      t = KEYS ? lvl : a.n_t - 1 - lvl;
+    } else {
+      bh = static_cast<int>(u / a.n_t);
+      t = static_cast<int>(u - static_cast<long long>(bh) * a.n_t);
+    }
+    return true;
+  }
+}
+
+// The streamed tiles of a unit: [first, last] (query tiles for dkdv, key tiles for dq).
+template <bool CAUSAL, bool KEYS>
+__device__ __forceinline__ void bwd_span(const BwdArgs& a, int t, int& first, int& last) {
+  if (KEYS) {
+    first = CAUSAL ? t : 0;
+    last = a.n_t - 1;
+  } else {
+    first = 0;
+    last = CAUSAL ? t : a.n_t - 1;
+  }
+}
+
+// TMA producer (one thread). KEYS (dK/dV): fixed K, V; streamed Q, dO and the
+// tile's lse2 / D vectors. Otherwise (dQ): fixed Q, dO; streamed K, V.
+template <int D, bool CAUSAL, bool KEYS>
+__device__ __forceinline__ void bwd_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                                             const CUtensorMap* tm_v, const CUtensorMap* tm_do,
+                                             const BwdArgs& a, uint32_t sbase, uint32_t bars,
+                                             const AbortCtx& ab) {
+  using L = BwdLayout<D>;
+  constexpr int S = L::kStages;
+  auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
+  const CUtensorMap* fix0 = KEYS ? tm_k : tm_q;
+  const CUtensorMap* fix1 = KEYS ? tm_v : tm_do;
+  const CUtensorMap* str0 = KEYS ? tm_q : tm_k;
+  const CUtensorMap* str1 = KEYS ? tm_do : tm_v;
+  for (const CUtensorMap* m : {tm_q, tm_k, tm_v, tm_do}) ptx::prefetch_tmap(m);
+  auto load_tile = [&](uint32_t dst, const CUtensorMap* tm, uint32_t b, int row, int hh, int bb) {
+    for (int p = 0; p < L::kPanels; ++p)
+      ptx::tma_load_4d(dst + p * kPanelBytes, tm, b, 64 * p, row, hh, bb);
+  };
+  uint32_t ring = 0, units = 0;
+  int round = 0, bh = 0, t = 0;
+  bool ok = true;
+  while (ok && bwd_next_unit<CAUSAL, KEYS>(round, a, bh, t)) {
+    int first, last;
+    bwd_span<CAUSAL, KEYS>(a, t, first, last);
+    const int hh = bh % a.H, bb = bh / a.H;
+    if (!(ok = wait_spin(bar(kBbFixEmpty), (units & 1u) ^ 1u, ab, kStatusProducer))) break;
+    ptx::mbar_arrive_expect_tx(bar(kBbFixFull), 2 * L::kTileBytes);
+    load_tile(sbase + L::kOffFix, fix0, bar(kBbFixFull), 128 * t, hh, bb);
+    load_tile(sbase + L::kOffFix + L::kTileBytes, fix1, bar(kBbFixFull), 128 * t, hh, bb);
+    ++units;
+    for (int st = first; st <= last && ok; ++st) {
+      const uint32_t slot = ring % S, ph = (ring / S) & 1u;
+      if (!(ok = wait_spin(bar(kBbRing + S + slot), ph ^ 1u, ab, kStatusProducer))) break;
+      const uint32_t dst = sbase + L::kOffRing + slot * L::kStageBytes;
+      ptx::mbar_arrive_expect_tx(bar(kBbRing + slot),
+                                 2 * L::kTileBytes + (KEYS ? L::kVecBytes : 0));
+      load_tile(dst, str0, bar(kBbRing + slot), 128 * st, hh, bb);
+      load_tile(dst + L::kTileBytes, str1, bar(kBbRing + slot), 128 * st, hh, bb);
+      if constexpr (KEYS) {
+        const size_t v0 = (static_cast<size_t>(bh) * a.n_t + st) * 128;
+        ptx::bulk_load(dst + 2 * L::kTileBytes, a.lse2 + v0, 512, bar(kBbRing + slot));
+        ptx::bulk_load(dst + 2 * L::kTileBytes + 512, a.delta + v0, 512, bar(kBbRing + slot));
+      }
+      ++ring;
+    }
+  }
+  if (!ok) {  // let the copies already issued land before the CTA exits
+    for (uint32_t sl = 0; sl < static_cast<uint32_t>(S) && sl < ring; ++sl) {
+      const uint32_t lastp = ring - 1 - ((ring - 1 - sl) % S);
+      wait_drain(bar(kBbRing + sl), (lastp / S) & 1u, ab, kStatusDrain);
+    }
+    if (units > 0) wait_drain(bar(kBbFixFull), (units - 1) & 1u, ab, kStatusDrain);
+  }
+}
+
+// The single MMA-issuing thread (see the order at the top of this file).
+template <int D, bool BF16, bool CAUSAL, bool KEYS>
+__device__ __forceinline__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32_t bars,
+                                        uint32_t tmem, const AbortCtx& ab) {
+  using L = BwdLayout<D>;
+  constexpr int S = L::kStages;
+  auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
+  const uint32_t tA = tmem + L::kColA, tB = tmem + L::kColB;
+  const uint32_t tAcc0 = tmem + L::kColAcc0, tAcc1 = tmem + L::kColAcc1;
+  const uint32_t fix0 = sbase + L::kOffFix, fix1 = fix0 + L::kTileBytes;
+  auto stage = [&](uint32_t r) { return sbase + L::kOffRing + (r % S) * L::kStageBytes; };
+  auto ring_wait = [&](uint32_t r) {
+    return wait_spin(bar(kBbRing + r % S), (r / S) & 1u, ab, kStatusMma);
+  };
+  // The two scratch products of streamed tile r: S^T = K Q^T, dP^T = V dO^T
+  // (dK/dV) or S = Q K^T, dP = dO V^T (dQ); all operands K-major.
+  auto scratch_a = [&](uint32_t r) {
+    issue_qk<D, BF16>(tA, fix0, stage(r));
+    ptx::umma_commit(bar(kBbAFull));
+  };
+  auto scratch_b = [&](uint32_t r) {
+    issue_qk<D, BF16>(tB, fix1, stage(r) + L::kTileBytes);
+    ptx::umma_commit(bar(kBbBFull));
+  };
+  uint32_t ring = 0, units = 0, cnt = 0;
+  int round = 0, bh = 0, t = 0;
+  bool ok = true;
+  while (ok && bwd_next_unit<CAUSAL, KEYS>(round, a, bh, t)) {
+    int first, last;
+    bwd_span<CAUSAL, KEYS>(a, t, first, last);
+    if (!(ok = wait_spin(bar(kBbFixFull), units & 1u, ab, kStatusMma))) break;
+    if (!(ok = ring_wait(ring))) break;
+    ptx::tc_fence_after();
+    scratch_a(ring);
+    scratch_b(ring);
+    for (int st = first; st <= last; ++st) {
+      const uint32_t r = ring++;
+      const uint32_t ph = (cnt++) & 1u;
+      const bool acc = st > first;
+      const bool more = st < last;
+      if constexpr (KEYS) {
+        // dV += P^T dO (P^T in TMEM over the S^T columns; dO used MN-major)
+        if (!(ok = wait_spin(bar(kBbPFull), ph, ab, kStatusMma))) break;
+        if (!acc && units > 0 &&
+            !(ok = wait_spin(bar(kBbAccFree), (units - 1) & 1u, ab, kStatusMma)))
+          break;
+        ptx::tc_fence_after();
+        issue_pv_ts<D, BF16>(tAcc0, tA, stage(r) + L::kTileBytes, acc);
+        if (more) {  // the next S^T while the element-wise role forms dS^T
+          if (!(ok = ring_wait(ring))) break;
+          scratch_a(ring);
+        }
+        // dK += dS^T Q (dS^T in TMEM over the dP^T columns; Q used MN-major)
+        if (!(ok = wait_spin(bar(kBbDsFull), ph, ab, kStatusMma))) break;
+        ptx::tc_fence_after();
+        issue_pv_ts<D, BF16>(tAcc1, tB, stage(r), acc);
+        ptx::umma_commit(bar(kBbRing + S + r % S));
+        if (more) scratch_b(ring);
+      } else {
+        // dQ += dS K (dS in TMEM over the S columns; K used MN-major)
+        if (!(ok = wait_spin(bar(kBbDsFull), ph, ab, kStatusMma))) break;
+        if (!acc && units > 0 &&
+            !(ok = wait_spin(bar(kBbAccFree), (units - 1) & 1u, ab, kStatusMma)))
+          break;
+        ptx::tc_fence_after();
+        issue_pv_ts<D, BF16>(tAcc0, tA, stage(r), acc);
+        ptx::umma_commit(bar(kBbRing + S + r % S));
+        if (more) {
+          if (!(ok = ring_wait(ring))) break;
+          scratch_a(ring);
+          scratch_b(ring);
+        }
+      }
+    }
+    if (!ok) break;
+    ptx::umma_commit(bar(kBbAccFull));
+    ptx::umma_commit(bar(kBbFixEmpty));
+    ++units;
+  }
+  ptx::umma_commit(bar(kBbDrain));
+  wait_drain(bar(kBbDrain), 0u, ab, kStatusDrain);
+}
+
+// Unpacks the 16-bit pair w to two floats.
+template <bool BF16>
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+  if constexpr (BF16) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+  } else {
+    const __half2 h = *reinterpret_cast<const __half2*>(&w);
+    return __half22float2(h);
+  }
+}
+
+// Element-wise softmax gradient, one thread per TMEM lane (row r of the
+// 128-row scratch tiles). KEYS (dK/dV): the row is key k = 128 t + r, the
+// columns are the queries of the streamed tile, whose lse2 / D come from the
+// stage's vectors. Otherwise (dQ): the row is query q = 128 t + r, the columns
+// are keys, lse2 / D are the row's own.
+template <int D, bool BF16, bool CAUSAL, bool KEYS>
+__device__ __forceinline__ void bwd_elementwise(const BwdArgs& a, uint32_t sbase, uint32_t bars,
+                                                uint32_t tmem, const AbortCtx& ab, int warp,
+                                                int lane) {
+  using L = BwdLayout<D>;
+  constexpr int S = L::kStages;
+  auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
+  const int r = (warp & 3) * 32 + lane;
+  const uint32_t tl = ptx::tmem_lane_base(tmem, warp);
+  const uint32_t tA = tl + L::kColA, tB = tl + L::kColB;
+  const float cl2 = a.scale_log2;
+  uint32_t ring = 0, cnt = 0;
+  int round = 0, bh = 0, t = 0;
+  bool ok = true;
+  while (ok && bwd_next_unit<CAUSAL, KEYS>(round, a, bh, t)) {
+    int first, last;
+    bwd_span<CAUSAL, KEYS>(a, t, first, last);
+    const int row = 128 * t + r;  // this thread's key (KEYS) or query
+    float my_lse2 = 0.f, my_d = 0.f;
+    if constexpr (!KEYS) {
+      const size_t v0 = (static_cast<size_t>(bh) * a.n_t + t) * 128 + r;
+      my_lse2 = a.lse2[v0];
+      my_d = a.delta[v0];
+    }
+    for (int st = first; st <= last; ++st) {
+      const uint32_t rr = ring++;
+      const uint32_t ph = (cnt++) & 1u;
+      // the stage's lse2 / D vectors (TMA-written): observe their barrier too
+      if (KEYS && !(ok = wait_bounded_warp(bar(kBbRing + rr % S), (rr / S) & 1u, ab,
+                                           kStatusSoftmax)))
+        break;
+      // ---- P: scores of this tile against the row's reference
+      if (!(ok = wait_bounded_warp(bar(kBbAFull), ph, ab, kStatusSoftmax))) break;
+      ptx::tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tA + 32u * c, sr[c]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) ptx::tmem_ld_wait(sr[c]);
+      const uint32_t vbase = sbase + L::kOffRing + (rr % S) * L::kStageBytes + 2 * L::kTileBytes;
+      uint32_t pk[2][32];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        float p[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int col = 2 * c + e;
+          const float sv = __uint_as_float(sr[col >> 5][col & 31]);
+          float ref;
+          bool keep;
+          if constexpr (KEYS) {
+            float l2;
+            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(l2) : "r"(vbase + 4u * col));
+            ref = l2;  // +inf past N: weight 0
+            keep = !CAUSAL || 128 * st + col >= row;
+          } else {
+            ref = my_lse2;
+            const int key = 128 * st + col;
+            keep = key < a.N && (!CAUSAL || key <= row);
+          }
+          p[e] = keep ? ptx::ex2(fmaf(sv, cl2, -ref)) : 0.f;
+        }
+        pk[c >> 5][c & 31] = pack2<BF16>(p[0], p[1]);
+      }
+      if constexpr (KEYS) {
+        // P^T to TMEM over the S^T columns, for dV += P^T dO
+        ptx::tmem_st32(tA, pk[0]);
+        ptx::tmem_st32(tA + 32u, pk[1]);
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar(kBbPFull));
+      }
+      // ---- dS = P (dP - D), 16-bit, over the first 64 columns of its tile
+      if (!(ok = wait_bounded_warp(bar(kBbBFull), ph, ab, kStatusSoftmax))) break;
+      ptx::tc_fence_after();
+      const uint32_t tDs = KEYS ? tB : tA;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t dp[2][32];
+        ptx::tmem_ld32(tB + 64u * h, dp[0]);
+        ptx::tmem_ld32(tB + 64u * h + 32u, dp[1]);
+        ptx::tmem_ld_wait(dp[0]);
+        ptx::tmem_ld_wait(dp[1]);
+        uint32_t ds[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float2 pv = unpack2<BF16>(pk[h][c]);
+          const int col = 64 * h + 2 * c;
+          float d0, d1;
+          if constexpr (KEYS) {
+            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(d0) : "r"(vbase + 512u + 4u * col));
+            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(d1) : "r"(vbase + 516u + 4u * col));
+          } else {
+            d0 = d1 = my_d;
+          }
+          const float g0 = pv.x * (__uint_as_float(dp[c >> 4][(2 * c) & 31]) - d0);
+          const float g1 = pv.y * (__uint_as_float(dp[c >> 4][(2 * c + 1) & 31]) - d1);
+          ds[c] = pack2<BF16>(g0, g1);
+        }
+        ptx::tmem_st32(tDs + 32u * h, ds);
+      }
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(kBbDsFull));
+    }
+  }
+}
+
+// Epilogue: the unit's accumulators (dV and dK, or dQ) from TMEM to global
+// memory; dK and dQ carry the score scale.
+template <int D, bool BF16, bool CAUSAL, bool KEYS>
+__device__ __forceinline__ void bwd_epilogue(const BwdArgs& a, uint32_t bars, uint32_t tmem,
+                                             const AbortCtx& ab, int warp, int lane) {
+  using L = BwdLayout<D>;
+  auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
+  const int r = (warp & 3) * 32 + lane;
+  const uint32_t tl = ptx::tmem_lane_base(tmem, warp);
+  uint32_t units = 0;
+  int round = 0, bh = 0, t = 0;
+  bool ok = true;
+  // tcgen05.ld is warp-collective (.sync.aligned): every lane loads, only the
+  // lanes of rows below N store.
+  auto store = [&](uint32_t tcol, void* base, size_t row, bool valid, float mul) {
+    uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(base) + row * D);
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t v[32];
+      ptx::tmem_ld32(tcol + 32u * c, v);
+      ptx::tmem_ld_wait(v);
+      uint32_t pk[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        pk[e] = pack2<BF16>(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+      if (valid) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          __stcs(orow + 4 * c + q,
+                 make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]));
+      }
+    }
+  };
+  while (ok && bwd_next_unit<CAUSAL, KEYS>(round, a, bh, t)) {
+    if (!(ok = wait_bounded_warp(bar(kBbAccFull), units & 1u, ab, kStatusEpilogue))) break;
+    ptx::tc_fence_after();
+    const int row = 128 * t + r;
+    const bool valid = row < a.N;
+    const size_t grow = static_cast<size_t>(bh) * a.N + (valid ? row : 0);
+    if constexpr (KEYS) {
+      store(tl + L::kColAcc0, a.dv, grow, valid, 1.f);
+      store(tl + L::kColAcc1, a.dk, grow, valid, a.scale);
+    } else {
+      store(tl + L::kColAcc0, a.dq, grow, valid, a.scale);
+    }
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(bar(kBbAccFree));
+    ++units;
+  }
+}
+
+// One backward kernel: KEYS = dK / dV, otherwise dQ. Maps: Q, K, V, dO.
+template <int D, bool BF16, bool CAUSAL, bool KEYS>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const BwdArgs a) {
+  using L = BwdLayout<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* sgen = smem_raw + (sbase - raw);
+  const uint32_t bars = sbase + L::kOffBar;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + L::kOffBar + kBwdSlotTmem);
+  volatile uint32_t* abort_flag =
+      reinterpret_cast<volatile uint32_t*>(sgen + L::kOffBar + kBwdSlotAbort);
+  const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
+  const AbortCtx ab{abort_flag, a.status};
+  auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar(kBbFixFull), 1);
+    ptx::mbar_init(bar(kBbFixEmpty), 1);
+    ptx::mbar_init(bar(kBbAFull), 1);
+    ptx::mbar_init(bar(kBbBFull), 1);
+    ptx::mbar_init(bar(kBbPFull), 4);
+    ptx::mbar_init(bar(kBbDsFull), 4);
+    ptx::mbar_init(bar(kBbAccFull), 1);
+    ptx::mbar_init(bar(kBbAccFree), 4);
+    ptx::mbar_init(bar(kBbDrain), 1);
+    for (int s = 0; s < L::kStages; ++s) {
+      ptx::mbar_init(bar(kBbRing + s), 1);
+      ptx::mbar_init(bar(kBbRing + L::kStages + s), 1);
+    }
+    *abort_flag = 0u;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int wgrp = warp >> 2;
+  if (wgrp == 0) {
+    ptx::setmaxnreg_to<kBwdRegsWG0, kBwdRegsLaunch>();
+    if (lane == 0) {
+      if (warp == 0) bwd_producer<D, CAUSAL, KEYS>(&tm_q, &tm_k, &tm_v, &tm_do, a, sbase, bars, ab);
+      else if (warp == 1) bwd_mma<D, BF16, CAUSAL, KEYS>(a, sbase, bars, tmem, ab);
+    }
+  } else if (wgrp == 1) {
+    ptx::setmaxnreg_to<kBwdRegsElem, kBwdRegsLaunch>();
+    bwd_elementwise<D, BF16, CAUSAL, KEYS>(a, sbase, bars, tmem, ab, warp, lane);
+  } else {
+    ptx::setmaxnreg_to<kBwdRegsEpi, kBwdRegsLaunch>();
+    bwd_epilogue<D, BF16, CAUSAL, KEYS>(a, bars, tmem, ab, warp, lane);
+  }
+  __syncwarp();
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc(tmem, 512);
+}
+
+// Host side (fa_bwd_d64.cu / fa_bwd_d128.cu): the three launches of one call.
+// maps: Q, K, V, dO ({d, N, H, B} 16-bit, 64 x 128 boxes); grid: persistent CTAs.
+cudaError_t launch_bwd_d64(bool bf16, bool causal, const CUtensorMap* maps, const BwdArgs& a,
+                           const void* o, const void* dout, const float* lse, int grid,
+                           cudaStream_t stream);
+cudaError_t launch_bwd_d128(bool bf16, bool causal, const CUtensorMap* maps, const BwdArgs& a,
+                            const void* o, const void* dout, const float* lse, int grid,
+                            cudaStream_t stream);
+
+}  // namespace fa

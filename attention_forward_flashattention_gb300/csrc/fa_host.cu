@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "fa.h"
+#include "fa_bwd.cuh"
 #include "fa_kernel.cuh"
 
 namespace fa {
@@ -307,6 +308,68 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* vt, void* o, floa
   (void)cudaGetLastError();
   const cudaError_t e =
       fa::launch_fwd_fp8(causal != 0, maps, a, grid, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_bwd_workspace_size(int B, int H, int N, int d, size_t* bytes) {
+  if (!bytes) return FA_ERR_INVALID_ARG;
+  const fa_status sz = fa::check_sizes(B, H, N, d);
+  if (sz != FA_OK) return sz;
+  const long long n_t = (static_cast<long long>(N) + 127) / 128;
+  *bytes = static_cast<size_t>(2LL * B * H * n_t * 128 * 4);
+  return FA_OK;
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv, void* workspace, int B, int H,
+                 int N, int d, int causal, float scale, fa_dtype dtype, void* stream) {
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace)
+    return FA_ERR_INVALID_ARG;
+  for (const void* p : {q, k, v, o, dout, static_cast<const void*>(lse),
+                        static_cast<const void*>(dq), static_cast<const void*>(dk),
+                        static_cast<const void*>(dv), static_cast<const void*>(workspace)})
+    if (!fa::aligned16(p)) return FA_ERR_INVALID_ARG;
+  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
+  const fa_status sz = fa::check_sizes(B, H, N, d);
+  if (sz != FA_OK) return sz;
+
+  int dev = 0;
+  fa::DeviceState* st = nullptr;
+  const fa_status ds = fa::current_device(&dev, &st, true);
+  if (ds != FA_OK) return ds;
+
+  const bool bf16 = dtype == FA_DTYPE_BF16;
+  const fa_strides c = fa::contiguous_strides(H, N, d);
+  CUtensorMap maps[4];
+  if (!fa::encode_qkv(&maps[0], q, c, bf16, B, H, N, d, 128) ||
+      !fa::encode_qkv(&maps[1], k, c, bf16, B, H, N, d, 128) ||
+      !fa::encode_qkv(&maps[2], v, c, bf16, B, H, N, d, 128) ||
+      !fa::encode_qkv(&maps[3], dout, c, bf16, B, H, N, d, 128))
+    return FA_ERR_CUDA;
+
+  fa::BwdArgs a{};
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.N = N;
+  a.H = H;
+  a.BH = B * H;
+  a.n_t = (N + 127) / 128;
+  a.n_units = a.BH * a.n_t;
+  const size_t vec = static_cast<size_t>(a.BH) * a.n_t * 128;
+  float* ws = static_cast<float*>(workspace);
+  a.lse2 = ws;
+  a.delta = ws + vec;
+  a.status = st->status;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.scale = scale;
+  const int grid = a.n_units < st->sm_count ? a.n_units : st->sm_count;
+
+  (void)cudaGetLastError();
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = d == 64 ? fa::launch_bwd_d64(bf16, causal != 0, maps, a, o, dout, lse, grid, s)
+                                : fa::launch_bwd_d128(bf16, causal != 0, maps, a, o, dout, lse, grid, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

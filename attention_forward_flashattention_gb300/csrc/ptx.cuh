@@ -92,6 +92,18 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint
       : "memory");
 }
 
+// Contiguous copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from global to shared memory, completing as transaction bytes on
+// `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // 4-D tiled load (same rules; coordinates innermost first).
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, uint32_t bar, int c0,
                                             int c1, int c2, int c3) {
@@ -412,6 +424,14 @@ __device__ __forceinline__ void setmaxnreg_inc() {
 template <uint32_t N>
 __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+// Moves the executing warpgroup from the launch allocation kLaunch to N
+// registers per thread: .inc when N is larger, .dec when smaller (each form
+// only moves one way).
+template <uint32_t N, uint32_t kLaunch>
+__device__ __forceinline__ void setmaxnreg_to() {
+  if constexpr (N > kLaunch) setmaxnreg_inc<N>();
+  else if constexpr (N < kLaunch) setmaxnreg_dec<N>();
 }
 
 // max(a, b, c) in one instruction.

@@ -23,6 +23,7 @@
 #ifndef FA_SM103_H
 #define FA_SM103_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -139,6 +140,40 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* vt, void* o, floa
                      int B, int H, int N, int d, int ldv, float q_scale,
                      const float* k_scales, float v_scale, int causal, float scale,
                      void* stream);
+
+/*
+ * fa_bwd - enqueue the backward pass of fa_fwd: gradients dq, dk, dv of a
+ * loss whose gradient at O is dout. The softmax weights are recomputed from
+ * the forward's lse (the reason the forward emits it; the Flash Attention 2
+ * section of "TCA 51%, MFU below 8%"):
+ *     P_ij = exp(scale q_i.k_j - lse_i),  D_i = dout_i . o_i
+ *     dv_j = sum_i P_ij dout_i,           dS_ij = P_ij (dout_i . v_j - D_i)
+ *     dq_i = scale sum_j dS_ij k_j,       dk_j = scale sum_i dS_ij q_i
+ * with j in J(i) as in fa_fwd.
+ *
+ * q, k, v, o, dout : device, contiguous [B][H][N][d] of `dtype` (o is the
+ *            forward's output for these q, k, v), read only.
+ * lse      : device, [B][H][N] float32, the forward's logsumexp.
+ * dq, dk, dv : device, contiguous [B][H][N][d] of `dtype`, written (fp32
+ *            accumulation, rounded to nearest even).
+ * workspace : device scratch of fa_bwd_workspace_size bytes, caller-owned; its
+ *            contents are overwritten (row logsumexps and D); it must not be
+ *            used by another call on another stream at the same time.
+ * All pointers 16-byte aligned. B, H, N, d, causal, scale, dtype, stream and
+ * the errors are as in fa_fwd. Three launches on `stream` (a pass forming D,
+ * one for dk / dv, one for dq); no atomics, bitwise reproducible. Tolerance
+ * of the 16-bit P and dS: see the library's tests.
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
+                 const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                 void* workspace, int B, int H, int N, int d, int causal, float scale,
+                 fa_dtype dtype, void* stream);
+
+/*
+ * fa_bwd_workspace_size - bytes of the workspace fa_bwd needs for these sizes
+ * (2 * B * H * ceil(N / 128) * 128 * 4). Host only; same size checks as fa_fwd.
+ */
+fa_status fa_bwd_workspace_size(int B, int H, int N, int d, size_t* bytes);
 
 /*
  * fa_fwd_noalloc - fa_fwd for callers that cannot allocate device memory.

@@ -19,8 +19,8 @@ def lib():
 
 def test_header_declares_expected_entry_points():
     names = fa.header_functions()
-    assert names == ["fa_fwd", "fa_fwd_strided", "fa_fwd_fp8", "fa_fwd_noalloc", "fa_check",
-                     "fa_query_launch",
+    assert names == ["fa_fwd", "fa_fwd_strided", "fa_fwd_fp8", "fa_bwd", "fa_bwd_workspace_size",
+                     "fa_fwd_noalloc", "fa_check", "fa_query_launch",
                      "fa_sm_clock_probe", "fa_status_string", "fa_version"]
 
 
@@ -164,3 +164,33 @@ def test_fp8_valid_arguments_reach_the_device(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert _fp8() in (fa.FA_ERR_CUDA, fa.FA_ERR_ARCH)
+
+
+def _bwd(**kw):
+    a = dict(q=GOOD, k=GOOD, v=GOOD, o=GOOD, dout=GOOD, lse=GOOD, dq=GOOD, dk=GOOD, dv=GOOD,
+             ws=GOOD, B=1, H=2, N=300, d=128, causal=0, scale=0.088, dtype=fa.FA_DTYPE_FP16)
+    a.update(kw)
+    return fa.fa_bwd(a["q"], a["k"], a["v"], a["o"], a["dout"], a["lse"], a["dq"], a["dk"],
+                     a["dv"], a["ws"], a["B"], a["H"], a["N"], a["d"], a["causal"], a["scale"],
+                     a["dtype"], 0)
+
+
+@pytest.mark.parametrize("kw", [dict(o=0), dict(dout=0), dict(lse=0), dict(dk=0), dict(ws=0),
+                                dict(dq=GOOD + 8), dict(ws=GOOD + 4), dict(scale=0.0),
+                                dict(dtype=3), dict(N=0)])
+def test_bwd_bad_arguments_rejected(lib, kw):
+    assert _bwd(**kw) == fa.FA_ERR_INVALID_ARG
+
+
+def test_bwd_unsupported_and_workspace_size(lib):
+    assert _bwd(d=96) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_bwd_workspace_size(2, 3, 300, 64) == 2 * 2 * 3 * 3 * 128 * 4
+    with pytest.raises(fa.FaError):
+        fa.fa_bwd_workspace_size(1, 1, 128, 96)
+
+
+def test_bwd_valid_arguments_reach_the_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _bwd() in (fa.FA_ERR_CUDA, fa.FA_ERR_ARCH)
