@@ -129,7 +129,8 @@ def to_bits(x: np.ndarray, dtype: str) -> np.ndarray:
 
 
 def tensor_bits(w: Workload, which: int, chunk: int = 1 << 22) -> np.ndarray:
-    """Stored 16-bit values of Q (0), K (1) or V (2) of workload ``w``: [B, H, N, d]."""
+    """Stored 16-bit values of Q (0), K (1), V (2) or the output gradient dO
+    (3) of workload ``w``: [B, H, N, d]."""
     n = w.B * w.H * w.N * w.d
     out = np.empty(n, dtype=np.uint16)
     seed = w.seed * 4 + which
@@ -146,6 +147,11 @@ def tensor_bits(w: Workload, which: int, chunk: int = 1 << 22) -> np.ndarray:
 def qkv_bits(w: Workload):
     """(Q, K, V) stored 16-bit values of workload ``w``."""
     return tensor_bits(w, 0), tensor_bits(w, 1), tensor_bits(w, 2)
+
+
+def dout_bits(w: Workload) -> np.ndarray:
+    """Stored 16-bit values of a seeded output gradient dO for the backward."""
+    return tensor_bits(w, 3)
 
 
 def custom(name: str, B: int, H: int, N: int, d: int, dtype: str, causal: bool,

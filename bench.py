@@ -1,17 +1,21 @@
 #!/usr/bin/env python3
-"""Benchmark of the fused attention forward on GB300.
+"""Benchmark of the fused attention forward (and backward) on GB300.
 
 One step = one fa_fwd launch over the whole workload (all B*H*N query rows),
 inputs resident in HBM. Default workload: non-causal MHA, B=4 H=16 N=4096
 d=128, fp16 in / fp16 out, fp32 accumulate, scale 1/sqrt(128).
 
 Metric: attention forward TFLOPS = 4 B H N^2 d / time (halved for causal),
-also reported as a percentage of 2.25 PFLOP/s dense fp16.
+also reported as a percentage of 2.25 PFLOP/s dense fp16. With
+--pass backward a step is one fa_bwd call (dQ, dK, dV from the forward's O
+and LSE) and the metric is 10 B H N^2 d / time (the five N x N x d products
+of the backward; halved for causal).
 
 Prints ONE JSON line (rank 0). Reference arm (--impl reference): the fp64 CPU
 oracle timed on this host's cores on a bounded sample of the same workload.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+                    [--pass forward|backward]
 """
 from __future__ import annotations
 
@@ -35,6 +39,7 @@ from attention_forward_flashattention_gb300 import inputs as I  # noqa: E402
 
 DEFAULT_WORKLOAD = "mha_b4_h16_n4096_d128_fp16"
 METRIC = "attention fwd TFLOPS (4BHN²d, causal halved) and % of 2.25 PF dense fp16"
+METRIC_BWD = "attention bwd TFLOPS (10BHN²d, causal halved) and % of 2.25 PF dense fp16"
 NOMINAL_DENSE_FP16_TFLOPS = 2250.0
 FALLBACK_PEAK_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
@@ -52,6 +57,8 @@ def parse_args():
     p.add_argument("--workload", default=DEFAULT_WORKLOAD,
                    choices=I.WORKLOAD_ORDER + list(I.FP8_WORKLOADS))
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "backward"],
+                   help="backward: time fa_bwd (dQ, dK, dV) on a 16-bit workload")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--soak-s", type=float, default=1.5,
@@ -224,27 +231,42 @@ def run_reference(args, rank: int, world: int):
     if rank != 0:
         return
     w = get_workload(args.workload)
-    x = workload_inputs(w)
     import oracle
     oracle.build()
-    step_target = 2.0
-    vals, secs, nrows, cores = [], [], 0, oracle.threads(0)
-    for s in range(args.warmup + args.steps):
-        tf, dt, n, cores = time_oracle(w, x, step_target, seed=w.seed * 7 + s)
-        if s >= args.warmup:
-            vals.append(tf)
-            secs.append(dt)
-            nrows += n
+    vals, secs = [], []
+    if args.pass_ == "backward":
+        # one step = the backward oracle on a few whole heads (about 12 s at N=4096)
+        x, dob = I.qkv_bits(w), I.dout_bits(w)
+        for s in range(args.warmup + args.steps):
+            t = time.perf_counter()
+            cpu = cpu_backward_sample(w, x, dob)
+            if s >= args.warmup:
+                vals.append(cpu["value"])
+                secs.append(time.perf_counter() - t)
+        metric, cores = METRIC_BWD, cpu["cores"]
+        sample = cpu["sample"].split(",")[0] + " per step; TFLOPS = heads x (metric FLOPs per " \
+                                               "head) / wall time"
+    else:
+        x = workload_inputs(w)
+        step_target = 2.0
+        nrows, cores = 0, oracle.threads(0)
+        for s in range(args.warmup + args.steps):
+            tf, dt, n, cores = time_oracle(w, x, step_target, seed=w.seed * 7 + s)
+            if s >= args.warmup:
+                vals.append(tf)
+                secs.append(dt)
+                nrows += n
+        metric = METRIC
+        sample = (f"{nrows // max(1, args.steps)} query rows per step (grouped over 4 heads) "
+                  f"of {w.name}; TFLOPS = rows x (metric FLOPs per row) / wall time")
     value = statistics.mean(vals)
     ms = statistics.mean(secs) * 1e3
-    sample = (f"{nrows // max(1, args.steps)} query rows per step (grouped over 4 heads) of "
-              f"{w.name}; TFLOPS = rows x (metric FLOPs per row) / wall time")
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
+        "impl": "reference", "metric": metric, "value": value, "unit": "TFLOPS",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded SplitMix64 + Box-Muller, N(0,1))",
-        "config": workload_config(w),
+        "config": {**workload_config(w), "pass": args.pass_},
         "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
@@ -259,18 +281,15 @@ def workload_config(w) -> dict:
             "global_batch": w.B, "seq_len": w.N}
 
 
-def run_ours(args, rank: int, world: int, local_rank: int):
-    import torch
-    import torch.distributed as dist
+class Plan:
+    """What one timed step runs: `step()` on device-resident inputs, and
+    `e2e_step()` with pinned host inputs copied in and results copied out."""
 
-    import attention_forward_flashattention_gb300 as fa
-    from attention_forward_flashattention_gb300 import build as fabuild
+    def __init__(self, **kw):
+        self.__dict__.update(kw)
 
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    fabuild.build()
-    fa.load_library()
-    w = get_workload(args.workload)
+
+def forward_plan(fa, torch, w, dev, stream) -> Plan:
     fp8 = w.dtype == "e4m3"
     x = workload_inputs(w)
     if fp8:
@@ -284,9 +303,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     dev_in = [h.to(dev) for h in host]
     o = torch.empty((w.B, w.H, w.N, w.d), dtype=tdt, device=dev)
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    sh = int(stream.cuda_stream)
+    oh = torch.empty(o.shape, dtype=tdt).pin_memory()
+    lh = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
     launch = fa.fa_query_launch(w.B, w.H, w.N, w.d, w.causal)
 
     def run(ins):
@@ -296,11 +314,112 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         else:
             fa.attention_forward_into(ins[0], ins[1], ins[2], o, lse, w.causal, w.scale, stream)
 
-    def step():
-        run(dev_in)
+    def e2e_step():
+        run([h.to(dev, non_blocking=True) for h in host])
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+
+    peak_note = ""
+    if fp8:   # e4m3 dense rate is twice the 16-bit one (4.5 vs 2.25 PFLOP/s nominal)
+        peak_note = " x 2 (e4m3 / bf16 nominal dense ratio)"
+    return Plan(
+        metric=METRIC, flops=w.flops, step=lambda: run(dev_in), e2e_step=e2e_step,
+        h2d=sum(h.numel() * h.element_size() for h in host),
+        d2h=o.numel() * o.element_size() + lse.numel() * 4,
+        launches=1, peak_mult=2.0 if fp8 else 1.0, peak_note=peak_note,
+        kernel="fa_fwd_kernel",
+        launch_cfg={"grid": launch["grid"], "threads": launch["threads"],
+                    "smem_bytes": None if fp8 else launch["smem_bytes"],
+                    "units": launch["units"]},
+        traffic=recorded_traffic(w.name),
+        cpu=lambda: cpu_forward_sample(w, x))
+
+
+def cpu_forward_sample(w, x) -> dict:
+    tf, dt, n, cores = time_oracle(w, x, target_s=12.0, seed=w.seed * 13)
+    return {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+            "sample": f"{n} query rows (grouped over 4 heads) of {w.name}, {dt:.1f} s wall; "
+                      f"TFLOPS = rows x (metric FLOPs per row) / wall time"}
+
+
+def backward_plan(fa, torch, w, dev, stream) -> Plan:
+    if w.dtype not in ("fp16", "bf16"):
+        raise SystemExit("--pass backward takes a 16-bit workload")
+    tdt = torch.float16 if w.dtype == "fp16" else torch.bfloat16
+    x = I.qkv_bits(w)
+    dob = I.dout_bits(w)
+    q, k, v, do = (torch.from_numpy(t.view(np.int16)).view(tdt).to(dev) for t in x + (dob,))
+    # the forward's outputs feed the backward, as in training (computed once)
+    o, lse = fa.attention_forward(q, k, v, causal=w.causal, scale=w.scale)
+    torch.cuda.synchronize(dev)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    ws = torch.empty(fa.fa_bwd_workspace_size(w.B, w.H, w.N, w.d) // 4, dtype=torch.float32,
+                     device=dev)
+    code = fa._dtype_code(q)
+    sh = int(stream.cuda_stream)
+    host = [t.cpu().pin_memory() for t in (q, k, v, o, lse, do)]
+    outs_h = [torch.empty(q.shape, dtype=tdt).pin_memory() for _ in range(3)]
+
+    def run(ins):
+        rc = fa.fa_bwd(*(t.data_ptr() for t in ins[:3]), ins[3].data_ptr(), ins[5].data_ptr(),
+                       ins[4].data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                       ws.data_ptr(), w.B, w.H, w.N, w.d, w.causal, w.scale, code, sh)
+        if rc != fa.FA_OK:
+            raise fa.FaError(rc, "fa_bwd")
+
+    dev_in = [q, k, v, o, lse, do]
+
+    def e2e_step():
+        run([h.to(dev, non_blocking=True) for h in host])
+        for hh, t in zip(outs_h, (dq, dk, dv)):
+            hh.copy_(t, non_blocking=True)
+
+    return Plan(
+        metric=METRIC_BWD, flops=2.5 * w.flops, step=lambda: run(dev_in), e2e_step=e2e_step,
+        h2d=sum(h.numel() * h.element_size() for h in host),
+        d2h=3 * q.numel() * q.element_size(),
+        launches=3, peak_mult=1.0, peak_note="",
+        kernel="fa_bwd (D/LSE prep + fa_bwd_kernel dK,dV + fa_bwd_kernel dQ; whole call)",
+        launch_cfg={"launches_per_step": 3, "workspace_bytes": ws.numel() * 4},
+        traffic=None,
+        cpu=lambda: cpu_backward_sample(w, x, dob))
+
+
+def cpu_backward_sample(w, x, dob) -> dict:
+    """The backward oracle on a few whole heads, one thread per head."""
+    import oracle
+    cores = oracle.threads(0)
+    nh = max(1, min(cores, 4))
+    heads = np.random.default_rng(w.seed * 17).choice(w.B * w.H, size=nh, replace=False)
+    t = time.perf_counter()
+    oracle.attn_bwd(*x, dob, w.dtype, w.causal, w.scale, heads=heads, nthreads=nh)
+    dt = time.perf_counter() - t
+    flops = 2.5 * w.flops / (w.B * w.H) * nh
+    return {"value": flops / dt / 1e12, "unit": "TFLOPS", "cores": nh, "kind": "oracle",
+            "sample": f"{nh} whole heads of {w.name} (one thread each), {dt:.1f} s wall; "
+                      f"TFLOPS = heads x (metric FLOPs per head) / wall time"}
+
+
+def run_ours(args, rank: int, world: int, local_rank: int):
+    import torch
+    import torch.distributed as dist
+
+    import attention_forward_flashattention_gb300 as fa
+    from attention_forward_flashattention_gb300 import build as fabuild
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    fabuild.build()
+    fa.load_library()
+    w = get_workload(args.workload)
+    stream = torch.cuda.current_stream(dev)
+    sh = int(stream.cuda_stream)
+    make = backward_plan if args.pass_ == "backward" else forward_plan
+    plan = make(fa, torch, w, dev, stream)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
 
     for _ in range(max(args.warmup, 3)):
-        step()
+        plan.step()
     rc = fa.fa_check(sh)
     if rc != fa.FA_OK:
         raise RuntimeError("warm-up failed: " + fa.status_string(rc))
@@ -309,7 +428,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     t_end = time.perf_counter() + args.soak_s
     while time.perf_counter() < t_end:   # untimed load so clock samples exist
         for _ in range(20):
-            step()
+            plan.step()
         torch.cuda.synchronize(dev)
 
     if world > 1:
@@ -320,7 +439,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     for i in range(args.steps):
         flush.zero_()                    # evict L2 between steps (outside the events)
         starts[i].record(stream)
-        step()
+        plan.step()
         ends[i].record(stream)
     torch.cuda.synchronize(dev)
     if world > 1:
@@ -332,7 +451,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = max_over_ranks(sum(times_ms), world, dev)
     ms_per_step = total_ms / args.steps
-    value = job_throughput(w.flops, total_ms, args.steps, world)
+    value = job_throughput(plan.flops, total_ms, args.steps, world)
     per_gpu_tflops = value / world
 
     # SM clock from clock64 (one CTA spinning 2e8 cycles right after the load)
@@ -346,29 +465,19 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     # end to end through the public API: pinned host in, pinned host out
     e2e = None
     if not args.no_e2e:
-        oh = torch.empty(o.shape, dtype=tdt).pin_memory()
-        lh = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
-
-        def e2e_step():
-            run([h.to(dev, non_blocking=True) for h in host])
-            oh.copy_(o, non_blocking=True)
-            lh.copy_(lse, non_blocking=True)
-
-        e2e_step()
+        plan.e2e_step()
         torch.cuda.synchronize(dev)
         n_e2e = max(3, min(args.steps, 10))
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(n_e2e):
-            e2e_step()
+            plan.e2e_step()
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, world, dev)
-        elem = w.B * w.H * w.N * w.d
-        e2e = {"value": w.flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
-               "ms_per_step": e2e_ms,
-               "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in host),
-               "d2h_bytes_per_step": elem * 2 + w.B * w.H * w.N * 4}
+        e2e = {"value": plan.flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": plan.h2d,
+               "d2h_bytes_per_step": plan.d2h}
 
     if rank != 0:
         return
@@ -377,31 +486,24 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         peak, peak_src = float(peaks["bf16_tflops"]), "measured bf16 burst (fp16 same nominal rate)"
     else:
         peak, peak_src = FALLBACK_PEAK_TFLOPS, "fallback"
-    if fp8:   # e4m3 dense rate is twice the 16-bit one (4.5 vs 2.25 PFLOP/s nominal)
-        peak, peak_src = 2.0 * peak, peak_src + " x 2 (e4m3 / bf16 nominal dense ratio)"
-    cpu = None
-    if not args.no_cpu_baseline:
-        tf, dt, n, cores = time_oracle(w, x, target_s=12.0, seed=w.seed * 13)
-        cpu = {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
-               "sample": f"{n} query rows (grouped over 4 heads) of {w.name}, {dt:.1f} s wall; "
-                         f"TFLOPS = rows x (metric FLOPs per row) / wall time"}
+    peak, peak_src = plan.peak_mult * peak, peak_src + plan.peak_note
+    cpu = None if args.no_cpu_baseline else plan.cpu()
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+        "metric": plan.metric, "value": value, "unit": "TFLOPS", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic (seeded SplitMix64 + Box-Muller, N(0,1)), resident in HBM",
-        "config": {**workload_config(w), "parallelism": f"replicas x{world}",
+        "config": {**workload_config(w), "pass": args.pass_,
+                   "parallelism": f"replicas x{world}",
                    "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)",
-                   "grid": launch["grid"], "threads": launch["threads"],
-                   "smem_bytes": None if fp8 else launch["smem_bytes"],
-                   "units": launch["units"]},
+                   **plan.launch_cfg},
         "pct_of_2250_tflops": 100.0 * per_gpu_tflops / NOMINAL_DENSE_FP16_TFLOPS,
         "roofline": {"bound": "tensor", "achieved": per_gpu_tflops, "peak": peak,
                      "unit": "TFLOP/s", "frac": per_gpu_tflops / peak,
-                     "traffic": recorded_traffic(w.name), "peak_source": peak_src,
-                     "kernel": "fa_fwd_kernel"},
+                     "traffic": plan.traffic, "peak_source": peak_src,
+                     "kernel": plan.kernel},
         "clocks": {**clocks, "clk64_mhz": clk64_mhz, "window": "soak + timed steps"},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * plan.launches,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "step_ms_min": min(times_ms), "step_ms_median": statistics.median(times_ms),

@@ -33,8 +33,7 @@ def _built(oracle_mod):
 
 
 def _dout_bits(w):
-    rng = np.random.default_rng(w.seed * 31 + 7)
-    return I.to_bits(rng.standard_normal((w.B, w.H, w.N, w.d)), w.dtype)
+    return I.dout_bits(w)
 
 
 def _run(w, q, k, v, dob):
