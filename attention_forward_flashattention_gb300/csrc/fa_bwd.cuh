@@ -10,7 +10,7 @@
 // Three launches, no atomics, deterministic:
 //   1. bwd_prep_kernel: D_i and LSE_i * log2(e) into a workspace padded to
 //      128-row tiles (padding rows: D = 0, lse2 = +inf, so their weights are 0).
-//   2. bwd_dkdv_kernel: one unit = one 128-key tile of one head; it loops over
+//   2. dK/dV kernel: one unit = one 128-key tile of one head; it loops over
 //      the 128-row query tiles that see it. Per query tile i (TMEM, lane = key):
 //        S^T = K Q_i^T, dP^T = V dO_i^T           (both operands in smem)
 //        P^T = 2^(c S^T - lse2_i)  -> 16 bit over the S^T columns
@@ -18,19 +18,26 @@
 //        dS^T = P^T (dP^T - D_i)   -> 16 bit over the dP^T columns
 //        dK += dS^T Q_i                           (A = dS^T from TMEM)
 //      dK and dV accumulate in TMEM; the epilogue scales dK and stores both.
-//   3. bwd_dq_kernel: one unit = one 128-row query tile; it loops over the key
+//   3. dQ kernel: one unit = one 128-row query tile; it loops over the key
 //      tiles it sees. Per key tile j (lane = query row):
 //        S = Q K_j^T, dP = dO V_j^T
-//        P = 2^(c S - lse2), dS = P (dP - D)  -> 16 bit over the S columns
+//        P = 2^(c S - lse2), dS = P (dP - D)  -> 16 bit over the dP columns
 //        dQ += dS K_j                             (A = dS from TMEM)
+//      S is released as soon as it is read, so S of tile j+1 is computed
+//      while dS of tile j is formed; the MMA order is S(j+1), dQ(j), dP(j+1).
 //
-// Roles (12 warps): warp 0 TMA producer (lane 0), warp 1 TMEM owner and MMA
-// issuer (lane 0), warpgroup 1 the element-wise softmax gradient (one thread
-// per TMEM lane), warpgroup 2 the epilogue. Every wait is bounded as in the
-// forward (abort flag, status bits, drain before TMEM is freed).
+// Roles (16 warps): warp 0 TMA producer (lane 0), warp 1 TMEM owner and MMA
+// issuer (lane 0), warpgroups 1 and 2 the element-wise softmax gradient (one
+// thread per TMEM lane; warpgroup 1 takes columns 0-63 of each 128-column
+// scratch tile, warpgroup 2 columns 64-127, and each packs its 16-bit result
+// over the first 32 of its own columns), warpgroup 3 the epilogue. Every wait
+// is bounded as in the forward (abort flag, status bits, drain before TMEM is
+// freed).
 #pragma once
 
 #include <cuda.h>
+
+#include <type_traits>
 
 #include "fa.h"
 #include "fa_common.cuh"
@@ -53,13 +60,14 @@ struct BwdArgs {
   float scale;
 };
 
-constexpr int kBwdThreads = 384;
-// setmaxnreg split: the 384-thread launch gives 168 registers per thread
-// (65536 / 384, rounded down to a multiple of 8); the three warpgroups move
-// to 64 / 256 / 184, which sum to the same 3 x 168.
-constexpr uint32_t kBwdRegsLaunch = 168;
-constexpr uint32_t kBwdRegsWG0 = 64, kBwdRegsElem = 256, kBwdRegsEpi = 184;
-static_assert(kBwdRegsWG0 + kBwdRegsElem + kBwdRegsEpi == 3 * kBwdRegsLaunch, "register split");
+constexpr int kBwdThreads = 512;
+// setmaxnreg split: the 512-thread launch gives 128 registers per thread
+// (65536 / 512); the four warpgroups move to 64 / 192 / 192 / 64, which sum
+// to the same 4 x 128.
+constexpr uint32_t kBwdRegsLaunch = 128;
+constexpr uint32_t kBwdRegsWG0 = 64, kBwdRegsElem = 192, kBwdRegsEpi = 64;
+static_assert(kBwdRegsWG0 + 2 * kBwdRegsElem + kBwdRegsEpi == 4 * kBwdRegsLaunch,
+              "register split");
 static_assert(kBwdRegsLaunch == (65536 / kBwdThreads) / 8 * 8, "launch allocation");
 
 template <int D>
@@ -76,8 +84,10 @@ struct BwdLayout {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kStageBytes % 1024 == 0, "stages keep tiles 1024-byte aligned");
   // TMEM columns: two 128-column fp32 scratch tiles, then the accumulators.
-  static constexpr uint32_t kColA = 0;    // S^T (dkdv) / S (dq); 16-bit P^T / dS over its first 64
-  static constexpr uint32_t kColB = 128;  // dP^T (dkdv) / dP (dq); dS^T over its first 64 (dkdv)
+  // A 16-bit operand written over a scratch tile sits in columns 0-31 (rows'
+  // elements 0-63) and 64-95 (elements 64-127).
+  static constexpr uint32_t kColA = 0;    // S^T (dkdv) / S (dq); 16-bit P^T (dkdv)
+  static constexpr uint32_t kColB = 128;  // dP^T (dkdv) / dP (dq); 16-bit dS^T / dS
   static constexpr uint32_t kColAcc0 = 256;      // dV (dkdv) / dQ (dq)
   static constexpr uint32_t kColAcc1 = 256 + D;  // dK (dkdv)
 };
@@ -87,8 +97,8 @@ enum BwdBar : int {
   kBbFixEmpty = 1,   // MMA: the unit's last use of the fixed tiles done
   kBbAFull = 2,      // MMA: scratch A (S^T / S) ready
   kBbBFull = 3,      // MMA: scratch B (dP^T / dP) ready
-  kBbPFull = 4,      // element-wise (4 warps): P^T in TMEM (dkdv only)
-  kBbDsFull = 5,     // element-wise (4 warps): dS^T / dS in TMEM
+  kBbPFull = 4,      // element-wise (8 warps): P^T in TMEM (dkdv) / S read (dq)
+  kBbDsFull = 5,     // element-wise (8 warps): dS^T / dS in TMEM
   kBbAccFull = 6,    // MMA: the unit's accumulators final
   kBbAccFree = 7,    // epilogue (4 warps): accumulators read
   kBbDrain = 8,      // MMA: all tcgen05 ops done
@@ -238,6 +248,23 @@ __device__ __forceinline__ void bwd_producer(const CUtensorMap* tm_q, const CUte
   }
 }
 
+// C[tmem] (+)= A[tmem] B: A is a 16-bit operand written over a scratch tile
+// (elements 0-63 in columns 0-31, 64-127 in columns 64-95, two per column),
+// B a 128-row tile used MN-major (K = its rows).
+template <int D, bool BF16>
+__device__ __forceinline__ void bwd_issue_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t sB,
+                                             bool accumulate) {
+  constexpr uint32_t id = ptx::idesc_f16(BF16, true, 128, D);
+  uint64_t db = desc_v(sB);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t acol = a_tmem + (kk < 4 ? 8u * kk : 64u + 8u * (kk - 4));
+    ptx::umma_f16_ts(d_tmem, acol, db, id, (accumulate || kk > 0) ? 1u : 0u);
+    db = desc_add(db, 2048u);
+    asm volatile("" : "+l"(db));
+  }
+}
+
 // The single MMA-issuing thread (see the order at the top of this file).
 template <int D, bool BF16, bool CAUSAL, bool KEYS>
 __device__ __forceinline__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32_t bars,
@@ -285,7 +312,7 @@ __device__ __forceinline__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32
             !(ok = wait_spin(bar(kBbAccFree), (units - 1) & 1u, ab, kStatusMma)))
           break;
         ptx::tc_fence_after();
-        issue_pv_ts<D, BF16>(tAcc0, tA, stage(r) + L::kTileBytes, acc);
+        bwd_issue_ts<D, BF16>(tAcc0, tA, stage(r) + L::kTileBytes, acc);
         if (more) {  // the next S^T while the element-wise role forms dS^T
           if (!(ok = ring_wait(ring))) break;
           scratch_a(ring);
@@ -293,23 +320,26 @@ __device__ __forceinline__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32
         // dK += dS^T Q (dS^T in TMEM over the dP^T columns; Q used MN-major)
         if (!(ok = wait_spin(bar(kBbDsFull), ph, ab, kStatusMma))) break;
         ptx::tc_fence_after();
-        issue_pv_ts<D, BF16>(tAcc1, tB, stage(r), acc);
+        bwd_issue_ts<D, BF16>(tAcc1, tB, stage(r), acc);
         ptx::umma_commit(bar(kBbRing + S + r % S));
         if (more) scratch_b(ring);
       } else {
-        // dQ += dS K (dS in TMEM over the S columns; K used MN-major)
+        // S was read: the next S while the element-wise role forms dS
+        if (!(ok = wait_spin(bar(kBbPFull), ph, ab, kStatusMma))) break;
+        if (more) {
+          if (!(ok = ring_wait(ring))) break;
+          ptx::tc_fence_after();
+          scratch_a(ring);
+        }
+        // dQ += dS K (dS in TMEM over the dP columns; K used MN-major)
         if (!(ok = wait_spin(bar(kBbDsFull), ph, ab, kStatusMma))) break;
         if (!acc && units > 0 &&
             !(ok = wait_spin(bar(kBbAccFree), (units - 1) & 1u, ab, kStatusMma)))
           break;
         ptx::tc_fence_after();
-        issue_pv_ts<D, BF16>(tAcc0, tA, stage(r), acc);
+        bwd_issue_ts<D, BF16>(tAcc0, tB, stage(r), acc);
         ptx::umma_commit(bar(kBbRing + S + r % S));
-        if (more) {
-          if (!(ok = ring_wait(ring))) break;
-          scratch_a(ring);
-          scratch_b(ring);
-        }
+        if (more) scratch_b(ring);  // after dQ has read dS (in-order execution)
       }
     }
     if (!ok) break;
@@ -333,21 +363,26 @@ __device__ __forceinline__ float2 unpack2(uint32_t w) {
 }
 
 // Element-wise softmax gradient, one thread per TMEM lane (row r of the
-// 128-row scratch tiles). KEYS (dK/dV): the row is key k = 128 t + r, the
-// columns are the queries of the streamed tile, whose lse2 / D come from the
-// stage's vectors. Otherwise (dQ): the row is query q = 128 t + r, the columns
-// are keys, lse2 / D are the row's own.
+// 128-row scratch tiles) and 64 columns per warpgroup (half h). KEYS (dK/dV):
+// the row is key k = 128 t + r, the columns are queries of the streamed tile,
+// whose lse2 / D come from the stage's vectors. Otherwise (dQ): the row is
+// query q = 128 t + r, the columns are keys, lse2 / D are the row's own.
+// P stays in fp32 registers; only the MMA operands are rounded to 16 bits.
 template <int D, bool BF16, bool CAUSAL, bool KEYS>
-__device__ __forceinline__ void bwd_elementwise(const BwdArgs& a, uint32_t sbase, uint32_t bars,
-                                                uint32_t tmem, const AbortCtx& ab, int warp,
-                                                int lane) {
+__device__ __forceinline__ void bwd_elementwise(const BwdArgs& a, const uint8_t* sgen,
+                                                uint32_t bars, uint32_t tmem, const AbortCtx& ab,
+                                                int warp, int lane) {
   using L = BwdLayout<D>;
   constexpr int S = L::kStages;
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
   const int r = (warp & 3) * 32 + lane;
+  const int h = (warp >> 2) - 1;  // column half of this warpgroup
+  const int c0 = 64 * h;
   const uint32_t tl = ptx::tmem_lane_base(tmem, warp);
-  const uint32_t tA = tl + L::kColA, tB = tl + L::kColB;
+  const uint32_t tA = tl + L::kColA + static_cast<uint32_t>(c0);
+  const uint32_t tB = tl + L::kColB + static_cast<uint32_t>(c0);
   const float cl2 = a.scale_log2;
+  const bool ragged = (a.N & 127) != 0;
   uint32_t ring = 0, cnt = 0;
   int round = 0, bh = 0, t = 0;
   bool ok = true;
@@ -368,77 +403,93 @@ __device__ __forceinline__ void bwd_elementwise(const BwdArgs& a, uint32_t sbase
       if (KEYS && !(ok = wait_bounded_warp(bar(kBbRing + rr % S), (rr / S) & 1u, ab,
                                            kStatusSoftmax)))
         break;
+      const float* vec = reinterpret_cast<const float*>(
+          sgen + L::kOffRing + (rr % S) * L::kStageBytes + 2 * L::kTileBytes);
       // ---- P: scores of this tile against the row's reference
       if (!(ok = wait_bounded_warp(bar(kBbAFull), ph, ab, kStatusSoftmax))) break;
       ptx::tc_fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tA + 32u * c, sr[c]);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) ptx::tmem_ld_wait(sr[c]);
-      const uint32_t vbase = sbase + L::kOffRing + (rr % S) * L::kStageBytes + 2 * L::kTileBytes;
-      uint32_t pk[2][32];
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        float p[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int col = 2 * c + e;
-          const float sv = __uint_as_float(sr[col >> 5][col & 31]);
-          float ref;
-          bool keep;
-          if constexpr (KEYS) {
-            float l2;
-            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(l2) : "r"(vbase + 4u * col));
-            ref = l2;  // +inf past N: weight 0
-            keep = !CAUSAL || 128 * st + col >= row;
-          } else {
-            ref = my_lse2;
-            const int key = 128 * st + col;
-            keep = key < a.N && (!CAUSAL || key <= row);
-          }
-          p[e] = keep ? ptx::ex2(fmaf(sv, cl2, -ref)) : 0.f;
-        }
-        pk[c >> 5][c & 31] = pack2<BF16>(p[0], p[1]);
+      uint32_t sr[2][32];
+      ptx::tmem_ld32(tA, sr[0]);
+      ptx::tmem_ld32(tA + 32u, sr[1]);
+      ptx::tmem_ld_wait(sr[0]);
+      ptx::tmem_ld_wait(sr[1]);
+      if constexpr (!KEYS) {  // S is in registers: the MMA may overwrite it
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar(kBbPFull));
       }
+      // masks only on the diagonal tile (causal) and the ragged last key tile
+      const bool masked = KEYS ? (CAUSAL && st == t)
+                               : ((CAUSAL && st == t) || (ragged && st == a.n_t - 1));
+      auto weights = [&](auto mask_tag) {
+        constexpr bool kMask = decltype(mask_tag)::value;
+#pragma unroll
+        for (int j = 0; j < 64; j += 4) {
+          float ref[4];
+          if constexpr (KEYS) {
+            const float4 l4 = *reinterpret_cast<const float4*>(vec + c0 + j);
+            ref[0] = l4.x; ref[1] = l4.y; ref[2] = l4.z; ref[3] = l4.w;
+          } else {
+            ref[0] = ref[1] = ref[2] = ref[3] = my_lse2;
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = j + e, col = 128 * st + c0 + c;
+            uint32_t& x = sr[c >> 5][c & 31];
+            bool keep = true;
+            if constexpr (kMask) {
+              if constexpr (KEYS) keep = col >= row;  // query col sees key row
+              else keep = col < a.N && (!CAUSAL || col <= row);
+            }
+            // +inf lse2 (queries past N) gives weight 0 unmasked
+            x = __float_as_uint(keep ? ptx::ex2(fmaf(__uint_as_float(x), cl2, -ref[e])) : 0.f);
+          }
+        }
+      };
+      if (masked) weights(std::true_type{});
+      else weights(std::false_type{});
       if constexpr (KEYS) {
-        // P^T to TMEM over the S^T columns, for dV += P^T dO
-        ptx::tmem_st32(tA, pk[0]);
-        ptx::tmem_st32(tA + 32u, pk[1]);
+        // P^T (16 bit) over this half's first 32 S^T columns, for dV += P^T dO
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          pk[c] = pack2<BF16>(__uint_as_float(sr[(2 * c) >> 5][(2 * c) & 31]),
+                              __uint_as_float(sr[(2 * c + 1) >> 5][(2 * c + 1) & 31]));
+        ptx::tmem_st32(tA, pk);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bar(kBbPFull));
       }
-      // ---- dS = P (dP - D), 16-bit, over the first 64 columns of its tile
+      // ---- dS = P (dP - D) (16 bit) over this half's first 32 dP columns
       if (!(ok = wait_bounded_warp(bar(kBbBFull), ph, ab, kStatusSoftmax))) break;
       ptx::tc_fence_after();
-      const uint32_t tDs = KEYS ? tB : tA;
+      uint32_t dp[2][32];
+      ptx::tmem_ld32(tB, dp[0]);
+      ptx::tmem_ld32(tB + 32u, dp[1]);
+      ptx::tmem_ld_wait(dp[0]);
+      ptx::tmem_ld_wait(dp[1]);
+      uint32_t ds[32];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t dp[2][32];
-        ptx::tmem_ld32(tB + 64u * h, dp[0]);
-        ptx::tmem_ld32(tB + 64u * h + 32u, dp[1]);
-        ptx::tmem_ld_wait(dp[0]);
-        ptx::tmem_ld_wait(dp[1]);
-        uint32_t ds[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float2 pv = unpack2<BF16>(pk[h][c]);
-          const int col = 64 * h + 2 * c;
-          float d0, d1;
-          if constexpr (KEYS) {
-            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(d0) : "r"(vbase + 512u + 4u * col));
-            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(d1) : "r"(vbase + 516u + 4u * col));
-          } else {
-            d0 = d1 = my_d;
-          }
-          const float g0 = pv.x * (__uint_as_float(dp[c >> 4][(2 * c) & 31]) - d0);
-          const float g1 = pv.y * (__uint_as_float(dp[c >> 4][(2 * c + 1) & 31]) - d1);
-          ds[c] = pack2<BF16>(g0, g1);
+      for (int j = 0; j < 64; j += 4) {
+        float dd[4];
+        if constexpr (KEYS) {
+          const float4 d4 = *reinterpret_cast<const float4*>(vec + 128 + c0 + j);
+          dd[0] = d4.x; dd[1] = d4.y; dd[2] = d4.z; dd[3] = d4.w;
+        } else {
+          dd[0] = dd[1] = dd[2] = dd[3] = my_d;
         }
-        ptx::tmem_st32(tDs + 32u * h, ds);
+#pragma unroll
+        for (int e = 0; e < 4; e += 2) {
+          const int c = j + e;
+          const float g0 = __uint_as_float(sr[c >> 5][c & 31]) *
+                           (__uint_as_float(dp[c >> 5][c & 31]) - dd[e]);
+          const float g1 = __uint_as_float(sr[(c + 1) >> 5][(c + 1) & 31]) *
+                           (__uint_as_float(dp[(c + 1) >> 5][(c + 1) & 31]) - dd[e + 1]);
+          ds[c >> 1] = pack2<BF16>(g0, g1);
+        }
       }
+      ptx::tmem_st32(tB, ds);
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       __syncwarp();
@@ -522,8 +573,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ptx::mbar_init(bar(kBbFixEmpty), 1);
     ptx::mbar_init(bar(kBbAFull), 1);
     ptx::mbar_init(bar(kBbBFull), 1);
-    ptx::mbar_init(bar(kBbPFull), 4);
-    ptx::mbar_init(bar(kBbDsFull), 4);
+    ptx::mbar_init(bar(kBbPFull), 8);
+    ptx::mbar_init(bar(kBbDsFull), 8);
     ptx::mbar_init(bar(kBbAccFull), 1);
     ptx::mbar_init(bar(kBbAccFree), 4);
     ptx::mbar_init(bar(kBbDrain), 1);
@@ -549,9 +600,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (warp == 0) bwd_producer<D, CAUSAL, KEYS>(&tm_q, &tm_k, &tm_v, &tm_do, a, sbase, bars, ab);
       else if (warp == 1) bwd_mma<D, BF16, CAUSAL, KEYS>(a, sbase, bars, tmem, ab);
     }
-  } else if (wgrp == 1) {
+  } else if (wgrp <= 2) {
     ptx::setmaxnreg_to<kBwdRegsElem, kBwdRegsLaunch>();
-    bwd_elementwise<D, BF16, CAUSAL, KEYS>(a, sbase, bars, tmem, ab, warp, lane);
+    bwd_elementwise<D, BF16, CAUSAL, KEYS>(a, sgen, bars, tmem, ab, warp, lane);
   } else {
     ptx::setmaxnreg_to<kBwdRegsEpi, kBwdRegsLaunch>();
     bwd_epilogue<D, BF16, CAUSAL, KEYS>(a, bars, tmem, ab, warp, lane);
