@@ -70,39 +70,52 @@ static_assert(kBwdRegsWG0 + 2 * kBwdRegsElem + kBwdRegsEpi == 4 * kBwdRegsLaunch
               "register split");
 static_assert(kBwdRegsLaunch == (65536 / kBwdThreads) / 8 * 8, "launch allocation");
 
-template <int D>
+// Shared memory and TMEM of one kernel (KEYS: dK/dV, else dQ).
+template <int D, bool KEYS>
 struct BwdLayout {
   static constexpr int kPanels = D / 64;
   static constexpr int kTileBytes = kPanels * kPanelBytes;  // a 128-row tile of Q, K, V, dO
-  static constexpr int kStages = (D == 128) ? 2 : 4;       // ring slots (two tiles + vectors each)
-  static constexpr int kVecBytes = 2 * 128 * 4;            // lse2 and D of one query tile
-  static constexpr int kStageBytes = 2 * kTileBytes + kVecBytes;
   static constexpr int kOffFix = 0;                         // two fixed tiles (K, V or Q, dO)
   static constexpr int kOffRing = 2 * kTileBytes;
-  static constexpr int kOffBar = kOffRing + kStages * kStageBytes;
+  // dK/dV: one ring of stages, each a Q tile, a dO tile and their lse2 / D
+  static constexpr int kStages = (D == 128) ? 2 : 4;
+  static constexpr int kVecBytes = 2 * 128 * 4;
+  static constexpr int kStageBytes = 2 * kTileBytes + kVecBytes;
+  // dQ: a K ring (a K tile lives from S to dQ) and a V ring (read by dP only)
+  static constexpr int kKSlots = (D == 128) ? 3 : 4;
+  static constexpr int kVSlots = (D == 128) ? 2 : 3;
+  static constexpr int kOffK = kOffRing;
+  static constexpr int kOffV = kOffK + kKSlots * kTileBytes;
+  static constexpr int kRingBytes =
+      KEYS ? kStages * kStageBytes : (kKSlots + kVSlots) * kTileBytes;
+  static constexpr int kOffBar = kOffRing + kRingBytes;
   static constexpr int kSmemBytes = kOffBar + 512 + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kStageBytes % 1024 == 0, "stages keep tiles 1024-byte aligned");
-  // TMEM columns: two 128-column fp32 scratch tiles, then the accumulators.
-  // A 16-bit operand written over a scratch tile sits in columns 0-31 (rows'
+  // TMEM columns: 128-column fp32 scratch tiles and the accumulators. A
+  // 16-bit operand written over a scratch tile sits in columns 0-31 (rows'
   // elements 0-63) and 64-95 (elements 64-127).
-  static constexpr uint32_t kColA = 0;    // S^T (dkdv) / S (dq); 16-bit P^T (dkdv)
-  static constexpr uint32_t kColB = 128;  // dP^T (dkdv) / dP (dq); 16-bit dS^T / dS
+  static constexpr uint32_t kColA = 0;    // S^T, then 16-bit P^T (dkdv) / S, then dS (dq, even tiles)
+  static constexpr uint32_t kColB = 128;  // dP^T, then 16-bit dS^T (dkdv) / dP (dq)
   static constexpr uint32_t kColAcc0 = 256;      // dV (dkdv) / dQ (dq)
   static constexpr uint32_t kColAcc1 = 256 + D;  // dK (dkdv)
+  static constexpr uint32_t kColA1 = 384;        // S, then dS (dq, odd tiles)
+  static_assert(KEYS || kColAcc0 + D <= kColA1, "dQ TMEM columns");
 };
 
 enum BwdBar : int {
   kBbFixFull = 0,    // the unit's two fixed tiles landed
   kBbFixEmpty = 1,   // MMA: the unit's last use of the fixed tiles done
-  kBbAFull = 2,      // MMA: scratch A (S^T / S) ready
+  kBbAFull = 2,      // MMA: scratch A (S^T / S of even tiles) ready
   kBbBFull = 3,      // MMA: scratch B (dP^T / dP) ready
-  kBbPFull = 4,      // element-wise (8 warps): P^T in TMEM (dkdv) / S read (dq)
+  kBbPFull = 4,      // element-wise (8 warps): P^T in TMEM (dkdv) / dP read (dq)
   kBbDsFull = 5,     // element-wise (8 warps): dS^T / dS in TMEM
   kBbAccFull = 6,    // MMA: the unit's accumulators final
   kBbAccFree = 7,    // epilogue (4 warps): accumulators read
   kBbDrain = 8,      // MMA: all tcgen05 ops done
-  kBbRing = 9,       // [stages] full, then [stages] empty
+  kBbA1Full = 9,     // MMA: S of odd tiles ready (dq)
+  kBbRing = 10,      // dkdv: [stages] full, [stages] empty;
+                     // dq: K [slots] full, K empty, V [slots] full, V empty
 };
 constexpr int kBwdSlotTmem = 480;
 constexpr int kBwdSlotAbort = 484;
@@ -199,7 +212,7 @@ __device__ __forceinline__ void bwd_producer(const CUtensorMap* tm_q, const CUte
                                              const CUtensorMap* tm_v, const CUtensorMap* tm_do,
                                              const BwdArgs& a, uint32_t sbase, uint32_t bars,
                                              const AbortCtx& ab) {
-  using L = BwdLayout<D>;
+  using L = BwdLayout<D, KEYS>;
   constexpr int S = L::kStages;
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
   const CUtensorMap* fix0 = KEYS ? tm_k : tm_q;
@@ -211,9 +224,22 @@ __device__ __forceinline__ void bwd_producer(const CUtensorMap* tm_q, const CUte
     for (int p = 0; p < L::kPanels; ++p)
       ptx::tma_load_4d(dst + p * kPanelBytes, tm, b, 64 * p, row, hh, bb);
   };
-  uint32_t ring = 0, units = 0;
+  constexpr int KS = L::kKSlots, VS = L::kVSlots;
+  // dq rings: K full / empty, V full / empty barrier slots
+  constexpr int kKFull = kBbRing, kKEmpty = kBbRing + KS;
+  constexpr int kVFull = kBbRing + 2 * KS, kVEmpty = kBbRing + 2 * KS + VS;
+  uint32_t ring = 0, kc = 0, vc = 0, units = 0;
   int round = 0, bh = 0, t = 0;
   bool ok = true;
+  // one tile into ring slot `count % slots`, once its previous use is done
+  auto ring_load = [&](int full, int empty, int slots, uint32_t count, uint32_t dst0,
+                       const CUtensorMap* tm, int row, int hh, int bb) {
+    const uint32_t sl = count % slots, ph = (count / slots) & 1u;
+    if (!wait_spin(bar(empty + sl), ph ^ 1u, ab, kStatusProducer)) return false;
+    ptx::mbar_arrive_expect_tx(bar(full + sl), L::kTileBytes);
+    load_tile(dst0 + sl * L::kTileBytes, tm, bar(full + sl), row, hh, bb);
+    return true;
+  };
   while (ok && bwd_next_unit<CAUSAL, KEYS>(round, a, bh, t)) {
     int first, last;
     bwd_span<CAUSAL, KEYS>(a, t, first, last);
@@ -224,25 +250,39 @@ __device__ __forceinline__ void bwd_producer(const CUtensorMap* tm_q, const CUte
     load_tile(sbase + L::kOffFix + L::kTileBytes, fix1, bar(kBbFixFull), 128 * t, hh, bb);
     ++units;
     for (int st = first; st <= last && ok; ++st) {
-      const uint32_t slot = ring % S, ph = (ring / S) & 1u;
-      if (!(ok = wait_spin(bar(kBbRing + S + slot), ph ^ 1u, ab, kStatusProducer))) break;
-      const uint32_t dst = sbase + L::kOffRing + slot * L::kStageBytes;
-      ptx::mbar_arrive_expect_tx(bar(kBbRing + slot),
-                                 2 * L::kTileBytes + (KEYS ? L::kVecBytes : 0));
-      load_tile(dst, str0, bar(kBbRing + slot), 128 * st, hh, bb);
-      load_tile(dst + L::kTileBytes, str1, bar(kBbRing + slot), 128 * st, hh, bb);
       if constexpr (KEYS) {
+        const uint32_t slot = ring % S, ph = (ring / S) & 1u;
+        if (!(ok = wait_spin(bar(kBbRing + S + slot), ph ^ 1u, ab, kStatusProducer))) break;
+        const uint32_t dst = sbase + L::kOffRing + slot * L::kStageBytes;
+        ptx::mbar_arrive_expect_tx(bar(kBbRing + slot), 2 * L::kTileBytes + L::kVecBytes);
+        load_tile(dst, str0, bar(kBbRing + slot), 128 * st, hh, bb);
+        load_tile(dst + L::kTileBytes, str1, bar(kBbRing + slot), 128 * st, hh, bb);
         const size_t v0 = (static_cast<size_t>(bh) * a.n_t + st) * 128;
         ptx::bulk_load(dst + 2 * L::kTileBytes, a.lse2 + v0, 512, bar(kBbRing + slot));
         ptx::bulk_load(dst + 2 * L::kTileBytes + 512, a.delta + v0, 512, bar(kBbRing + slot));
+        ++ring;
+      } else {
+        if (!(ok = ring_load(kKFull, kKEmpty, KS, kc, sbase + L::kOffK, str0, 128 * st, hh, bb)))
+          break;
+        ++kc;
+        if (!(ok = ring_load(kVFull, kVEmpty, VS, vc, sbase + L::kOffV, str1, 128 * st, hh, bb)))
+          break;
+        ++vc;
       }
-      ++ring;
     }
   }
   if (!ok) {  // let the copies already issued land before the CTA exits
-    for (uint32_t sl = 0; sl < static_cast<uint32_t>(S) && sl < ring; ++sl) {
-      const uint32_t lastp = ring - 1 - ((ring - 1 - sl) % S);
-      wait_drain(bar(kBbRing + sl), (lastp / S) & 1u, ab, kStatusDrain);
+    auto drain = [&](int full, int slots, uint32_t count) {
+      for (uint32_t sl = 0; sl < static_cast<uint32_t>(slots) && sl < count; ++sl) {
+        const uint32_t lastp = count - 1 - ((count - 1 - sl) % slots);
+        wait_drain(bar(full + sl), (lastp / slots) & 1u, ab, kStatusDrain);
+      }
+    };
+    if constexpr (KEYS) {
+      drain(kBbRing, S, ring);
+    } else {
+      drain(kKFull, KS, kc);
+      drain(kVFull, VS, vc);
     }
     if (units > 0) wait_drain(bar(kBbFixFull), (units - 1) & 1u, ab, kStatusDrain);
   }
@@ -265,11 +305,11 @@ __device__ __forceinline__ void bwd_issue_ts(uint32_t d_tmem, uint32_t a_tmem, u
   }
 }
 
-// The single MMA-issuing thread (see the order at the top of this file).
+// The single MMA-issuing thread of the dK/dV kernel (order at the top of this file).
 template <int D, bool BF16, bool CAUSAL, bool KEYS>
 __device__ __forceinline__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32_t bars,
                                         uint32_t tmem, const AbortCtx& ab) {
-  using L = BwdLayout<D>;
+  using L = BwdLayout<D, KEYS>;
   constexpr int S = L::kStages;
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
   const uint32_t tA = tmem + L::kColA, tB = tmem + L::kColB;
@@ -280,7 +320,7 @@ __device__ __forceinline__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32
     return wait_spin(bar(kBbRing + r % S), (r / S) & 1u, ab, kStatusMma);
   };
   // The two scratch products of streamed tile r: S^T = K Q^T, dP^T = V dO^T
-  // (dK/dV) or S = Q K^T, dP = dO V^T (dQ); all operands K-major.
+  // (all operands K-major).
   auto scratch_a = [&](uint32_t r) {
     issue_qk<D, BF16>(tA, fix0, stage(r));
     ptx::umma_commit(bar(kBbAFull));
@@ -305,7 +345,7 @@ __device__ __forceinline__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32
       const uint32_t ph = (cnt++) & 1u;
       const bool acc = st > first;
       const bool more = st < last;
-      if constexpr (KEYS) {
+      {
         // dV += P^T dO (P^T in TMEM over the S^T columns; dO used MN-major)
         if (!(ok = wait_spin(bar(kBbPFull), ph, ab, kStatusMma))) break;
         if (!acc && units > 0 &&
@@ -323,26 +363,92 @@ __device__ __forceinline__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32
         bwd_issue_ts<D, BF16>(tAcc1, tB, stage(r), acc);
         ptx::umma_commit(bar(kBbRing + S + r % S));
         if (more) scratch_b(ring);
-      } else {
-        // S was read: the next S while the element-wise role forms dS
-        if (!(ok = wait_spin(bar(kBbPFull), ph, ab, kStatusMma))) break;
-        if (more) {
-          if (!(ok = ring_wait(ring))) break;
-          ptx::tc_fence_after();
-          scratch_a(ring);
-        }
-        // dQ += dS K (dS in TMEM over the dP columns; K used MN-major)
-        if (!(ok = wait_spin(bar(kBbDsFull), ph, ab, kStatusMma))) break;
-        if (!acc && units > 0 &&
-            !(ok = wait_spin(bar(kBbAccFree), (units - 1) & 1u, ab, kStatusMma)))
-          break;
-        ptx::tc_fence_after();
-        bwd_issue_ts<D, BF16>(tAcc0, tB, stage(r), acc);
-        ptx::umma_commit(bar(kBbRing + S + r % S));
-        if (more) scratch_b(ring);  // after dQ has read dS (in-order execution)
       }
     }
     if (!ok) break;
+    ptx::umma_commit(bar(kBbAccFull));
+    ptx::umma_commit(bar(kBbFixEmpty));
+    ++units;
+  }
+  ptx::umma_commit(bar(kBbDrain));
+  wait_drain(bar(kBbDrain), 0u, ab, kStatusDrain);
+}
+
+// The single MMA-issuing thread of the dQ kernel. S of tile j goes to scratch
+// A (even j) or A1 (odd j), dP to B. Per tile j: dP(j+1) once dP(j) was read,
+// dQ(j) += dS(j) K_j once dS(j) is written over S(j), then S(j+2) over it.
+template <int D, bool BF16, bool CAUSAL>
+__device__ __forceinline__ void bwd_mma_dq(const BwdArgs& a, uint32_t sbase, uint32_t bars,
+                                           uint32_t tmem, const AbortCtx& ab) {
+  using L = BwdLayout<D, false>;
+  constexpr int KS = L::kKSlots, VS = L::kVSlots;
+  constexpr int kKFull = kBbRing, kKEmpty = kBbRing + KS;
+  constexpr int kVFull = kBbRing + 2 * KS, kVEmpty = kBbRing + 2 * KS + VS;
+  auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
+  const uint32_t tB = tmem + L::kColB, tAcc = tmem + L::kColAcc0;
+  const uint32_t fixq = sbase + L::kOffFix, fixdo = fixq + L::kTileBytes;
+  auto sbuf = [&](uint32_t c) { return tmem + ((c & 1u) ? L::kColA1 : L::kColA); };
+  auto kslot = [&](uint32_t k) { return sbase + L::kOffK + (k % KS) * L::kTileBytes; };
+  auto vslot = [&](uint32_t v) { return sbase + L::kOffV + (v % VS) * L::kTileBytes; };
+  auto kwait = [&](uint32_t k) {
+    return wait_spin(bar(kKFull + k % KS), (k / KS) & 1u, ab, kStatusMma);
+  };
+  auto vwait = [&](uint32_t v) {
+    return wait_spin(bar(kVFull + v % VS), (v / VS) & 1u, ab, kStatusMma);
+  };
+  // S(c) = Q K^T into its buffer; dP = dO V^T into B (V slot released after)
+  auto issue_s = [&](uint32_t c, uint32_t k) {
+    issue_qk<D, BF16>(sbuf(c), fixq, kslot(k));
+    ptx::umma_commit(bar((c & 1u) ? kBbA1Full : kBbAFull));
+  };
+  auto issue_dp = [&](uint32_t v) {
+    issue_qk<D, BF16>(tB, fixdo, vslot(v));
+    ptx::umma_commit(bar(kBbBFull));
+    ptx::umma_commit(bar(kVEmpty + v % VS));
+  };
+  uint32_t cnt = 0, kc = 0, vc = 0, units = 0;
+  int round = 0, bh = 0, t = 0;
+  bool ok = true;
+  while (ok && bwd_next_unit<CAUSAL, false>(round, a, bh, t)) {
+    int first, last;
+    bwd_span<CAUSAL, false>(a, t, first, last);
+    const uint32_t n = static_cast<uint32_t>(last - first + 1);
+    if (!(ok = wait_spin(bar(kBbFixFull), units & 1u, ab, kStatusMma))) break;
+    if (!(ok = kwait(kc))) break;
+    ptx::tc_fence_after();
+    issue_s(cnt, kc);
+    if (!(ok = vwait(vc))) break;
+    issue_dp(vc);
+    if (n > 1) {
+      if (!(ok = kwait(kc + 1))) break;
+      issue_s(cnt + 1, kc + 1);
+    }
+    for (uint32_t i = 0; i < n; ++i) {
+      const uint32_t c = cnt + i;
+      // dP(c) was read: the next dP into B
+      if (!(ok = wait_spin(bar(kBbPFull), c & 1u, ab, kStatusMma))) break;
+      if (i + 1 < n) {
+        if (!(ok = vwait(vc + i + 1))) break;
+        ptx::tc_fence_after();
+        issue_dp(vc + i + 1);
+      }
+      // dQ += dS K (dS over the S columns of its buffer; K used MN-major)
+      if (!(ok = wait_spin(bar(kBbDsFull), c & 1u, ab, kStatusMma))) break;
+      if (i == 0 && units > 0 &&
+          !(ok = wait_spin(bar(kBbAccFree), (units - 1) & 1u, ab, kStatusMma)))
+        break;
+      ptx::tc_fence_after();
+      bwd_issue_ts<D, BF16>(tAcc, sbuf(c), kslot(kc + i), i > 0);
+      ptx::umma_commit(bar(kKEmpty + (kc + i) % KS));
+      if (i + 2 < n) {  // in-order execution: after dQ(c) has read dS(c)
+        if (!(ok = kwait(kc + i + 2))) break;
+        issue_s(c + 2, kc + i + 2);
+      }
+    }
+    if (!ok) break;
+    cnt += n;
+    kc += n;
+    vc += n;
     ptx::umma_commit(bar(kBbAccFull));
     ptx::umma_commit(bar(kBbFixEmpty));
     ++units;
@@ -372,14 +478,15 @@ template <int D, bool BF16, bool CAUSAL, bool KEYS>
 __device__ __forceinline__ void bwd_elementwise(const BwdArgs& a, const uint8_t* sgen,
                                                 uint32_t bars, uint32_t tmem, const AbortCtx& ab,
                                                 int warp, int lane) {
-  using L = BwdLayout<D>;
+  using L = BwdLayout<D, KEYS>;
   constexpr int S = L::kStages;
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
   const int r = (warp & 3) * 32 + lane;
   const int h = (warp >> 2) - 1;  // column half of this warpgroup
   const int c0 = 64 * h;
   const uint32_t tl = ptx::tmem_lane_base(tmem, warp);
-  const uint32_t tA = tl + L::kColA + static_cast<uint32_t>(c0);
+  const uint32_t tA0 = tl + L::kColA + static_cast<uint32_t>(c0);
+  const uint32_t tA1 = tl + L::kColA1 + static_cast<uint32_t>(c0);
   const uint32_t tB = tl + L::kColB + static_cast<uint32_t>(c0);
   const float cl2 = a.scale_log2;
   const bool ragged = (a.N & 127) != 0;
@@ -398,7 +505,11 @@ __device__ __forceinline__ void bwd_elementwise(const BwdArgs& a, const uint8_t*
     }
     for (int st = first; st <= last; ++st) {
       const uint32_t rr = ring++;
-      const uint32_t ph = (cnt++) & 1u;
+      const uint32_t c = cnt++;
+      const uint32_t ph = c & 1u;
+      // dK/dV: S^T in A every tile; dQ: S alternates between A and A1
+      const bool odd = !KEYS && (c & 1u);
+      const uint32_t tA = odd ? tA1 : tA0;
       // the stage's lse2 / D vectors (TMA-written): observe their barrier too
       if (KEYS && !(ok = wait_bounded_warp(bar(kBbRing + rr % S), (rr / S) & 1u, ab,
                                            kStatusSoftmax)))
@@ -406,18 +517,16 @@ __device__ __forceinline__ void bwd_elementwise(const BwdArgs& a, const uint8_t*
       const float* vec = reinterpret_cast<const float*>(
           sgen + L::kOffRing + (rr % S) * L::kStageBytes + 2 * L::kTileBytes);
       // ---- P: scores of this tile against the row's reference
-      if (!(ok = wait_bounded_warp(bar(kBbAFull), ph, ab, kStatusSoftmax))) break;
+      if (!(ok = KEYS ? wait_bounded_warp(bar(kBbAFull), ph, ab, kStatusSoftmax)
+                      : wait_bounded_warp(bar(odd ? kBbA1Full : kBbAFull), (c >> 1) & 1u, ab,
+                                          kStatusSoftmax)))
+        break;
       ptx::tc_fence_after();
       uint32_t sr[2][32];
       ptx::tmem_ld32(tA, sr[0]);
       ptx::tmem_ld32(tA + 32u, sr[1]);
       ptx::tmem_ld_wait(sr[0]);
       ptx::tmem_ld_wait(sr[1]);
-      if constexpr (!KEYS) {  // S is in registers: the MMA may overwrite it
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar(kBbPFull));
-      }
       // masks only on the diagonal tile (causal) and the ragged last key tile
       const bool masked = KEYS ? (CAUSAL && st == t)
                                : ((CAUSAL && st == t) || (ragged && st == a.n_t - 1));
@@ -461,7 +570,8 @@ __device__ __forceinline__ void bwd_elementwise(const BwdArgs& a, const uint8_t*
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bar(kBbPFull));
       }
-      // ---- dS = P (dP - D) (16 bit) over this half's first 32 dP columns
+      // ---- dS = P (dP - D) (16 bit) over this half's first 32 dP^T columns
+      // (dK/dV) or its first 32 S columns (dQ)
       if (!(ok = wait_bounded_warp(bar(kBbBFull), ph, ab, kStatusSoftmax))) break;
       ptx::tc_fence_after();
       uint32_t dp[2][32];
@@ -469,6 +579,11 @@ __device__ __forceinline__ void bwd_elementwise(const BwdArgs& a, const uint8_t*
       ptx::tmem_ld32(tB + 32u, dp[1]);
       ptx::tmem_ld_wait(dp[0]);
       ptx::tmem_ld_wait(dp[1]);
+      if constexpr (!KEYS) {  // dP is in registers: the MMA may overwrite B
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar(kBbPFull));
+      }
       uint32_t ds[32];
 #pragma unroll
       for (int j = 0; j < 64; j += 4) {
@@ -489,7 +604,7 @@ __device__ __forceinline__ void bwd_elementwise(const BwdArgs& a, const uint8_t*
           ds[c >> 1] = pack2<BF16>(g0, g1);
         }
       }
-      ptx::tmem_st32(tB, ds);
+      ptx::tmem_st32(KEYS ? tB : tA, ds);
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       __syncwarp();
@@ -503,7 +618,7 @@ __device__ __forceinline__ void bwd_elementwise(const BwdArgs& a, const uint8_t*
 template <int D, bool BF16, bool CAUSAL, bool KEYS>
 __device__ __forceinline__ void bwd_epilogue(const BwdArgs& a, uint32_t bars, uint32_t tmem,
                                              const AbortCtx& ab, int warp, int lane) {
-  using L = BwdLayout<D>;
+  using L = BwdLayout<D, KEYS>;
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
   const int r = (warp & 3) * 32 + lane;
   const uint32_t tl = ptx::tmem_lane_base(tmem, warp);
@@ -556,7 +671,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const BwdArgs a) {
-  using L = BwdLayout<D>;
+  using L = BwdLayout<D, KEYS>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -578,10 +693,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ptx::mbar_init(bar(kBbAccFull), 1);
     ptx::mbar_init(bar(kBbAccFree), 4);
     ptx::mbar_init(bar(kBbDrain), 1);
-    for (int s = 0; s < L::kStages; ++s) {
-      ptx::mbar_init(bar(kBbRing + s), 1);
-      ptx::mbar_init(bar(kBbRing + L::kStages + s), 1);
-    }
+    ptx::mbar_init(bar(kBbA1Full), 1);
+    const int ring_bars = KEYS ? 2 * L::kStages : 2 * (L::kKSlots + L::kVSlots);
+    for (int s = 0; s < ring_bars; ++s) ptx::mbar_init(bar(kBbRing + s), 1);
     *abort_flag = 0u;
     ptx::fence_mbar_init();
   }
@@ -598,7 +712,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ptx::setmaxnreg_to<kBwdRegsWG0, kBwdRegsLaunch>();
     if (lane == 0) {
       if (warp == 0) bwd_producer<D, CAUSAL, KEYS>(&tm_q, &tm_k, &tm_v, &tm_do, a, sbase, bars, ab);
-      else if (warp == 1) bwd_mma<D, BF16, CAUSAL, KEYS>(a, sbase, bars, tmem, ab);
+      else if (warp == 1) {
+        if constexpr (KEYS) bwd_mma<D, BF16, CAUSAL, true>(a, sbase, bars, tmem, ab);
+        else bwd_mma_dq<D, BF16, CAUSAL>(a, sbase, bars, tmem, ab);
+      }
     }
   } else if (wgrp <= 2) {
     ptx::setmaxnreg_to<kBwdRegsElem, kBwdRegsLaunch>();

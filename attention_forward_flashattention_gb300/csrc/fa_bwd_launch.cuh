@@ -15,17 +15,18 @@ cudaError_t launch(const CUtensorMap* m, const BwdArgs& a, const void* o, const 
       o, dout, lse, const_cast<float*>(a.lse2), const_cast<float*>(a.delta), a.N, a.n_t, rows);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  constexpr int kSmem = BwdLayout<D>::kSmemBytes;
+  constexpr int kSmemKV = BwdLayout<D, true>::kSmemBytes;
+  constexpr int kSmemQ = BwdLayout<D, false>::kSmemBytes;
   auto kv = fa_bwd_kernel<D, BF16, CAUSAL, true>;
   auto kq = fa_bwd_kernel<D, BF16, CAUSAL, false>;
-  if ((e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem)) !=
+  if ((e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemKV)) !=
           cudaSuccess ||
-      (e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem)) !=
+      (e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemQ)) !=
           cudaSuccess)
     return e;
-  kv<<<grid, kBwdThreads, kSmem, st>>>(m[0], m[1], m[2], m[3], a);
+  kv<<<grid, kBwdThreads, kSmemKV, st>>>(m[0], m[1], m[2], m[3], a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  kq<<<grid, kBwdThreads, kSmem, st>>>(m[0], m[1], m[2], m[3], a);
+  kq<<<grid, kBwdThreads, kSmemQ, st>>>(m[0], m[1], m[2], m[3], a);
   return cudaGetLastError();
 }
 

@@ -76,10 +76,17 @@ def measured_peaks() -> dict:
         return {}
 
 
+# the files fa_fwd_kernel (16-bit) is built and launched from
+FWD_SOURCES = ("ptx.cuh", "fa_common.cuh", "fa_kernel.cuh", "fa_launch.cuh", "fa_fwd_d64.cu",
+               "fa_fwd_d128.cu", "fa_host.cu")
+
+
 def kernel_source_sha256() -> str:
+    """Hash of the forward kernel's sources: a recorded DRAM traffic figure
+    holds only for the sources it was measured on."""
     from attention_forward_flashattention_gb300 import build as fabuild
     h = hashlib.sha256()
-    for name in sorted(fabuild.HEADERS + fabuild.LIB_UNITS):
+    for name in sorted(FWD_SOURCES):
         with open(os.path.join(fabuild.CSRC, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()
