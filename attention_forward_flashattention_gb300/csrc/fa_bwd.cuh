@@ -27,7 +27,7 @@
 //      while dS of tile j is formed; the MMA order is S(j+1), dQ(j), dP(j+1).
 //
 // Roles (16 warps): warp 0 TMA producer (lane 0), warp 1 TMEM owner and MMA
-// issuer (lane 0), warpgroups 1 and 2 the element-wise softmax gradient (one
+// issuer (the whole warp; one elected lane issues), warpgroups 1 and 2 the element-wise softmax gradient (one
 // thread per TMEM lane; warpgroup 1 takes columns 0-63 of each 128-column
 // scratch tile, warpgroup 2 columns 64-127, and each packs its 16-bit result
 // over the first 32 of its own columns), warpgroup 3 the epilogue. Every wait
@@ -62,10 +62,10 @@ struct BwdArgs {
 
 constexpr int kBwdThreads = 512;
 // setmaxnreg split: the 512-thread launch gives 128 registers per thread
-// (65536 / 512); the four warpgroups move to 64 / 192 / 192 / 64, which sum
+// (65536 / 512); the four warpgroups move to 72 / 192 / 192 / 56, which sum
 // to the same 4 x 128.
 constexpr uint32_t kBwdRegsLaunch = 128;
-constexpr uint32_t kBwdRegsWG0 = 64, kBwdRegsElem = 192, kBwdRegsEpi = 64;
+constexpr uint32_t kBwdRegsWG0 = 72, kBwdRegsElem = 192, kBwdRegsEpi = 56;
 static_assert(kBwdRegsWG0 + 2 * kBwdRegsElem + kBwdRegsEpi == 4 * kBwdRegsLaunch,
               "register split");
 static_assert(kBwdRegsLaunch == (65536 / kBwdThreads) / 8 * 8, "launch allocation");
@@ -288,6 +288,74 @@ __device__ __forceinline__ void bwd_producer(const CUtensorMap* tm_q, const CUte
   }
 }
 
+// The MMA issuer is a whole converged warp: waits are warp-uniform, and one
+// elected lane issues each tcgen05 op (cheaper per op than a lone thread).
+__device__ __forceinline__ void mma_ss_elect(uint32_t d, uint64_t a, uint64_t b, uint32_t id,
+                                             uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(id), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_elect(uint32_t d, uint32_t a, uint64_t b, uint32_t id,
+                                             uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a), "l"(b), "r"(id), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void commit_elect(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
+      ::"r"(bar)
+      : "memory");
+}
+
+// Warp-uniform spinning wait (every lane polls; the warp leaves together).
+__device__ __forceinline__ bool wait_spin_warp(uint32_t bar, uint32_t parity, const AbortCtx& ab,
+                                               uint32_t code) {
+  if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
+    if ((it & 63u) == 0u) {
+      const bool late = ptx::globaltimer_ns() - t0 > kWaitLimitNs;
+      const bool stop = *ab.flag != 0u || late;
+      if (__any_sync(0xffffffffu, stop)) {
+        if (__any_sync(0xffffffffu, late)) {
+          *ab.flag = 1u;
+          atomicOr(ab.status, code);
+        }
+        return false;
+      }
+    }
+  }
+}
+
+// C[tmem] = A B^T with A, B 128-row K-major tiles in shared memory (K = D).
+template <int D, bool BF16>
+__device__ __forceinline__ void bwd_issue_ss(uint32_t d_tmem, uint32_t sA, uint32_t sB) {
+  constexpr uint32_t id = ptx::idesc_f16(BF16, false, 128, 128);
+  uint64_t da = desc_kmajor(sA), db = desc_kmajor(sB);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    mma_ss_elect(d_tmem, da, db, id, kk > 0 ? 1u : 0u);
+    // next K step: +32 B inside a panel, or on to the next panel
+    const uint32_t step = ((kk & 3) == 3) ? static_cast<uint32_t>(kPanelBytes - 96) : 32u;
+    da = desc_add(da, step);
+    db = desc_add(db, step);
+    asm volatile("" : "+l"(da), "+l"(db));
+  }
+}
+
 // C[tmem] (+)= A[tmem] B: A is a 16-bit operand written over a scratch tile
 // (elements 0-63 in columns 0-31, 64-127 in columns 64-95, two per column),
 // B a 128-row tile used MN-major (K = its rows).
@@ -299,13 +367,13 @@ __device__ __forceinline__ void bwd_issue_ts(uint32_t d_tmem, uint32_t a_tmem, u
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
     const uint32_t acol = a_tmem + (kk < 4 ? 8u * kk : 64u + 8u * (kk - 4));
-    ptx::umma_f16_ts(d_tmem, acol, db, id, (accumulate || kk > 0) ? 1u : 0u);
+    mma_ts_elect(d_tmem, acol, db, id, (accumulate || kk > 0) ? 1u : 0u);
     db = desc_add(db, 2048u);
     asm volatile("" : "+l"(db));
   }
 }
 
-// The single MMA-issuing thread of the dK/dV kernel (order at the top of this file).
+// The MMA-issuing warp of the dK/dV kernel (order at the top of this file).
 template <int D, bool BF16, bool CAUSAL, bool KEYS>
 __device__ __forceinline__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32_t bars,
                                         uint32_t tmem, const AbortCtx& ab) {
@@ -317,17 +385,17 @@ __device__ __forceinline__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32
   const uint32_t fix0 = sbase + L::kOffFix, fix1 = fix0 + L::kTileBytes;
   auto stage = [&](uint32_t r) { return sbase + L::kOffRing + (r % S) * L::kStageBytes; };
   auto ring_wait = [&](uint32_t r) {
-    return wait_spin(bar(kBbRing + r % S), (r / S) & 1u, ab, kStatusMma);
+    return wait_spin_warp(bar(kBbRing + r % S), (r / S) & 1u, ab, kStatusMma);
   };
   // The two scratch products of streamed tile r: S^T = K Q^T, dP^T = V dO^T
   // (all operands K-major).
   auto scratch_a = [&](uint32_t r) {
-    issue_qk<D, BF16>(tA, fix0, stage(r));
-    ptx::umma_commit(bar(kBbAFull));
+    bwd_issue_ss<D, BF16>(tA, fix0, stage(r));
+    commit_elect(bar(kBbAFull));
   };
   auto scratch_b = [&](uint32_t r) {
-    issue_qk<D, BF16>(tB, fix1, stage(r) + L::kTileBytes);
-    ptx::umma_commit(bar(kBbBFull));
+    bwd_issue_ss<D, BF16>(tB, fix1, stage(r) + L::kTileBytes);
+    commit_elect(bar(kBbBFull));
   };
   uint32_t ring = 0, units = 0, cnt = 0;
   int round = 0, bh = 0, t = 0;
@@ -335,7 +403,7 @@ __device__ __forceinline__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32
   while (ok && bwd_next_unit<CAUSAL, KEYS>(round, a, bh, t)) {
     int first, last;
     bwd_span<CAUSAL, KEYS>(a, t, first, last);
-    if (!(ok = wait_spin(bar(kBbFixFull), units & 1u, ab, kStatusMma))) break;
+    if (!(ok = wait_spin_warp(bar(kBbFixFull), units & 1u, ab, kStatusMma))) break;
     if (!(ok = ring_wait(ring))) break;
     ptx::tc_fence_after();
     scratch_a(ring);
@@ -347,9 +415,9 @@ __device__ __forceinline__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32
       const bool more = st < last;
       {
         // dV += P^T dO (P^T in TMEM over the S^T columns; dO used MN-major)
-        if (!(ok = wait_spin(bar(kBbPFull), ph, ab, kStatusMma))) break;
+        if (!(ok = wait_spin_warp(bar(kBbPFull), ph, ab, kStatusMma))) break;
         if (!acc && units > 0 &&
-            !(ok = wait_spin(bar(kBbAccFree), (units - 1) & 1u, ab, kStatusMma)))
+            !(ok = wait_spin_warp(bar(kBbAccFree), (units - 1) & 1u, ab, kStatusMma)))
           break;
         ptx::tc_fence_after();
         bwd_issue_ts<D, BF16>(tAcc0, tA, stage(r) + L::kTileBytes, acc);
@@ -358,23 +426,23 @@ __device__ __forceinline__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32
           scratch_a(ring);
         }
         // dK += dS^T Q (dS^T in TMEM over the dP^T columns; Q used MN-major)
-        if (!(ok = wait_spin(bar(kBbDsFull), ph, ab, kStatusMma))) break;
+        if (!(ok = wait_spin_warp(bar(kBbDsFull), ph, ab, kStatusMma))) break;
         ptx::tc_fence_after();
         bwd_issue_ts<D, BF16>(tAcc1, tB, stage(r), acc);
-        ptx::umma_commit(bar(kBbRing + S + r % S));
+        commit_elect(bar(kBbRing + S + r % S));
         if (more) scratch_b(ring);
       }
     }
     if (!ok) break;
-    ptx::umma_commit(bar(kBbAccFull));
-    ptx::umma_commit(bar(kBbFixEmpty));
+    commit_elect(bar(kBbAccFull));
+    commit_elect(bar(kBbFixEmpty));
     ++units;
   }
-  ptx::umma_commit(bar(kBbDrain));
+  commit_elect(bar(kBbDrain));
   wait_drain(bar(kBbDrain), 0u, ab, kStatusDrain);
 }
 
-// The single MMA-issuing thread of the dQ kernel. S of tile j goes to scratch
+// The MMA-issuing warp of the dQ kernel. S of tile j goes to scratch
 // A (even j) or A1 (odd j), dP to B. Per tile j: dP(j+1) once dP(j) was read,
 // dQ(j) += dS(j) K_j once dS(j) is written over S(j), then S(j+2) over it.
 template <int D, bool BF16, bool CAUSAL>
@@ -391,20 +459,20 @@ __device__ __forceinline__ void bwd_mma_dq(const BwdArgs& a, uint32_t sbase, uin
   auto kslot = [&](uint32_t k) { return sbase + L::kOffK + (k % KS) * L::kTileBytes; };
   auto vslot = [&](uint32_t v) { return sbase + L::kOffV + (v % VS) * L::kTileBytes; };
   auto kwait = [&](uint32_t k) {
-    return wait_spin(bar(kKFull + k % KS), (k / KS) & 1u, ab, kStatusMma);
+    return wait_spin_warp(bar(kKFull + k % KS), (k / KS) & 1u, ab, kStatusMma);
   };
   auto vwait = [&](uint32_t v) {
-    return wait_spin(bar(kVFull + v % VS), (v / VS) & 1u, ab, kStatusMma);
+    return wait_spin_warp(bar(kVFull + v % VS), (v / VS) & 1u, ab, kStatusMma);
   };
   // S(c) = Q K^T into its buffer; dP = dO V^T into B (V slot released after)
   auto issue_s = [&](uint32_t c, uint32_t k) {
-    issue_qk<D, BF16>(sbuf(c), fixq, kslot(k));
-    ptx::umma_commit(bar((c & 1u) ? kBbA1Full : kBbAFull));
+    bwd_issue_ss<D, BF16>(sbuf(c), fixq, kslot(k));
+    commit_elect(bar((c & 1u) ? kBbA1Full : kBbAFull));
   };
   auto issue_dp = [&](uint32_t v) {
-    issue_qk<D, BF16>(tB, fixdo, vslot(v));
-    ptx::umma_commit(bar(kBbBFull));
-    ptx::umma_commit(bar(kVEmpty + v % VS));
+    bwd_issue_ss<D, BF16>(tB, fixdo, vslot(v));
+    commit_elect(bar(kBbBFull));
+    commit_elect(bar(kVEmpty + v % VS));
   };
   uint32_t cnt = 0, kc = 0, vc = 0, units = 0;
   int round = 0, bh = 0, t = 0;
@@ -413,7 +481,7 @@ __device__ __forceinline__ void bwd_mma_dq(const BwdArgs& a, uint32_t sbase, uin
     int first, last;
     bwd_span<CAUSAL, false>(a, t, first, last);
     const uint32_t n = static_cast<uint32_t>(last - first + 1);
-    if (!(ok = wait_spin(bar(kBbFixFull), units & 1u, ab, kStatusMma))) break;
+    if (!(ok = wait_spin_warp(bar(kBbFixFull), units & 1u, ab, kStatusMma))) break;
     if (!(ok = kwait(kc))) break;
     ptx::tc_fence_after();
     issue_s(cnt, kc);
@@ -426,20 +494,20 @@ __device__ __forceinline__ void bwd_mma_dq(const BwdArgs& a, uint32_t sbase, uin
     for (uint32_t i = 0; i < n; ++i) {
       const uint32_t c = cnt + i;
       // dP(c) was read: the next dP into B
-      if (!(ok = wait_spin(bar(kBbPFull), c & 1u, ab, kStatusMma))) break;
+      if (!(ok = wait_spin_warp(bar(kBbPFull), c & 1u, ab, kStatusMma))) break;
       if (i + 1 < n) {
         if (!(ok = vwait(vc + i + 1))) break;
         ptx::tc_fence_after();
         issue_dp(vc + i + 1);
       }
       // dQ += dS K (dS over the S columns of its buffer; K used MN-major)
-      if (!(ok = wait_spin(bar(kBbDsFull), c & 1u, ab, kStatusMma))) break;
+      if (!(ok = wait_spin_warp(bar(kBbDsFull), c & 1u, ab, kStatusMma))) break;
       if (i == 0 && units > 0 &&
-          !(ok = wait_spin(bar(kBbAccFree), (units - 1) & 1u, ab, kStatusMma)))
+          !(ok = wait_spin_warp(bar(kBbAccFree), (units - 1) & 1u, ab, kStatusMma)))
         break;
       ptx::tc_fence_after();
       bwd_issue_ts<D, BF16>(tAcc, sbuf(c), kslot(kc + i), i > 0);
-      ptx::umma_commit(bar(kKEmpty + (kc + i) % KS));
+      commit_elect(bar(kKEmpty + (kc + i) % KS));
       if (i + 2 < n) {  // in-order execution: after dQ(c) has read dS(c)
         if (!(ok = kwait(kc + i + 2))) break;
         issue_s(c + 2, kc + i + 2);
@@ -449,11 +517,11 @@ __device__ __forceinline__ void bwd_mma_dq(const BwdArgs& a, uint32_t sbase, uin
     cnt += n;
     kc += n;
     vc += n;
-    ptx::umma_commit(bar(kBbAccFull));
-    ptx::umma_commit(bar(kBbFixEmpty));
+    commit_elect(bar(kBbAccFull));
+    commit_elect(bar(kBbFixEmpty));
     ++units;
   }
-  ptx::umma_commit(bar(kBbDrain));
+  commit_elect(bar(kBbDrain));
   wait_drain(bar(kBbDrain), 0u, ab, kStatusDrain);
 }
 
@@ -710,12 +778,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int wgrp = warp >> 2;
   if (wgrp == 0) {
     ptx::setmaxnreg_to<kBwdRegsWG0, kBwdRegsLaunch>();
-    if (lane == 0) {
-      if (warp == 0) bwd_producer<D, CAUSAL, KEYS>(&tm_q, &tm_k, &tm_v, &tm_do, a, sbase, bars, ab);
-      else if (warp == 1) {
-        if constexpr (KEYS) bwd_mma<D, BF16, CAUSAL, true>(a, sbase, bars, tmem, ab);
-        else bwd_mma_dq<D, BF16, CAUSAL>(a, sbase, bars, tmem, ab);
-      }
+    if (warp == 0) {
+      if (lane == 0) bwd_producer<D, CAUSAL, KEYS>(&tm_q, &tm_k, &tm_v, &tm_do, a, sbase, bars, ab);
+    } else if (warp == 1) {  // the whole warp
+      if constexpr (KEYS) bwd_mma<D, BF16, CAUSAL, true>(a, sbase, bars, tmem, ab);
+      else bwd_mma_dq<D, BF16, CAUSAL>(a, sbase, bars, tmem, ab);
     }
   } else if (wgrp <= 2) {
     ptx::setmaxnreg_to<kBwdRegsElem, kBwdRegsLaunch>();
