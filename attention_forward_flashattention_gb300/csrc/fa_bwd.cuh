@@ -20,19 +20,19 @@
 //      dK and dV accumulate in TMEM; the epilogue scales dK and stores both.
 //   3. dQ kernel: one unit = one 128-row query tile; it loops over the key
 //      tiles it sees. Per key tile j (lane = query row):
-//        S = Q K_j^T, dP = dO V_j^T
-//        P = 2^(c S - lse2), dS = P (dP - D)  -> 16 bit over the dP columns
+//        S = Q K_j^T (into one of two S buffers), dP = dO V_j^T
+//        P = 2^(c S - lse2), dS = P (dP - D)  -> 16 bit over the S columns
 //        dQ += dS K_j                             (A = dS from TMEM)
-//      S is released as soon as it is read, so S of tile j+1 is computed
-//      while dS of tile j is formed; the MMA order is S(j+1), dQ(j), dP(j+1).
+//      dP is released as soon as it is read, so dP of tile j+1 is computed
+//      while dS of tile j is formed; the MMA order is dP(j+1), dQ(j), S(j+2).
 //
-// Roles (16 warps): warp 0 TMA producer (lane 0), warp 1 TMEM owner and MMA
-// issuer (the whole warp; one elected lane issues), warpgroups 1 and 2 the element-wise softmax gradient (one
-// thread per TMEM lane; warpgroup 1 takes columns 0-63 of each 128-column
-// scratch tile, warpgroup 2 columns 64-127, and each packs its 16-bit result
-// over the first 32 of its own columns), warpgroup 3 the epilogue. Every wait
-// is bounded as in the forward (abort flag, status bits, drain before TMEM is
-// freed).
+// Roles (16 warps): warp 0 TMA producer (lane 0); warp 1 TMEM owner and MMA
+// issuer (the whole warp, one elected lane issuing); warpgroups 1 and 2 the
+// element-wise softmax gradient (one thread per TMEM lane; warpgroup 1 takes
+// columns 0-63 of each 128-column scratch tile, warpgroup 2 columns 64-127,
+// and each packs its 16-bit result over the first 32 of its own columns);
+// warpgroup 3 the epilogue. Every wait is bounded as in the forward (abort
+// flag, status bits, drain before TMEM is freed).
 #pragma once
 
 #include <cuda.h>
@@ -288,74 +288,6 @@ __device__ __forceinline__ void bwd_producer(const CUtensorMap* tm_q, const CUte
   }
 }
 
-// The MMA issuer is a whole converged warp: waits are warp-uniform, and one
-// elected lane issues each tcgen05 op (cheaper per op than a lone thread).
-__device__ __forceinline__ void mma_ss_elect(uint32_t d, uint64_t a, uint64_t b, uint32_t id,
-                                             uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred e, p;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-      "l"(a), "l"(b), "r"(id), "r"(acc)
-      : "memory");
-}
-__device__ __forceinline__ void mma_ts_elect(uint32_t d, uint32_t a, uint64_t b, uint32_t id,
-                                             uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred e, p;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
-      "r"(a), "l"(b), "r"(id), "r"(acc)
-      : "memory");
-}
-__device__ __forceinline__ void commit_elect(uint32_t bar) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
-      ::"r"(bar)
-      : "memory");
-}
-
-// Warp-uniform spinning wait (every lane polls; the warp leaves together).
-__device__ __forceinline__ bool wait_spin_warp(uint32_t bar, uint32_t parity, const AbortCtx& ab,
-                                               uint32_t code) {
-  if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
-  const uint64_t t0 = ptx::globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
-    if ((it & 63u) == 0u) {
-      const bool late = ptx::globaltimer_ns() - t0 > kWaitLimitNs;
-      const bool stop = *ab.flag != 0u || late;
-      if (__any_sync(0xffffffffu, stop)) {
-        if (__any_sync(0xffffffffu, late)) {
-          *ab.flag = 1u;
-          atomicOr(ab.status, code);
-        }
-        return false;
-      }
-    }
-  }
-}
-
-// C[tmem] = A B^T with A, B 128-row K-major tiles in shared memory (K = D).
-template <int D, bool BF16>
-__device__ __forceinline__ void bwd_issue_ss(uint32_t d_tmem, uint32_t sA, uint32_t sB) {
-  constexpr uint32_t id = ptx::idesc_f16(BF16, false, 128, 128);
-  uint64_t da = desc_kmajor(sA), db = desc_kmajor(sB);
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    mma_ss_elect(d_tmem, da, db, id, kk > 0 ? 1u : 0u);
-    // next K step: +32 B inside a panel, or on to the next panel
-    const uint32_t step = ((kk & 3) == 3) ? static_cast<uint32_t>(kPanelBytes - 96) : 32u;
-    da = desc_add(da, step);
-    db = desc_add(db, step);
-    asm volatile("" : "+l"(da), "+l"(db));
-  }
-}
-
 // C[tmem] (+)= A[tmem] B: A is a 16-bit operand written over a scratch tile
 // (elements 0-63 in columns 0-31, 64-127 in columns 64-95, two per column),
 // B a 128-row tile used MN-major (K = its rows).
@@ -367,7 +299,7 @@ __device__ __forceinline__ void bwd_issue_ts(uint32_t d_tmem, uint32_t a_tmem, u
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
     const uint32_t acol = a_tmem + (kk < 4 ? 8u * kk : 64u + 8u * (kk - 4));
-    mma_ts_elect(d_tmem, acol, db, id, (accumulate || kk > 0) ? 1u : 0u);
+    ptx::umma_f16_ts_elect(d_tmem, acol, db, id, (accumulate || kk > 0) ? 1u : 0u);
     db = desc_add(db, 2048u);
     asm volatile("" : "+l"(db));
   }
@@ -390,12 +322,12 @@ __device__ __forceinline__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32
   // The two scratch products of streamed tile r: S^T = K Q^T, dP^T = V dO^T
   // (all operands K-major).
   auto scratch_a = [&](uint32_t r) {
-    bwd_issue_ss<D, BF16>(tA, fix0, stage(r));
-    commit_elect(bar(kBbAFull));
+    issue_qk<D, BF16, true>(tA, fix0, stage(r));
+    ptx::umma_commit_elect(bar(kBbAFull));
   };
   auto scratch_b = [&](uint32_t r) {
-    bwd_issue_ss<D, BF16>(tB, fix1, stage(r) + L::kTileBytes);
-    commit_elect(bar(kBbBFull));
+    issue_qk<D, BF16, true>(tB, fix1, stage(r) + L::kTileBytes);
+    ptx::umma_commit_elect(bar(kBbBFull));
   };
   uint32_t ring = 0, units = 0, cnt = 0;
   int round = 0, bh = 0, t = 0;
@@ -429,16 +361,16 @@ __device__ __forceinline__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32
         if (!(ok = wait_spin_warp(bar(kBbDsFull), ph, ab, kStatusMma))) break;
         ptx::tc_fence_after();
         bwd_issue_ts<D, BF16>(tAcc1, tB, stage(r), acc);
-        commit_elect(bar(kBbRing + S + r % S));
+        ptx::umma_commit_elect(bar(kBbRing + S + r % S));
         if (more) scratch_b(ring);
       }
     }
     if (!ok) break;
-    commit_elect(bar(kBbAccFull));
-    commit_elect(bar(kBbFixEmpty));
+    ptx::umma_commit_elect(bar(kBbAccFull));
+    ptx::umma_commit_elect(bar(kBbFixEmpty));
     ++units;
   }
-  commit_elect(bar(kBbDrain));
+  ptx::umma_commit_elect(bar(kBbDrain));
   wait_drain(bar(kBbDrain), 0u, ab, kStatusDrain);
 }
 
@@ -466,13 +398,13 @@ __device__ __forceinline__ void bwd_mma_dq(const BwdArgs& a, uint32_t sbase, uin
   };
   // S(c) = Q K^T into its buffer; dP = dO V^T into B (V slot released after)
   auto issue_s = [&](uint32_t c, uint32_t k) {
-    bwd_issue_ss<D, BF16>(sbuf(c), fixq, kslot(k));
-    commit_elect(bar((c & 1u) ? kBbA1Full : kBbAFull));
+    issue_qk<D, BF16, true>(sbuf(c), fixq, kslot(k));
+    ptx::umma_commit_elect(bar((c & 1u) ? kBbA1Full : kBbAFull));
   };
   auto issue_dp = [&](uint32_t v) {
-    bwd_issue_ss<D, BF16>(tB, fixdo, vslot(v));
-    commit_elect(bar(kBbBFull));
-    commit_elect(bar(kVEmpty + v % VS));
+    issue_qk<D, BF16, true>(tB, fixdo, vslot(v));
+    ptx::umma_commit_elect(bar(kBbBFull));
+    ptx::umma_commit_elect(bar(kVEmpty + v % VS));
   };
   uint32_t cnt = 0, kc = 0, vc = 0, units = 0;
   int round = 0, bh = 0, t = 0;
@@ -507,7 +439,7 @@ __device__ __forceinline__ void bwd_mma_dq(const BwdArgs& a, uint32_t sbase, uin
         break;
       ptx::tc_fence_after();
       bwd_issue_ts<D, BF16>(tAcc, sbuf(c), kslot(kc + i), i > 0);
-      commit_elect(bar(kKEmpty + (kc + i) % KS));
+      ptx::umma_commit_elect(bar(kKEmpty + (kc + i) % KS));
       if (i + 2 < n) {  // in-order execution: after dQ(c) has read dS(c)
         if (!(ok = kwait(kc + i + 2))) break;
         issue_s(c + 2, kc + i + 2);
@@ -517,11 +449,11 @@ __device__ __forceinline__ void bwd_mma_dq(const BwdArgs& a, uint32_t sbase, uin
     cnt += n;
     kc += n;
     vc += n;
-    commit_elect(bar(kBbAccFull));
-    commit_elect(bar(kBbFixEmpty));
+    ptx::umma_commit_elect(bar(kBbAccFull));
+    ptx::umma_commit_elect(bar(kBbFixEmpty));
     ++units;
   }
-  commit_elect(bar(kBbDrain));
+  ptx::umma_commit_elect(bar(kBbDrain));
   wait_drain(bar(kBbDrain), 0u, ab, kStatusDrain);
 }
 

@@ -86,6 +86,28 @@ __device__ __forceinline__ bool wait_spin(uint32_t bar, uint32_t parity, const A
   }
 }
 
+// Warp-uniform spinning wait for a role run by a whole warp (every lane
+// polls; the warp leaves the loop together, so it stays converged).
+__device__ __forceinline__ bool wait_spin_warp(uint32_t bar, uint32_t parity, const AbortCtx& ab,
+                                               uint32_t code) {
+  if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
+    if ((it & 63u) == 0u) {
+      const bool late = ptx::globaltimer_ns() - t0 > kWaitLimitNs;
+      const bool stop = *ab.flag != 0u || late;
+      if (__any_sync(0xffffffffu, stop)) {
+        if (__any_sync(0xffffffffu, late)) {
+          *ab.flag = 1u;
+          atomicOr(ab.status, code);
+        }
+        return false;
+      }
+    }
+  }
+}
+
 // Same, ignoring the abort flag: used to drain work already in flight
 // (TMA loads, MMAs) before a CTA exits.
 __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, const AbortCtx& ab,
@@ -197,12 +219,13 @@ __device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) {
 // S[tmem: 128 lanes x 128 cols] = Q[128 x D] * K[128 x D]^T, both K-major,
 // from precomputed base descriptors (a K step of 16 is +32 B inside a panel,
 // the next panel every 4 steps).
-template <int D, bool BF16>
+template <int D, bool BF16, bool kElect = false>
 __device__ __forceinline__ void issue_qk_desc(uint32_t d_tmem, uint64_t dq, uint64_t dk) {
   constexpr uint32_t id = ptx::idesc_f16(BF16, false, 128, 128);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    ptx::umma_f16_ss(d_tmem, dq, dk, id, kk > 0 ? 1u : 0u);
+    if constexpr (kElect) ptx::umma_f16_ss_elect(d_tmem, dq, dk, id, kk > 0 ? 1u : 0u);
+    else ptx::umma_f16_ss(d_tmem, dq, dk, id, kk > 0 ? 1u : 0u);
     // next K step: +32 B inside a panel, or on to the next panel
     const uint32_t step = ((kk & 3) == 3) ? static_cast<uint32_t>(kPanelBytes - 96) : 32u;
     dq = desc_add(dq, step);
@@ -211,9 +234,9 @@ __device__ __forceinline__ void issue_qk_desc(uint32_t d_tmem, uint64_t dq, uint
   }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool kElect = false>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t sQ, uint32_t sK) {
-  issue_qk_desc<D, BF16>(d_tmem, desc_kmajor(sQ), desc_kmajor(sK));
+  issue_qk_desc<D, BF16, kElect>(d_tmem, desc_kmajor(sQ), desc_kmajor(sK));
 }
 
 // O[tmem: 128 lanes x D cols] (+)= P[128 x 128] * V[128 x D]. P is K-major
@@ -236,13 +259,15 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t sP, uint32_t 
 
 // O[tmem] (+)= P[tmem] * V[smem]: the P operand comes from tensor memory
 // (128 lanes x 64 columns holding 128 packed 16-bit keys), V as in issue_pv.
-template <int D, bool BF16>
+template <int D, bool BF16, bool kElect = false>
 __device__ __forceinline__ void issue_pv_ts_desc(uint32_t d_tmem, uint32_t p_tmem, uint64_t dv,
                                                  bool accumulate) {
   constexpr uint32_t id = ptx::idesc_f16(BF16, true, 128, D);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
-    ptx::umma_f16_ts(d_tmem, p_tmem + 8u * kk, dv, id, (accumulate || kk > 0) ? 1u : 0u);
+    const uint32_t acc = (accumulate || kk > 0) ? 1u : 0u;
+    if constexpr (kElect) ptx::umma_f16_ts_elect(d_tmem, p_tmem + 8u * kk, dv, id, acc);
+    else ptx::umma_f16_ts(d_tmem, p_tmem + 8u * kk, dv, id, acc);
     dv = desc_add(dv, 2048u);
     asm volatile("" : "+l"(dv));
   }
@@ -257,11 +282,13 @@ __device__ __forceinline__ void issue_pv_ts(uint32_t d_tmem, uint32_t p_tmem, ui
 // 8-bit (e4m3) products for head dimension 128: a 128-element row is one
 // 128-byte SW128 panel, and one MMA covers K = 32 (+32 bytes per step).
 // S[tmem] = Q[128 x 128] K[128 x 128]^T, both K-major in shared memory.
+template <bool kElect = false>
 __device__ __forceinline__ void issue_qk_fp8(uint32_t d_tmem, uint64_t dq, uint64_t dk) {
   constexpr uint32_t id = ptx::idesc_f8(128, 128);
 #pragma unroll
   for (int kk = 0; kk < 4; ++kk) {
-    ptx::umma_f8_ss(d_tmem, dq, dk, id, kk > 0 ? 1u : 0u);
+    if constexpr (kElect) ptx::umma_f8_ss_elect(d_tmem, dq, dk, id, kk > 0 ? 1u : 0u);
+    else ptx::umma_f8_ss(d_tmem, dq, dk, id, kk > 0 ? 1u : 0u);
     dq = desc_add(dq, 32u);
     dk = desc_add(dk, 32u);
     asm volatile("" : "+l"(dq), "+l"(dk));
@@ -269,12 +296,15 @@ __device__ __forceinline__ void issue_qk_fp8(uint32_t d_tmem, uint64_t dq, uint6
 }
 // O[tmem] (+)= P[tmem: 128 lanes x 32 columns, four keys per column] V with V
 // given transposed, V^T[128 columns of O][128 keys], K-major in shared memory.
+template <bool kElect = false>
 __device__ __forceinline__ void issue_pv_fp8(uint32_t d_tmem, uint32_t p_tmem, uint64_t dvt,
                                              bool accumulate) {
   constexpr uint32_t id = ptx::idesc_f8(128, 128);
 #pragma unroll
   for (int kk = 0; kk < 4; ++kk) {
-    ptx::umma_f8_ts(d_tmem, p_tmem + 8u * kk, dvt, id, (accumulate || kk > 0) ? 1u : 0u);
+    const uint32_t acc = (accumulate || kk > 0) ? 1u : 0u;
+    if constexpr (kElect) ptx::umma_f8_ts_elect(d_tmem, p_tmem + 8u * kk, dvt, id, acc);
+    else ptx::umma_f8_ts(d_tmem, p_tmem + 8u * kk, dvt, id, acc);
     dvt = desc_add(dvt, 32u);
     asm volatile("" : "+l"(dvt));
   }

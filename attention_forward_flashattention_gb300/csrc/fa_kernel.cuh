@@ -9,7 +9,8 @@
 // Warp roles (16 warps = 4 warpgroups, 512 threads):
 //   WG0  warp 0: TMA producer: Q tiles, then K_j, V_j into a ring of stages
 //                (the producer loop of "TMA + Warp Specialization", 17.4).
-//        warp 1: TMEM owner and single-thread MMA issuer (tcgen05.mma is
+//        warp 1: TMEM owner and MMA issuer: the whole warp runs the loop and
+//                one elected lane issues each tcgen05 op (tcgen05.mma is
 //                issued by one thread, "TCA 51%, MFU below 8%", B200 section).
 //        warps 2-3 idle.
 //   WG1  softmax of Q tile 0, one thread per row = TMEM lane (the B300
@@ -28,7 +29,7 @@
 //
 // MMA order: S0 = Q0 K_0^T, S1 = Q1 K_0^T, then per KV tile j
 //   O0 += P0 V_j, S0 = Q0 K_{j+1}^T, O1 += P1 V_j, S1 = Q1 K_{j+1}^T.
-// Tensor-core ops of one thread execute in issue order, so S_i(j+1) may
+// Tensor-core ops of the issuer execute in issue order, so S_i(j+1) may
 // overwrite the S_i / P_i columns right after the PV that consumed P_i(j),
 // and the commit that signals S_i(j+1) also implies O_i holds PV_i(j).
 //
@@ -201,11 +202,13 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tm_q, const CUt
   }
 }
 
-// One thread issues every tcgen05 instruction. An MMA of 128x128x16 keeps the
-// tensor core busy ~64 cycles while its issue costs ~50, so the loop keeps
+// One warp issues every tcgen05 instruction through an elected lane. An MMA
+// of 128x128x16 keeps the tensor core busy ~64 cycles while its issue costs
+// ~40-50, and the queue drains whenever the issuer waits, so the loop keeps
 // everything else minimal: descriptors are built once and advanced in place,
-// waits are single-thread try_waits, and each step commits only what a
-// waiter needs.
+// waits are warp-uniform try_waits, commits are elected (a few cycles each,
+// against ~47 from a lone thread), and each step commits only what a waiter
+// needs.
 template <int D, bool BF16, bool CAUSAL, bool FP8>
 __device__ __forceinline__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t bars,
                                          uint32_t tmem, const AbortCtx& ab) {
@@ -220,20 +223,20 @@ __device__ __forceinline__ void mma_role(const FwdArgs& a, uint32_t sbase, uint3
   const uint32_t tS[2] = {tmem + L::kColS, tmem + L::kColS + 128};
   const uint32_t tO[2] = {tmem + L::kColO, tmem + L::kColO + D};
   auto qk = [&](int i, uint64_t dk) {
-    if constexpr (FP8) issue_qk_fp8(tS[i], dQ[i], dk);
-    else issue_qk_desc<D, BF16>(tS[i], dQ[i], dk);
+    if constexpr (FP8) issue_qk_fp8<true>(tS[i], dQ[i], dk);
+    else issue_qk_desc<D, BF16, true>(tS[i], dQ[i], dk);
   };
   auto slot_off = [](uint32_t idx) { return (idx % S) * static_cast<uint32_t>(L::kTileBytes); };
   auto kv_wait = [&](uint32_t idx) {
-    return wait_spin(bar(kBarKVFull + idx % S), (idx / S) & 1u, ab, kStatusMma);
+    return wait_spin_warp(bar(kBarKVFull + idx % S), (idx / S) & 1u, ab, kStatusMma);
   };
   uint32_t ring = 0, units = 0, pcnt[2] = {0u, 0u};
   int round = 0, bh = 0, mblk = 0;
   bool ok = true;
   while (ok && next_unit<CAUSAL>(round, a, bh, mblk)) {
     const int nkv = unit_kv_tiles<CAUSAL>(a, mblk);
-    ok = wait_spin(bar(kBarQFull + 0), units & 1u, ab, kStatusMma) &&
-         wait_spin(bar(kBarQFull + 1), units & 1u, ab, kStatusMma);
+    ok = wait_spin_warp(bar(kBarQFull + 0), units & 1u, ab, kStatusMma) &&
+         wait_spin_warp(bar(kBarQFull + 1), units & 1u, ab, kStatusMma);
     if (!ok) break;
     // S_i(0) = Q_i K_0^T
     const uint32_t k0 = ring++;
@@ -242,11 +245,11 @@ __device__ __forceinline__ void mma_role(const FwdArgs& a, uint32_t sbase, uint3
     {
       const uint64_t dk = desc_add(dK0, slot_off(k0));
       qk(0, dk);
-      ptx::umma_commit(bar(kBarSFull + 0));
+      ptx::umma_commit_elect(bar(kBarSFull + 0));
       qk(1, dk);
-      ptx::umma_commit(bar(kBarSFull + 1));
-      ptx::umma_commit(bar(kBarKVFull + S + k0 % S));
-      if (nkv == 1) ptx::umma_commit(bar(kBarQEmpty));
+      ptx::umma_commit_elect(bar(kBarSFull + 1));
+      ptx::umma_commit_elect(bar(kBarKVFull + S + k0 % S));
+      if (nkv == 1) ptx::umma_commit_elect(bar(kBarQEmpty));
     }
     // Slot releases of a step are committed after the next step's first PV is
     // queued, so the path from "P ready" to the tensor core stays short.
@@ -261,45 +264,45 @@ __device__ __forceinline__ void mma_role(const FwdArgs& a, uint32_t sbase, uint3
       const uint64_t dk = desc_add(dK0, slot_off(kn));
       for (int i = 0; i < 2; ++i) {
         // O_i += P_i V_j (P_i read from TMEM), then S_i = Q_i K_{j+1}^T
-        if (!(ok = wait_spin(bar(kBarPFull + i), (pcnt[i]++) & 1u, ab, kStatusMma))) break;
+        if (!(ok = wait_spin_warp(bar(kBarPFull + i), (pcnt[i]++) & 1u, ab, kStatusMma))) break;
         if (j == 0 && units > 0 &&
-            !(ok = wait_spin(bar(kBarOFree + i), (units - 1) & 1u, ab, kStatusMma)))
+            !(ok = wait_spin_warp(bar(kBarOFree + i), (units - 1) & 1u, ab, kStatusMma)))
           break;
         ptx::tc_fence_after();
-        if constexpr (FP8) issue_pv_fp8(tO[i], tS[i], dv, j > 0);
-        else issue_pv_ts_desc<D, BF16>(tO[i], tS[i], dv, j > 0);
+        if constexpr (FP8) issue_pv_fp8<true>(tO[i], tS[i], dv, j > 0);
+        else issue_pv_ts_desc<D, BF16, true>(tO[i], tS[i], dv, j > 0);
         if (i == 0 && rel_pending) {
-          ptx::umma_commit(bar(kBarKVFull + S + rel_v % S));
-          ptx::umma_commit(bar(kBarKVFull + S + rel_k % S));
+          ptx::umma_commit_elect(bar(kBarKVFull + S + rel_v % S));
+          ptx::umma_commit_elect(bar(kBarKVFull + S + rel_k % S));
           rel_pending = false;
         }
         if (!more) {
-          if (i == 1) ptx::umma_commit(bar(kBarKVFull + S + vj % S));
-          ptx::umma_commit(bar(kBarOFull + i));
+          if (i == 1) ptx::umma_commit_elect(bar(kBarKVFull + S + vj % S));
+          ptx::umma_commit_elect(bar(kBarOFull + i));
           continue;
         }
         if (i == 0 && !(ok = kv_wait(kn))) break;
         qk(i, dk);
-        ptx::umma_commit(bar(kBarSFull + i));
+        ptx::umma_commit_elect(bar(kBarSFull + i));
         if (i == 1) {
           // V_j and K_{j+1} are both consumed once S1(j+1) completes
           rel_v = vj;
           rel_k = kn;
           rel_pending = true;
-          if (j + 2 == nkv) ptx::umma_commit(bar(kBarQEmpty));
+          if (j + 2 == nkv) ptx::umma_commit_elect(bar(kBarQEmpty));
         }
       }
       if (!ok) break;
       if (more) ++ring;
     }
     if (rel_pending) {  // (only when the unit ended early on an abort)
-      ptx::umma_commit(bar(kBarKVFull + S + rel_v % S));
-      ptx::umma_commit(bar(kBarKVFull + S + rel_k % S));
+      ptx::umma_commit_elect(bar(kBarKVFull + S + rel_v % S));
+      ptx::umma_commit_elect(bar(kBarKVFull + S + rel_k % S));
     }
     ++units;
   }
-  // Every tcgen05 op this thread issued must finish before TMEM is freed.
-  ptx::umma_commit(bar(kBarDrain));
+  // Every tcgen05 op this warp issued must finish before TMEM is freed.
+  ptx::umma_commit_elect(bar(kBarDrain));
   wait_drain(bar(kBarDrain), 0u, ab, kStatusDrain);
 }
 
@@ -557,7 +560,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (warp == 0) {
       if (lane == 0) producer_role<D, BF16, CAUSAL, FP8>(&tm_q, &tm_k, &tm_v, a, sbase, bars, ab);
     } else if (warp == 1) {
-      if (lane == 0) mma_role<D, BF16, CAUSAL, FP8>(a, sbase, bars, tmem, ab);
+      mma_role<D, BF16, CAUSAL, FP8>(a, sbase, bars, tmem, ab);  // the whole warp
     }
   } else if (wgrp < 3) {
     ptx::setmaxnreg_inc<kRegsSoftmax>();
