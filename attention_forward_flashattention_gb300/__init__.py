@@ -78,6 +78,13 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             lib.fa_bwd.restype = i
             lib.fa_bwd_workspace_size.argtypes = [i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
             lib.fa_bwd_workspace_size.restype = i
+        if hasattr(lib, "fa_fwd_host"):
+            lib.fa_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp,
+                                        ctypes.c_size_t, vp]
+            lib.fa_fwd_host.restype = i
+            lib.fa_fwd_host_workspace_size.argtypes = [i, i, i, i,
+                                                       ctypes.POINTER(ctypes.c_size_t)]
+            lib.fa_fwd_host_workspace_size.restype = i
         lib.fa_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
         lib.fa_fwd_noalloc.restype = i
         lib.fa_check.argtypes = [vp]
@@ -141,6 +148,24 @@ def fa_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
     rc = load_library().fa_bwd_workspace_size(B, H, N, d, ctypes.byref(n))
     if rc != FA_OK:
         raise FaError(rc, "fa_bwd_workspace_size")
+    return int(n.value)
+
+
+def fa_fwd_host(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, d: int,
+                causal: bool, scale: float, dtype: int, workspace: int, workspace_size: int,
+                stream: int = 0) -> int:
+    """Same arguments as the C function (host q, k, v, o, lse and a device
+    workspace, pointers as ints); returns the status."""
+    return load_library().fa_fwd_host(q, k, v, o, lse, B, H, N, d, int(bool(causal)),
+                                      float(scale), int(dtype), workspace, int(workspace_size),
+                                      stream)
+
+
+def fa_fwd_host_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    n = ctypes.c_size_t(0)
+    rc = load_library().fa_fwd_host_workspace_size(B, H, N, d, ctypes.byref(n))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_host_workspace_size")
     return int(n.value)
 
 
@@ -225,6 +250,50 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     attention_forward_into(q, k, v, o, lse, causal, scale, stream)
+    return o, lse
+
+
+def attention_forward_host_into(q, k, v, o, lse, workspace, causal: bool = False,
+                                scale: float | None = None, stream=None) -> None:
+    """Enqueues fa_fwd_host: q, k, v, o contiguous CPU tensors [B, H, N, d] of
+    one dtype (fp16 / bf16; page-locked for copy / compute overlap), lse a
+    contiguous CPU float32 [B, H, N] tensor, workspace a CUDA uint8 tensor of
+    at least fa_fwd_host_workspace_size(B, H, N, d) bytes. o and lse hold the
+    result once the stream has passed the call."""
+    import torch
+    B, H, N, d = q.shape
+    ok = (all(tuple(t.shape) == (B, H, N, d) and t.dtype == q.dtype for t in (k, v, o))
+          and tuple(lse.shape) == (B, H, N) and lse.dtype == torch.float32
+          and all(not t.is_cuda and t.is_contiguous() for t in (q, k, v, o, lse))
+          and workspace.is_cuda and workspace.is_contiguous())
+    if not ok:
+        raise ValueError("fa_fwd_host: bad shapes, dtypes or devices")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    nbytes = workspace.numel() * workspace.element_size()
+    with torch.cuda.device(workspace.device):
+        rc = fa_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                         B, H, N, d, causal, scale, _dtype_code(q), workspace.data_ptr(), nbytes,
+                         _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_host")
+
+
+def attention_forward_host(q, k, v, causal: bool = False, scale: float | None = None,
+                           device=None):
+    """Forward of CPU tensors on the GPU `device` (default: the current one):
+    returns (O, LSE) as page-locked CPU tensors, synchronised."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None \
+        else torch.device(device)
+    B, H, N, d = q.shape
+    o = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    lse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    ws = torch.empty(fa_fwd_host_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev)
+        attention_forward_host_into(q, k, v, o, lse, ws, causal, scale, stream)
+        stream.synchronize()
     return o, lse
 
 

@@ -203,6 +203,42 @@ fa_status fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, f
                          fa_dtype dtype, void* stream);
 
 /*
+ * fa_fwd_host - fa_fwd on HOST buffers: copies Q, K, V in, runs the forward
+ * and copies O and LSE out, the three overlapped across chunks of heads (the
+ * (b, h) slices of the method are independent, "TCA 51%, MFU below 8%",
+ * Flash Attention 2 section: one block per (batch, head) and query tile).
+ * Chunk c+1 is copied in while chunk c computes and chunk c-1 is copied out,
+ * on three internal non-blocking streams of the device (created on the first
+ * call, kept until process exit) that fork from and join back to `stream`.
+ * The heads are cut into at most 8 chunks, each keeping at least one wave
+ * of the forward's persistent grid busy (one chunk for small problems).
+ *
+ * q, k, v   : HOST pointers, contiguous [B][H][N][d] of `dtype`, read.
+ * o, lse    : HOST pointers, contiguous [B][H][N][d] of `dtype` and
+ *             [B][H][N] float32, written. Page-locked host memory
+ *             (cudaHostAlloc / cudaHostRegister) lets the copies overlap;
+ *             pageable memory gives the same results without the overlap.
+ * workspace : DEVICE pointer, 16-byte aligned, of at least the size
+ *             fa_fwd_host_workspace_size returns; caller-owned, not to be
+ *             touched until `stream` has passed this call.
+ * Everything else (arguments, numerics, status word) is as in fa_fwd. All
+ * arguments are checked before anything is enqueued. Asynchronous: O and LSE
+ * hold the result once `stream` reaches the point after this call (e.g.
+ * after cudaStreamSynchronize(stream)); the host buffers must stay valid
+ * until then.
+ */
+fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
+                      int B, int H, int N, int d, int causal, float scale, fa_dtype dtype,
+                      void* workspace, size_t workspace_size, void* stream);
+
+/*
+ * fa_fwd_host_workspace_size - bytes of device workspace fa_fwd_host needs:
+ * 4 B H N d 2-byte elements (Q, K, V, O) plus B H N float32 and 128 bytes of
+ * alignment padding. Host only.
+ */
+fa_status fa_fwd_host_workspace_size(int B, int H, int N, int d, size_t* bytes);
+
+/*
  * fa_check - synchronise `stream`, then read and clear the current device's
  * status word. Returns FA_OK, FA_ERR_TIMEOUT if a launch since the last check
  * stopped on a wait limit, or FA_ERR_CUDA if the stream reports an error.

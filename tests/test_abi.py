@@ -20,7 +20,8 @@ def lib():
 def test_header_declares_expected_entry_points():
     names = fa.header_functions()
     assert names == ["fa_fwd", "fa_fwd_strided", "fa_fwd_fp8", "fa_bwd", "fa_bwd_workspace_size",
-                     "fa_fwd_noalloc", "fa_check", "fa_query_launch",
+                     "fa_fwd_noalloc", "fa_fwd_host", "fa_fwd_host_workspace_size", "fa_check",
+                     "fa_query_launch",
                      "fa_sm_clock_probe", "fa_status_string", "fa_version"]
 
 
@@ -194,3 +195,36 @@ def test_bwd_valid_arguments_reach_the_device(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert _bwd() in (fa.FA_ERR_CUDA, fa.FA_ERR_ARCH)
+
+
+def _host(**kw):
+    a = dict(q=GOOD, k=GOOD, v=GOOD, o=GOOD, lse=GOOD, B=2, H=3, N=300, d=128, causal=0,
+             scale=0.088, dtype=fa.FA_DTYPE_FP16, ws=GOOD, wsz=None)
+    a.update(kw)
+    if a["wsz"] is None:
+        a["wsz"] = 4 * a["B"] * a["H"] * a["N"] * 128 * 2 + a["B"] * a["H"] * a["N"] * 4 + 128
+    return fa.fa_fwd_host(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"],
+                          a["d"], a["causal"], a["scale"], a["dtype"], a["ws"], a["wsz"], 0)
+
+
+@pytest.mark.parametrize("kw", [dict(q=0), dict(v=0), dict(o=0), dict(lse=0), dict(ws=0),
+                                dict(ws=GOOD + 8), dict(wsz=1000), dict(scale=0.0),
+                                dict(scale=float("inf")), dict(dtype=2), dict(N=0), dict(H=-1)])
+def test_host_bad_arguments_rejected(lib, kw):
+    assert _host(**kw) == fa.FA_ERR_INVALID_ARG
+
+
+def test_host_unsupported_and_workspace_size(lib):
+    assert _host(d=96) == fa.FA_ERR_UNSUPPORTED
+    # Q, K, V, O (2 bytes each), LSE (4 bytes), 128 bytes of alignment padding
+    assert fa.fa_fwd_host_workspace_size(2, 3, 300, 64) == 4 * 2 * 3 * 300 * 64 * 2 + \
+        2 * 3 * 300 * 4 + 128
+    with pytest.raises(fa.FaError):
+        fa.fa_fwd_host_workspace_size(1, 1, 128, 96)
+
+
+def test_host_valid_arguments_reach_the_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _host() in (fa.FA_ERR_CUDA, fa.FA_ERR_ARCH)
