@@ -1,6 +1,7 @@
-// Fused attention backward for sm_103a: dQ, dK, dV of the forward, with the
-// softmax weights recomputed from the forward's row logsumexp (the reason the
-// forward emits it: "TCA 51%, MFU below 8%", Flash Attention 2 section).
+// Fused attention backward for sm_103a: dQ, dK, dV of the forward. The
+// backward recomputes the scores instead of storing them ("TCA 51%, MFU below
+// 8%", section "MFU is always a little below TCA"); the softmax weights come
+// back from the forward's row logsumexp, which is why the forward emits it.
 //
 // With P_ij = exp(scale q_i.k_j - LSE_i), D_i = dO_i . O_i:
 //   dV_j = sum_i P_ij dO_i            dP_ij = dO_i . v_j

@@ -143,9 +143,10 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* vt, void* o, floa
 
 /*
  * fa_bwd - enqueue the backward pass of fa_fwd: gradients dq, dk, dv of a
- * loss whose gradient at O is dout. The softmax weights are recomputed from
- * the forward's lse (the reason the forward emits it; the Flash Attention 2
- * section of "TCA 51%, MFU below 8%"):
+ * loss whose gradient at O is dout. The backward recomputes the scores
+ * instead of storing them ("TCA 51%, MFU below 8%", section "MFU is always a
+ * little below TCA"); here the softmax weights are recomputed from the
+ * forward's lse, which is why the forward emits it (this library's reading):
  *     P_ij = exp(scale q_i.k_j - lse_i),  D_i = dout_i . o_i
  *     dv_j = sum_i P_ij dout_i,           dS_ij = P_ij (dout_i . v_j - D_i)
  *     dq_i = scale sum_j dS_ij k_j,       dk_j = scale sum_i dS_ij q_i
@@ -205,8 +206,9 @@ fa_status fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, f
 /*
  * fa_fwd_host - fa_fwd on HOST buffers: copies Q, K, V in, runs the forward
  * and copies O and LSE out, the three overlapped across chunks of heads (the
- * (b, h) slices of the method are independent, "TCA 51%, MFU below 8%",
- * Flash Attention 2 section: one block per (batch, head) and query tile).
+ * method's only serial dependency runs along the keys of one query row, "TCA
+ * 51%, MFU below 8%", section "Flash Attention 2 inflates TCA", so (b, h)
+ * slices are independent).
  * Chunk c+1 is copied in while chunk c computes and chunk c-1 is copied out,
  * on three internal non-blocking streams of the device (created on the first
  * call, kept until process exit) that fork from and join back to `stream`.

@@ -312,9 +312,10 @@ void oracle_decode_e4m3(const uint8_t* x, int64_t n, double* out) {
 //   dQ_i  = scale * sum_j dS_ij k_j
 //   dK_j  = scale * sum_i dS_ij q_i
 // (the chain rule through s = scale q.k and the softmax Jacobian
-// diag(P) - P P^T; sources: the Flash Attention 2 discussion of
-// "TCA 51%, MFU below 8%" names the recomputation of P from the saved
-// logsumexp, which is why the forward emits the LSE).
+// diag(P) - P P^T. Source: "TCA 51%, MFU below 8%", section "MFU is always
+// a little below TCA": the backward recomputes rather than storing the
+// scores; recomputing P from the forward's logsumexp is this library's
+// reading, and here P comes from the same definition as the forward's).
 // Besides the gradients, mag_* hold the sums of the magnitudes of the terms
 // of each element: sum_i |P_ij dO_it| for dV; for dQ and dK the sums
 // scale * sum_j A_ij |k_jt| and scale * sum_i A_ij |q_it| with
