@@ -100,8 +100,11 @@ struct BwdLayout {
   static constexpr uint32_t kColB = 128;  // dP^T, then 16-bit dS^T (dkdv) / dP (dq)
   static constexpr uint32_t kColAcc0 = 256;      // dV (dkdv) / dQ (dq)
   static constexpr uint32_t kColAcc1 = 256 + D;  // dK (dkdv)
-  static constexpr uint32_t kColA1 = 384;        // S, then dS (dq, odd tiles)
-  static_assert(KEYS || kColAcc0 + D <= kColA1, "dQ TMEM columns");
+  static constexpr uint32_t kColA1 = 384;        // S (dq) / S^T (dkdv, d=64), odd tiles
+  // Two S buffers (tile c in A or A1 by parity): always in the dQ kernel; in
+  // the dK/dV kernel where the accumulators leave room (d = 64).
+  static constexpr bool kDblS = !KEYS || D == 64;
+  static_assert(!kDblS || (KEYS ? kColAcc1 : kColAcc0) + D <= kColA1, "TMEM columns");
 };
 
 enum BwdBar : int {
@@ -320,11 +323,13 @@ __device__ __forceinline__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32
   auto ring_wait = [&](uint32_t r) {
     return wait_spin_warp(bar(kBbRing + r % S), (r / S) & 1u, ab, kStatusMma);
   };
-  // The two scratch products of streamed tile r: S^T = K Q^T, dP^T = V dO^T
-  // (all operands K-major).
-  auto scratch_a = [&](uint32_t r) {
-    issue_qk<D, BF16, true>(tA, fix0, stage(r));
-    ptx::umma_commit_elect(bar(kBbAFull));
+  // The two scratch products of streamed tile r: S^T = K Q^T into tile c's S^T
+  // buffer, dP^T = V dO^T into B (all operands K-major).
+  constexpr bool kDbl = L::kDblS;
+  auto sbuf = [&](uint32_t c) { return tmem + ((kDbl && (c & 1u)) ? L::kColA1 : L::kColA); };
+  auto scratch_a = [&](uint32_t r, uint32_t c) {
+    issue_qk<D, BF16, true>(sbuf(c), fix0, stage(r));
+    ptx::umma_commit_elect(bar((kDbl && (c & 1u)) ? kBbA1Full : kBbAFull));
   };
   auto scratch_b = [&](uint32_t r) {
     issue_qk<D, BF16, true>(tB, fix1, stage(r) + L::kTileBytes);
@@ -336,37 +341,42 @@ __device__ __forceinline__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32
   while (ok && bwd_next_unit<CAUSAL, KEYS>(round, a, bh, t)) {
     int first, last;
     bwd_span<CAUSAL, KEYS>(a, t, first, last);
+    const uint32_t n = static_cast<uint32_t>(last - first + 1);
     if (!(ok = wait_spin_warp(bar(kBbFixFull), units & 1u, ab, kStatusMma))) break;
     if (!(ok = ring_wait(ring))) break;
     ptx::tc_fence_after();
-    scratch_a(ring);
+    scratch_a(ring, cnt);
     scratch_b(ring);
-    for (int st = first; st <= last; ++st) {
-      const uint32_t r = ring++;
-      const uint32_t ph = (cnt++) & 1u;
-      const bool acc = st > first;
-      const bool more = st < last;
-      {
-        // dV += P^T dO (P^T in TMEM over the S^T columns; dO used MN-major)
-        if (!(ok = wait_spin_warp(bar(kBbPFull), ph, ab, kStatusMma))) break;
-        if (!acc && units > 0 &&
-            !(ok = wait_spin_warp(bar(kBbAccFree), (units - 1) & 1u, ab, kStatusMma)))
-          break;
-        ptx::tc_fence_after();
-        bwd_issue_ts<D, BF16>(tAcc0, tA, stage(r) + L::kTileBytes, acc);
-        if (more) {  // the next S^T while the element-wise role forms dS^T
-          if (!(ok = ring_wait(ring))) break;
-          scratch_a(ring);
-        }
-        // dK += dS^T Q (dS^T in TMEM over the dP^T columns; Q used MN-major)
-        if (!(ok = wait_spin_warp(bar(kBbDsFull), ph, ab, kStatusMma))) break;
-        ptx::tc_fence_after();
-        bwd_issue_ts<D, BF16>(tAcc1, tB, stage(r), acc);
-        ptx::umma_commit_elect(bar(kBbRing + S + r % S));
-        if (more) scratch_b(ring);
+    if (kDbl && n > 1) {  // two S^T buffers: the next tile's S^T right away
+      if (!(ok = ring_wait(ring + 1))) break;
+      scratch_a(ring + 1, cnt + 1);
+    }
+    // ahead = how many tiles past the current one S^T is issued
+    constexpr uint32_t ahead = kDbl ? 2u : 1u;
+    for (uint32_t i = 0; i < n; ++i) {
+      const uint32_t r = ring + i, c = cnt + i, ph = c & 1u;
+      const bool acc = i > 0;
+      // dV += P^T dO (P^T in TMEM over tile c's S^T columns; dO used MN-major)
+      if (!(ok = wait_spin_warp(bar(kBbPFull), ph, ab, kStatusMma))) break;
+      if (!acc && units > 0 &&
+          !(ok = wait_spin_warp(bar(kBbAccFree), (units - 1) & 1u, ab, kStatusMma)))
+        break;
+      ptx::tc_fence_after();
+      bwd_issue_ts<D, BF16>(tAcc0, sbuf(c), stage(r) + L::kTileBytes, acc);
+      if (i + ahead < n) {  // S^T of a later tile into the buffer dV has just read
+        if (!(ok = ring_wait(r + ahead))) break;
+        scratch_a(r + ahead, c + ahead);
       }
+      // dK += dS^T Q (dS^T in TMEM over the dP^T columns; Q used MN-major)
+      if (!(ok = wait_spin_warp(bar(kBbDsFull), ph, ab, kStatusMma))) break;
+      ptx::tc_fence_after();
+      bwd_issue_ts<D, BF16>(tAcc1, tB, stage(r), acc);
+      ptx::umma_commit_elect(bar(kBbRing + S + r % S));
+      if (i + 1 < n) scratch_b(r + 1);  // stage r+1 was waited for with its S^T
     }
     if (!ok) break;
+    ring += n;
+    cnt += n;
     ptx::umma_commit_elect(bar(kBbAccFull));
     ptx::umma_commit_elect(bar(kBbFixEmpty));
     ++units;
@@ -508,8 +518,8 @@ __device__ __forceinline__ void bwd_elementwise(const BwdArgs& a, const uint8_t*
       const uint32_t rr = ring++;
       const uint32_t c = cnt++;
       const uint32_t ph = c & 1u;
-      // dK/dV: S^T in A every tile; dQ: S alternates between A and A1
-      const bool odd = !KEYS && (c & 1u);
+      // S (S^T) alternates between A and A1 where there are two buffers
+      const bool odd = L::kDblS && (c & 1u);
       const uint32_t tA = odd ? tA1 : tA0;
       // the stage's lse2 / D vectors (TMA-written): observe their barrier too
       if (KEYS && !(ok = wait_bounded_warp(bar(kBbRing + rr % S), (rr / S) & 1u, ab,
@@ -518,9 +528,8 @@ __device__ __forceinline__ void bwd_elementwise(const BwdArgs& a, const uint8_t*
       const float* vec = reinterpret_cast<const float*>(
           sgen + L::kOffRing + (rr % S) * L::kStageBytes + 2 * L::kTileBytes);
       // ---- P: scores of this tile against the row's reference
-      if (!(ok = KEYS ? wait_bounded_warp(bar(kBbAFull), ph, ab, kStatusSoftmax)
-                      : wait_bounded_warp(bar(odd ? kBbA1Full : kBbAFull), (c >> 1) & 1u, ab,
-                                          kStatusSoftmax)))
+      if (!(ok = wait_bounded_warp(bar(odd ? kBbA1Full : kBbAFull),
+                                   L::kDblS ? (c >> 1) & 1u : ph, ab, kStatusSoftmax)))
         break;
       ptx::tc_fence_after();
       uint32_t sr[2][32];
