@@ -83,8 +83,13 @@ struct Layout {
   static constexpr int kOffBar = kOffStats + 2 * 128 * 4;
   static constexpr int kSmemBytes = kOffBar + 512 + 1024;  // barriers + alignment slack
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColS = 0;    // S_i (and P_i) at columns i*128
+  static constexpr uint32_t kColS = 0;    // S_i (and P_i unless kSepP) at columns i*128
   static constexpr uint32_t kColO = 256;  // O_i at columns 256 + i*D
+  // d = 64 leaves room for P_i in columns of its own (64 each: two 16-bit
+  // values per column), so S_i(j+1) can be computed while softmax(j) runs.
+  static constexpr bool kSepP = D == 64 && !FP8;
+  static constexpr uint32_t kColP = 256 + 2 * D;  // P_i at kColP + i*64 (kSepP)
+  static_assert(!kSepP || kColP + 128 <= kTmemCols, "TMEM columns");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -99,7 +104,9 @@ enum BarSlot : int {
   kBarStatsFull = 11, // [2] 128 softmax threads: row sums l of tile i in smem
   kBarDrain = 13,     // MMA: every tcgen05 op of the CTA completed
   kBarStatsFree = 14, // [2] 128 epilogue threads: row sums of tile i read
-  kBarKVFull = 16,    // [stages] TMA: ring slot loaded; then [stages] ring slot free
+  kBarSFree = 16,     // [2] 128 softmax threads: S_i read (kSepP)
+  kBarPFree = 18,     // [2] MMA: O_i += P_i V done, P_i reusable (kSepP)
+  kBarKVFull = 20,    // [stages] TMA: ring slot loaded; then [stages] ring slot free
 };
 constexpr int kSlotTmem = 480;   // byte offset of the TMEM base address
 constexpr int kSlotAbort = 484;  // byte offset of the abort flag
@@ -306,6 +313,90 @@ __device__ __forceinline__ void mma_role(const FwdArgs& a, uint32_t sbase, uint3
   wait_drain(bar(kBarDrain), 0u, ab, kStatusDrain);
 }
 
+// The MMA warp when P_i has TMEM columns of its own (d = 64). Per KV tile j:
+//   S0(j+1) once softmax 0 has read S0(j), S1(j+1) likewise, then
+//   O0 += P0(j) V_j and O1 += P1(j) V_j once P_i(j) is written; each PV
+//   commits P-free (O_i updated, P_i reusable), the last one of a unit O-full.
+// The softmax of tile j+1 thus never waits for PV(j): only its P store and O
+// rescale do.
+template <int D, bool BF16, bool CAUSAL>
+__device__ __forceinline__ void mma_role_sep(const FwdArgs& a, uint32_t sbase, uint32_t bars,
+                                             uint32_t tmem, const AbortCtx& ab) {
+  using L = Layout<D, false>;
+  constexpr int S = L::kStages;
+  auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
+  const uint64_t dQ[2] = {desc_kmajor(sbase + L::kOffQ),
+                          desc_kmajor(sbase + L::kOffQ + L::kTileBytes)};
+  const uint64_t dK0 = desc_kmajor(sbase + L::kOffKV);
+  const uint64_t dV0 = desc_v(sbase + L::kOffKV);
+  const uint32_t tS[2] = {tmem + L::kColS, tmem + L::kColS + 128};
+  const uint32_t tO[2] = {tmem + L::kColO, tmem + L::kColO + D};
+  const uint32_t tP[2] = {tmem + L::kColP, tmem + L::kColP + 64};
+  auto slot_off = [](uint32_t idx) { return (idx % S) * static_cast<uint32_t>(L::kTileBytes); };
+  auto kv_wait = [&](uint32_t idx) {
+    return wait_spin_warp(bar(kBarKVFull + idx % S), (idx / S) & 1u, ab, kStatusMma);
+  };
+  auto release = [&](uint32_t idx) { ptx::umma_commit_elect(bar(kBarKVFull + S + idx % S)); };
+  uint32_t ring = 0, units = 0, scnt[2] = {0u, 0u}, pcnt[2] = {0u, 0u};
+  int round = 0, bh = 0, mblk = 0;
+  bool ok = true;
+  while (ok && next_unit<CAUSAL>(round, a, bh, mblk)) {
+    const int nkv = unit_kv_tiles<CAUSAL>(a, mblk);
+    ok = wait_spin_warp(bar(kBarQFull + 0), units & 1u, ab, kStatusMma) &&
+         wait_spin_warp(bar(kBarQFull + 1), units & 1u, ab, kStatusMma);
+    if (!ok) break;
+    // S_i(0) = Q_i K_0^T (S_i free: softmax read the previous unit's last S_i)
+    const uint32_t k0 = ring++;
+    if (!(ok = kv_wait(k0))) break;
+    for (int i = 0; i < 2 && ok; ++i) {
+      if (units > 0) ok = wait_spin_warp(bar(kBarSFree + i), (scnt[i]++) & 1u, ab, kStatusMma);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      issue_qk_desc<D, BF16, true>(tS[i], dQ[i], desc_add(dK0, slot_off(k0)));
+      ptx::umma_commit_elect(bar(kBarSFull + i));
+    }
+    if (!ok) break;
+    release(k0);
+    if (nkv == 1) ptx::umma_commit_elect(bar(kBarQEmpty));
+    for (int j = 0; j < nkv && ok; ++j) {
+      const uint32_t vj = ring++;
+      const bool more = j + 1 < nkv;
+      if (more) {
+        // S_i(j+1) = Q_i K_{j+1}^T once softmax i has read S_i(j)
+        const uint32_t kn = ring++;
+        if (!(ok = kv_wait(kn))) break;
+        for (int i = 0; i < 2 && ok; ++i) {
+          if (!(ok = wait_spin_warp(bar(kBarSFree + i), (scnt[i]++) & 1u, ab, kStatusMma))) break;
+          ptx::tc_fence_after();
+          issue_qk_desc<D, BF16, true>(tS[i], dQ[i], desc_add(dK0, slot_off(kn)));
+          ptx::umma_commit_elect(bar(kBarSFull + i));
+        }
+        if (!ok) break;
+        release(kn);
+        if (j + 2 == nkv) ptx::umma_commit_elect(bar(kBarQEmpty));
+      }
+      // O_i += P_i(j) V_j
+      if (!(ok = kv_wait(vj))) break;
+      for (int i = 0; i < 2 && ok; ++i) {
+        if (!(ok = wait_spin_warp(bar(kBarPFull + i), (pcnt[i]++) & 1u, ab, kStatusMma))) break;
+        if (j == 0 && units > 0 &&
+            !(ok = wait_spin_warp(bar(kBarOFree + i), (units - 1) & 1u, ab, kStatusMma)))
+          break;
+        ptx::tc_fence_after();
+        issue_pv_ts_desc<D, BF16, true>(tO[i], tP[i], desc_add(dV0, slot_off(vj)), j > 0);
+        ptx::umma_commit_elect(bar(kBarPFree + i));
+        if (!more) ptx::umma_commit_elect(bar(kBarOFull + i));
+      }
+      if (!ok) break;
+      release(vj);
+    }
+    ++units;
+  }
+  // Every tcgen05 op this warp issued must finish before TMEM is freed.
+  ptx::umma_commit_elect(bar(kBarDrain));
+  wait_drain(bar(kBarDrain), 0u, ab, kStatusDrain);
+}
+
 template <int D, bool BF16, bool CAUSAL, bool FP8>
 __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t bars, uint32_t tmem,
                                              float* stats, const AbortCtx& ab, int warp,
@@ -316,6 +407,9 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t bars, ui
   const int r = (warp & 3) * 32 + lane;     // row in the tile = TMEM lane
   const uint32_t tl = ptx::tmem_lane_base(tmem, warp);
   const uint32_t tS = tl + L::kColS + 128u * wg;  // S_i; P_i over its first 64 columns
+  // or in columns of its own (kSepP)
+  const uint32_t tP = L::kSepP ? tl + L::kColP + 64u * wg : tS;
+  uint32_t pstores = 0;  // P_i stores so far (kSepP: each but the first waits for P-free)
   const uint32_t tO = tl + L::kColO + static_cast<uint32_t>(D) * wg;
   const float cl2 = a.scale_log2;
   uint32_t scnt = 0, units = 0;
@@ -340,6 +434,10 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t bars, ui
       for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + 32u * c, sr[c]);
 #pragma unroll
       for (int c = 0; c < 4; ++c) ptx::tmem_ld_wait(sr[c]);
+      if constexpr (L::kSepP) {  // S_i is in registers: S_i(j+1) may overwrite it
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(kBarSFree + wg));
+      }
       float s[128];
 #pragma unroll
       for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
@@ -402,13 +500,24 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t bars, ui
             // the rounded weights the PV product actually uses (a row dominated
             // by one key then returns that V row exactly), while the LSE keeps
             // the unrounded sum.
-            lr[c & 3] = ptx::fadd2(lr[c & 3], make_float2(__uint_as_float(w << 16),
-                                                          __uint_as_float(w & 0xFFFF0000u)));
+            lr[c & 3].x = ptx::add_f32_bf16_lo(lr[c & 3].x, w);
+            lr[c & 3].y = ptx::add_f32_bf16_hi(lr[c & 3].y, w);
           }
         }
-        // P_i into TMEM over the S_i columns this thread has already read.
-        ptx::tmem_st32(tS, pk[0]);
-        ptx::tmem_st32(tS + 32u, pk[1]);
+        if constexpr (L::kSepP) {
+          // P_i(j-1) read and O_i updated by its PV before P_i is rewritten
+          // (and before the O rescale below)
+          if (pstores > 0 &&
+              !(ok = wait_bounded_warp(bar(kBarPFree + wg), (pstores - 1) & 1u, ab,
+                                       kStatusSoftmax)))
+            break;
+          ptx::tc_fence_after();
+        }
+        ++pstores;
+        // P_i into TMEM: over the S_i columns this thread has already read, or
+        // into its own columns (kSepP)
+        ptx::tmem_st32(tP, pk[0]);
+        ptx::tmem_st32(tP + 32u, pk[1]);
       }
       const float2 s01 = ptx::fadd2(ptx::fadd2(ls[0], ls[1]), ptx::fadd2(ls[2], ls[3]));
       const float lsum = s01.x + s01.y;
@@ -535,6 +644,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       ptx::mbar_init(bar(kBarOFree + i), 128);
       ptx::mbar_init(bar(kBarStatsFull + i), 128);
       ptx::mbar_init(bar(kBarStatsFree + i), 128);
+      ptx::mbar_init(bar(kBarSFree + i), 128);
+      ptx::mbar_init(bar(kBarPFree + i), 1);
     }
     ptx::mbar_init(bar(kBarQEmpty), 1);
     ptx::mbar_init(bar(kBarDrain), 1);
@@ -560,7 +671,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (warp == 0) {
       if (lane == 0) producer_role<D, BF16, CAUSAL, FP8>(&tm_q, &tm_k, &tm_v, a, sbase, bars, ab);
     } else if (warp == 1) {
-      mma_role<D, BF16, CAUSAL, FP8>(a, sbase, bars, tmem, ab);  // the whole warp
+      if constexpr (L::kSepP) mma_role_sep<D, BF16, CAUSAL>(a, sbase, bars, tmem, ab);
+      else mma_role<D, BF16, CAUSAL, FP8>(a, sbase, bars, tmem, ab);  // the whole warp
     }
   } else if (wgrp < 3) {
     ptx::setmaxnreg_inc<kRegsSoftmax>();

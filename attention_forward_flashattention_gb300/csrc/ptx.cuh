@@ -220,6 +220,22 @@ __device__ __forceinline__ void umma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uin
 
 // The mbarrier receives one arrival when all tcgen05 operations this thread
 // issued before the commit have completed.
+// acc + (the low / high bf16 half of w), in fp32 with round-to-nearest:
+// the mixed-precision add converts the bf16 operand exactly, so no unpacking
+// instructions are needed.
+__device__ __forceinline__ float add_f32_bf16_lo(float acc, uint32_t w) {
+  float d;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+      "add.rn.f32.bf16 %0, lo, %2;\n\t}" : "=f"(d) : "r"(w), "f"(acc));
+  return d;
+}
+__device__ __forceinline__ float add_f32_bf16_hi(float acc, uint32_t w) {
+  float d;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+      "add.rn.f32.bf16 %0, hi, %2;\n\t}" : "=f"(d) : "r"(w), "f"(acc));
+  return d;
+}
+
 // Elected forms: the whole converged warp executes them and the one lane
 // elect.sync picks issues the op (fewer cycles per op than a lone thread).
 __device__ __forceinline__ void umma_f16_ss_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
