@@ -107,6 +107,7 @@ enum BarSlot : int {
   kBarSFree = 16,     // [2] 128 softmax threads: S_i read (kSepP)
   kBarPFree = 18,     // [2] MMA: O_i += P_i V done, P_i reusable (kSepP)
   kBarKVFull = 20,    // [stages] TMA: ring slot loaded; then [stages] ring slot free
+  kBarDrainPV = 36,   // PV-issuing warp (kSepP): every tcgen05 op it issued completed
 };
 constexpr int kSlotTmem = 480;   // byte offset of the TMEM base address
 constexpr int kSlotAbort = 484;  // byte offset of the abort flag
@@ -313,69 +314,83 @@ __device__ __forceinline__ void mma_role(const FwdArgs& a, uint32_t sbase, uint3
   wait_drain(bar(kBarDrain), 0u, ab, kStatusDrain);
 }
 
-// The MMA warp when P_i has TMEM columns of its own (d = 64). Per KV tile j:
-//   S0(j+1) once softmax 0 has read S0(j), S1(j+1) likewise, then
-//   O0 += P0(j) V_j and O1 += P1(j) V_j once P_i(j) is written; each PV
-//   commits P-free (O_i updated, P_i reusable), the last one of a unit O-full.
-// The softmax of tile j+1 thus never waits for PV(j): only its P store and O
-// rescale do.
+// MMA issue when P_i has TMEM columns of its own (d = 64), split over two
+// warps on different SM sub-partitions (each tcgen05.mma takes issue cycles
+// from the softmax warps sharing its sub-partition, and those hold the rows
+// the MMAs wait for). S products never touch the P or O columns, so the two
+// need no ordering between them beyond the softmax's own barriers:
+//   S warp:  S_i(j+1) = Q_i K_{j+1}^T once softmax i has read S_i(j);
+//   PV warp: O_i += P_i(j) V_j once P_i(j) is written, then P-free (O_i
+//            updated, P_i reusable), and O-full after a unit's last one.
+// The softmax of tile j+1 never waits for PV(j): only its P store and O
+// rescale do. Both walk the same K, V ring: K_j at index 2j, V_j at 2j+1 of
+// the unit's tiles.
 template <int D, bool BF16, bool CAUSAL>
-__device__ __forceinline__ void mma_role_sep(const FwdArgs& a, uint32_t sbase, uint32_t bars,
-                                             uint32_t tmem, const AbortCtx& ab) {
+__device__ __forceinline__ void mma_s_role(const FwdArgs& a, uint32_t sbase, uint32_t bars,
+                                           uint32_t tmem, const AbortCtx& ab) {
   using L = Layout<D, false>;
   constexpr int S = L::kStages;
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
   const uint64_t dQ[2] = {desc_kmajor(sbase + L::kOffQ),
                           desc_kmajor(sbase + L::kOffQ + L::kTileBytes)};
   const uint64_t dK0 = desc_kmajor(sbase + L::kOffKV);
-  const uint64_t dV0 = desc_v(sbase + L::kOffKV);
   const uint32_t tS[2] = {tmem + L::kColS, tmem + L::kColS + 128};
-  const uint32_t tO[2] = {tmem + L::kColO, tmem + L::kColO + D};
-  const uint32_t tP[2] = {tmem + L::kColP, tmem + L::kColP + 64};
   auto slot_off = [](uint32_t idx) { return (idx % S) * static_cast<uint32_t>(L::kTileBytes); };
   auto kv_wait = [&](uint32_t idx) {
     return wait_spin_warp(bar(kBarKVFull + idx % S), (idx / S) & 1u, ab, kStatusMma);
   };
-  auto release = [&](uint32_t idx) { ptx::umma_commit_elect(bar(kBarKVFull + S + idx % S)); };
-  uint32_t ring = 0, units = 0, scnt[2] = {0u, 0u}, pcnt[2] = {0u, 0u};
+  uint32_t ring = 0, units = 0, scnt[2] = {0u, 0u};
   int round = 0, bh = 0, mblk = 0;
   bool ok = true;
   while (ok && next_unit<CAUSAL>(round, a, bh, mblk)) {
     const int nkv = unit_kv_tiles<CAUSAL>(a, mblk);
     ok = wait_spin_warp(bar(kBarQFull + 0), units & 1u, ab, kStatusMma) &&
          wait_spin_warp(bar(kBarQFull + 1), units & 1u, ab, kStatusMma);
-    if (!ok) break;
-    // S_i(0) = Q_i K_0^T (S_i free: softmax read the previous unit's last S_i)
-    const uint32_t k0 = ring++;
-    if (!(ok = kv_wait(k0))) break;
-    for (int i = 0; i < 2 && ok; ++i) {
-      if (units > 0) ok = wait_spin_warp(bar(kBarSFree + i), (scnt[i]++) & 1u, ab, kStatusMma);
-      if (!ok) break;
-      ptx::tc_fence_after();
-      issue_qk_desc<D, BF16, true>(tS[i], dQ[i], desc_add(dK0, slot_off(k0)));
-      ptx::umma_commit_elect(bar(kBarSFull + i));
-    }
-    if (!ok) break;
-    release(k0);
-    if (nkv == 1) ptx::umma_commit_elect(bar(kBarQEmpty));
-    for (int j = 0; j < nkv && ok; ++j) {
-      const uint32_t vj = ring++;
-      const bool more = j + 1 < nkv;
-      if (more) {
-        // S_i(j+1) = Q_i K_{j+1}^T once softmax i has read S_i(j)
-        const uint32_t kn = ring++;
-        if (!(ok = kv_wait(kn))) break;
-        for (int i = 0; i < 2 && ok; ++i) {
-          if (!(ok = wait_spin_warp(bar(kBarSFree + i), (scnt[i]++) & 1u, ab, kStatusMma))) break;
-          ptx::tc_fence_after();
-          issue_qk_desc<D, BF16, true>(tS[i], dQ[i], desc_add(dK0, slot_off(kn)));
-          ptx::umma_commit_elect(bar(kBarSFull + i));
-        }
+    for (int j = -1; ok && j + 1 < nkv; ++j) {
+      // S_i(j+1) = Q_i K_{j+1}^T (the first one of all waits for nothing)
+      const uint32_t kn = ring + 2u * static_cast<uint32_t>(j + 1);
+      if (!(ok = kv_wait(kn))) break;
+      for (int i = 0; i < 2 && ok; ++i) {
+        if (units > 0 || j >= 0)
+          ok = wait_spin_warp(bar(kBarSFree + i), (scnt[i]++) & 1u, ab, kStatusMma);
         if (!ok) break;
-        release(kn);
-        if (j + 2 == nkv) ptx::umma_commit_elect(bar(kBarQEmpty));
+        ptx::tc_fence_after();
+        issue_qk_desc<D, BF16, true>(tS[i], dQ[i], desc_add(dK0, slot_off(kn)));
+        ptx::umma_commit_elect(bar(kBarSFull + i));
       }
+      if (!ok) break;
+      ptx::umma_commit_elect(bar(kBarKVFull + S + kn % S));  // K_{j+1} consumed
+      if (j + 2 == nkv) ptx::umma_commit_elect(bar(kBarQEmpty));
+    }
+    ring += 2u * static_cast<uint32_t>(nkv);
+    ++units;
+  }
+  // Every tcgen05 op this warp issued must finish before TMEM is freed.
+  ptx::umma_commit_elect(bar(kBarDrain));
+  wait_drain(bar(kBarDrain), 0u, ab, kStatusDrain);
+}
+
+template <int D, bool BF16, bool CAUSAL>
+__device__ __forceinline__ void mma_pv_role(const FwdArgs& a, uint32_t sbase, uint32_t bars,
+                                            uint32_t tmem, const AbortCtx& ab) {
+  using L = Layout<D, false>;
+  constexpr int S = L::kStages;
+  auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
+  const uint64_t dV0 = desc_v(sbase + L::kOffKV);
+  const uint32_t tO[2] = {tmem + L::kColO, tmem + L::kColO + D};
+  const uint32_t tP[2] = {tmem + L::kColP, tmem + L::kColP + 64};
+  auto slot_off = [](uint32_t idx) { return (idx % S) * static_cast<uint32_t>(L::kTileBytes); };
+  auto kv_wait = [&](uint32_t idx) {
+    return wait_spin_warp(bar(kBarKVFull + idx % S), (idx / S) & 1u, ab, kStatusMma);
+  };
+  uint32_t ring = 0, units = 0, pcnt[2] = {0u, 0u};
+  int round = 0, bh = 0, mblk = 0;
+  bool ok = true;
+  while (ok && next_unit<CAUSAL>(round, a, bh, mblk)) {
+    const int nkv = unit_kv_tiles<CAUSAL>(a, mblk);
+    for (int j = 0; j < nkv && ok; ++j) {
       // O_i += P_i(j) V_j
+      const uint32_t vj = ring + 2u * static_cast<uint32_t>(j) + 1u;
       if (!(ok = kv_wait(vj))) break;
       for (int i = 0; i < 2 && ok; ++i) {
         if (!(ok = wait_spin_warp(bar(kBarPFull + i), (pcnt[i]++) & 1u, ab, kStatusMma))) break;
@@ -385,16 +400,16 @@ __device__ __forceinline__ void mma_role_sep(const FwdArgs& a, uint32_t sbase, u
         ptx::tc_fence_after();
         issue_pv_ts_desc<D, BF16, true>(tO[i], tP[i], desc_add(dV0, slot_off(vj)), j > 0);
         ptx::umma_commit_elect(bar(kBarPFree + i));
-        if (!more) ptx::umma_commit_elect(bar(kBarOFull + i));
+        if (j + 1 == nkv) ptx::umma_commit_elect(bar(kBarOFull + i));
       }
       if (!ok) break;
-      release(vj);
+      ptx::umma_commit_elect(bar(kBarKVFull + S + vj % S));  // V_j consumed
     }
+    ring += 2u * static_cast<uint32_t>(nkv);
     ++units;
   }
-  // Every tcgen05 op this warp issued must finish before TMEM is freed.
-  ptx::umma_commit_elect(bar(kBarDrain));
-  wait_drain(bar(kBarDrain), 0u, ab, kStatusDrain);
+  ptx::umma_commit_elect(bar(kBarDrainPV));
+  wait_drain(bar(kBarDrainPV), 0u, ab, kStatusDrain);
 }
 
 template <int D, bool BF16, bool CAUSAL, bool FP8>
@@ -649,6 +664,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     ptx::mbar_init(bar(kBarQEmpty), 1);
     ptx::mbar_init(bar(kBarDrain), 1);
+    ptx::mbar_init(bar(kBarDrainPV), 1);
     for (int s = 0; s < L::kStages; ++s) {
       ptx::mbar_init(bar(kBarKVFull + s), 1);
       ptx::mbar_init(bar(kBarKVFull + L::kStages + s), 1);
@@ -670,9 +686,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     ptx::setmaxnreg_dec<kRegsWG0>();
     if (warp == 0) {
       if (lane == 0) producer_role<D, BF16, CAUSAL, FP8>(&tm_q, &tm_k, &tm_v, a, sbase, bars, ab);
+    } else if constexpr (L::kSepP) {  // MMA issue split over warps 2 and 3
+      if (warp == 2) mma_s_role<D, BF16, CAUSAL>(a, sbase, bars, tmem, ab);
+      else if (warp == 3) mma_pv_role<D, BF16, CAUSAL>(a, sbase, bars, tmem, ab);
     } else if (warp == 1) {
-      if constexpr (L::kSepP) mma_role_sep<D, BF16, CAUSAL>(a, sbase, bars, tmem, ab);
-      else mma_role<D, BF16, CAUSAL, FP8>(a, sbase, bars, tmem, ab);  // the whole warp
+      mma_role<D, BF16, CAUSAL, FP8>(a, sbase, bars, tmem, ab);  // the whole warp
     }
   } else if (wgrp < 3) {
     ptx::setmaxnreg_inc<kRegsSoftmax>();
