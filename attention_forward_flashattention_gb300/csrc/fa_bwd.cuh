@@ -28,7 +28,8 @@
 //      while dS of tile j is formed; the MMA order is dP(j+1), dQ(j), S(j+2).
 //
 // Roles (16 warps): warp 0 TMA producer (lane 0); warp 1 TMEM owner and MMA
-// issuer (the whole warp, one elected lane issuing); warpgroups 1 and 2 the
+// issuer (the whole warp, one elected lane issuing; the d = 64 dK/dV kernel
+// splits its MMAs over warps 2 and 3 instead); warpgroups 1 and 2 the
 // element-wise softmax gradient (one thread per TMEM lane; warpgroup 1 takes
 // columns 0-63 of each 128-column scratch tile, warpgroup 2 columns 64-127,
 // and each packs its 16-bit result over the first 32 of its own columns);
@@ -120,6 +121,7 @@ enum BwdBar : int {
   kBbA1Full = 9,     // MMA: S of odd tiles ready (dq)
   kBbRing = 10,      // dkdv: [stages] full, [stages] empty;
                      // dq: K [slots] full, K empty, V [slots] full, V empty
+  kBbDrainB = 30,    // dkdv: chain B's MMAs all done
 };
 constexpr int kBwdSlotTmem = 480;
 constexpr int kBwdSlotAbort = 484;
@@ -309,7 +311,8 @@ __device__ __forceinline__ void bwd_issue_ts(uint32_t d_tmem, uint32_t a_tmem, u
   }
 }
 
-// The MMA-issuing warp of the dK/dV kernel (order at the top of this file).
+// The MMA-issuing warp of the dK/dV kernel at d = 128 (order at the top of
+// this file): one warp, so S^T(c+1) reaches the tensor core right after dV(c).
 template <int D, bool BF16, bool CAUSAL, bool KEYS>
 __device__ __forceinline__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32_t bars,
                                         uint32_t tmem, const AbortCtx& ab) {
@@ -383,6 +386,86 @@ __device__ __forceinline__ void bwd_mma(const BwdArgs& a, uint32_t sbase, uint32
   }
   ptx::umma_commit_elect(bar(kBbDrain));
   wait_drain(bar(kBbDrain), 0u, ab, kStatusDrain);
+}
+
+// At d = 64 (two S^T buffers) the dK/dV kernel's MMAs form two chains that
+// share no TMEM columns, each issued in order by its own warp (on SM
+// sub-partitions 2 and 3, away from the element-wise warps that share one
+// with a busy issuer; at d = 128, where S^T(c+1) must follow dV(c) closely,
+// a single issuer is faster):
+//   chain A (warp 2): S^T(c) = K Q_c^T into tile c's S^T buffer, then
+//                     dV += P^T(c) dO_c once P^T(c) is written over it;
+//   chain B (warp 3): dP^T(c) = V dO_c^T into B, then dK += dS^T(c) Q_c
+//                     once dS^T(c) is written over it.
+// A streamed stage is free once both dV(c) and dK(c) are done, the fixed K, V
+// once both chains' last products are, and the accumulators are final once
+// both chains' last ones are: those barriers take one commit from each chain.
+template <int D, bool BF16, bool CAUSAL, bool A>
+__device__ __forceinline__ void bwd_mma_kv(const BwdArgs& a, uint32_t sbase, uint32_t bars,
+                                           uint32_t tmem, const AbortCtx& ab) {
+  using L = BwdLayout<D, true>;
+  constexpr int S = L::kStages;
+  constexpr bool kDbl = L::kDblS;
+  auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
+  const uint32_t tB = tmem + L::kColB;
+  const uint32_t tAcc = tmem + (A ? L::kColAcc0 : L::kColAcc1);
+  const uint32_t fix = sbase + L::kOffFix + (A ? 0 : L::kTileBytes);  // K (A) or V (B)
+  auto stage = [&](uint32_t r) { return sbase + L::kOffRing + (r % S) * L::kStageBytes; };
+  auto ring_wait = [&](uint32_t r) {
+    return wait_spin_warp(bar(kBbRing + r % S), (r / S) & 1u, ab, kStatusMma);
+  };
+  auto sbuf = [&](uint32_t c) { return tmem + ((kDbl && (c & 1u)) ? L::kColA1 : L::kColA); };
+  // the chain's scratch product of tile c (stage r): S^T = K Q^T or dP^T = V dO^T
+  auto scratch = [&](uint32_t r, uint32_t c) {
+    if constexpr (A) {
+      issue_qk<D, BF16, true>(sbuf(c), fix, stage(r));
+      ptx::umma_commit_elect(bar((kDbl && (c & 1u)) ? kBbA1Full : kBbAFull));
+    } else {
+      issue_qk<D, BF16, true>(tB, fix, stage(r) + L::kTileBytes);
+      ptx::umma_commit_elect(bar(kBbBFull));
+    }
+  };
+  // chain A issues S^T two tiles ahead where there are two S^T buffers
+  constexpr uint32_t ahead = (A && kDbl) ? 2u : 1u;
+  uint32_t ring = 0, units = 0, cnt = 0;
+  int round = 0, bh = 0, t = 0;
+  bool ok = true;
+  while (ok && bwd_next_unit<CAUSAL, true>(round, a, bh, t)) {
+    int first, last;
+    bwd_span<CAUSAL, true>(a, t, first, last);
+    const uint32_t n = static_cast<uint32_t>(last - first + 1);
+    if (!(ok = wait_spin_warp(bar(kBbFixFull), units & 1u, ab, kStatusMma))) break;
+    for (uint32_t k = 0; k < ahead && k < n && ok; ++k) {
+      if (!(ok = ring_wait(ring + k))) break;
+      ptx::tc_fence_after();
+      scratch(ring + k, cnt + k);
+    }
+    for (uint32_t i = 0; i < n && ok; ++i) {
+      const uint32_t r = ring + i, c = cnt + i, ph = c & 1u;
+      // dV += P^T dO (chain A) or dK += dS^T Q (chain B), from TMEM over the
+      // scratch columns; dO / Q used MN-major
+      if (!(ok = wait_spin_warp(bar(A ? kBbPFull : kBbDsFull), ph, ab, kStatusMma))) break;
+      if (i == 0 && units > 0 &&
+          !(ok = wait_spin_warp(bar(kBbAccFree), (units - 1) & 1u, ab, kStatusMma)))
+        break;
+      ptx::tc_fence_after();
+      if constexpr (A) bwd_issue_ts<D, BF16>(tAcc, sbuf(c), stage(r) + L::kTileBytes, i > 0);
+      else bwd_issue_ts<D, BF16>(tAcc, tB, stage(r), i > 0);
+      ptx::umma_commit_elect(bar(kBbRing + S + r % S));  // this chain's use of stage r done
+      if (i + ahead < n) {  // the chain's next scratch product, after the one just read
+        if (!(ok = ring_wait(r + ahead))) break;
+        scratch(r + ahead, c + ahead);
+      }
+    }
+    if (!ok) break;
+    ring += n;
+    cnt += n;
+    ptx::umma_commit_elect(bar(kBbAccFull));
+    ptx::umma_commit_elect(bar(kBbFixEmpty));
+    ++units;
+  }
+  ptx::umma_commit_elect(bar(A ? kBbDrain : kBbDrainB));
+  wait_drain(bar(A ? kBbDrain : kBbDrainB), 0u, ab, kStatusDrain);
 }
 
 // The MMA-issuing warp of the dQ kernel. S of tile j goes to scratch
@@ -694,18 +777,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const AbortCtx ab{abort_flag, a.status};
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
   if (threadIdx.x == 0) {
+    // dK/dV at d = 64: two MMA chains each commit the shared-resource barriers
+    constexpr uint32_t kChains = (KEYS && L::kDblS) ? 2u : 1u;
     ptx::mbar_init(bar(kBbFixFull), 1);
-    ptx::mbar_init(bar(kBbFixEmpty), 1);
+    ptx::mbar_init(bar(kBbFixEmpty), kChains);
     ptx::mbar_init(bar(kBbAFull), 1);
     ptx::mbar_init(bar(kBbBFull), 1);
     ptx::mbar_init(bar(kBbPFull), 8);
     ptx::mbar_init(bar(kBbDsFull), 8);
-    ptx::mbar_init(bar(kBbAccFull), 1);
+    ptx::mbar_init(bar(kBbAccFull), kChains);
     ptx::mbar_init(bar(kBbAccFree), 4);
     ptx::mbar_init(bar(kBbDrain), 1);
     ptx::mbar_init(bar(kBbA1Full), 1);
-    const int ring_bars = KEYS ? 2 * L::kStages : 2 * (L::kKSlots + L::kVSlots);
-    for (int s = 0; s < ring_bars; ++s) ptx::mbar_init(bar(kBbRing + s), 1);
+    ptx::mbar_init(bar(kBbDrainB), 1);
+    if constexpr (KEYS) {  // stage full (TMA), stage empty (both chains)
+      for (int s = 0; s < L::kStages; ++s) {
+        ptx::mbar_init(bar(kBbRing + s), 1);
+        ptx::mbar_init(bar(kBbRing + L::kStages + s), kChains);
+      }
+    } else {
+      for (int s = 0; s < 2 * (L::kKSlots + L::kVSlots); ++s) ptx::mbar_init(bar(kBbRing + s), 1);
+    }
     *abort_flag = 0u;
     ptx::fence_mbar_init();
   }
@@ -722,6 +814,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ptx::setmaxnreg_to<kBwdRegsWG0, kBwdRegsLaunch>();
     if (warp == 0) {
       if (lane == 0) bwd_producer<D, CAUSAL, KEYS>(&tm_q, &tm_k, &tm_v, &tm_do, a, sbase, bars, ab);
+    } else if constexpr (KEYS && L::kDblS) {  // the two MMA chains, each a whole warp
+      if (warp == 2) bwd_mma_kv<D, BF16, CAUSAL, true>(a, sbase, bars, tmem, ab);
+      else if (warp == 3) bwd_mma_kv<D, BF16, CAUSAL, false>(a, sbase, bars, tmem, ab);
     } else if (warp == 1) {  // the whole warp
       if constexpr (KEYS) bwd_mma<D, BF16, CAUSAL, true>(a, sbase, bars, tmem, ab);
       else bwd_mma_dq<D, BF16, CAUSAL>(a, sbase, bars, tmem, ab);
