@@ -216,19 +216,25 @@ def oracle_rows(w, x, rows):
     return oracle.attn_rows(q, k, v, w.dtype, w.causal, w.scale, rows)
 
 
-def time_oracle(w, x, target_s: float, seed: int):
-    """Times the oracle on a row sample sized to about target_s seconds."""
+def time_oracle(w, x, target_s: float, seed: int, max_rows: int = 500_000):
+    """Times the oracle on a row sample sized to about target_s seconds: a
+    small calibration run, then sized runs (re-sized while the last one took
+    under half the target, at most three times)."""
     import oracle
     cores = oracle.threads(0)
-    calib = oracle_sample_rows(w, 2 * cores, seed)
-    t = time.perf_counter()
-    oracle_rows(w, x, calib)
-    dt = max(time.perf_counter() - t, 1e-3)
-    n = int(min(max(len(calib) * target_s / dt, len(calib)), 200000))
-    rows = oracle_sample_rows(w, n, seed + 1)
+    n = 16 * cores
+    rows = oracle_sample_rows(w, n, seed)
     t = time.perf_counter()
     oracle_rows(w, x, rows)
-    dt = time.perf_counter() - t
+    dt = max(time.perf_counter() - t, 1e-3)
+    for attempt in range(3):
+        n = int(min(max(len(rows) * target_s / dt, len(rows)), max_rows))
+        rows = oracle_sample_rows(w, n, seed + 1 + attempt)
+        t = time.perf_counter()
+        oracle_rows(w, x, rows)
+        dt = time.perf_counter() - t
+        if dt >= 0.5 * target_s or len(rows) >= max_rows:
+            break
     return sample_flops(w, rows) / dt / 1e12, dt, len(rows), cores
 
 
