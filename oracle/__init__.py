@@ -1,4 +1,5 @@
-"""fp64 CPU oracle for the attention forward pass (TEST INFRASTRUCTURE ONLY).
+"""fp64 CPU oracle for the attention forward (16-bit and e4m3) and backward
+passes (TEST INFRASTRUCTURE ONLY).
 
 Only the test suite, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU
 baseline / reference arm may import this package. The CUDA library never
