@@ -25,11 +25,13 @@
 //        P = 2^(c S - lse2), dS = P (dP - D)  -> 16 bit over the S columns
 //        dQ += dS K_j                             (A = dS from TMEM)
 //      dP is released as soon as it is read, so dP of tile j+1 is computed
-//      while dS of tile j is formed; the MMA order is dP(j+1), dQ(j), S(j+2).
+//      while dS of tile j is formed. Two warps issue the MMAs: one S and dQ
+//      (S(j+2) after dQ(j) has read its buffer), one dP.
 //
-// Roles (16 warps): warp 0 TMA producer (lane 0); warp 1 TMEM owner and MMA
-// issuer (the whole warp, one elected lane issuing; the d = 64 dK/dV kernel
-// splits its MMAs over warps 2 and 3 instead); warpgroups 1 and 2 the
+// Roles (16 warps): warp 0 TMA producer (lane 0); warp 1 TMEM owner and, in
+// the d = 128 dK/dV kernel, MMA issuer (the whole warp, one elected lane
+// issuing); the dQ kernel and the d = 64 dK/dV kernel issue their MMAs as two
+// chains on warps 2 and 3 instead; warpgroups 1 and 2 the
 // element-wise softmax gradient (one thread per TMEM lane; warpgroup 1 takes
 // columns 0-63 of each 128-column scratch tile, warpgroup 2 columns 64-127,
 // and each packs its 16-bit result over the first 32 of its own columns);
@@ -468,12 +470,14 @@ __device__ __forceinline__ void bwd_mma_kv(const BwdArgs& a, uint32_t sbase, uin
   wait_drain(bar(A ? kBbDrain : kBbDrainB), 0u, ab, kStatusDrain);
 }
 
-// The MMA-issuing warp of the dQ kernel. S of tile j goes to scratch
-// A (even j) or A1 (odd j), dP to B. Per tile j: dP(j+1) once dP(j) was read,
-// dQ(j) += dS(j) K_j once dS(j) is written over S(j), then S(j+2) over it.
-template <int D, bool BF16, bool CAUSAL>
-__device__ __forceinline__ void bwd_mma_dq(const BwdArgs& a, uint32_t sbase, uint32_t bars,
-                                           uint32_t tmem, const AbortCtx& ab) {
+// The dQ kernel's MMAs as two chains on their own warps (they share no TMEM
+// columns): chain SQ (warp 2) issues S into the two S buffers and dQ += dS K
+// from them (S(j+2) reuses a buffer after dQ(j) has read it, in order);
+// chain P (warp 3) issues dP into B as soon as the element-wise role has read
+// the previous one. Q, dO are released once both chains are done with them.
+template <int D, bool BF16, bool CAUSAL, bool SQ>
+__device__ __forceinline__ void bwd_mma_dq_chain(const BwdArgs& a, uint32_t sbase, uint32_t bars,
+                                                 uint32_t tmem, const AbortCtx& ab) {
   using L = BwdLayout<D, false>;
   constexpr int KS = L::kKSlots, VS = L::kVSlots;
   constexpr int kKFull = kBbRing, kKEmpty = kBbRing + KS;
@@ -490,7 +494,6 @@ __device__ __forceinline__ void bwd_mma_dq(const BwdArgs& a, uint32_t sbase, uin
   auto vwait = [&](uint32_t v) {
     return wait_spin_warp(bar(kVFull + v % VS), (v / VS) & 1u, ab, kStatusMma);
   };
-  // S(c) = Q K^T into its buffer; dP = dO V^T into B (V slot released after)
   auto issue_s = [&](uint32_t c, uint32_t k) {
     issue_qk<D, BF16, true>(sbuf(c), fixq, kslot(k));
     ptx::umma_commit_elect(bar((c & 1u) ? kBbA1Full : kBbAFull));
@@ -500,7 +503,7 @@ __device__ __forceinline__ void bwd_mma_dq(const BwdArgs& a, uint32_t sbase, uin
     ptx::umma_commit_elect(bar(kBbBFull));
     ptx::umma_commit_elect(bar(kVEmpty + v % VS));
   };
-  uint32_t cnt = 0, kc = 0, vc = 0, units = 0;
+  uint32_t cnt = 0, kv = 0, units = 0;  // kv: K (chain SQ) or V (chain P) ring index
   int round = 0, bh = 0, t = 0;
   bool ok = true;
   while (ok && bwd_next_unit<CAUSAL, false>(round, a, bh, t)) {
@@ -508,47 +511,52 @@ __device__ __forceinline__ void bwd_mma_dq(const BwdArgs& a, uint32_t sbase, uin
     bwd_span<CAUSAL, false>(a, t, first, last);
     const uint32_t n = static_cast<uint32_t>(last - first + 1);
     if (!(ok = wait_spin_warp(bar(kBbFixFull), units & 1u, ab, kStatusMma))) break;
-    if (!(ok = kwait(kc))) break;
-    ptx::tc_fence_after();
-    issue_s(cnt, kc);
-    if (!(ok = vwait(vc))) break;
-    issue_dp(vc);
-    if (n > 1) {
-      if (!(ok = kwait(kc + 1))) break;
-      issue_s(cnt + 1, kc + 1);
-    }
-    for (uint32_t i = 0; i < n; ++i) {
-      const uint32_t c = cnt + i;
-      // dP(c) was read: the next dP into B
-      if (!(ok = wait_spin_warp(bar(kBbPFull), c & 1u, ab, kStatusMma))) break;
-      if (i + 1 < n) {
-        if (!(ok = vwait(vc + i + 1))) break;
+    if constexpr (SQ) {
+      for (uint32_t k = 0; k < 2 && k < n && ok; ++k) {
+        if (!(ok = kwait(kv + k))) break;
         ptx::tc_fence_after();
-        issue_dp(vc + i + 1);
+        issue_s(cnt + k, kv + k);
       }
-      // dQ += dS K (dS over the S columns of its buffer; K used MN-major)
-      if (!(ok = wait_spin_warp(bar(kBbDsFull), c & 1u, ab, kStatusMma))) break;
-      if (i == 0 && units > 0 &&
-          !(ok = wait_spin_warp(bar(kBbAccFree), (units - 1) & 1u, ab, kStatusMma)))
-        break;
+      for (uint32_t i = 0; i < n && ok; ++i) {
+        const uint32_t c = cnt + i;
+        // dQ += dS K (dS over the S columns of its buffer; K used MN-major)
+        if (!(ok = wait_spin_warp(bar(kBbDsFull), c & 1u, ab, kStatusMma))) break;
+        if (i == 0 && units > 0 &&
+            !(ok = wait_spin_warp(bar(kBbAccFree), (units - 1) & 1u, ab, kStatusMma)))
+          break;
+        ptx::tc_fence_after();
+        bwd_issue_ts<D, BF16>(tAcc, sbuf(c), kslot(kv + i), i > 0);
+        ptx::umma_commit_elect(bar(kKEmpty + (kv + i) % KS));
+        if (i + 2 < n) {  // in-order: after dQ(c) has read dS(c)
+          if (!(ok = kwait(kv + i + 2))) break;
+          issue_s(c + 2, kv + i + 2);
+        }
+      }
+      if (!ok) break;
+      ptx::umma_commit_elect(bar(kBbAccFull));
+    } else {
+      if (!(ok = vwait(kv))) break;
       ptx::tc_fence_after();
-      bwd_issue_ts<D, BF16>(tAcc, sbuf(c), kslot(kc + i), i > 0);
-      ptx::umma_commit_elect(bar(kKEmpty + (kc + i) % KS));
-      if (i + 2 < n) {  // in-order execution: after dQ(c) has read dS(c)
-        if (!(ok = kwait(kc + i + 2))) break;
-        issue_s(c + 2, kc + i + 2);
+      issue_dp(kv);
+      for (uint32_t i = 0; i < n && ok; ++i) {
+        const uint32_t c = cnt + i;
+        // dP(c) was read: the next dP into B
+        if (!(ok = wait_spin_warp(bar(kBbPFull), c & 1u, ab, kStatusMma))) break;
+        if (i + 1 < n) {
+          if (!(ok = vwait(kv + i + 1))) break;
+          ptx::tc_fence_after();
+          issue_dp(kv + i + 1);
+        }
       }
+      if (!ok) break;
     }
-    if (!ok) break;
     cnt += n;
-    kc += n;
-    vc += n;
-    ptx::umma_commit_elect(bar(kBbAccFull));
+    kv += n;
     ptx::umma_commit_elect(bar(kBbFixEmpty));
     ++units;
   }
-  ptx::umma_commit_elect(bar(kBbDrain));
-  wait_drain(bar(kBbDrain), 0u, ab, kStatusDrain);
+  ptx::umma_commit_elect(bar(SQ ? kBbDrain : kBbDrainB));
+  wait_drain(bar(SQ ? kBbDrain : kBbDrainB), 0u, ab, kStatusDrain);
 }
 
 // Unpacks the 16-bit pair w to two floats.
@@ -777,15 +785,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const AbortCtx ab{abort_flag, a.status};
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
   if (threadIdx.x == 0) {
-    // dK/dV at d = 64: two MMA chains each commit the shared-resource barriers
-    constexpr uint32_t kChains = (KEYS && L::kDblS) ? 2u : 1u;
+    // two MMA chains (dK/dV at d = 64, dQ always) each commit the
+    // shared-resource barriers
+    constexpr uint32_t kChains = KEYS ? (L::kDblS ? 2u : 1u) : 2u;
     ptx::mbar_init(bar(kBbFixFull), 1);
     ptx::mbar_init(bar(kBbFixEmpty), kChains);
     ptx::mbar_init(bar(kBbAFull), 1);
     ptx::mbar_init(bar(kBbBFull), 1);
     ptx::mbar_init(bar(kBbPFull), 8);
     ptx::mbar_init(bar(kBbDsFull), 8);
-    ptx::mbar_init(bar(kBbAccFull), kChains);
+    ptx::mbar_init(bar(kBbAccFull), KEYS ? kChains : 1u);  // dQ: chain SQ alone
     ptx::mbar_init(bar(kBbAccFree), 4);
     ptx::mbar_init(bar(kBbDrain), 1);
     ptx::mbar_init(bar(kBbA1Full), 1);
@@ -817,9 +826,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     } else if constexpr (KEYS && L::kDblS) {  // the two MMA chains, each a whole warp
       if (warp == 2) bwd_mma_kv<D, BF16, CAUSAL, true>(a, sbase, bars, tmem, ab);
       else if (warp == 3) bwd_mma_kv<D, BF16, CAUSAL, false>(a, sbase, bars, tmem, ab);
+    } else if constexpr (!KEYS) {  // the dQ kernel's two MMA chains
+      if (warp == 2) bwd_mma_dq_chain<D, BF16, CAUSAL, true>(a, sbase, bars, tmem, ab);
+      else if (warp == 3) bwd_mma_dq_chain<D, BF16, CAUSAL, false>(a, sbase, bars, tmem, ab);
     } else if (warp == 1) {  // the whole warp
-      if constexpr (KEYS) bwd_mma<D, BF16, CAUSAL, true>(a, sbase, bars, tmem, ab);
-      else bwd_mma_dq<D, BF16, CAUSAL>(a, sbase, bars, tmem, ab);
+      bwd_mma<D, BF16, CAUSAL, true>(a, sbase, bars, tmem, ab);
     }
   } else if (wgrp <= 2) {
     ptx::setmaxnreg_to<kBwdRegsElem, kBwdRegsLaunch>();
