@@ -333,6 +333,9 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
   const fa_status sz = fa::check_sizes(B, H, N, d);
   if (sz != FA_OK) return sz;
+  // the backward's units are 128-row tiles: their count must stay in int range
+  if (static_cast<long long>(B) * H * ((static_cast<long long>(N) + 127) / 128) > 0x7FFFFFFFLL)
+    return FA_ERR_UNSUPPORTED;
 
   int dev = 0;
   fa::DeviceState* st = nullptr;

@@ -161,7 +161,8 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* vt, void* o, floa
  *            contents are overwritten (row logsumexps and D); it must not be
  *            used by another call on another stream at the same time.
  * All pointers 16-byte aligned. B, H, N, d, causal, scale, dtype, stream and
- * the errors are as in fa_fwd. Three launches on `stream` (a pass forming D,
+ * the errors are as in fa_fwd, and B*H*ceil(N/128) >= 2^31 returns
+ * FA_ERR_UNSUPPORTED. Three launches on `stream` (a pass forming D,
  * one for dk / dv, one for dq); no atomics, bitwise reproducible. Tolerance
  * of the 16-bit P and dS: see the library's tests.
  */
