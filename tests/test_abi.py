@@ -185,6 +185,8 @@ def test_bwd_bad_arguments_rejected(lib, kw):
 
 def test_bwd_unsupported_and_workspace_size(lib):
     assert _bwd(d=96) == fa.FA_ERR_UNSUPPORTED
+    # 2^30 units of 256 rows pass the forward's limit; 2^31 tiles of 128 rows do not
+    assert _bwd(B=1, H=1 << 14, N=1 << 24) == fa.FA_ERR_UNSUPPORTED
     assert fa.fa_bwd_workspace_size(2, 3, 300, 64) == 2 * 2 * 3 * 3 * 128 * 4
     with pytest.raises(fa.FaError):
         fa.fa_bwd_workspace_size(1, 1, 128, 96)
