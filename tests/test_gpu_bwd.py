@@ -86,7 +86,8 @@ def _inputs(name):
     return I.qkv_bits(w) + (_dout_bits(w),)
 
 
-@pytest.mark.parametrize("name", ["mha_b4_h16_n4096_d128_fp16", "causal_b4_h16_n4096_d128_bf16"])
+@pytest.mark.parametrize("name", ["mha_b4_h16_n4096_d128_fp16", "causal_b4_h16_n4096_d128_bf16",
+                                  "mha_b2_h32_n8192_d64_fp16"])
 def test_bwd_full_size_sampled_heads(oracle_mod, name):
     w = I.WORKLOADS[name]
     q, k, v, dob = _inputs(name)
