@@ -438,7 +438,14 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t bars, ui
     // exponentials, for the LSE. They differ only for bf16 (see below).
     float m_ref = -INFINITY, l = 0.f, l_exp = 0.f;
     for (int j = 0; j < nkv; ++j) {
-      if (!(ok = wait_bounded_warp(bar(kBarSFull + wg), (scnt++) & 1u, ab, kStatusSoftmax))) break;
+      // d = 64 computes S_i(j+1) during softmax(j), so S is usually ready: poll
+      // (resumes sooner); otherwise suspend, leaving issue slots to the other
+      // tile's softmax on the same sub-partition
+      if (!(ok = L::kSepP
+                     ? wait_spin_warp(bar(kBarSFull + wg), scnt & 1u, ab, kStatusSoftmax)
+                     : wait_bounded_warp(bar(kBarSFull + wg), scnt & 1u, ab, kStatusSoftmax)))
+        break;
+      ++scnt;
       ptx::tc_fence_after();
       // base-2 score scale of this tile (8-bit inputs: times its K block's scale)
       float cj = cl2;
