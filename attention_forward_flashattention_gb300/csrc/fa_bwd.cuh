@@ -592,6 +592,13 @@ __device__ __forceinline__ void bwd_elementwise(const BwdArgs& a, const uint8_t*
   const uint32_t tB = tl + L::kColB + static_cast<uint32_t>(c0);
   const float cl2 = a.scale_log2;
   const bool ragged = (a.N & 127) != 0;
+  // Where the scores are issued ahead (dQ kernel; dK/dV at d = 64, two S^T
+  // buffers) the waits are usually already satisfied: poll, which resumes
+  // sooner; otherwise suspend and leave issue slots to the other warps.
+  auto ew_wait = [&](uint32_t b, uint32_t parity) {
+    return L::kDblS ? wait_spin_warp(b, parity, ab, kStatusSoftmax)
+                    : wait_bounded_warp(b, parity, ab, kStatusSoftmax);
+  };
   uint32_t ring = 0, cnt = 0;
   int round = 0, bh = 0, t = 0;
   bool ok = true;
@@ -613,15 +620,11 @@ __device__ __forceinline__ void bwd_elementwise(const BwdArgs& a, const uint8_t*
       const bool odd = L::kDblS && (c & 1u);
       const uint32_t tA = odd ? tA1 : tA0;
       // the stage's lse2 / D vectors (TMA-written): observe their barrier too
-      if (KEYS && !(ok = wait_bounded_warp(bar(kBbRing + rr % S), (rr / S) & 1u, ab,
-                                           kStatusSoftmax)))
-        break;
+      if (KEYS && !(ok = ew_wait(bar(kBbRing + rr % S), (rr / S) & 1u))) break;
       const float* vec = reinterpret_cast<const float*>(
           sgen + L::kOffRing + (rr % S) * L::kStageBytes + 2 * L::kTileBytes);
       // ---- P: scores of this tile against the row's reference
-      if (!(ok = wait_bounded_warp(bar(odd ? kBbA1Full : kBbAFull),
-                                   L::kDblS ? (c >> 1) & 1u : ph, ab, kStatusSoftmax)))
-        break;
+      if (!(ok = ew_wait(bar(odd ? kBbA1Full : kBbAFull), L::kDblS ? (c >> 1) & 1u : ph))) break;
       ptx::tc_fence_after();
       uint32_t sr[2][32];
       ptx::tmem_ld32(tA, sr[0]);
@@ -673,7 +676,7 @@ __device__ __forceinline__ void bwd_elementwise(const BwdArgs& a, const uint8_t*
       }
       // ---- dS = P (dP - D) (16 bit) over this half's first 32 dP^T columns
       // (dK/dV) or its first 32 S columns (dQ)
-      if (!(ok = wait_bounded_warp(bar(kBbBFull), ph, ab, kStatusSoftmax))) break;
+      if (!(ok = ew_wait(bar(kBbBFull), ph))) break;
       ptx::tc_fence_after();
       uint32_t dp[2][32];
       ptx::tmem_ld32(tB, dp[0]);

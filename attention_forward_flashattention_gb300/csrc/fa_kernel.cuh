@@ -530,8 +530,8 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t bars, ui
           // P_i(j-1) read and O_i updated by its PV before P_i is rewritten
           // (and before the O rescale below)
           if (pstores > 0 &&
-              !(ok = wait_bounded_warp(bar(kBarPFree + wg), (pstores - 1) & 1u, ab,
-                                       kStatusSoftmax)))
+              !(ok = wait_spin_warp(bar(kBarPFree + wg), (pstores - 1) & 1u, ab,
+                                    kStatusSoftmax)))
             break;
           ptx::tc_fence_after();
         }
