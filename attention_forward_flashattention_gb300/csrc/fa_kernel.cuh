@@ -12,7 +12,9 @@
 //        warp 1: TMEM owner and MMA issuer: the whole warp runs the loop and
 //                one elected lane issues each tcgen05 op (tcgen05.mma is
 //                issued by one thread, "TCA 51%, MFU below 8%", B200 section).
-//        warps 2-3 idle.
+//        warps 2-3 idle, except at d = 64, where P has TMEM columns of its
+//                own and the S products (warp 2) and the PV products
+//                (warp 3) are issued by separate warps instead of warp 1.
 //   WG1  softmax of Q tile 0, one thread per row = TMEM lane (the B300
 //        walkthrough, V14 item d);
 //   WG2  softmax of Q tile 1;
@@ -25,7 +27,9 @@
 //
 // TMEM (512 columns): S0 0-127, S1 128-255, O0 256.., O1 256+D..; P_i is
 // written by the softmax over the first 64 columns of S_i (two 16-bit values
-// per column) and read from there by the O += P V MMA (A operand in TMEM).
+// per column; 8-bit P: four per column over the first 32) and read from there
+// by the O += P V MMA (A operand in TMEM). At d = 64, P_i sits in columns
+// 384 + 64 i instead (see mma_s_role).
 //
 // MMA order: S0 = Q0 K_0^T, S1 = Q1 K_0^T, then per KV tile j
 //   O0 += P0 V_j, S0 = Q0 K_{j+1}^T, O1 += P1 V_j, S1 = Q1 K_{j+1}^T.
