@@ -81,14 +81,25 @@ FWD_SOURCES = ("ptx.cuh", "fa_common.cuh", "fa_kernel.cuh", "fa_launch.cuh", "fa
                "fa_fwd_d128.cu", "fa_host.cu")
 
 
+def _code_only(text: str) -> str:
+    """The source without // comments and blank lines (comment edits leave
+    the compiled kernel, and so its traffic, unchanged)."""
+    lines = []
+    for ln in text.splitlines():
+        code = ln.split("//", 1)[0].rstrip()
+        if code.strip():
+            lines.append(code)
+    return "\n".join(lines)
+
+
 def kernel_source_sha256() -> str:
-    """Hash of the forward kernel's sources: a recorded DRAM traffic figure
-    holds only for the sources it was measured on."""
+    """Hash of the forward kernel's source code: a recorded DRAM traffic
+    figure holds only for the code it was measured on."""
     from attention_forward_flashattention_gb300 import build as fabuild
     h = hashlib.sha256()
     for name in sorted(FWD_SOURCES):
-        with open(os.path.join(fabuild.CSRC, name), "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
+        with open(os.path.join(fabuild.CSRC, name), encoding="utf-8") as f:
+            h.update(name.encode() + b"\0" + _code_only(f.read()).encode())
     return h.hexdigest()
 
 
