@@ -128,51 +128,64 @@ enum BwdBar : int {
 constexpr int kBwdSlotTmem = 480;
 constexpr int kBwdSlotAbort = 484;
 
-// D_i and LSE_i * log2(e) into the tile-padded workspace. One thread per
-// padded row (grid covers BH * n_t * 128 rows).
+// D_i and LSE_i * log2(e) into the tile-padded workspace. Eight lanes per
+// padded row: lane p of a row reads its 16-byte chunks p, p + 8, ..., so a
+// warp's loads cover four rows contiguously, and a shuffle sums the eight
+// partial dot products. Grid-stride over rows * 8 threads (rows is a multiple
+// of 128, so every warp runs the same iterations and all its lanes shuffle).
 template <int D, bool BF16>
 __global__ void bwd_prep_kernel(const void* o, const void* dout, const float* lse, float* lse2,
                                 float* delta, int N, int n_t, long long rows) {
-  const long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (g >= rows) return;
-  const long long bh = g / (static_cast<long long>(n_t) * 128);
-  const int i = static_cast<int>(g - bh * n_t * 128);
-  if (i >= N) {
-    lse2[g] = INFINITY;
-    delta[g] = 0.f;
-    return;
-  }
-  const size_t row = static_cast<size_t>(bh) * N + i;
-  const uint4* po = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(o) + row * D);
-  const uint4* pd = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(dout) + row * D);
-  float acc = 0.f;
-#pragma unroll 4
-  for (int c = 0; c < D / 8; ++c) {
-    const uint4 a = po[c], b = pd[c];
-    const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+  constexpr int kLanes = 8, kChunks = D / 8;  // 16-byte chunks per row
+  const long long total = rows * kLanes;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
+       t += stride) {
+    const long long g = t / kLanes;  // padded row
+    const int part = static_cast<int>(t % kLanes);
+    const long long bh = g / (static_cast<long long>(n_t) * 128);
+    const int i = static_cast<int>(g - bh * n_t * 128);
+    const size_t row = static_cast<size_t>(bh) * N + i;
+    float acc = 0.f;
+    if (i < N) {
+      const uint4* po = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(o) + row * D);
+      const uint4* pd =
+          reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(dout) + row * D);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      float a0, a1, b0, b1;
-      if constexpr (BF16) {
-        a0 = __uint_as_float(wa[e] << 16);
-        a1 = __uint_as_float(wa[e] & 0xFFFF0000u);
-        b0 = __uint_as_float(wb[e] << 16);
-        b1 = __uint_as_float(wb[e] & 0xFFFF0000u);
-      } else {
-        const __half2 ha = *reinterpret_cast<const __half2*>(&wa[e]);
-        const __half2 hb = *reinterpret_cast<const __half2*>(&wb[e]);
-        const float2 fa = __half22float2(ha), fb = __half22float2(hb);
-        a0 = fa.x;
-        a1 = fa.y;
-        b0 = fb.x;
-        b1 = fb.y;
+      for (int c = part; c < kChunks; c += kLanes) {
+        const uint4 ua = po[c], ub = pd[c];
+        const uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wb[4] = {ub.x, ub.y, ub.z, ub.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float a0, a1, b0, b1;
+          if constexpr (BF16) {
+            a0 = __uint_as_float(wa[e] << 16);
+            a1 = __uint_as_float(wa[e] & 0xFFFF0000u);
+            b0 = __uint_as_float(wb[e] << 16);
+            b1 = __uint_as_float(wb[e] & 0xFFFF0000u);
+          } else {
+            const __half2 ha = *reinterpret_cast<const __half2*>(&wa[e]);
+            const __half2 hb = *reinterpret_cast<const __half2*>(&wb[e]);
+            const float2 fa = __half22float2(ha), fb = __half22float2(hb);
+            a0 = fa.x;
+            a1 = fa.y;
+            b0 = fb.x;
+            b1 = fb.y;
+          }
+          acc = fmaf(a0, b0, acc);
+          acc = fmaf(a1, b1, acc);
+        }
       }
-      acc = fmaf(a0, b0, acc);
-      acc = fmaf(a1, b1, acc);
+    }
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+    if (part == 0) {
+      // padding rows: D = 0, lse2 = +inf, so their weights are exactly 0
+      delta[g] = i < N ? acc : 0.f;
+      lse2[g] = i < N ? lse[row] * 1.4426950408889634f : INFINITY;
     }
   }
-  delta[g] = acc;
-  lse2[g] = lse[row] * 1.4426950408889634f;
 }
 
 // Unit order: causal problems longest first, odd rounds reversed (as the

@@ -11,7 +11,10 @@ template <int D, bool BF16, bool CAUSAL>
 cudaError_t launch(const CUtensorMap* m, const BwdArgs& a, const void* o, const void* dout,
                    const float* lse, int grid, cudaStream_t st) {
   const long long rows = static_cast<long long>(a.BH) * a.n_t * 128;
-  bwd_prep_kernel<D, BF16><<<static_cast<unsigned>((rows + 255) / 256), 256, 0, st>>>(
+  // eight threads per padded row, at most 2^20 blocks (the kernel strides)
+  const long long blocks = (rows * 8 + 255) / 256;
+  bwd_prep_kernel<D, BF16><<<static_cast<unsigned>(blocks < (1LL << 20) ? blocks : (1LL << 20)),
+                             256, 0, st>>>(
       o, dout, lse, const_cast<float*>(a.lse2), const_cast<float*>(a.delta), a.N, a.n_t, rows);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
