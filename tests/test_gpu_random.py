@@ -1,0 +1,69 @@
+"""Seeded random shapes, forward and backward, every element against the fp64
+oracle: B, H, N (ragged, 1 to 1100), d, dtype and causality drawn from a fixed
+generator, so that tile edges, unit boundaries, short causal units and both
+MMA issue layouts of each head dimension are exercised together. The bounds
+are those of the dedicated parity tests (forward: 1e-2 plus half an output
+spacing per element, 1e-3 on the LSE; backward: 4 unit roundoffs of the term
+magnitudes plus half a spacing)."""
+import numpy as np
+import pytest
+
+import attention_forward_flashattention_gb300 as fa
+from attention_forward_flashattention_gb300 import inputs as I
+
+from parity_util import bits_to_f64, half_ulp, to_bits, to_device
+
+pytestmark = pytest.mark.gpu
+
+EPS = {"fp16": 2.0 ** -11, "bf16": 2.0 ** -8}
+
+
+def _cases(n=48, seed=20261202):
+    rng = np.random.default_rng(seed)
+    out = []
+    for k in range(n):
+        d = int(rng.choice([64, 128]))
+        dtype = str(rng.choice(["fp16", "bf16"]))
+        causal = bool(rng.integers(0, 2))
+        N = int(rng.integers(1, 1101))
+        B = int(rng.integers(1, 3))
+        H = int(rng.integers(1, 4))
+        out.append((k, B, H, N, d, dtype, causal))
+    return out
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import torch
+    torch.cuda.init()
+    fa.build.build()
+    fa.load_library()
+
+
+@pytest.mark.parametrize("k,B,H,N,d,dtype,causal", _cases())
+def test_random_shape_forward_and_backward(oracle_mod, k, B, H, N, d, dtype, causal):
+    import torch
+    w = I.custom(f"rand{k}", B, H, N, d, dtype, causal, seed_index=3000 + k)
+    q, kk, v = I.qkv_bits(w)
+    dob = I.dout_bits(w)
+    qd, kd, vd, dod = (to_device(x, dtype) for x in (q, kk, v, dob))
+    o, lse = fa.attention_forward(qd, kd, vd, causal=causal, scale=w.scale)
+    dq, dk, dv = fa.attention_backward(qd, kd, vd, o, lse, dod, causal=causal, scale=w.scale)
+    torch.cuda.synchronize()
+    assert fa.fa_check(0) == fa.FA_OK
+
+    o_ref, l_ref = oracle_mod.attn_fwd(q, kk, v, dtype, causal, w.scale)
+    got = bits_to_f64(to_bits(o), dtype).reshape(o_ref.shape)
+    err = np.abs(got - o_ref)
+    assert np.all(err <= 1e-2 + half_ulp(o_ref, dtype)), (k, float(err.max()))
+    assert float(err.mean()) <= 1e-3, k
+    assert float(np.abs(lse.cpu().numpy().astype(np.float64).reshape(l_ref.shape) - l_ref).max()) \
+        <= 1e-3, k
+
+    g = oracle_mod.attn_bwd(q, kk, v, dob, dtype, causal, w.scale)
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        ref = g[name]
+        got = bits_to_f64(to_bits(t), dtype).reshape(ref.shape)
+        limit = 4 * EPS[dtype] * g["mag_" + name] + half_ulp(ref, dtype) + 1e-6
+        bad = np.abs(got - ref) > limit
+        assert np.all(np.isfinite(got)) and not bad.any(), (k, name, int(bad.sum()))
