@@ -230,3 +230,61 @@ def test_host_valid_arguments_reach_the_device(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert _host() in (fa.FA_ERR_CUDA, fa.FA_ERR_ARCH)
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include <string.h>
+#include "fa.h"
+
+int main(void) {
+  /* every entry point is a plain C function */
+  typedef void (*fn_t)(void);
+  fn_t fns[] = {(fn_t)fa_fwd, (fn_t)fa_fwd_strided, (fn_t)fa_fwd_fp8, (fn_t)fa_bwd,
+                (fn_t)fa_bwd_workspace_size, (fn_t)fa_fwd_noalloc, (fn_t)fa_fwd_host,
+                (fn_t)fa_fwd_host_workspace_size, (fn_t)fa_check, (fn_t)fa_query_launch,
+                (fn_t)fa_sm_clock_probe, (fn_t)fa_status_string, (fn_t)fa_version};
+  size_t i;
+  size_t ws = 0;
+  for (i = 0; i < sizeof(fns) / sizeof(fns[0]); ++i)
+    if (!fns[i]) return 1;
+  if (strcmp(fa_status_string(FA_OK), "FA_OK") != 0) return 2;
+  if (fa_version() <= 0) return 3;
+  /* argument checks run before any device call */
+  if (fa_fwd(NULL, NULL, NULL, NULL, NULL, 1, 1, 128, 128, 0, 0.125f, FA_DTYPE_FP16, NULL) !=
+      FA_ERR_INVALID_ARG)
+    return 4;
+  if (fa_bwd_workspace_size(1, 1, 128, 96, &ws) != FA_ERR_UNSUPPORTED) return 5;
+  printf("ok %d\n", fa_version());
+  return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_links(tmp_path):
+    """include/fa.h compiles as strict C99 and a C program links against the
+    library and runs its host-side checks (no GPU needed)."""
+    import os
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    lib_path, _ = fabuild.build()
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    src = tmp_path / "use_fa.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "use_fa"
+    lib_dir = os.path.dirname(lib_path)
+    lib_name = os.path.basename(lib_path)
+    subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                    "-I", os.path.join(root, "include"), str(src), "-o", str(exe),
+                    os.path.join(lib_dir, lib_name), f"-Wl,-rpath,{lib_dir}"],
+                   check=True, capture_output=True, text=True)
+    env = dict(os.environ)
+    nvcc = shutil.which("nvcc")
+    if nvcc:  # the library's CUDA runtime
+        cuda_lib = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc))), "lib64")
+        env["LD_LIBRARY_PATH"] = cuda_lib + os.pathsep + env.get("LD_LIBRARY_PATH", "")
+    out = subprocess.run([str(exe)], capture_output=True, text=True, env=env, timeout=60)
+    assert out.returncode == 0 and out.stdout.startswith("ok"), (out.returncode, out.stderr)
