@@ -455,18 +455,17 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t bars, ui
       float cj = cl2;
       if constexpr (FP8) cj = cl2 * __ldg(a.k_scales + static_cast<size_t>(bh) * a.n_kv + j);
       const float2 c2j = make_float2(cj, cj);
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) ptx::tmem_ld32(tS + 32u * c, sr[c]);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) ptx::tmem_ld_wait(sr[c]);
+      uint32_t sr[2][2][32];  // columns 0-63, 64-127
+      ptx::tmem_ld64(tS, sr[0]);
+      ptx::tmem_ld64(tS + 64u, sr[1]);
+      ptx::tmem_ld_wait64x2(sr[0], sr[1]);
       if constexpr (L::kSepP) {  // S_i is in registers: S_i(j+1) may overwrite it
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(kBarSFree + wg));
       }
       float s[128];
 #pragma unroll
-      for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
+      for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 6][(c >> 5) & 1][c & 31]);
       // Mask keys past the end of the sequence and (causal) past the row.
       const int k0 = j * kTileRows;
       const bool need_mask = (k0 + kTileRows > a.N) || (CAUSAL && k0 + kTileRows - 1 > tile_row0);

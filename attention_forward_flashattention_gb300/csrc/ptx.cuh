@@ -322,6 +322,60 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
                : "memory");
 }
 
+// Warp-collective load of 64 consecutive fp32 columns per lane (32x32b.x64)
+// into r[0] (columns 0-31) and r[1] (32-63). Fewer, wider loads reach the
+// registers sooner than 32-column ones.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[2][32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {"
+      "%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+      "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+      "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];"
+      : "=r"(r[0][0]), "=r"(r[0][1]), "=r"(r[0][2]), "=r"(r[0][3]), "=r"(r[0][4]), "=r"(r[0][5]),
+        "=r"(r[0][6]), "=r"(r[0][7]), "=r"(r[0][8]), "=r"(r[0][9]), "=r"(r[0][10]), "=r"(r[0][11]),
+        "=r"(r[0][12]), "=r"(r[0][13]), "=r"(r[0][14]), "=r"(r[0][15]), "=r"(r[0][16]), "=r"(r[0][17]),
+        "=r"(r[0][18]), "=r"(r[0][19]), "=r"(r[0][20]), "=r"(r[0][21]), "=r"(r[0][22]), "=r"(r[0][23]),
+        "=r"(r[0][24]), "=r"(r[0][25]), "=r"(r[0][26]), "=r"(r[0][27]), "=r"(r[0][28]), "=r"(r[0][29]),
+        "=r"(r[0][30]), "=r"(r[0][31]), "=r"(r[1][0]), "=r"(r[1][1]), "=r"(r[1][2]), "=r"(r[1][3]),
+        "=r"(r[1][4]), "=r"(r[1][5]), "=r"(r[1][6]), "=r"(r[1][7]), "=r"(r[1][8]), "=r"(r[1][9]),
+        "=r"(r[1][10]), "=r"(r[1][11]), "=r"(r[1][12]), "=r"(r[1][13]), "=r"(r[1][14]), "=r"(r[1][15]),
+        "=r"(r[1][16]), "=r"(r[1][17]), "=r"(r[1][18]), "=r"(r[1][19]), "=r"(r[1][20]), "=r"(r[1][21]),
+        "=r"(r[1][22]), "=r"(r[1][23]), "=r"(r[1][24]), "=r"(r[1][25]), "=r"(r[1][26]), "=r"(r[1][27]),
+        "=r"(r[1][28]), "=r"(r[1][29]), "=r"(r[1][30]), "=r"(r[1][31])
+      : "r"(taddr));
+}
+
+// Waits for this thread's outstanding TMEM loads into a and b (two 64-column
+// loads): the registers are tied to the wait so no use moves above it.
+__device__ __forceinline__ void tmem_ld_wait64x2(uint32_t (&a)[2][32], uint32_t (&b)[2][32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(a[0][0]), "+r"(a[0][1]), "+r"(a[0][2]), "+r"(a[0][3]), "+r"(a[0][4]), "+r"(a[0][5]),
+        "+r"(a[0][6]), "+r"(a[0][7]), "+r"(a[0][8]), "+r"(a[0][9]), "+r"(a[0][10]), "+r"(a[0][11]),
+        "+r"(a[0][12]), "+r"(a[0][13]), "+r"(a[0][14]), "+r"(a[0][15]), "+r"(a[0][16]), "+r"(a[0][17]),
+        "+r"(a[0][18]), "+r"(a[0][19]), "+r"(a[0][20]), "+r"(a[0][21]), "+r"(a[0][22]), "+r"(a[0][23]),
+        "+r"(a[0][24]), "+r"(a[0][25]), "+r"(a[0][26]), "+r"(a[0][27]), "+r"(a[0][28]), "+r"(a[0][29]),
+        "+r"(a[0][30]), "+r"(a[0][31]), "+r"(a[1][0]), "+r"(a[1][1]), "+r"(a[1][2]), "+r"(a[1][3]),
+        "+r"(a[1][4]), "+r"(a[1][5]), "+r"(a[1][6]), "+r"(a[1][7]), "+r"(a[1][8]), "+r"(a[1][9]),
+        "+r"(a[1][10]), "+r"(a[1][11]), "+r"(a[1][12]), "+r"(a[1][13]), "+r"(a[1][14]), "+r"(a[1][15]),
+        "+r"(a[1][16]), "+r"(a[1][17]), "+r"(a[1][18]), "+r"(a[1][19]), "+r"(a[1][20]), "+r"(a[1][21]),
+        "+r"(a[1][22]), "+r"(a[1][23]), "+r"(a[1][24]), "+r"(a[1][25]), "+r"(a[1][26]), "+r"(a[1][27]),
+        "+r"(a[1][28]), "+r"(a[1][29]), "+r"(a[1][30]), "+r"(a[1][31]),
+                 "+r"(b[0][0]), "+r"(b[0][1]), "+r"(b[0][2]), "+r"(b[0][3]), "+r"(b[0][4]), "+r"(b[0][5]),
+        "+r"(b[0][6]), "+r"(b[0][7]), "+r"(b[0][8]), "+r"(b[0][9]), "+r"(b[0][10]), "+r"(b[0][11]),
+        "+r"(b[0][12]), "+r"(b[0][13]), "+r"(b[0][14]), "+r"(b[0][15]), "+r"(b[0][16]), "+r"(b[0][17]),
+        "+r"(b[0][18]), "+r"(b[0][19]), "+r"(b[0][20]), "+r"(b[0][21]), "+r"(b[0][22]), "+r"(b[0][23]),
+        "+r"(b[0][24]), "+r"(b[0][25]), "+r"(b[0][26]), "+r"(b[0][27]), "+r"(b[0][28]), "+r"(b[0][29]),
+        "+r"(b[0][30]), "+r"(b[0][31]), "+r"(b[1][0]), "+r"(b[1][1]), "+r"(b[1][2]), "+r"(b[1][3]),
+        "+r"(b[1][4]), "+r"(b[1][5]), "+r"(b[1][6]), "+r"(b[1][7]), "+r"(b[1][8]), "+r"(b[1][9]),
+        "+r"(b[1][10]), "+r"(b[1][11]), "+r"(b[1][12]), "+r"(b[1][13]), "+r"(b[1][14]), "+r"(b[1][15]),
+        "+r"(b[1][16]), "+r"(b[1][17]), "+r"(b[1][18]), "+r"(b[1][19]), "+r"(b[1][20]), "+r"(b[1][21]),
+        "+r"(b[1][22]), "+r"(b[1][23]), "+r"(b[1][24]), "+r"(b[1][25]), "+r"(b[1][26]), "+r"(b[1][27]),
+        "+r"(b[1][28]), "+r"(b[1][29]), "+r"(b[1][30]), "+r"(b[1][31])
+               :
+               : "memory");
+}
+
 // Warp-collective store of 32 consecutive fp32 columns per lane.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
