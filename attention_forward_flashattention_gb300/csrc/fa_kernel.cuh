@@ -475,15 +475,18 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t bars, ui
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
       }
-      float mx[4] = {s[0], s[1], s[2], s[3]};
+      // Row max over exactly s[0..127]: eight independent chains, elements
+      // 2t and 2t + 1 of each 16-element group in chain t.
+      float mx[8];
 #pragma unroll
-      for (int c = 4; c < 128; c += 8) {
-        mx[0] = ptx::fmax3(mx[0], s[c], s[c + 1]);
-        mx[1] = ptx::fmax3(mx[1], s[c + 2], s[c + 3]);
-        mx[2] = ptx::fmax3(mx[2], s[c + 4], s[c + 5]);
-        mx[3] = ptx::fmax3(mx[3], s[c + 6], s[c + 7]);
+      for (int t = 0; t < 8; ++t) mx[t] = fmaxf(s[2 * t], s[2 * t + 1]);
+#pragma unroll
+      for (int c = 16; c < 128; c += 16) {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) mx[t] = ptx::fmax3(mx[t], s[c + 2 * t], s[c + 2 * t + 1]);
       }
-      const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * cj;
+      const float m_tile = fmaxf(ptx::fmax3(mx[0], mx[1], mx[2]),
+                                 ptx::fmax3(ptx::fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7])) * cj;
       const float m_new = fmaxf(m_ref, m_tile);
       float alpha = 1.f;
       if (j == 0) {

@@ -179,3 +179,34 @@ def test_fp8_deterministic(slib):
     o1, l1 = _run_fp8(f, w)
     o2, l2 = _run_fp8(f, w)
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_masked_keys_never_set_the_reference(slib, oracle_mod, causal):
+    """Causal: keys 128.. score far above keys 0..127 (masked for rows
+    0..127 on a whole KV tile). Non-causal, N = 200: every visible score is
+    far below zero while the zero-filled keys past N would score 0. Either
+    way a reference taken from a masked score underflows whole rows."""
+    N = 384 if causal else 200
+    B, H, d = 1, 2, 128
+    w = I.custom("fp8mask", B, H, N, d, "e4m3", causal, 900 + N)
+    rng = np.random.default_rng(N)
+    q = np.zeros((B, H, N, d))
+    q[..., 0] = 16.0
+    k = np.zeros((B, H, N, d))
+    k[..., 0] = np.where(np.arange(N) >= 128, 16.0, 0.0) if causal else -16.0
+    nt = (N + 127) // 128
+    k_scales = np.full((B, H, nt), 16.0, dtype=np.float32)   # scores 16 * 16 * 16 * scale
+    ldv = (N + 15) // 16 * 16
+    vt = np.zeros((B, H, d, ldv), dtype=np.uint8)
+    vt[:, :, :, :N] = I.to_e4m3_bits(rng.standard_normal((B, H, N, d)) / 4.0).transpose(0, 1, 3, 2)
+    f = I.Fp8Inputs(I.to_e4m3_bits(q), I.to_e4m3_bits(k), vt, 1.0, k_scales, 4.0)
+    o, lse = _run_fp8(f, w)
+    o_ref, l_ref, bound = oracle_mod.attn_fp8(f.q, f.k, f.vt, f.q_scale, f.k_scales, f.v_scale,
+                                              causal, w.scale)
+    # every weight is 0 or 1 (exact in e4m3), so the rounded-weight bound is
+    # ~0: check the per-element limit and the LSE, not the mean against it
+    got = bits_to_f64(o.reshape(-1, 128), "bf16")
+    assert np.all(np.isfinite(got)) and np.all(np.isfinite(lse)), causal
+    assert np.all(np.abs(got - o_ref) <= bound + SLACK + half_ulp(o_ref, "bf16")), causal
+    assert float(np.abs(lse.reshape(-1).astype(np.float64) - l_ref).max()) <= LSE_MAX_ABS, causal

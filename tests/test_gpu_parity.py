@@ -108,6 +108,51 @@ def test_q_zero_gives_mean_of_v(causal, d):
         assert np.array_equal(o[:, :, 0, :], v[:, :, 0, :])   # row 0 = v_0 exactly
 
 
+# ------------------------------------------------------------ masked keys never set the reference
+
+def _axis_qk(B, H, N, d, dtype, q0, k0):
+    """Q and K zero except component 0: q_i[0] = q0, k_j[0] = k0[j], so every
+    score is exactly q0 * k0[j] * scale; V random."""
+    rng = np.random.default_rng(N + d)
+    q = np.zeros((B, H, N, d))
+    q[..., 0] = q0
+    k = np.zeros((B, H, N, d))
+    k[..., 0] = np.asarray(k0, dtype=np.float64)[None, None, :]
+    v = rng.standard_normal((B, H, N, d))
+    return I.to_bits(q, dtype), I.to_bits(k, dtype), I.to_bits(v, dtype)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_causal_masked_keys_far_above_visible_ones(oracle_mod, d, dtype):
+    """Keys 128.. score ~4096 * scale (hundreds) and keys 0..127 score 0, so
+    rows 0..127 meet a whole KV tile of masked scores far above everything
+    they see. A reference taken from any masked score would underflow every
+    weight of those rows (0 / 0); the result is the mean of their visible V
+    rows, and rows from 128 on average V over keys 128..i."""
+    N = 384
+    k0 = np.where(np.arange(N) >= 128, 64.0, 0.0)
+    q, k, v = _axis_qk(1, 2, N, d, dtype, 64.0, k0)
+    scale = 1.0 / np.sqrt(d)
+    o, lse = run_fa(q, k, v, dtype, True, scale)
+    o_ref, l_ref = oracle_mod.attn_fwd(q, k, v, dtype, True, scale)
+    _check(compare(o, lse, o_ref, l_ref, dtype), f"masked-high causal d{d} {dtype}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_ragged_tail_keys_below_zero_scores(oracle_mod, d, dtype):
+    """Every visible score is -4096 * scale; the keys past N that the last KV
+    tile reads as zeros would score 0. The row reference must ignore them:
+    the result is the plain mean of V."""
+    N = 200
+    q, k, v = _axis_qk(1, 2, N, d, dtype, 64.0, np.full(N, -64.0))
+    scale = 1.0 / np.sqrt(d)
+    o, lse = run_fa(q, k, v, dtype, False, scale)
+    o_ref, l_ref = oracle_mod.attn_fwd(q, k, v, dtype, False, scale)
+    _check(compare(o, lse, o_ref, l_ref, dtype), f"ragged-low d{d} {dtype}")
+
+
 # ------------------------------------------------------------ named workloads, full size
 
 @pytest.mark.parametrize("name", I.WORKLOAD_ORDER)
