@@ -14,7 +14,7 @@
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kMaxChunks = 8;
+constexpr int kMaxChunks = 9;
 
 struct Streams {
   bool ready = false;
@@ -57,18 +57,28 @@ fa_status workspace_bytes(long long BH, int N, int d, size_t* bytes) {
   return FA_OK;
 }
 
-// Chunks: as many as keep one persistent wave of 256-row units busy in each,
-// at most kMaxChunks, at most one per head. The host link (about 200 GB/s
-// each way) is slower than the forward on every workload of interest, so
-// the forward of a chunk hides under the next chunk's copy and only the last
-// chunk's forward and copy-out are exposed: smaller chunks shorten that tail.
+// Chunk count n: as many as keep one persistent wave of 256-row units busy
+// in each, at most kMaxChunks - 1, at most one per head. The host link (about
+// 200 GB/s each way) is about as slow as the forward or slower on every
+// workload of interest, so a chunk's forward hides under the next chunk's
+// copy; what is exposed is the first chunk's copy-in and the last chunk's
+// forward and copy-out. So the call uses n + 1 chunks whose first and last
+// are half the size of the others.
 int pick_chunks(long long BH, int N, int sm_count) {
   const long long units = BH * ((static_cast<long long>(N) + 255) / 256);
   long long n = units / (sm_count > 0 ? sm_count : 1);
   if (n < 1) n = 1;
-  if (n > kMaxChunks) n = kMaxChunks;
+  if (n > kMaxChunks - 1) n = kMaxChunks - 1;
   if (n > BH) n = BH;
   return static_cast<int>(n);
+}
+
+// First head of chunk c of m: weights 1, 2, ..., 2, 1 (a single chunk when m
+// is 1); edges are nondecreasing from 0 to BH, and a chunk may be empty.
+long long chunk_edge(long long BH, int m, int c) {
+  if (m == 1) return BH * c;
+  const long long w = (c == 0) ? 0 : (c == m ? 2LL * (m - 1) : 2LL * c - 1);
+  return BH * w / (2LL * (m - 1));
 }
 
 }  // namespace
@@ -107,6 +117,7 @@ fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* o, floa
   if ((st = device_streams(dev, &s)) != FA_OK) return st;
 
   const int n = pick_chunks(BH, N, sms);
+  const int m = n > 1 ? n + 1 : 1;
   const size_t head_elems = static_cast<size_t>(N) * static_cast<size_t>(d);
   const size_t total = static_cast<size_t>(BH) * head_elems;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -136,9 +147,10 @@ fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* o, floa
             cudaStreamWaitEvent(s->out, fork, 0) == cudaSuccess;
   fa_status fwd_status = FA_OK;
   size_t lse_off = 0;
-  for (int c = 0; ok && c < n; ++c) {
-    const long long h0 = BH * c / n, h1 = BH * (c + 1) / n;
+  for (int c = 0; ok && c < m; ++c) {
+    const long long h0 = chunk_edge(BH, m, c), h1 = chunk_edge(BH, m, c + 1);
     const long long nh = h1 - h0;
+    if (nh == 0) continue;
     const size_t off = static_cast<size_t>(h0) * head_elems;
     const size_t cnt = static_cast<size_t>(nh) * head_elems;
     const size_t lrows = static_cast<size_t>(nh) * static_cast<size_t>(N);

@@ -213,8 +213,11 @@ fa_status fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, f
  * Chunk c+1 is copied in while chunk c computes and chunk c-1 is copied out,
  * on three internal non-blocking streams of the device (created on the first
  * call, kept until process exit) that fork from and join back to `stream`.
- * The heads are cut into at most 8 chunks, each keeping at least one wave
- * of the forward's persistent grid busy (one chunk for small problems).
+ * The heads are cut into at most 9 chunks: n (at most 8) chunks that each
+ * keep at least one wave of the forward's persistent grid busy, with the
+ * first and last split to half that size so the exposed copy-in at the start
+ * and forward plus copy-out at the end are short (one chunk for small
+ * problems).
  *
  * q, k, v   : HOST pointers, contiguous [B][H][N][d] of `dtype`, read.
  * o, lse    : HOST pointers, contiguous [B][H][N][d] of `dtype` and
@@ -236,8 +239,8 @@ fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* o, floa
 
 /*
  * fa_fwd_host_workspace_size - bytes of device workspace fa_fwd_host needs:
- * 4 B H N d 2-byte elements (Q, K, V, O) plus B H N float32 and 128 bytes of
- * alignment padding. Host only.
+ * 4 B H N d 2-byte elements (Q, K, V, O) plus B H N float32 and 144 bytes of
+ * alignment padding (16 for each of up to 9 chunks' LSE blocks). Host only.
  */
 fa_status fa_fwd_host_workspace_size(int B, int H, int N, int d, size_t* bytes);
 

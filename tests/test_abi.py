@@ -204,7 +204,7 @@ def _host(**kw):
              scale=0.088, dtype=fa.FA_DTYPE_FP16, ws=GOOD, wsz=None)
     a.update(kw)
     if a["wsz"] is None:
-        a["wsz"] = 4 * a["B"] * a["H"] * a["N"] * 128 * 2 + a["B"] * a["H"] * a["N"] * 4 + 128
+        a["wsz"] = 4 * a["B"] * a["H"] * a["N"] * 128 * 2 + a["B"] * a["H"] * a["N"] * 4 + 144
     return fa.fa_fwd_host(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"],
                           a["d"], a["causal"], a["scale"], a["dtype"], a["ws"], a["wsz"], 0)
 
@@ -218,9 +218,10 @@ def test_host_bad_arguments_rejected(lib, kw):
 
 def test_host_unsupported_and_workspace_size(lib):
     assert _host(d=96) == fa.FA_ERR_UNSUPPORTED
-    # Q, K, V, O (2 bytes each), LSE (4 bytes), 128 bytes of alignment padding
+    # Q, K, V, O (2 bytes each), LSE (4 bytes), 16 bytes of alignment padding
+    # for each of up to 9 chunks
     assert fa.fa_fwd_host_workspace_size(2, 3, 300, 64) == 4 * 2 * 3 * 300 * 64 * 2 + \
-        2 * 3 * 300 * 4 + 128
+        2 * 3 * 300 * 4 + 144
     with pytest.raises(fa.FaError):
         fa.fa_fwd_host_workspace_size(1, 1, 128, 96)
 

@@ -1,9 +1,9 @@
 """fa_fwd_host: the forward on host buffers with chunked copy / compute
 overlap gives, bit for bit, what the device entry point gives on the same
 inputs (each row's arithmetic does not depend on how the heads are chunked),
-for one chunk and several uneven ones, odd N (per-chunk LSE blocks padded to
-16 bytes), page-locked and pageable host memory; plus sampled rows against
-the fp64 oracle."""
+for one chunk and several uneven ones (the first and last half size), odd N
+(per-chunk LSE blocks padded to 16 bytes), page-locked and pageable host
+memory; plus sampled rows against the fp64 oracle."""
 import numpy as np
 import pytest
 
@@ -33,8 +33,8 @@ def _host_tensors(x, dtype, pin):
 CASES = [
     # B, H, N, d, dtype, causal, pinned
     (2, 3, 300, 128, "fp16", True, True),     # one chunk
-    (1, 701, 255, 64, "bf16", False, True),   # two uneven chunks, odd N
-    (4, 16, 4096, 128, "fp16", False, True),  # the default workload's shape: three chunks
+    (1, 701, 255, 64, "bf16", False, True),   # five uneven chunks (4 + 1), odd N
+    (4, 16, 4096, 128, "fp16", False, True),  # the default workload's shape: seven chunks
     (1, 701, 255, 64, "fp16", True, False),   # pageable host memory
 ]
 
