@@ -11,7 +11,7 @@ cudaError_t launch_one_fp8(const CUtensorMap* m, const FwdArgs& a, int grid, cud
   auto kern = fa_fwd_kernel<128, true, CAUSAL, true>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kFwdThreads, kSmem, st>>>(m[0], m[1], m[2], a);
+  kern<<<grid, kFwdThreads, kSmem, st>>>(m[0], m[1], m[2], m[3], a);
   return cudaGetLastError();
 }
 

@@ -172,10 +172,11 @@ fa_status check_strides(const fa_strides* s, int d) {
 }
 
 bool encode_fwd_maps(CUtensorMap* maps, const void* q, const void* k, const void* v,
-                     const fa_strides* s, bool bf16, int B, int H, int N, int d) {
+                     const void* o, const fa_strides* s, bool bf16, int B, int H, int N, int d) {
   return encode_qkv(&maps[0], q, s[0], bf16, B, H, N, d, 128) &&
          encode_qkv(&maps[1], k, s[1], bf16, B, H, N, d, fwd_k_box_rows(d)) &&
-         encode_qkv(&maps[2], v, s[2], bf16, B, H, N, d, 128);
+         encode_qkv(&maps[2], v, s[2], bf16, B, H, N, d, 128) &&
+         encode_qkv(&maps[3], o, s[3], bf16, B, H, N, d, kFwdOutBoxRows);
 }
 
 void plan_fwd(int d, int N, int H, long long BH, int sm_count, FwdArgs* a, int* grid) {
@@ -223,14 +224,10 @@ fa_status fwd_call(const void* q, const void* k, const void* v, void* o, float* 
 
   const bool bf16 = dtype == FA_DTYPE_BF16;
   const long long BH = static_cast<long long>(B) * H;
-  CUtensorMap maps[3];
-  if (!fa::encode_fwd_maps(maps, q, k, v, s, bf16, B, H, N, d)) return FA_ERR_CUDA;
+  CUtensorMap maps[4];
+  if (!fa::encode_fwd_maps(maps, q, k, v, o, s, bf16, B, H, N, d)) return FA_ERR_CUDA;
 
   fa::FwdArgs a{};
-  a.o = o;
-  a.o_sb = s[3].b;
-  a.o_sh = s[3].h;
-  a.o_sn = s[3].n;
   a.lse = lse;
   a.status = st->status;
   a.scale_log2 = scale * 1.4426950408889634f;
@@ -281,22 +278,19 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* vt, void* o, floa
 
   const cuuint64_t n = static_cast<cuuint64_t>(N), h = static_cast<cuuint64_t>(H),
                    b = static_cast<cuuint64_t>(B), lv = static_cast<cuuint64_t>(ldv);
-  CUtensorMap maps[3];
+  CUtensorMap maps[4];
   const cuuint64_t qk_dims[4] = {128u, n, h, b};
   const cuuint64_t qk_strides[3] = {128u, 128u * n, 128u * n * h};
   const cuuint64_t vt_dims[4] = {n, 128u, h, b};
   const cuuint64_t vt_strides[3] = {lv, 128u * lv, 128u * lv * h};
   if (!fa::encode_bytes4(&maps[0], q, qk_dims, qk_strides) ||
       !fa::encode_bytes4(&maps[1], k, qk_dims, qk_strides) ||
-      !fa::encode_bytes4(&maps[2], vt, vt_dims, vt_strides))
+      !fa::encode_bytes4(&maps[2], vt, vt_dims, vt_strides) ||
+      !fa::encode_qkv(&maps[3], o, fa::contiguous_strides(H, N, d), true, B, H, N, d,
+                      fa::kFwdOutBoxRows))
     return FA_ERR_CUDA;
 
   fa::FwdArgs a{};
-  const fa_strides c = fa::contiguous_strides(H, N, d);
-  a.o = o;
-  a.o_sb = c.b;
-  a.o_sh = c.h;
-  a.o_sn = c.n;
   a.lse = lse;
   a.status = st->status;
   a.scale_log2 = scale * q_scale * 1.4426950408889634f;

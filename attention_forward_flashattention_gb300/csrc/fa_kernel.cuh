@@ -53,10 +53,8 @@
 namespace fa {
 
 struct FwdArgs {
-  void* o;           // 16-bit output: row (b, h, n) at o + b*o_sb + h*o_sh + n*o_sn elements
-  float* lse;        // [BH][N] fp32, natural-log logsumexp
+  float* lse;        // [BH][N] fp32, natural-log logsumexp (O goes through its tensor map)
   uint32_t* status;  // device status word (timeouts)
-  long long o_sb, o_sh, o_sn;  // output strides in elements (multiples of 8)
   int N;             // sequence length
   int H;             // heads
   int BH;            // batch * heads
@@ -84,7 +82,11 @@ struct Layout {
   static constexpr int kOffQ = 0;                           // Q0, Q1
   static constexpr int kOffKV = 2 * kTileBytes;             // ring
   static constexpr int kOffStats = kOffKV + kStages * kTileBytes;  // [2 tiles][128] row sums l
-  static constexpr int kOffBar = kOffStats + 2 * 128 * 4;
+  // O staging for the TMA-store epilogue: one 32-row x 128-byte slice per
+  // epilogue warp (1024-byte aligned, as the 128-byte swizzle requires)
+  static constexpr int kOffOut = kOffStats + 1024;
+  static constexpr int kOutSliceBytes = 32 * 128;
+  static constexpr int kOffBar = kOffOut + 4 * kOutSliceBytes;
   static constexpr int kSmemBytes = kOffBar + 512 + 1024;  // barriers + alignment slack
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0;    // S_i (and P_i unless kSepP) at columns i*128
@@ -594,19 +596,33 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t bars, ui
   }
 }
 
+// Epilogue: O_i / l_i in 16 bits, written by TMA stores. Each warp owns the
+// 32 rows of its TMEM lane quarter and a private 32-row staging slice (the
+// store's box), so the four warps never wait for one another: per 64-column
+// panel a warp reads its rows from TMEM, writes them to its slice in the
+// 128-byte swizzled layout, and one lane stores the slice (rows past N are
+// clipped by the tensor map). The slice is rewritten only after the
+// previous store has read it.
 template <int D, bool BF16, bool CAUSAL, bool FP8>
-__device__ __forceinline__ void epilogue_role(const FwdArgs& a, uint32_t bars, uint32_t tmem,
+__device__ __forceinline__ void epilogue_role(const CUtensorMap* tm_o, const FwdArgs& a,
+                                              uint32_t sbase, uint32_t bars, uint32_t tmem,
                                               const float* stats, const AbortCtx& ab, int warp,
                                               int lane) {
   using L = Layout<D, FP8>;
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
-  const int r = (warp & 3) * 32 + lane;
+  const int w = warp & 3;
+  const int r = w * 32 + lane;
   const uint32_t tl = ptx::tmem_lane_base(tmem, warp);
-  uint16_t* out = static_cast<uint16_t*>(a.o);
+  const uint32_t slice = sbase + L::kOffOut + static_cast<uint32_t>(w) * L::kOutSliceBytes;
+  const uint32_t srow = slice + static_cast<uint32_t>(lane) * 128u;  // this thread's row
+  const uint32_t sx = static_cast<uint32_t>(lane & 7);               // its swizzle
+  if (lane == 0) ptx::prefetch_tmap(tm_o);
+  bool pending = false;  // (lane 0) a store of this warp may still be reading the slice
   uint32_t units = 0;
   int round = 0, bh = 0, mblk = 0;
   bool ok = true;
   while (ok && next_unit<CAUSAL>(round, a, bh, mblk)) {
+    const int hh = bh % a.H, bb = bh / a.H;  // tensor-map coordinates {d, n, h, b}
     for (int i = 0; i < 2 && ok; ++i) {
       ok = wait_bounded_warp(bar(kBarOFull + i), units & 1u, ab, kStatusEpilogue) &&
            wait_bounded_warp(bar(kBarStatsFull + i), units & 1u, ab, kStatusEpilogue);
@@ -615,26 +631,34 @@ __device__ __forceinline__ void epilogue_role(const FwdArgs& a, uint32_t bars, u
       const float inv_l = (FP8 ? a.v_scale : 1.f) / stats[i * 128 + r];
       ptx::mbar_arrive(bar(kBarStatsFree + i));
       const float2 il2 = make_float2(inv_l, inv_l);
-      const int grow = mblk * 256 + 128 * i + r;
-      const long long hh = bh % a.H, bb = bh / a.H;
-      uint4* orow = reinterpret_cast<uint4*>(out + bb * a.o_sb + hh * a.o_sh + grow * a.o_sn);
+      const int row0 = mblk * 256 + 128 * i + 32 * w;  // this warp's first row
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        ptx::tmem_ld32(tl + L::kColO + static_cast<uint32_t>(D) * i + 32u * c, o);
-        ptx::tmem_ld_wait(o);
-        uint32_t pk[16];
+      for (int p = 0; p < D / 64; ++p) {
+        if (lane == 0 && pending) ptx::bulk_wait_read_all();
+        __syncwarp();
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          uint32_t o[32];
+          ptx::tmem_ld32(tl + L::kColO + static_cast<uint32_t>(D * i + 64 * p + 32 * h), o);
+          ptx::tmem_ld_wait(o);
+          uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float2 v = ptx::fmul2(
-              make_float2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), il2);
-          pk[e] = pack2<BF16>(v.x, v.y);
-        }
-        if (grow < a.N) {
+          for (int e = 0; e < 16; ++e) {
+            const float2 v = ptx::fmul2(
+                make_float2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), il2);
+            pk[e] = pack2<BF16>(v.x, v.y);
+          }
 #pragma unroll
           for (int t = 0; t < 4; ++t)
-            __stcs(orow + 4 * c + t,
-                   make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]));
+            ptx::st_shared_v4(srow + (((static_cast<uint32_t>(4 * h + t)) ^ sx) << 4), pk[4 * t],
+                              pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
+        }
+        ptx::fence_proxy_async_smem();  // the slice is visible to the TMA engine
+        __syncwarp();
+        if (lane == 0 && row0 < a.N) {
+          ptx::tma_store_4d(tm_o, slice, 64 * p, row0, hh, bb);
+          ptx::bulk_commit();
+          pending = true;
         }
       }
       ptx::tc_fence_before();
@@ -642,13 +666,15 @@ __device__ __forceinline__ void epilogue_role(const FwdArgs& a, uint32_t bars, u
     }
     ++units;
   }
+  if (lane == 0 && pending) ptx::bulk_wait_all();  // before the CTA's shared memory goes
 }
 
 // FP8: e4m3 Q, K, V^T (d = 128), bf16 O (instantiate with BF16 = true).
 template <int D, bool BF16, bool CAUSAL, bool FP8 = false>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  const FwdArgs a) {
   using L = Layout<D, FP8>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -710,7 +736,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     softmax_role<D, BF16, CAUSAL, FP8>(a, bars, tmem, stats, ab, warp, lane);
   } else {
     ptx::setmaxnreg_dec<kRegsEpilogue>();
-    epilogue_role<D, BF16, CAUSAL, FP8>(a, bars, tmem, stats, ab, warp, lane);
+    epilogue_role<D, BF16, CAUSAL, FP8>(&tm_o, a, sbase, bars, tmem, stats, ab, warp, lane);
   }
   __syncwarp();
   ptx::tc_fence_before();
@@ -723,10 +749,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 // Rows of Q per unit, and of K per TMA box.
 constexpr int fwd_unit_rows(int) { return 256; }
 constexpr int fwd_k_box_rows(int) { return 128; }
+// Rows of O per TMA store: one epilogue warp's rows.
+constexpr int kFwdOutBoxRows = 32;
 // Persistent grid for n_units units on the current device.
 int fwd_grid_d64(int n_units, int sm_count);
 int fwd_grid_d128(int n_units, int sm_count);
-// maps: Q, K, V tensor maps.
+// maps: Q, K, V (loads) and O (stores) tensor maps.
 cudaError_t launch_fwd_d64(bool bf16, bool causal, const CUtensorMap* maps, const FwdArgs& a,
                            int grid, cudaStream_t stream);
 cudaError_t launch_fwd_d128(bool bf16, bool causal, const CUtensorMap* maps, const FwdArgs& a,
@@ -736,15 +764,15 @@ int fwd_smem_bytes(int d);
 // call's strides (fa_host.cu).
 fa_strides contiguous_strides(int H, int N, int d);
 fa_status check_strides(const fa_strides* s /* q, k, v, o */, int d);
-// Q, K, V tensor maps of a call (s: q, k, v strides).
+// Q, K, V, O tensor maps of a call (s: q, k, v, o strides).
 bool encode_fwd_maps(CUtensorMap* maps, const void* q, const void* k, const void* v,
-                     const fa_strides* s, bool bf16, int B, int H, int N, int d);
+                     const void* o, const fa_strides* s, bool bf16, int B, int H, int N, int d);
 // Unit counts of a call into `a` (N, H, BH, n_mblk, n_units, n_kv) and its grid.
 void plan_fwd(int d, int N, int H, long long BH, int sm_count, FwdArgs* a, int* grid);
 cudaError_t launch_fwd(int d, bool bf16, bool causal, const CUtensorMap* maps, const FwdArgs& a,
                        int grid, cudaStream_t stream);
 // 8-bit inputs (fa_fwd_fp8.cu): maps = Q, K ({128 bytes, N, H, B}) and V^T
-// ({keys, 128, H, B}), all e4m3 bytes.
+// ({keys, 128, H, B}), all e4m3 bytes, and the bf16 O.
 cudaError_t launch_fwd_fp8(bool causal, const CUtensorMap* maps, const FwdArgs& a, int grid,
                            cudaStream_t stream);
 int fwd_smem_bytes_fp8();

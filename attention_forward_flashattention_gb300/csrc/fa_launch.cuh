@@ -14,7 +14,7 @@ cudaError_t launch_one(const CUtensorMap* m, const FwdArgs& a, int grid, cudaStr
   auto kern = fa_fwd_kernel<D, BF16, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kFwdThreads, kSmem, st>>>(m[0], m[1], m[2], a);
+  kern<<<grid, kFwdThreads, kSmem, st>>>(m[0], m[1], m[2], m[3], a);
   return cudaGetLastError();
 }
 

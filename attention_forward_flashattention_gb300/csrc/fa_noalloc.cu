@@ -93,15 +93,11 @@ extern "C" fa_status fa_fwd_noalloc(const void* q, const void* k, const void* v,
 
   const bool bf16 = dtype == FA_DTYPE_BF16;
   const fa_strides c = fa::contiguous_strides(H, N, d);
-  const fa_strides strides[3] = {c, c, c};
-  CUtensorMap maps[3];  // same tensor maps, unit plan and kernels as fa_fwd
-  if (!fa::encode_fwd_maps(maps, q, k, v, strides, bf16, B, H, N, d)) return FA_ERR_CUDA;
+  const fa_strides strides[4] = {c, c, c, c};
+  CUtensorMap maps[4];  // same tensor maps, unit plan and kernels as fa_fwd
+  if (!fa::encode_fwd_maps(maps, q, k, v, o, strides, bf16, B, H, N, d)) return FA_ERR_CUDA;
 
   fa::FwdArgs a{};
-  a.o = o;
-  a.o_sb = c.b;
-  a.o_sh = c.h;
-  a.o_sn = c.n;
   a.lse = lse;
   a.status = st->scratch;
   a.scale_log2 = scale * 1.4426950408889634f;

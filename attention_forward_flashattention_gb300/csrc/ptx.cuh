@@ -123,6 +123,17 @@ __device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int
       : "memory");
 }
 
+// 4-D tiled store from shared memory (bulk-group completion); the box is
+// clipped at the tensor's bounds, and no coordinate may be negative.
+__device__ __forceinline__ void tma_store_4d(const void* tmap, uint32_t src, int c0, int c1,
+                                             int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
