@@ -1,5 +1,5 @@
 // Fused attention forward for sm_103a: TMA loads, tcgen05.mma with S, P and O
-// in TMEM, online softmax in registers, direct epilogue from TMEM.
+// in TMEM, online softmax in registers, TMA-store epilogue from TMEM.
 //
 // Work unit: 256 query rows of one (batch, head), split into two 128-row
 // Q tiles that share every K / V tile (ping-pong: while the softmax of one
@@ -18,7 +18,9 @@
 //   WG1  softmax of Q tile 0, one thread per row = TMEM lane (the B300
 //        walkthrough, V14 item d);
 //   WG2  softmax of Q tile 1;
-//   WG3  epilogue of both tiles: O / l from TMEM straight to global memory.
+//   WG3  epilogue of both tiles: O / l (the consumer's last step in "TMA +
+//        Warp Specialization", 17.5) from TMEM through a per-warp shared
+//        staging slice to global memory by TMA store.
 // Each warpgroup's four warps cover the four TMEM lane quarters (warp w
 // reaches lanes 32*(w%4)..+31). Registers are rebalanced with setmaxnreg
 // (the register reallocation of "TMA + Warp Specialization", 17.4-17.5):
