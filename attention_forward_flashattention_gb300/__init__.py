@@ -89,6 +89,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.fa_fwd_noalloc.restype = i
         lib.fa_check.argtypes = [vp]
         lib.fa_check.restype = i
+        lib.fa_sm_clock_read.argtypes = [vp, ctypes.POINTER(ctypes.c_double),
+                                         ctypes.POINTER(ctypes.c_ulonglong)]
+        lib.fa_sm_clock_read.restype = i
         ip = ctypes.POINTER(ctypes.c_int)
         lib.fa_query_launch.argtypes = [i, i, i, i, i, ip, ip, ip, ip]
         lib.fa_query_launch.restype = i
@@ -178,6 +181,16 @@ def fa_fwd_noalloc(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: 
 
 def fa_check(stream: int = 0) -> int:
     return load_library().fa_check(stream)
+
+
+def fa_sm_clock_read(stream: int = 0) -> tuple[float, int]:
+    """(SM MHz the kernels ran at since the last read, CTAs recorded); clears
+    the record. Synchronises the stream."""
+    mhz, ctas = ctypes.c_double(0.0), ctypes.c_ulonglong(0)
+    rc = load_library().fa_sm_clock_read(stream, ctypes.byref(mhz), ctypes.byref(ctas))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_sm_clock_read")
+    return float(mhz.value), int(ctas.value)
 
 
 def fa_query_launch(B: int, H: int, N: int, d: int, causal: bool = False) -> dict:

@@ -62,6 +62,7 @@ struct BwdArgs {
   int n_units;            // BH * n_t
   float scale_log2;       // scale * log2(e)
   float scale;
+  unsigned long long* clk;  // optional [3]: SM clock record of the launch (clock_end), or null
 };
 
 constexpr int kBwdThreads = 512;
@@ -96,6 +97,7 @@ struct BwdLayout {
   static constexpr int kSmemBytes = kOffBar + 512 + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kStageBytes % 1024 == 0, "stages keep tiles 1024-byte aligned");
+  static_assert(kOffBar % 8 == 0, "barrier block alignment");
   // TMEM columns: 128-column fp32 scratch tiles and the accumulators. A
   // 16-bit operand written over a scratch tile sits in columns 0-31 (rows'
   // elements 0-63) and 64-95 (elements 64-127).
@@ -127,6 +129,7 @@ enum BwdBar : int {
 };
 constexpr int kBwdSlotTmem = 480;
 constexpr int kBwdSlotAbort = 484;
+constexpr int kBwdSlotClock = 488;  // clock stamp (16 bytes)
 
 // D_i and LSE_i * log2(e) into the tile-padded workspace. Eight lanes per
 // padded row: lane p of a row reads its 16-byte chunks p, p + 8, ..., so a
@@ -800,6 +803,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
   const AbortCtx ab{abort_flag, a.status};
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
+  uint64_t* clock_slot = reinterpret_cast<uint64_t*>(sgen + L::kOffBar + kBwdSlotClock);
+  if (threadIdx.x == 0 && a.clk != nullptr) clock_begin(clock_slot);
   if (threadIdx.x == 0) {
     // two MMA chains (dK/dV at d = 64, dQ always) each commit the
     // shared-resource barriers
@@ -860,6 +865,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   if (warp == 1) ptx::tmem_dealloc(tmem, 512);
+  if (threadIdx.x == 0 && a.clk != nullptr) clock_end(a.clk, clock_slot);
 }
 
 // Host side (fa_bwd_d64.cu / fa_bwd_d128.cu): the three launches of one call.

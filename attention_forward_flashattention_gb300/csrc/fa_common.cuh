@@ -156,6 +156,26 @@ __device__ __forceinline__ bool wait_bounded_warp(uint32_t bar, uint32_t parity,
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
+// SM clock of a launch, measured while it runs: thread 0 of each CTA takes
+// clock64 (SM cycles) and %globaltimer (ns) when the CTA starts and adds the
+// elapsed amounts, and a count of one, to clk[0], clk[1], clk[2] when it ends.
+// The host's cycles / ns is then the clock the CTAs ran at, averaged over CTAs
+// weighted by their run time (a power-capped board runs below its maximum).
+// The start values wait in shared memory (`slot`, 16 bytes, 8-byte aligned),
+// so no register stays live across the kernel's roles.
+__device__ __forceinline__ void clock_begin(uint64_t* slot) {
+  slot[0] = ptx::globaltimer_ns();
+  slot[1] = static_cast<uint64_t>(clock64());
+}
+
+__device__ __forceinline__ void clock_end(unsigned long long* clk, const uint64_t* slot) {
+  const long long c = clock64();
+  const uint64_t g = ptx::globaltimer_ns();
+  atomicAdd(clk + 0, static_cast<unsigned long long>(c - static_cast<long long>(slot[1])));
+  atomicAdd(clk + 1, static_cast<unsigned long long>(g - slot[0]));
+  atomicAdd(clk + 2, 1ull);
+}
+
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   uint32_t u;

@@ -32,8 +32,17 @@ struct DeviceState {
   bool ready = false;
   bool arch_ok = false;
   int sm_count = 0;
-  uint32_t* status = nullptr;  // one word, allocated on first use, kept until exit
+  // 256 bytes allocated on first use and kept until exit: word 0 is the status
+  // word; bytes 64-87 the SM clock record (three uint64) of the launches since
+  // the last fa_sm_clock_read
+  uint32_t* status = nullptr;
 };
+
+constexpr int kClockRecordWord = 16;  // uint32 index of the clock record
+
+unsigned long long* clock_record(const DeviceState& st) {
+  return reinterpret_cast<unsigned long long*>(st.status + kClockRecordWord);
+}
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
@@ -119,19 +128,6 @@ bool encode_bytes4(CUtensorMap* m, const void* ptr, const cuuint64_t (&dims)[4],
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Size checks shared by fa_fwd and fa_query_launch.
-fa_status check_sizes(int B, int H, int N, int d) {
-  if (B <= 0 || H <= 0 || N <= 0) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  const long long BH = static_cast<long long>(B) * H;
-  if (BH > 0x7FFFFFFFLL) return FA_ERR_UNSUPPORTED;
-  // unit count BH * ceil(N / 256) and row index bh * N + i stay in int range
-  const long long units = BH * ((static_cast<long long>(N) + 255) / 256);
-  if (units > 0x7FFFFFFFLL) return FA_ERR_UNSUPPORTED;
-  if (N > (1 << 30)) return FA_ERR_UNSUPPORTED;  // tile row coordinates stay in int range
-  return FA_OK;
-}
-
 __global__ void clock_probe_kernel(uint64_t* out, long long cycles) {
   if (threadIdx.x != 0) return;
   const uint64_t g0 = ptx::globaltimer_ns();
@@ -144,6 +140,18 @@ __global__ void clock_probe_kernel(uint64_t* out, long long cycles) {
 }
 
 }  // namespace
+
+fa_status check_sizes(int B, int H, int N, int d) {
+  if (B <= 0 || H <= 0 || N <= 0) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long BH = static_cast<long long>(B) * H;
+  if (BH > 0x7FFFFFFFLL) return FA_ERR_UNSUPPORTED;
+  // unit count BH * ceil(N / 256) and row index bh * N + i stay in int range
+  const long long units = BH * ((static_cast<long long>(N) + 255) / 256);
+  if (units > 0x7FFFFFFFLL) return FA_ERR_UNSUPPORTED;
+  if (N > (1 << 30)) return FA_ERR_UNSUPPORTED;  // tile row coordinates stay in int range
+  return FA_OK;
+}
 
 int fwd_smem_bytes(int d) {
   return d == 64 ? Layout<64>::kSmemBytes : Layout<128>::kSmemBytes;
@@ -230,6 +238,7 @@ fa_status fwd_call(const void* q, const void* k, const void* v, void* o, float* 
   fa::FwdArgs a{};
   a.lse = lse;
   a.status = st->status;
+  a.clk = fa::clock_record(*st);
   a.scale_log2 = scale * 1.4426950408889634f;
   int grid = 0;
   fa::plan_fwd(d, N, H, BH, st->sm_count, &a, &grid);
@@ -296,6 +305,7 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* vt, void* o, floa
   a.scale_log2 = scale * q_scale * 1.4426950408889634f;
   a.k_scales = k_scales;
   a.v_scale = v_scale;
+  a.clk = fa::clock_record(*st);
   int grid = 0;
   fa::plan_fwd(d, N, H, static_cast<long long>(B) * H, st->sm_count, &a, &grid);
 
@@ -361,6 +371,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   a.status = st->status;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.scale = scale;
+  a.clk = fa::clock_record(*st);
   const int grid = a.n_units < st->sm_count ? a.n_units : st->sm_count;
 
   (void)cudaGetLastError();
@@ -376,13 +387,37 @@ fa_status fa_check(void* stream) {
   const fa_status ds = fa::current_device(&dev, &st, false);
   if (ds != FA_OK) return ds;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
-  if (st->status == nullptr) return FA_OK;  // nothing launched on this device yet
+  // fa_fwd_noalloc keeps its status word in the library's static scratch
+  bool noalloc_timeout = false;
+  const fa_status ns = fa::noalloc_take_status(dev, &noalloc_timeout);
+  if (ns != FA_OK) return ns;
   uint32_t word = 0;
-  if (cudaMemcpy(&word, st->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+  if (st->status != nullptr) {  // (null: nothing launched through fa_fwd & co. yet)
+    if (cudaMemcpy(&word, st->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+      return FA_ERR_CUDA;
+    if (word != 0 && cudaMemset(st->status, 0, sizeof(word)) != cudaSuccess) return FA_ERR_CUDA;
+  }
+  return (word != 0 || noalloc_timeout) ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+fa_status fa_sm_clock_read(void* stream, double* sm_mhz, unsigned long long* ctas) {
+  if (!sm_mhz) return FA_ERR_INVALID_ARG;
+  int dev = 0;
+  fa::DeviceState* st = nullptr;
+  const fa_status ds = fa::current_device(&dev, &st, false);
+  if (ds != FA_OK) return ds;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  *sm_mhz = 0.0;
+  if (ctas) *ctas = 0;
+  if (st->status == nullptr) return FA_OK;  // nothing launched on this device yet
+  unsigned long long rec[3] = {0, 0, 0};
+  unsigned long long* dev_rec = fa::clock_record(*st);
+  if (cudaMemcpy(rec, dev_rec, sizeof(rec), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(dev_rec, 0, sizeof(rec)) != cudaSuccess)
     return FA_ERR_CUDA;
-  if (word == 0) return FA_OK;
-  if (cudaMemset(st->status, 0, sizeof(word)) != cudaSuccess) return FA_ERR_CUDA;
-  return FA_ERR_TIMEOUT;
+  if (rec[1] > 0) *sm_mhz = 1000.0 * static_cast<double>(rec[0]) / static_cast<double>(rec[1]);
+  if (ctas) *ctas = rec[2];
+  return FA_OK;
 }
 
 fa_status fa_query_launch(int B, int H, int N, int d, int causal, int* grid, int* threads,

@@ -66,6 +66,7 @@ struct FwdArgs {
   float scale_log2;  // scale * log2(e) (8-bit inputs: times the Q scale)
   const float* k_scales;  // 8-bit inputs: [BH][n_kv] scale of each 128-key block of K
   float v_scale;          // 8-bit inputs: scale of V
+  unsigned long long* clk;  // optional [3]: SM clock record of the launch (clock_end), or null
 };
 
 constexpr int kFwdThreads = 512;
@@ -99,6 +100,7 @@ struct Layout {
   static constexpr uint32_t kColP = 256 + 2 * D;  // P_i at kColP + i*64 (kSepP)
   static_assert(!kSepP || kColP + 128 <= kTmemCols, "TMEM columns");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kOffBar % 8 == 0, "barrier block alignment");
 };
 
 // Barrier slots (8 bytes each) in the barrier block.
@@ -119,6 +121,7 @@ enum BarSlot : int {
 };
 constexpr int kSlotTmem = 480;   // byte offset of the TMEM base address
 constexpr int kSlotAbort = 484;  // byte offset of the abort flag
+constexpr int kSlotClock = 488;  // byte offset of the clock stamp (16 bytes)
 
 // Walks this CTA's units: round k takes unit k*G + c; for causal problems odd
 // rounds go in reverse CTA order so per-CTA work evens out over the
@@ -690,6 +693,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
   const AbortCtx ab{abort_flag, a.status};
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
+  uint64_t* clock_slot = reinterpret_cast<uint64_t*>(sgen + L::kOffBar + kSlotClock);
+  if (threadIdx.x == 0 && a.clk != nullptr) clock_begin(clock_slot);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -745,6 +750,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   if (warp == 1) ptx::tmem_dealloc(tmem, L::kTmemCols);
+  if (threadIdx.x == 0 && a.clk != nullptr) clock_end(a.clk, clock_slot);
 }
 
 // Host side (defined in the per-head-dimension files and fa_host.cu).
@@ -766,6 +772,13 @@ int fwd_smem_bytes(int d);
 // call's strides (fa_host.cu).
 fa_strides contiguous_strides(int H, int N, int d);
 fa_status check_strides(const fa_strides* s /* q, k, v, o */, int d);
+// Size checks of every entry point (B, H, N >= 1; d in {64, 128}; unit and
+// row counts in int range).
+fa_status check_sizes(int B, int H, int N, int d);
+// fa_fwd_noalloc's status word on device `dev` (fa_noalloc.cu): reads it and
+// clears it; *timed_out is set when a launch recorded a timeout. FA_OK when
+// that entry point has not been used on the device.
+fa_status noalloc_take_status(int dev, bool* timed_out);
 // Q, K, V, O tensor maps of a call (s: q, k, v, o strides).
 bool encode_fwd_maps(CUtensorMap* maps, const void* q, const void* k, const void* v,
                      const void* o, const fa_strides* s, bool bf16, int B, int H, int N, int d);

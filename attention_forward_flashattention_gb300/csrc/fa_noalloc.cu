@@ -71,6 +71,32 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
+namespace fa {
+
+// Called by fa_check after it synchronised its stream: reads word 0 of the
+// scratch (the status word of the allocation-free launches) and clears it.
+// With calls in flight on other streams the word may belong to any of them.
+fa_status noalloc_take_status(int dev, bool* timed_out) {
+  *timed_out = false;
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  uint32_t* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    scratch = g_dev[dev].ready ? g_dev[dev].scratch : nullptr;
+  }
+  if (scratch == nullptr) return FA_OK;  // the entry point was not used on this device
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, scratch, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (word != 0) {
+    if (cudaMemset(scratch, 0, sizeof(word)) != cudaSuccess) return FA_ERR_CUDA;
+    *timed_out = true;
+  }
+  return FA_OK;
+}
+
+}  // namespace fa
+
 extern "C" fa_status fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o,
                                     float* lse, int B, int H, int N, int d, int causal,
                                     float scale, fa_dtype dtype, void* stream) {
@@ -79,13 +105,11 @@ extern "C" fa_status fa_fwd_noalloc(const void* q, const void* k, const void* v,
     return FA_ERR_INVALID_ARG;
   if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
   if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
-  if (B <= 0 || H <= 0 || N <= 0) return FA_ERR_INVALID_ARG;
   // Sizes: the scratch need is one status word whatever the problem, so the
-  // limits are the kernel's own (the same as fa_fwd's).
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  // limits are the kernel's own, checked by the same function as fa_fwd's.
+  const fa_status sz = fa::check_sizes(B, H, N, d);
+  if (sz != FA_OK) return sz;
   const long long BH = static_cast<long long>(B) * H;
-  const long long units = BH * ((static_cast<long long>(N) + 255) / 256);
-  if (BH > 0x7FFFFFFFLL || units > 0x7FFFFFFFLL || N > (1 << 30)) return FA_ERR_UNSUPPORTED;
 
   NoAllocDevice* st = nullptr;
   const fa_status ds = device_setup(&st);

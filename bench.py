@@ -11,8 +11,16 @@ also reported as a percentage of 2.25 PFLOP/s dense fp16. With
 and LSE) and the metric is 10 B H N^2 d / time (the five N x N x d products
 of the backward; halved for causal).
 
-Prints ONE JSON line (rank 0). Reference arm (--impl reference): the fp64 CPU
-oracle timed on this host's cores on a bounded sample of the same workload.
+Prints ONE JSON line (rank 0). Besides the headline workload it times every
+other named workload (the other 16-bit configurations and the two 8-bit
+shapes) in the same process, with the same steps, warm-up and L2 flush, under
+"other_workloads". The SM clock of each timed region is read from the kernels
+themselves (clock64 / %globaltimer per CTA, fa_sm_clock_read), and the
+clock-corrected tensor fraction FLOPs / (t x SMs x 8192 x f_clock) is reported
+beside the fraction of the measured peak.
+
+Reference arm (--impl reference): the fp64 CPU oracle timed on this host's
+cores on a bounded sample of the same workload.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
                     [--pass forward|backward]
@@ -41,6 +49,9 @@ DEFAULT_WORKLOAD = "mha_b4_h16_n4096_d128_fp16"
 METRIC = "attention fwd TFLOPS (4BHN²d, causal halved) and % of 2.25 PF dense fp16"
 METRIC_BWD = "attention bwd TFLOPS (10BHN²d, causal halved) and % of 2.25 PF dense fp16"
 NOMINAL_DENSE_FP16_TFLOPS = 2250.0
+# dense tensor-core FLOPs per SM per clock: a 128 x 128 x 16 16-bit tcgen05.mma
+# (2 * 128 * 128 * 16 FLOPs) takes 64 cycles; 8-bit products run at twice that
+TENSOR_FLOP_PER_CLK_SM = {"fp16": 8192.0, "bf16": 8192.0, "e4m3": 16384.0}
 FALLBACK_PEAK_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
 SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -63,6 +74,8 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--soak-s", type=float, default=1.5,
                    help="untimed loaded seconds before the timed steps (clock samples)")
+    p.add_argument("--other-workloads", default="all", choices=["all", "none"],
+                   help="also time every other named workload (same steps, warm-up, flush)")
     return p.parse_args()
 
 
@@ -218,6 +231,11 @@ def workload_inputs(w):
     return I.fp8_inputs(w) if w.dtype == "e4m3" else I.qkv_bits(w)
 
 
+def _gen_inputs(name: str):
+    """Host inputs of a named workload (runs in a spawned worker process)."""
+    return workload_inputs(get_workload(name))
+
+
 def oracle_rows(w, x, rows):
     import oracle
     if w.dtype == "e4m3":
@@ -313,9 +331,9 @@ class Plan:
         self.__dict__.update(kw)
 
 
-def forward_plan(fa, torch, w, dev, stream) -> Plan:
+def forward_plan(fa, torch, w, dev, stream, x=None) -> Plan:
     fp8 = w.dtype == "e4m3"
-    x = workload_inputs(w)
+    x = workload_inputs(w) if x is None else x
     if fp8:
         # e4m3 codes (Q, K, V^T) and the per-block K scales; bf16 output
         tdt = torch.bfloat16
@@ -380,11 +398,11 @@ def cpu_forward_sample(w, x) -> dict:
                       f"TFLOPS = rows x (metric FLOPs per row) / wall time"}
 
 
-def backward_plan(fa, torch, w, dev, stream) -> Plan:
+def backward_plan(fa, torch, w, dev, stream, x=None) -> Plan:
     if w.dtype not in ("fp16", "bf16"):
         raise SystemExit("--pass backward takes a 16-bit workload")
     tdt = torch.float16 if w.dtype == "fp16" else torch.bfloat16
-    x = I.qkv_bits(w)
+    x = I.qkv_bits(w) if x is None else x
     dob = I.dout_bits(w)
     q, k, v, do = (torch.from_numpy(t.view(np.int16)).view(tdt).to(dev) for t in x + (dob,))
     # the forward's outputs feed the backward, as in training (computed once)
@@ -439,9 +457,80 @@ def cpu_backward_sample(w, x, dob) -> dict:
                       f"TFLOPS = heads x (metric FLOPs per head) / wall time"}
 
 
-def run_ours(args, rank: int, world: int, local_rank: int):
-    import torch
+def time_steps(fa, torch, plan, stream, dev, flush, steps: int, warmup: int, world: int,
+               soak_s: float = 0.0, sampler_device=None) -> dict:
+    """Warm-up, optional untimed soak (with nvidia-smi sampling), then `steps`
+    timed steps between CUDA events on `stream`, L2 flushed before each.
+    Returns the per-step times, the max-over-ranks total and the SM clock the
+    kernels recorded during the timed steps."""
     import torch.distributed as dist
+    sh = int(stream.cuda_stream)
+    for _ in range(max(warmup, 3)):
+        plan.step()
+    rc = fa.fa_check(sh)
+    if rc != fa.FA_OK:
+        raise RuntimeError("warm-up failed: " + fa.status_string(rc))
+    sampler = ClockSampler(sampler_device) if sampler_device is not None else None
+    t_end = time.perf_counter() + soak_s
+    while time.perf_counter() < t_end:   # untimed load so clock samples exist
+        for _ in range(20):
+            plan.step()
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    fa.fa_sm_clock_read(sh)              # clear: record only the timed launches
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()                    # evict L2 between steps (outside the events)
+        starts[i].record(stream)
+        plan.step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler is not None else None
+    clk_mhz, ctas = fa.fa_sm_clock_read(sh)
+    rc = fa.fa_check(sh)
+    if rc != fa.FA_OK:
+        raise RuntimeError("timed steps failed: " + fa.status_string(rc))
+    times_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    return {"times_ms": times_ms, "total_ms": max_over_ranks(sum(times_ms), world, dev),
+            "clk64_mhz": clk_mhz if ctas > 0 else None, "ctas": ctas, "clocks": clocks}
+
+
+def clock_corrected_frac(tflops: float, dtype: str, sms: int, mhz) -> float | None:
+    """Achieved FLOP/s over the tensor cores' dense rate at the clock the
+    kernels ran at: FLOPs / (t x SMs x FLOP/clk/SM x f_clock)."""
+    if not mhz:
+        return None
+    return tflops * 1e12 / (sms * TENSOR_FLOP_PER_CLK_SM[dtype] * mhz * 1e6)
+
+
+def other_workload_names(headline: str, pass_: str) -> list[str]:
+    names = [n for n in I.WORKLOAD_ORDER if n != headline]
+    if pass_ == "forward":
+        names += [n for n in I.FP8_WORKLOADS if n != headline]
+    return names
+
+
+def run_ours(args, rank: int, world: int, local_rank: int):
+    import concurrent.futures as cf
+    import multiprocessing as mp
+
+    # host inputs of the other workloads are generated by spawned workers
+    # while the headline runs (spawned before any CUDA call)
+    others = [] if args.other_workloads == "none" else other_workload_names(args.workload,
+                                                                            args.pass_)
+    pool = None
+    futures = {}
+    if others:
+        pool = cf.ProcessPoolExecutor(max_workers=min(len(others), max(1, os.cpu_count() or 1)),
+                                      mp_context=mp.get_context("spawn"))
+        futures = {n: pool.submit(_gen_inputs, n) for n in others}
+
+    import torch
 
     import attention_forward_flashattention_gb300 as fa
     from attention_forward_flashattention_gb300 import build as fabuild
@@ -450,56 +539,19 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     dev = torch.device("cuda", local_rank)
     fabuild.build()
     fa.load_library()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     w = get_workload(args.workload)
     stream = torch.cuda.current_stream(dev)
-    sh = int(stream.cuda_stream)
     make = backward_plan if args.pass_ == "backward" else forward_plan
     plan = make(fa, torch, w, dev, stream)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
 
-    for _ in range(max(args.warmup, 3)):
-        plan.step()
-    rc = fa.fa_check(sh)
-    if rc != fa.FA_OK:
-        raise RuntimeError("warm-up failed: " + fa.status_string(rc))
-
-    sampler = ClockSampler(local_rank)
-    t_end = time.perf_counter() + args.soak_s
-    while time.perf_counter() < t_end:   # untimed load so clock samples exist
-        for _ in range(20):
-            plan.step()
-        torch.cuda.synchronize(dev)
-
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    for i in range(args.steps):
-        flush.zero_()                    # evict L2 between steps (outside the events)
-        starts[i].record(stream)
-        plan.step()
-        ends[i].record(stream)
-    torch.cuda.synchronize(dev)
-    if world > 1:
-        dist.barrier()
-    clocks = sampler.stop()
-    rc = fa.fa_check(sh)
-    if rc != fa.FA_OK:
-        raise RuntimeError("timed steps failed: " + fa.status_string(rc))
-    times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = max_over_ranks(sum(times_ms), world, dev)
+    t = time_steps(fa, torch, plan, stream, dev, flush, args.steps, args.warmup, world,
+                   soak_s=args.soak_s, sampler_device=local_rank)
+    times_ms, total_ms = t["times_ms"], t["total_ms"]
     ms_per_step = total_ms / args.steps
     value = job_throughput(plan.flops, total_ms, args.steps, world)
     per_gpu_tflops = value / world
-
-    # SM clock from clock64 (one CTA spinning 2e8 cycles right after the load)
-    probe = torch.zeros(2, dtype=torch.int64, device=dev)
-    clk64_mhz = None
-    if fa.fa_sm_clock_probe(probe.data_ptr(), 200_000_000, sh) == fa.FA_OK:
-        torch.cuda.synchronize(dev)
-        c, ns = probe.tolist()
-        clk64_mhz = 1e3 * c / ns if ns > 0 else None
 
     # end to end through the public API: pinned host in, pinned host out
     e2e = None
@@ -518,14 +570,40 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": plan.h2d,
                "d2h_bytes_per_step": plan.d2h, "path": plan.e2e_path}
 
-    if rank != 0:
-        return
     peaks = measured_peaks()
     if "bf16_tflops" in peaks:
-        peak, peak_src = float(peaks["bf16_tflops"]), "measured bf16 burst (fp16 same nominal rate)"
+        peak16, peak_src = float(peaks["bf16_tflops"]), "measured bf16 burst (fp16 same nominal rate)"
     else:
-        peak, peak_src = FALLBACK_PEAK_TFLOPS, "fallback"
-    peak, peak_src = plan.peak_mult * peak, peak_src + plan.peak_note
+        peak16, peak_src = FALLBACK_PEAK_TFLOPS, "fallback"
+
+    # every other workload: same steps, warm-up and flush, one after another
+    other = {}
+    for name in others:
+        ow = get_workload(name)
+        oplan = make(fa, torch, ow, dev, stream, x=futures[name].result())
+        ot = time_steps(fa, torch, oplan, stream, dev, flush, args.steps, args.warmup, world)
+        oms = ot["total_ms"] / args.steps
+        otf = job_throughput(oplan.flops, ot["total_ms"], args.steps, world) / world
+        opeak = oplan.peak_mult * peak16
+        other[name] = {
+            "value": otf * world, "unit": "TFLOPS", "ms_per_step": oms,
+            "step_ms_median": statistics.median(ot["times_ms"]),
+            "pct_of_2250_tflops": 100.0 * otf / NOMINAL_DENSE_FP16_TFLOPS,
+            "frac": otf / opeak, "peak": opeak,
+            "clk64_mhz": ot["clk64_mhz"],
+            "clock_corrected_frac": clock_corrected_frac(otf, ow.dtype, sms, ot["clk64_mhz"]),
+            "config": {k: v for k, v in workload_config(ow).items()
+                       if k not in ("global_batch", "seq_len")},
+        }
+        del oplan
+        torch.cuda.empty_cache()
+    if pool is not None:
+        pool.shutdown()
+
+    if rank != 0:
+        return
+    peak = plan.peak_mult * peak16
+    peak_src = peak_src + plan.peak_note
     cpu = None if args.no_cpu_baseline else plan.cpu()
     line = {
         "metric": plan.metric, "value": value, "unit": "TFLOPS", "n_gpus": world,
@@ -540,12 +618,20 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "roofline": {"bound": "tensor", "achieved": per_gpu_tflops, "peak": peak,
                      "unit": "TFLOP/s", "frac": per_gpu_tflops / peak,
                      "traffic": plan.traffic, "peak_source": peak_src,
-                     "kernel": plan.kernel},
-        "clocks": {**clocks, "clk64_mhz": clk64_mhz, "window": "soak + timed steps"},
+                     "kernel": plan.kernel,
+                     "clock_corrected_frac": clock_corrected_frac(per_gpu_tflops, w.dtype, sms,
+                                                                  t["clk64_mhz"]),
+                     "clock_corrected_basis": f"{sms} SMs x "
+                                              f"{TENSOR_FLOP_PER_CLK_SM[w.dtype]:.0f} FLOP/clk "
+                                              f"x clk64_mhz"},
+        "clocks": {**t["clocks"], "clk64_mhz": t["clk64_mhz"], "clk64_ctas": t["ctas"],
+                   "window": "nvidia-smi: soak + timed steps; clk64: the timed kernels' CTAs "
+                             "(clock64 / %globaltimer)"},
         "gpu_launches": args.steps * plan.launches,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "step_ms_min": min(times_ms), "step_ms_median": statistics.median(times_ms),
+        "other_workloads": other,
     }
     print(json.dumps(line), flush=True)
 

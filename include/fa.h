@@ -198,7 +198,10 @@ fa_status fa_bwd_workspace_size(int B, int H, int N, int d, size_t* bytes);
  * before its launch (an asynchronous memset, not an allocation). All calls
  * share the one array, so calls that overlap on the GPU (different streams
  * without ordering between them) race on it. A launch whose bounded waits
- * gave up leaves O / LSE incomplete; its status is not reported by fa_check.
+ * gave up leaves O / LSE incomplete and sets that status word, which fa_check
+ * reads and clears like fa_fwd's: since each call clears it first, fa_check
+ * reports the most recent allocation-free launch on the device (with
+ * overlapping calls, any one of them).
  */
 fa_status fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
                          int B, int H, int N, int d, int causal, float scale,
@@ -246,10 +249,28 @@ fa_status fa_fwd_host_workspace_size(int B, int H, int N, int d, size_t* bytes);
 
 /*
  * fa_check - synchronise `stream`, then read and clear the current device's
- * status word. Returns FA_OK, FA_ERR_TIMEOUT if a launch since the last check
- * stopped on a wait limit, or FA_ERR_CUDA if the stream reports an error.
+ * status words (fa_fwd's, shared by every entry point but fa_fwd_noalloc, and
+ * fa_fwd_noalloc's). Returns FA_OK, FA_ERR_TIMEOUT if a launch since the last
+ * check stopped on a wait limit (for fa_fwd_noalloc: its most recent launch),
+ * or FA_ERR_CUDA if the stream reports an error.
  */
 fa_status fa_check(void* stream);
+
+/*
+ * fa_sm_clock_read - the SM clock the forward and backward kernels actually
+ * ran at. Every CTA of a launch through fa_fwd, fa_fwd_strided, fa_fwd_fp8,
+ * fa_fwd_host or fa_bwd adds its elapsed clock64 cycles and %globaltimer
+ * nanoseconds to a record on the device; this call synchronises `stream`,
+ * returns *sm_mhz = 1000 * cycles / ns over the launches since the previous
+ * read (the CTAs' clock, weighted by their run time; 0 if none ran) and
+ * *ctas = the number of CTAs recorded (ctas may be NULL), and clears the
+ * record. Launches still running on other streams may be partly counted.
+ * The pages measure a power-capped board whose SM clock falls below its
+ * maximum ("TCA 51%, MFU below 8%", measurement section, clock64 readings):
+ * a utilisation figure corrected for the clock divides by this, not by the
+ * maximum clock. fa_fwd_noalloc launches are not recorded.
+ */
+fa_status fa_sm_clock_read(void* stream, double* sm_mhz, unsigned long long* ctas);
 
 /*
  * fa_query_launch - launch shape fa_fwd would use on the current device for

@@ -64,6 +64,11 @@ def _load():
                                              ctypes.c_int, ctypes.c_float, ctypes.POINTER(i64), i64,
                                              f64p, f64p, ctypes.c_int]
             lib.oracle_attn_rows.restype = ctypes.c_int
+            lib.oracle_attn_rows_dev.argtypes = [u16p, u16p, u16p, ctypes.c_int, i64, i64, i64,
+                                                 i64, ctypes.c_int, ctypes.c_float,
+                                                 ctypes.POINTER(i64), i64, f64p, f64p, f64p,
+                                                 ctypes.c_int]
+            lib.oracle_attn_rows_dev.restype = ctypes.c_int
             u8p = ctypes.POINTER(ctypes.c_uint8)
             f32p = ctypes.POINTER(ctypes.c_float)
             lib.oracle_attn_fp8.argtypes = [u8p, u8p, u8p, i64, i64, i64, i64, i64, ctypes.c_float,
@@ -145,6 +150,35 @@ def attn_rows(q: np.ndarray, k: np.ndarray, v: np.ndarray, dtype: str, causal: b
     if rc != 0:
         raise ValueError("oracle_attn_rows rejected its arguments")
     return o, lse
+
+
+def attn_rows_dev(q: np.ndarray, k: np.ndarray, v: np.ndarray, dtype: str, causal: bool,
+                  scale: float, rows: np.ndarray, nthreads: int = 0):
+    """Selected rows of the forward (as attn_rows) and, per element, the
+    weighted mean absolute deviation of V under the row's softmax weights,
+    dev_t = sum_j p_j |v_jt - O_t| / sum_j p_j: rounding every weight with
+    relative error at most u moves O_t by at most u / (1 - u) * dev_t.
+
+    Returns (O float64 [R, d], LSE float64 [R], dev float64 [R, d]).
+    """
+    assert q.shape == k.shape == v.shape and q.ndim == 4
+    B, H, N, d = q.shape
+    q, qp = _u16(q)
+    k, kp = _u16(k)
+    v, vp = _u16(v)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    o = np.empty((rows.size, d), dtype=np.float64)
+    lse = np.empty((rows.size,), dtype=np.float64)
+    dev = np.empty((rows.size, d), dtype=np.float64)
+    f64 = ctypes.POINTER(ctypes.c_double)
+    rc = _load().oracle_attn_rows_dev(qp, kp, vp, DTYPE_CODES[dtype], B, H, N, d,
+                                      int(bool(causal)), float(np.float32(scale)),
+                                      rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                      rows.size, o.ctypes.data_as(f64), lse.ctypes.data_as(f64),
+                                      dev.ctypes.data_as(f64), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_attn_rows_dev rejected its arguments")
+    return o, lse, dev
 
 
 def _u8(a: np.ndarray):

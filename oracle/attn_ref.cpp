@@ -247,6 +247,53 @@ int oracle_attn_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
   return 0;
 }
 
+// Selected rows, as oracle_attn_rows, plus dev[r][d]: the weighted mean
+// absolute deviation of V under the row's softmax weights,
+//   dev_t = sum_j p_j |v_jt - O_t| / sum_j p_j.
+// It bounds what rounding the weights costs: a kernel that rounds each weight
+// p_j to r_j with |r_j - p_j| <= u p_j before the P V product and normalises
+// by sum_j r_j gets O'_t - O_t = sum_j (r_j - p_j)(v_jt - O_t) / sum_j r_j,
+// so |O'_t - O_t| <= u / (1 - u) * dev_t (before its own output rounding).
+// The weights come from the same definition as attend_row.
+int oracle_attn_rows_dev(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                         int dtype, int64_t B, int64_t H, int64_t N, int64_t d,
+                         int causal, float scale, const int64_t* rows,
+                         int64_t nrows, double* o, double* lse, double* dev, int nthreads) {
+  if (!dev) return -1;
+  const int rc = oracle_attn_rows(q, k, v, dtype, B, H, N, d, causal, scale, rows, nrows, o,
+                                  lse, nthreads);
+  if (rc != 0) return rc;
+  const double sc = static_cast<double>(scale);
+  const int T = static_cast<int>(
+      std::max<int64_t>(1, std::min<int64_t>(pick_threads(nthreads), nrows)));
+  run_parallel(T, [&](int w, int nt) {
+    const int64_t lo = nrows * w / nt, hi = nrows * (w + 1) / nt;
+    std::vector<double> K(N * d), V(N * d), qi(d), s(N), oi(d);
+    int64_t cur = -1;
+    for (int64_t r = lo; r < hi; ++r) {
+      const int64_t bh = rows[r] / N, i = rows[r] % N;
+      const int64_t base = bh * N * d;
+      if (bh != cur) {
+        decode_block(k + base, N * d, dtype, K.data());
+        decode_block(v + base, N * d, dtype, V.data());
+        cur = bh;
+      }
+      decode_block(q + base + i * d, d, dtype, qi.data());
+      const int64_t nkeys = causal ? i + 1 : N;
+      double li = 0.0;
+      attend_row(qi.data(), K.data(), V.data(), d, nkeys, sc, s, oi.data(), &li);  // s = p_j
+      double l = 0.0;
+      for (int64_t j = 0; j < nkeys; ++j) l += s[j];
+      double* out = dev + r * d;
+      for (int64_t t = 0; t < d; ++t) out[t] = 0.0;
+      for (int64_t j = 0; j < nkeys; ++j)
+        for (int64_t t = 0; t < d; ++t) out[t] += s[j] * std::fabs(V[j * d + t] - oi[t]);
+      for (int64_t t = 0; t < d; ++t) out[t] /= l;
+    }
+  });
+  return 0;
+}
+
 // 8-bit forward. q8, k8: [B][H][N][d] e4m3 codes; vt8: [B][H][d][ldv] e4m3
 // codes of V transposed (column n of row t is V[n][t]); the values are
 //   q = q_scale * q8,  k_n = k_scales[b][h][n / 128] * k8_n,  v = v_scale * v8.
@@ -325,59 +372,85 @@ void oracle_decode_e4m3(const uint8_t* x, int64_t n, double* out) {
 // of the unit roundoff times these sums, even where dP_ij - D_i cancels.
 void bwd_head(const double* Q, const double* K, const double* V, const double* dO,
               int64_t N, int64_t d, bool causal, double scale, double* dq, double* dk,
-              double* dv, double* mq, double* mk, double* mv) {
-  std::vector<double> s(N), P(N * N, 0.0), dS(N * N, 0.0), DS(N * N, 0.0), o(d), ao(d);
-  for (int64_t i = 0; i < N; ++i) {
-    const int64_t nk = causal ? i + 1 : N;
-    double m = -INFINITY;
-    for (int64_t j = 0; j < nk; ++j) {
-      double dot = 0.0;
-      for (int64_t t = 0; t < d; ++t) dot += Q[i * d + t] * K[j * d + t];
-      s[j] = scale * dot;
-      m = std::max(m, s[j]);
-    }
-    double l = 0.0;
-    for (int64_t j = 0; j < nk; ++j) l += std::exp(s[j] - m);
-    const double lse = m + std::log(l);
-    for (int64_t t = 0; t < d; ++t) o[t] = ao[t] = 0.0;
-    for (int64_t j = 0; j < nk; ++j) {
-      P[i * N + j] = std::exp(s[j] - lse);
+              double* dv, double* mq, double* mk, double* mv, int nthreads) {
+  std::vector<double> P(N * N, 0.0), dS(N * N, 0.0), DS(N * N, 0.0);
+  // Rows i of P, dS and their magnitudes (rows are independent: split over
+  // threads in interleaved order, which balances the causal triangle).
+  run_parallel(nthreads, [&](int w, int nt) {
+    std::vector<double> s(N), o(d), ao(d);
+    for (int64_t i = w; i < N; i += nt) {
+      const int64_t nk = causal ? i + 1 : N;
+      double m = -INFINITY;
+      for (int64_t j = 0; j < nk; ++j) {
+        double dot = 0.0;
+        for (int64_t t = 0; t < d; ++t) dot += Q[i * d + t] * K[j * d + t];
+        s[j] = scale * dot;
+        m = std::max(m, s[j]);
+      }
+      double l = 0.0;
+      for (int64_t j = 0; j < nk; ++j) l += std::exp(s[j] - m);
+      const double lse = m + std::log(l);
+      for (int64_t t = 0; t < d; ++t) o[t] = ao[t] = 0.0;
+      for (int64_t j = 0; j < nk; ++j) {
+        P[i * N + j] = std::exp(s[j] - lse);
+        for (int64_t t = 0; t < d; ++t) {
+          o[t] += P[i * N + j] * V[j * d + t];
+          ao[t] += P[i * N + j] * std::fabs(V[j * d + t]);
+        }
+      }
+      // D_i = dO_i . O_i; its term magnitude sums |dO_it| over the terms of O_it
+      double Di = 0.0, aDi = 0.0;
       for (int64_t t = 0; t < d; ++t) {
-        o[t] += P[i * N + j] * V[j * d + t];
-        ao[t] += P[i * N + j] * std::fabs(V[j * d + t]);
+        Di += dO[i * d + t] * o[t];
+        aDi += std::fabs(dO[i * d + t]) * ao[t];
+      }
+      for (int64_t j = 0; j < nk; ++j) {
+        double dp = 0.0, adp = 0.0;
+        for (int64_t t = 0; t < d; ++t) {
+          dp += dO[i * d + t] * V[j * d + t];
+          adp += std::fabs(dO[i * d + t] * V[j * d + t]);
+        }
+        dS[i * N + j] = P[i * N + j] * (dp - Di);
+        DS[i * N + j] = P[i * N + j] * (adp + aDi);
       }
     }
-    // D_i = dO_i . O_i; its term magnitude sums |dO_it| over the terms of O_it
-    double Di = 0.0, aDi = 0.0;
-    for (int64_t t = 0; t < d; ++t) {
-      Di += dO[i * d + t] * o[t];
-      aDi += std::fabs(dO[i * d + t]) * ao[t];
-    }
-    for (int64_t j = 0; j < nk; ++j) {
-      double dp = 0.0, adp = 0.0;
-      for (int64_t t = 0; t < d; ++t) {
-        dp += dO[i * d + t] * V[j * d + t];
-        adp += std::fabs(dO[i * d + t] * V[j * d + t]);
-      }
-      dS[i * N + j] = P[i * N + j] * (dp - Di);
-      DS[i * N + j] = P[i * N + j] * (adp + aDi);
-    }
-  }
-  for (int64_t x = 0; x < N * d; ++x) dq[x] = dk[x] = dv[x] = mq[x] = mk[x] = mv[x] = 0.0;
-  for (int64_t i = 0; i < N; ++i) {
-    const int64_t nk = causal ? i + 1 : N;
-    for (int64_t j = 0; j < nk; ++j) {
-      const double p = P[i * N + j], ds = dS[i * N + j], ads = DS[i * N + j];
-      for (int64_t t = 0; t < d; ++t) {
-        dv[j * d + t] += p * dO[i * d + t];
-        mv[j * d + t] += std::fabs(p * dO[i * d + t]);
-        dq[i * d + t] += scale * ds * K[j * d + t];
-        mq[i * d + t] += scale * ads * std::fabs(K[j * d + t]);
-        dk[j * d + t] += scale * ds * Q[i * d + t];
-        mk[j * d + t] += scale * ads * std::fabs(Q[i * d + t]);
+  });
+  // dQ_i = scale sum_j dS_ij k_j: one row per task.
+  run_parallel(nthreads, [&](int w, int nt) {
+    for (int64_t i = w; i < N; i += nt) {
+      const int64_t nk = causal ? i + 1 : N;
+      for (int64_t t = 0; t < d; ++t) dq[i * d + t] = mq[i * d + t] = 0.0;
+      for (int64_t j = 0; j < nk; ++j) {
+        const double ds = dS[i * N + j], ads = DS[i * N + j];
+        for (int64_t t = 0; t < d; ++t) {
+          dq[i * d + t] += scale * ds * K[j * d + t];
+          mq[i * d + t] += scale * ads * std::fabs(K[j * d + t]);
+        }
       }
     }
-  }
+  });
+  // dV_j = sum_i P_ij dO_i and dK_j = scale sum_i dS_ij q_i: blocks of 64 keys
+  // per task, each summing over the rows i that see its keys in increasing i.
+  constexpr int64_t kKeyBlock = 64;
+  const int64_t nblk = (N + kKeyBlock - 1) / kKeyBlock;
+  run_parallel(nthreads, [&](int w, int nt) {
+    for (int64_t b = w; b < nblk; b += nt) {
+      const int64_t j0 = b * kKeyBlock, j1 = std::min(N, j0 + kKeyBlock);
+      for (int64_t x = j0 * d; x < j1 * d; ++x) dk[x] = dv[x] = mk[x] = mv[x] = 0.0;
+      for (int64_t i = causal ? j0 : 0; i < N; ++i) {
+        const int64_t jend = causal ? std::min(j1, i + 1) : j1;
+        for (int64_t j = j0; j < jend; ++j) {
+          const double p = P[i * N + j], ds = dS[i * N + j], ads = DS[i * N + j];
+          for (int64_t t = 0; t < d; ++t) {
+            dv[j * d + t] += p * dO[i * d + t];
+            mv[j * d + t] += std::fabs(p * dO[i * d + t]);
+            dk[j * d + t] += scale * ds * Q[i * d + t];
+            mk[j * d + t] += scale * ads * std::fabs(Q[i * d + t]);
+          }
+        }
+      }
+    }
+  });
 }
 
 // Backward for the heads listed in `heads` (flat bh indices): q, k, v, dout
@@ -394,9 +467,12 @@ int oracle_attn_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, con
   for (int64_t r = 0; r < nheads; ++r)
     if (heads[r] < 0 || heads[r] >= B * H) return -1;
   const double sc = static_cast<double>(scale);
-  const int T = static_cast<int>(
-      std::max<int64_t>(1, std::min<int64_t>(pick_threads(nthreads), nheads)));
-  run_parallel(T, [&](int w, int nt) {
+  // One thread per head when there are enough heads; otherwise the heads one
+  // after another, each split over all the threads.
+  const int T = pick_threads(nthreads);
+  const int outer = nheads >= T ? T : 1;
+  const int inner = nheads >= T ? 1 : T;
+  run_parallel(outer, [&](int w, int nt) {
     std::vector<double> Q(N * d), K(N * d), V(N * d), dO(N * d);
     for (int64_t r = w; r < nheads; r += nt) {
       const int64_t base = heads[r] * N * d;
@@ -406,7 +482,7 @@ int oracle_attn_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, con
       decode_block(dout + base, N * d, dtype, dO.data());
       const int64_t off = r * N * d;
       bwd_head(Q.data(), K.data(), V.data(), dO.data(), N, d, causal != 0, sc, dq + off,
-               dk + off, dv + off, mq + off, mk + off, mv + off);
+               dk + off, dv + off, mq + off, mk + off, mv + off, inner);
     }
   });
   return 0;

@@ -1,15 +1,30 @@
 """Helpers shared by the GPU parity tests: run the CUDA path through the C ABI,
 decode its outputs, and compare them with the fp64 oracle.
 
-Tolerances (the stated bounds of the library's specification):
-  * O: mean |O_gpu - O_ref| <= 1e-3, and every element
-    |O_gpu - O_ref| <= 1e-2 + half_ulp_X(O_ref). The second term is the
-    rounding of the exact result to the 16-bit output format X, which no
-    X-output kernel can avoid (for bf16 it reaches 0.0156 at |O| >= 4).
-    The plain max |O_gpu - O_ref| is reported alongside.
+Tolerances (the stated bounds of the library's specification, for N(0, 1)
+inputs), asserted as stated:
+  * O: every element |O_gpu - O_ref| <= 1e-2 and mean |O_gpu - O_ref| <= 1e-3;
   * LSE: max |LSE_gpu - LSE_ref| <= 1e-3.
+One case is set apart rather than passed: an element whose exact value lies
+more than 1e-2 from every value of the 16-bit output format X (the rounding
+floor |round_X(O_ref) - O_ref| > 1e-2, possible for bf16 at |O| >= 4, where
+the spacing is 2^-5) cannot meet the bound in any X-output kernel. Such
+elements are counted as "unattainable" in the result and must lie within
+1e-2 + half an X spacing of O_ref; every other element must meet 1e-2.
+
+Inputs that are not N(0, 1) (Q scaled x 3 to sharpen the softmax) fall
+outside the stated bound. There an element above 1e-2 must lie within the
+bound derived from the two roundings the method prescribes (explain_over):
+half an X spacing of O_ref (the output) plus u / (1 - u) times the weighted
+mean absolute deviation of V under the row's softmax weights (every weight
+rounded to X, unit roundoff u, before the P V product), plus 2e-5 of fp32
+arithmetic. The count of such elements is reported.
+The rounding floor's maximum over all elements is reported alongside.
 """
 from __future__ import annotations
+
+import json
+import os
 
 import numpy as np
 
@@ -36,23 +51,91 @@ def half_ulp(x: np.ndarray, dtype: str) -> np.ndarray:
     return np.ldexp(1.0, (e - (p - 1) - 1).astype(np.int64))
 
 
+def round_to(x: np.ndarray, dtype: str) -> np.ndarray:
+    """x rounded to the nearest value of format `dtype` (ties to even), as float64."""
+    x = np.asarray(x, dtype=np.float64)
+    if dtype == "fp16":
+        return x.astype(np.float16).astype(np.float64)
+    # bf16: float64 -> float32 is exact only to 24 bits, so round the float64
+    # value directly to 8 significant bits (ties to even on the scaled value)
+    m, e = np.frexp(x)                    # x = m 2^e, |m| in [0.5, 1)
+    return np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)
+
+
 def compare(o_bits: np.ndarray, lse: np.ndarray, o_ref: np.ndarray, lse_ref: np.ndarray,
             dtype: str) -> dict:
     o = bits_to_f64(o_bits, dtype)
+    o_ref = np.asarray(o_ref, dtype=np.float64)
     err = np.abs(o - o_ref)
     lerr = np.abs(np.asarray(lse, dtype=np.float64) - lse_ref)
-    excess = err - half_ulp(o_ref, dtype)
+    floor = np.abs(round_to(o_ref, dtype) - o_ref)
+    over = err > O_MAX_ABS
+    unattainable = over & (floor > O_MAX_ABS)
+    attainable_over = over & ~unattainable
+    relaxed_bad = unattainable & (err > O_MAX_ABS + half_ulp(o_ref, dtype))
     res = {
         "o_max_abs": float(err.max()) if err.size else 0.0,
         "o_mean_abs": float(err.mean()) if err.size else 0.0,
-        "o_max_excess_over_rounding": float(excess.max()) if err.size else 0.0,
+        "o_rounding_floor_max": float(floor.max()) if err.size else 0.0,
+        "o_over_bound": int(attainable_over.sum()),
+        "o_unattainable": int(unattainable.sum()),
         "lse_max_abs": float(lerr.max()) if lerr.size else 0.0,
+        "elements": int(err.size),
         "finite": bool(np.all(np.isfinite(o)) and np.all(np.isfinite(lse))),
     }
+    if over.any():  # the largest errors above the bound, for the record
+        idx = np.flatnonzero(over.reshape(-1))
+        res["_over_flat"] = idx
+        res["_over_err"] = err.reshape(-1)[idx]
+        top = idx[np.argsort(-res["_over_err"])][:32]
+        res["over_elements"] = [
+            {"flat": int(i), "o_gpu": float(o.reshape(-1)[i]), "o_ref": float(o_ref.reshape(-1)[i]),
+             "floor": float(floor.reshape(-1)[i])} for i in top]
     res["ok"] = (res["finite"] and res["o_mean_abs"] <= O_MEAN_ABS
-                 and res["o_max_excess_over_rounding"] <= O_MAX_ABS
+                 and res["o_over_bound"] == 0 and not relaxed_bad.any()
                  and res["lse_max_abs"] <= LSE_MAX_ABS)
     return res
+
+
+# unit roundoff 2^-p of a p-significant-bit format: the largest relative error
+# of round-to-nearest (half the spacing 2^(e + 1 - p) over the smallest value
+# 2^e of a binade)
+UNIT_ROUNDOFF = {"fp16": 2.0 ** -11, "bf16": 2.0 ** -8}
+
+
+def explain_over(res: dict, oracle, q, k, v, dtype: str, causal: bool, scale: float,
+                 d: int) -> dict:
+    """For inputs outside the stated bound's N(0, 1) clause: checks every
+    element above 1e-2 against the bound derived from the method's two
+    roundings (16-bit P, 16-bit O) and sets res["ok"] accordingly. Adds
+    o_over_bound_within_rounding_bound (count) and the largest ratio of error
+    to that bound."""
+    idx = res.get("_over_flat")
+    if idx is None or idx.size == 0:
+        res["o_over_bound_within_rounding_bound"] = 0
+        return res
+    rows, cols = idx // d, idx % d
+    urows, inv = np.unique(rows, return_inverse=True)
+    o_ref, _, dev = oracle.attn_rows_dev(q, k, v, dtype, causal, scale, urows)
+    ref = o_ref[inv, cols]
+    u = UNIT_ROUNDOFF[dtype]
+    allowed = half_ulp(ref, dtype) + u / (1.0 - u) * dev[inv, cols] + 2e-5
+    ratio = res["_over_err"] / allowed
+    res["o_over_bound_within_rounding_bound"] = int((ratio <= 1.0).sum())
+    res["o_over_bound_max_ratio_to_rounding_bound"] = float(ratio.max())
+    res["ok"] = (res["finite"] and res["o_mean_abs"] <= O_MEAN_ABS
+                 and bool(np.all(ratio <= 1.0)) and res["lse_max_abs"] <= LSE_MAX_ABS)
+    return res
+
+
+def record(name: str, res: dict, **extra) -> None:
+    """Appends one JSON line (a parity result) to the file named by the
+    FA_PARITY_RECORD environment variable, if it is set."""
+    path = os.environ.get("FA_PARITY_RECORD")
+    if path:
+        keep = {k: v for k, v in res.items() if not k.startswith("_")}
+        with open(path, "a") as f:
+            f.write(json.dumps({"case": name, **keep, **extra}) + "\n")
 
 
 def torch_dtype(dtype: str):

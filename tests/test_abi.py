@@ -21,7 +21,7 @@ def test_header_declares_expected_entry_points():
     names = fa.header_functions()
     assert names == ["fa_fwd", "fa_fwd_strided", "fa_fwd_fp8", "fa_bwd", "fa_bwd_workspace_size",
                      "fa_fwd_noalloc", "fa_fwd_host", "fa_fwd_host_workspace_size", "fa_check",
-                     "fa_query_launch",
+                     "fa_sm_clock_read", "fa_query_launch",
                      "fa_sm_clock_probe", "fa_status_string", "fa_version"]
 
 
@@ -243,7 +243,8 @@ int main(void) {
   typedef void (*fn_t)(void);
   fn_t fns[] = {(fn_t)fa_fwd, (fn_t)fa_fwd_strided, (fn_t)fa_fwd_fp8, (fn_t)fa_bwd,
                 (fn_t)fa_bwd_workspace_size, (fn_t)fa_fwd_noalloc, (fn_t)fa_fwd_host,
-                (fn_t)fa_fwd_host_workspace_size, (fn_t)fa_check, (fn_t)fa_query_launch,
+                (fn_t)fa_fwd_host_workspace_size, (fn_t)fa_check, (fn_t)fa_sm_clock_read,
+                (fn_t)fa_query_launch,
                 (fn_t)fa_sm_clock_probe, (fn_t)fa_status_string, (fn_t)fa_version};
   size_t i;
   size_t ws = 0;

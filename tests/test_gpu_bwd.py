@@ -17,7 +17,7 @@ import pytest
 import attention_forward_flashattention_gb300 as fa
 from attention_forward_flashattention_gb300 import inputs as I
 
-from parity_util import bits_to_f64, half_ulp, to_bits, to_device
+from parity_util import bits_to_f64, half_ulp, record, to_bits, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -50,6 +50,8 @@ def _check(got_bits, ref, mag, dtype, what):
     got = bits_to_f64(got_bits, dtype)
     err = np.abs(got - ref)
     limit = 4 * EPS[dtype] * mag + half_ulp(ref, dtype) + 1e-6
+    record(what, {"max_abs": float(err.max()), "mean_abs": float(err.mean()),
+                  "max_err_over_limit": float((err / limit).max()), "elements": int(err.size)})
     assert np.all(np.isfinite(got)), what
     bad = err > limit
     assert not bad.any(), (what, int(bad.sum()), float((err - limit).max()), float(err.max()))
@@ -87,12 +89,14 @@ def _inputs(name):
 
 
 @pytest.mark.parametrize("name", ["mha_b4_h16_n4096_d128_fp16", "causal_b4_h16_n4096_d128_bf16",
-                                  "mha_b2_h32_n8192_d64_fp16"])
+                                  "mha_b2_h32_n8192_d64_fp16",
+                                  "causal_b1_h32_n16384_d128_bf16_q3"])
 def test_bwd_full_size_sampled_heads(oracle_mod, name):
     w = I.WORKLOADS[name]
     q, k, v, dob = _inputs(name)
     dq, dk, dv = _run(w, q, k, v, dob)
-    heads = np.array([0, w.B * w.H - 1])
+    # two heads; one at N = 16384 (its fp64 N x N buffers take 6.4 GB of host memory)
+    heads = np.array([0, w.B * w.H - 1]) if w.N <= 8192 else np.array([w.B * w.H - 1])
     g = oracle_mod.attn_bwd(q, k, v, dob, w.dtype, w.causal, w.scale, heads=heads)
     shape = (w.B * w.H, w.N, w.d)
     for nm, got in (("dq", dq), ("dk", dk), ("dv", dv)):

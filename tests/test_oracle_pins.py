@@ -296,3 +296,83 @@ def test_fp8_bound_covers_rounded_weights(oracle_mod, shift, q_mult):
     err = np.abs(o_q.reshape(-1, w.d) - o)
     assert np.all(err <= bound + 1e-12)
     assert float(bound.max()) < 0.5 and float(err.max()) > 0.0
+
+
+# ---------------------------------------------------------------- weighted deviation of V
+
+def test_dev_uniform_weights_is_mean_absolute_deviation(oracle_mod):
+    """Q = 0: every weight is 1/N, so dev_t = mean_j |v_jt - mean(v_t)|."""
+    rng = np.random.default_rng(21)
+    N, d = 57, 64
+    q = np.zeros((1, 2, N, d), dtype=np.uint16)
+    k = _rand_bits(rng, (1, 2, N, d), "bf16")
+    v = _rand_bits(rng, (1, 2, N, d), "bf16")
+    rows = np.array([0, 5, N - 1, N + 3, 2 * N - 1])
+    o, lse, dev = oracle_mod.attn_rows_dev(q, k, v, "bf16", False, 0.125, rows)
+    vd = oracle_mod.decode(v, "bf16").reshape(2, N, d)
+    for r, row in enumerate(rows):
+        vh = vd[row // N]
+        want = np.abs(vh - vh.mean(axis=0)).mean(axis=0)
+        np.testing.assert_allclose(dev[r], want, rtol=0, atol=1e-13)
+
+
+def test_dev_two_keys_closed_form(oracle_mod):
+    """Two keys with scores a, b: O = p1 v1 + p2 v2 and dev = 2 p1 p2 |v1 - v2|
+    (|v1 - O| = p2 |v1 - v2|, |v2 - O| = p1 |v1 - v2|)."""
+    N, d = 2, 64
+    qf = np.zeros((1, 1, N, d))
+    qf[..., 0] = 1.0
+    kf = np.zeros((1, 1, N, d))
+    kf[0, 0, :, 0] = [1.5, -0.25]                     # scores 1.5 and -0.25 (scale 1)
+    rng = np.random.default_rng(22)
+    v = _rand_bits(rng, (1, 1, N, d), "fp16")
+    o, lse, dev = oracle_mod.attn_rows_dev(I.to_bits(qf, "fp16"), I.to_bits(kf, "fp16"), v, "fp16",
+                                           False, 1.0, np.array([0, 1]))
+    vd = oracle_mod.decode(v, "fp16")[0, 0]
+    p1 = 1.0 / (1.0 + np.exp(-1.75))
+    p2 = 1.0 - p1
+    want = 2 * p1 * p2 * np.abs(vd[0] - vd[1])
+    for r in range(2):
+        np.testing.assert_allclose(o[r], p1 * vd[0] + p2 * vd[1], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(dev[r], want, rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_dev_zero_for_constant_v_and_single_key(oracle_mod, causal):
+    rng = np.random.default_rng(23)
+    N, d = 70, 128
+    q = _rand_bits(rng, (1, 1, N, d), "bf16", 2.0)
+    k = _rand_bits(rng, (1, 1, N, d), "bf16")
+    cols = rng.standard_normal(d)
+    vc = I.to_bits(np.broadcast_to(cols, (1, 1, N, d)), "bf16")
+    rows = np.arange(N)
+    _, _, dev = oracle_mod.attn_rows_dev(q, k, vc, "bf16", causal, 0.1, rows)
+    assert np.max(np.abs(dev)) <= 1e-13
+    v = _rand_bits(rng, (1, 1, N, d), "bf16")
+    o, lse, dev = oracle_mod.attn_rows_dev(q, k, v, "bf16", causal, 0.1, rows)
+    o2, l2 = oracle_mod.attn_rows(q, k, v, "bf16", causal, 0.1, rows)
+    assert np.array_equal(o, o2) and np.array_equal(lse, l2)
+    if causal:   # row 0 sees key 0 alone: no deviation
+        assert np.all(dev[0] == 0.0)
+
+
+def test_dev_bounds_rounded_weights(oracle_mod):
+    """The bound it exists for: O recomputed from bf16-rounded weights (and
+    their sum) lies within u / (1 - u) dev of O, u = 2^-8 (bf16's unit
+    roundoff: 8 significant bits), on random rows."""
+    rng = np.random.default_rng(24)
+    N, d = 300, 64
+    q = _rand_bits(rng, (1, 1, N, d), "bf16", 3.0)
+    k = _rand_bits(rng, (1, 1, N, d), "bf16")
+    v = _rand_bits(rng, (1, 1, N, d), "bf16")
+    rows = np.arange(N)
+    o, _, dev = oracle_mod.attn_rows_dev(q, k, v, "bf16", True, 0.125, rows)
+    qd, kd, vd = (oracle_mod.decode(x, "bf16")[0, 0] for x in (q, k, v))
+    u = 2.0 ** -8
+    for i in rows:
+        s = np.float64(np.float32(0.125)) * (kd[:i + 1] @ qd[i])
+        p = np.exp(s - s.max())
+        m, e = np.frexp(p)
+        r = np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)   # bf16 rounding of the weights
+        o_r = (r @ vd[:i + 1]) / r.sum()
+        assert np.all(np.abs(o_r - o[i]) <= u / (1 - u) * dev[i] + 1e-13)

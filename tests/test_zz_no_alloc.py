@@ -4,9 +4,11 @@ It exists for callers that cannot allocate device memory (their allocator owns
 all of HBM, or they must never call cudaMalloc / cudaFree while running): it
 runs the same kernel as fa_fwd with the kernel's scratch (one status word) in
 a fixed array inside the library. This test calls it through the C ABI twice
-in a row and checks both results against fa_fwd's, within the tolerances the
-parity tests use. It must pass alone in a fresh process and after the other
-tests; the file name makes pytest collect it last.
+in a row and checks that both results equal fa_fwd's bit for bit (the same
+deterministic kernel on the same inputs), and that fa_check, which reads the
+allocation-free status word too, reports no timeout. It must pass alone in a
+fresh process and after the other tests; the file name makes pytest collect
+it last.
 """
 import numpy as np
 import pytest
@@ -14,7 +16,7 @@ import pytest
 import attention_forward_flashattention_gb300 as fa
 from attention_forward_flashattention_gb300 import inputs as I
 
-from parity_util import compare, bits_to_f64, to_bits, to_device
+from parity_util import to_bits, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -44,12 +46,14 @@ def test_noalloc_matches_fa_fwd_twice(B, H, N, d, dtype, causal):
     w = I.custom("noalloc", B, H, N, d, dtype, causal, seed_index=500 + d)
     qb, kb, vb = I.qkv_bits(w)
     q, k, v = (to_device(x, dtype) for x in (qb, kb, vb))
+    sh = int(torch.cuda.current_stream().cuda_stream)
     o_ref, l_ref = _run(fa.fa_fwd, q, k, v, w)
-    assert fa.fa_check(int(torch.cuda.current_stream().cuda_stream)) == fa.FA_OK
+    assert fa.fa_check(sh) == fa.FA_OK
     for _ in range(2):
         o, lse = _run(fa.fa_fwd_noalloc, q, k, v, w)
-        res = compare(o, lse, bits_to_f64(o_ref, dtype), l_ref.astype(np.float64), dtype)
-        assert res["ok"], res
+        assert np.array_equal(o, o_ref)
+        assert np.array_equal(lse.view(np.uint32), l_ref.view(np.uint32))
+        assert fa.fa_check(sh) == fa.FA_OK
 
 
 def test_noalloc_rejects_bad_arguments():
@@ -62,3 +66,4 @@ def test_noalloc_rejects_bad_arguments():
     assert fa.fa_fwd_noalloc(p, p, p, p, lse.data_ptr(), 1, 1, 128, 96, 0, 0.1, 0, 0) == fa.FA_ERR_UNSUPPORTED
     assert fa.fa_fwd_noalloc(p, p, p, p, 0, 1, 1, 128, 64, 0, 0.1, 0, 0) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_fwd_noalloc(p, p, p, p, lse.data_ptr(), 1, 1, (1 << 30) + 1, 64, 0, 0.1, 0, 0) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_fwd_noalloc(p, p, p, p, lse.data_ptr(), 0, 1, 128, 64, 0, 0.1, 0, 0) == fa.FA_ERR_INVALID_ARG
