@@ -66,6 +66,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
         lib.fa_fwd.restype = i
+        lib.fa_fwd_pair.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+        lib.fa_fwd_pair.restype = i
         if hasattr(lib, "fa_fwd_strided"):
             lib.fa_fwd_strided.argtypes = [vp, vp, vp, vp, vp, i, i, i, i,
                                            ctypes.POINTER(FaStrides), i, f, i, vp]
@@ -117,6 +119,13 @@ def fa_fwd(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, d: 
     """Same arguments as the C function (device pointers as ints); returns the status."""
     return load_library().fa_fwd(q, k, v, o, lse, B, H, N, d, int(bool(causal)), float(scale),
                                  int(dtype), stream)
+
+
+def fa_fwd_pair(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, d: int,
+                causal: bool, scale: float, dtype: int, stream: int = 0) -> int:
+    """The CTA-pair forward (same arguments as fa_fwd, d = 128); returns the status."""
+    return load_library().fa_fwd_pair(q, k, v, o, lse, B, H, N, d, int(bool(causal)),
+                                      float(scale), int(dtype), stream)
 
 
 def fa_fwd_strided(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, d: int,
@@ -254,6 +263,24 @@ def attention_forward_into(q, k, v, o, lse, causal: bool = False, scale: float |
         what = "fa_fwd_strided"
     if rc != FA_OK:
         raise FaError(rc, what)
+
+
+def attention_forward_pair_into(q, k, v, o, lse, causal: bool = False,
+                                scale: float | None = None, stream=None) -> None:
+    """Enqueues fa_fwd_pair (CTA-pair kernel) on contiguous [B, H, N, 128]
+    CUDA tensors q, k, v, o (fp16 / bf16) and a contiguous float32 [B, H, N] lse."""
+    B, H, N, d = q.shape
+    for t in (q, k, v, o):
+        if tuple(t.shape) != (B, H, N, d) or not (t.is_cuda and t.is_contiguous()):
+            raise ValueError("q, k, v, o must be contiguous [B, H, N, d] CUDA tensors")
+    if tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous [B, H, N] float32 CUDA tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    rc = fa_fwd_pair(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                     B, H, N, d, causal, scale, _dtype_code(q), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_pair")
 
 
 def attention_forward(q, k, v, causal: bool = False, scale: float | None = None, stream=None):

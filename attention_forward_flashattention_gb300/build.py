@@ -22,10 +22,10 @@ INCLUDE = os.path.join(ROOT, "include")
 
 LIB_NAME = "libfa_sm103.so"
 SELFTEST_NAME = "libfa_selftest.so"
-LIB_UNITS = ["fa_host.cu", "fa_fwd_d64.cu", "fa_fwd_d128.cu", "fa_fwd_fp8.cu", "fa_bwd_d64.cu",
-             "fa_bwd_d128.cu", "fa_noalloc.cu", "fa_pipeline.cu"]
+LIB_UNITS = ["fa_host.cu", "fa_fwd_d64.cu", "fa_fwd_d128.cu", "fa_fwd_fp8.cu", "fa_fwd_pair.cu",
+             "fa_bwd_d64.cu", "fa_bwd_d128.cu", "fa_noalloc.cu", "fa_pipeline.cu"]
 SELFTEST_UNITS = ["selftest.cu"]
-HEADERS = ["ptx.cuh", "fa_common.cuh", "fa_kernel.cuh", "fa_launch.cuh", "fa_bwd.cuh",
+HEADERS = ["ptx.cuh", "fa_common.cuh", "fa_kernel.cuh", "fa_launch.cuh", "fa_pair.cuh", "fa_bwd.cuh",
            "fa_bwd_launch.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -148,6 +148,27 @@ __device__ __forceinline__ bool wait_cluster(uint32_t bar, uint32_t parity, cons
   }
 }
 
+// Warp-uniform cluster-scope wait (every lane polls, the warp leaves together).
+__device__ __forceinline__ bool wait_cluster_warp(uint32_t bar, uint32_t parity,
+                                                  const AbortCtx& ab, uint32_t code) {
+  if (__all_sync(0xffffffffu, ptx::mbar_test_cluster(bar, parity))) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (__all_sync(0xffffffffu, ptx::mbar_test_cluster(bar, parity))) return true;
+    if ((it & 63u) == 0u) {
+      const bool late = ptx::globaltimer_ns() - t0 > kWaitLimitNs;
+      const bool stop = *ab.flag != 0u || late;
+      if (__any_sync(0xffffffffu, stop)) {
+        if (__any_sync(0xffffffffu, late)) {
+          *ab.flag = 1u;
+          atomicOr(ab.status, code);
+        }
+        return false;
+      }
+    }
+  }
+}
+
 // Warp-uniform variant: every lane polls; the warp proceeds only if all
 // lanes saw the phase complete.
 __device__ __forceinline__ bool wait_bounded_warp(uint32_t bar, uint32_t parity,

@@ -17,6 +17,7 @@
 #include "fa.h"
 #include "fa_bwd.cuh"
 #include "fa_kernel.cuh"
+#include "fa_pair.cuh"
 
 namespace fa {
 namespace {
@@ -180,9 +181,11 @@ fa_status check_strides(const fa_strides* s, int d) {
 }
 
 bool encode_fwd_maps(CUtensorMap* maps, const void* q, const void* k, const void* v,
-                     const void* o, const fa_strides* s, bool bf16, int B, int H, int N, int d) {
+                     const void* o, const fa_strides* s, bool bf16, int B, int H, int N, int d,
+                     int k_box_rows) {
   return encode_qkv(&maps[0], q, s[0], bf16, B, H, N, d, 128) &&
-         encode_qkv(&maps[1], k, s[1], bf16, B, H, N, d, fwd_k_box_rows(d)) &&
+         encode_qkv(&maps[1], k, s[1], bf16, B, H, N, d,
+                    k_box_rows > 0 ? k_box_rows : fwd_k_box_rows(d)) &&
          encode_qkv(&maps[2], v, s[2], bf16, B, H, N, d, 128) &&
          encode_qkv(&maps[3], o, s[3], bf16, B, H, N, d, kFwdOutBoxRows);
 }
@@ -210,10 +213,11 @@ extern "C" {
 
 namespace {
 
-// fa_fwd and fa_fwd_strided: checks, tensor maps, plan, launch.
+// fa_fwd, fa_fwd_strided and fa_fwd_pair: checks, tensor maps, plan, launch
+// (pair: the CTA-pair kernel, head dimension 128 only).
 fa_status fwd_call(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                    int N, int d, const fa_strides* s, int causal, float scale, fa_dtype dtype,
-                   void* stream) {
+                   void* stream, bool pair = false) {
   if (!q || !k || !v || !o || !lse || !s) return FA_ERR_INVALID_ARG;
   if (!fa::aligned16(q) || !fa::aligned16(k) || !fa::aligned16(v) || !fa::aligned16(o) ||
       !fa::aligned16(lse))
@@ -222,6 +226,7 @@ fa_status fwd_call(const void* q, const void* k, const void* v, void* o, float* 
   if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
   const fa_status sz = fa::check_sizes(B, H, N, d);
   if (sz != FA_OK) return sz;
+  if (pair && d != 128) return FA_ERR_UNSUPPORTED;
   const fa_status ss = fa::check_strides(s, d);
   if (ss != FA_OK) return ss;
 
@@ -233,7 +238,8 @@ fa_status fwd_call(const void* q, const void* k, const void* v, void* o, float* 
   const bool bf16 = dtype == FA_DTYPE_BF16;
   const long long BH = static_cast<long long>(B) * H;
   CUtensorMap maps[4];
-  if (!fa::encode_fwd_maps(maps, q, k, v, o, s, bf16, B, H, N, d)) return FA_ERR_CUDA;
+  if (!fa::encode_fwd_maps(maps, q, k, v, o, s, bf16, B, H, N, d, pair ? 64 : 0))
+    return FA_ERR_CUDA;
 
   fa::FwdArgs a{};
   a.lse = lse;
@@ -242,10 +248,12 @@ fa_status fwd_call(const void* q, const void* k, const void* v, void* o, float* 
   a.scale_log2 = scale * 1.4426950408889634f;
   int grid = 0;
   fa::plan_fwd(d, N, H, BH, st->sm_count, &a, &grid);
+  if (pair) grid = fa::fwd_grid_pair(a.n_units, st->sm_count);
 
   (void)cudaGetLastError();  // do not report an earlier, unrelated error as ours
-  const cudaError_t e =
-      fa::launch_fwd(d, bf16, causal != 0, maps, a, grid, static_cast<cudaStream_t>(stream));
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = pair ? fa::launch_fwd_pair(bf16, causal != 0, maps, a, grid, cs)
+                             : fa::launch_fwd(d, bf16, causal != 0, maps, a, grid, cs);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -258,6 +266,15 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   const fa_strides c = fa::contiguous_strides(H, N, d);
   const fa_strides s[4] = {c, c, c, c};
   return fwd_call(q, k, v, o, lse, B, H, N, d, s, causal, scale, dtype, stream);
+}
+
+fa_status fa_fwd_pair(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int H, int N, int d, int causal, float scale, fa_dtype dtype, void* stream) {
+  if (B <= 0 || H <= 0 || N <= 0) return FA_ERR_INVALID_ARG;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  const fa_strides c = fa::contiguous_strides(H, N, d);
+  const fa_strides s[4] = {c, c, c, c};
+  return fwd_call(q, k, v, o, lse, B, H, N, d, s, causal, scale, dtype, stream, true);
 }
 
 fa_status fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B,

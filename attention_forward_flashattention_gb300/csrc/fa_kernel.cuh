@@ -779,9 +779,11 @@ fa_status check_sizes(int B, int H, int N, int d);
 // clears it; *timed_out is set when a launch recorded a timeout. FA_OK when
 // that entry point has not been used on the device.
 fa_status noalloc_take_status(int dev, bool* timed_out);
-// Q, K, V, O tensor maps of a call (s: q, k, v, o strides).
+// Q, K, V, O tensor maps of a call (s: q, k, v, o strides); k_box_rows: keys
+// per K box (0: the one-CTA kernel's 128; the CTA-pair kernel loads 64).
 bool encode_fwd_maps(CUtensorMap* maps, const void* q, const void* k, const void* v,
-                     const void* o, const fa_strides* s, bool bf16, int B, int H, int N, int d);
+                     const void* o, const fa_strides* s, bool bf16, int B, int H, int N, int d,
+                     int k_box_rows = 0);
 // Unit counts of a call into `a` (N, H, BH, n_mblk, n_units, n_kv) and its grid.
 void plan_fwd(int d, int N, int H, long long BH, int sm_count, FwdArgs* a, int* grid);
 cudaError_t launch_fwd(int d, bool bf16, bool causal, const CUtensorMap* maps, const FwdArgs& a,

@@ -357,6 +357,27 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[2][32]) 
       : "r"(taddr));
 }
 
+// Waits for this thread's outstanding TMEM load into r (one 64-column load),
+// with the registers tied to the wait.
+__device__ __forceinline__ void tmem_ld_wait64(uint32_t (&r)[2][32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0][0]), "+r"(r[0][1]), "+r"(r[0][2]), "+r"(r[0][3]), "+r"(r[0][4]),
+                 "+r"(r[0][5]), "+r"(r[0][6]), "+r"(r[0][7]), "+r"(r[0][8]), "+r"(r[0][9]),
+                 "+r"(r[0][10]), "+r"(r[0][11]), "+r"(r[0][12]), "+r"(r[0][13]), "+r"(r[0][14]),
+                 "+r"(r[0][15]), "+r"(r[0][16]), "+r"(r[0][17]), "+r"(r[0][18]), "+r"(r[0][19]),
+                 "+r"(r[0][20]), "+r"(r[0][21]), "+r"(r[0][22]), "+r"(r[0][23]), "+r"(r[0][24]),
+                 "+r"(r[0][25]), "+r"(r[0][26]), "+r"(r[0][27]), "+r"(r[0][28]), "+r"(r[0][29]),
+                 "+r"(r[0][30]), "+r"(r[0][31]), "+r"(r[1][0]), "+r"(r[1][1]), "+r"(r[1][2]),
+                 "+r"(r[1][3]), "+r"(r[1][4]), "+r"(r[1][5]), "+r"(r[1][6]), "+r"(r[1][7]),
+                 "+r"(r[1][8]), "+r"(r[1][9]), "+r"(r[1][10]), "+r"(r[1][11]), "+r"(r[1][12]),
+                 "+r"(r[1][13]), "+r"(r[1][14]), "+r"(r[1][15]), "+r"(r[1][16]), "+r"(r[1][17]),
+                 "+r"(r[1][18]), "+r"(r[1][19]), "+r"(r[1][20]), "+r"(r[1][21]), "+r"(r[1][22]),
+                 "+r"(r[1][23]), "+r"(r[1][24]), "+r"(r[1][25]), "+r"(r[1][26]), "+r"(r[1][27]),
+                 "+r"(r[1][28]), "+r"(r[1][29]), "+r"(r[1][30]), "+r"(r[1][31])
+               :
+               : "memory");
+}
+
 // Waits for this thread's outstanding TMEM loads into a and b (two 64-column
 // loads): the registers are tied to the wait so no use moves above it.
 __device__ __forceinline__ void tmem_ld_wait64x2(uint32_t (&a)[2][32], uint32_t (&b)[2][32]) {
@@ -460,10 +481,16 @@ __device__ __forceinline__ void cluster_sync() {
       "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Arrive on a barrier given by its shared::cluster address (possibly in the peer CTA).
+// Arrive on a barrier given by its shared::cluster address (possibly in the peer
+// CTA), with the arrive's default release semantics. The cluster-scope release
+// form (.release.cluster) makes every arriving thread wait until its earlier
+// memory operations are visible to the whole cluster: measured on the pair
+// kernel, where each softmax warp arrives twice per KV tile, it doubled the
+// tile time (C2 shape 764 against 1247 TFLOPS, identical output bits). The
+// operands these arrivals hand over live in tensor memory and are ordered by
+// tcgen05.wait and the tcgen05 thread-sync fences on both sides.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // try_wait with cluster-scope acquire, for barriers that receive arrivals from
@@ -503,6 +530,17 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap,
       : "memory");
 }
 
+// 4-D form of the same (coordinates innermost first).
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const void* tmap,
+                                                 uint32_t bar_cluster, int c0, int c1, int c2,
+                                                 int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
 // TMEM allocation shared by the pair: one warp of each CTA executes these.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),
@@ -536,6 +574,40 @@ __device__ __forceinline__ void umma_f16_ts_pair(uint32_t d_tmem, uint32_t a_tme
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Elected forms of the pair MMAs and commit (the whole converged warp executes
+// them; the lane elect.sync picks issues).
+__device__ __forceinline__ void umma_f16_ss_pair_elect(uint32_t d_tmem, uint64_t adesc,
+                                                       uint64_t bdesc, uint32_t idesc,
+                                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_f16_ts_pair_elect(uint32_t d_tmem, uint32_t a_tmem,
+                                                       uint64_t bdesc, uint32_t idesc,
+                                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit_pair_elect(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;\n\t}" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
+
 // One arrival on the barrier at this offset in every CTA of `cta_mask` once
 // all pair MMAs issued by this thread have completed.
 __device__ __forceinline__ void umma_commit_pair(uint32_t bar, uint16_t cta_mask) {

@@ -331,7 +331,8 @@ class Plan:
         self.__dict__.update(kw)
 
 
-def forward_plan(fa, torch, w, dev, stream, x=None) -> Plan:
+def forward_plan(fa, torch, w, dev, stream, x=None, pair=False) -> Plan:
+    """pair: time the CTA-pair kernel (fa_fwd_pair) instead of fa_fwd."""
     fp8 = w.dtype == "e4m3"
     x = workload_inputs(w) if x is None else x
     if fp8:
@@ -353,6 +354,9 @@ def forward_plan(fa, torch, w, dev, stream, x=None) -> Plan:
         if fp8:
             fa.attention_forward_fp8_into(ins[0], ins[1], ins[2], o, lse, x.q_scale, ins[3],
                                           x.v_scale, w.causal, w.scale, stream)
+        elif pair:
+            fa.attention_forward_pair_into(ins[0], ins[1], ins[2], o, lse, w.causal, w.scale,
+                                           stream)
         else:
             fa.attention_forward_into(ins[0], ins[1], ins[2], o, lse, w.causal, w.scale, stream)
 
@@ -383,7 +387,7 @@ def forward_plan(fa, torch, w, dev, stream, x=None) -> Plan:
         h2d=sum(h.numel() * h.element_size() for h in host),
         d2h=o.numel() * o.element_size() + lse.numel() * 4,
         launches=1, peak_mult=2.0 if fp8 else 1.0, peak_note=peak_note,
-        kernel="fa_fwd_kernel",
+        kernel="fa_fwd_pair_kernel" if pair else "fa_fwd_kernel",
         launch_cfg={"grid": launch["grid"], "threads": launch["threads"],
                     "smem_bytes": None if fp8 else launch["smem_bytes"],
                     "units": launch["units"]},
@@ -508,10 +512,17 @@ def clock_corrected_frac(tflops: float, dtype: str, sms: int, mhz) -> float | No
     return tflops * 1e12 / (sms * TENSOR_FLOP_PER_CLK_SM[dtype] * mhz * 1e6)
 
 
+PAIR_PREFIX = "cta_pair:"   # other_workloads key of the CTA-pair kernel on a workload
+
+
 def other_workload_names(headline: str, pass_: str) -> list[str]:
+    """Every other named workload; in the forward pass also the 8-bit shapes and
+    the CTA-pair kernel on every head-dimension-128 16-bit workload (the
+    headline's included), so the two kernels are timed in the same run."""
     names = [n for n in I.WORKLOAD_ORDER if n != headline]
     if pass_ == "forward":
         names += [n for n in I.FP8_WORKLOADS if n != headline]
+        names += [PAIR_PREFIX + n for n in I.WORKLOAD_ORDER if I.WORKLOADS[n].d == 128]
     return names
 
 
@@ -528,7 +539,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     if others:
         pool = cf.ProcessPoolExecutor(max_workers=min(len(others), max(1, os.cpu_count() or 1)),
                                       mp_context=mp.get_context("spawn"))
-        futures = {n: pool.submit(_gen_inputs, n) for n in others}
+        futures = {n: pool.submit(_gen_inputs, n.removeprefix(PAIR_PREFIX)) for n in others
+                   if not (n.startswith(PAIR_PREFIX) and n.removeprefix(PAIR_PREFIX) == args.workload)}
 
     import torch
 
@@ -578,9 +590,19 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     # every other workload: same steps, warm-up and flush, one after another
     other = {}
+    head_inputs = None
     for name in others:
-        ow = get_workload(name)
-        oplan = make(fa, torch, ow, dev, stream, x=futures[name].result())
+        base = name.removeprefix(PAIR_PREFIX)
+        ow = get_workload(base)
+        if name in futures:
+            x = futures[name].result()
+        else:  # the headline workload on the pair kernel: its own inputs
+            head_inputs = head_inputs if head_inputs is not None else workload_inputs(ow)
+            x = head_inputs
+        if name.startswith(PAIR_PREFIX):
+            oplan = forward_plan(fa, torch, ow, dev, stream, x=x, pair=True)
+        else:
+            oplan = make(fa, torch, ow, dev, stream, x=x)
         ot = time_steps(fa, torch, oplan, stream, dev, flush, args.steps, args.warmup, world)
         oms = ot["total_ms"] / args.steps
         otf = job_throughput(oplan.flops, ot["total_ms"], args.steps, world) / world
@@ -594,6 +616,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             "clock_corrected_frac": clock_corrected_frac(otf, ow.dtype, sms, ot["clk64_mhz"]),
             "config": {k: v for k, v in workload_config(ow).items()
                        if k not in ("global_batch", "seq_len")},
+            "kernel": oplan.kernel,
         }
         del oplan
         torch.cuda.empty_cache()

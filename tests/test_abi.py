@@ -19,7 +19,7 @@ def lib():
 
 def test_header_declares_expected_entry_points():
     names = fa.header_functions()
-    assert names == ["fa_fwd", "fa_fwd_strided", "fa_fwd_fp8", "fa_bwd", "fa_bwd_workspace_size",
+    assert names == ["fa_fwd", "fa_fwd_pair", "fa_fwd_strided", "fa_fwd_fp8", "fa_bwd", "fa_bwd_workspace_size",
                      "fa_fwd_noalloc", "fa_fwd_host", "fa_fwd_host_workspace_size", "fa_check",
                      "fa_sm_clock_read", "fa_query_launch",
                      "fa_sm_clock_probe", "fa_status_string", "fa_version"]
@@ -241,7 +241,7 @@ C_PROGRAM = r"""
 int main(void) {
   /* every entry point is a plain C function */
   typedef void (*fn_t)(void);
-  fn_t fns[] = {(fn_t)fa_fwd, (fn_t)fa_fwd_strided, (fn_t)fa_fwd_fp8, (fn_t)fa_bwd,
+  fn_t fns[] = {(fn_t)fa_fwd, (fn_t)fa_fwd_pair, (fn_t)fa_fwd_strided, (fn_t)fa_fwd_fp8, (fn_t)fa_bwd,
                 (fn_t)fa_bwd_workspace_size, (fn_t)fa_fwd_noalloc, (fn_t)fa_fwd_host,
                 (fn_t)fa_fwd_host_workspace_size, (fn_t)fa_check, (fn_t)fa_sm_clock_read,
                 (fn_t)fa_query_launch,
@@ -290,3 +290,26 @@ def test_header_is_plain_c_and_links(tmp_path):
         env["LD_LIBRARY_PATH"] = cuda_lib + os.pathsep + env.get("LD_LIBRARY_PATH", "")
     out = subprocess.run([str(exe)], capture_output=True, text=True, env=env, timeout=60)
     assert out.returncode == 0 and out.stdout.startswith("ok"), (out.returncode, out.stderr)
+
+
+def _pair(q=GOOD, k=GOOD, v=GOOD, o=GOOD, lse=GOOD, B=1, H=1, N=128, d=128, causal=0,
+          scale=0.125, dtype=fa.FA_DTYPE_FP16):
+    return fa.fa_fwd_pair(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, 0)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(q=0), fa.FA_ERR_INVALID_ARG), (dict(lse=GOOD + 4), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=0.0), fa.FA_ERR_INVALID_ARG), (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(dtype=2), fa.FA_ERR_INVALID_ARG), (dict(d=64), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED), (dict(N=(1 << 30) + 1), fa.FA_ERR_UNSUPPORTED),
+])
+def test_pair_bad_arguments_rejected(lib, kw, want):
+    """fa_fwd_pair checks its arguments like fa_fwd, and takes head dimension 128 only."""
+    assert _pair(**kw) == want
+
+
+def test_pair_no_device_is_an_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _pair() in (fa.FA_ERR_CUDA, fa.FA_ERR_ARCH)
