@@ -76,6 +76,9 @@ def parse_args():
                    help="untimed loaded seconds before the timed steps (clock samples)")
     p.add_argument("--other-workloads", default="all", choices=["all", "none"],
                    help="also time every other named workload (same steps, warm-up, flush)")
+    p.add_argument("--kernel", default="one-cta", choices=["one-cta", "pair"],
+                   help="forward kernel of the headline: fa_fwd (one CTA per tile pair) or "
+                        "fa_fwd_pair (CTA pairs, head dimension 128)")
     return p.parse_args()
 
 
@@ -91,7 +94,7 @@ def measured_peaks() -> dict:
 
 # the files fa_fwd_kernel (16-bit) is built and launched from
 FWD_SOURCES = ("ptx.cuh", "fa_common.cuh", "fa_kernel.cuh", "fa_launch.cuh", "fa_fwd_d64.cu",
-               "fa_fwd_d128.cu", "fa_host.cu")
+               "fa_fwd_d128.cu", "fa_host.cu", "fa_pair.cuh", "fa_fwd_pair.cu")
 
 
 def _code_only(text: str) -> str:
@@ -349,6 +352,7 @@ def forward_plan(fa, torch, w, dev, stream, x=None, pair=False) -> Plan:
     oh = torch.empty(o.shape, dtype=tdt).pin_memory()
     lh = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
     launch = fa.fa_query_launch(w.B, w.H, w.N, w.d, w.causal)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
 
     def run(ins):
         if fp8:
@@ -388,10 +392,12 @@ def forward_plan(fa, torch, w, dev, stream, x=None, pair=False) -> Plan:
         d2h=o.numel() * o.element_size() + lse.numel() * 4,
         launches=1, peak_mult=2.0 if fp8 else 1.0, peak_note=peak_note,
         kernel="fa_fwd_pair_kernel" if pair else "fa_fwd_kernel",
-        launch_cfg={"grid": launch["grid"], "threads": launch["threads"],
-                    "smem_bytes": None if fp8 else launch["smem_bytes"],
-                    "units": launch["units"]},
-        traffic=recorded_traffic(w.name),
+        launch_cfg=({"grid": 2 * min(launch["units"], sms // 2), "threads": launch["threads"],
+                     "cluster": 2, "units": launch["units"]} if pair else
+                    {"grid": launch["grid"], "threads": launch["threads"],
+                     "smem_bytes": None if fp8 else launch["smem_bytes"],
+                     "units": launch["units"]}),
+        traffic=recorded_traffic(PAIR_PREFIX + w.name if pair else w.name),
         cpu=lambda: cpu_forward_sample(w, x))
 
 
@@ -555,7 +561,12 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     w = get_workload(args.workload)
     stream = torch.cuda.current_stream(dev)
     make = backward_plan if args.pass_ == "backward" else forward_plan
-    plan = make(fa, torch, w, dev, stream)
+    if args.kernel == "pair":
+        if args.pass_ != "forward" or w.dtype == "e4m3" or w.d != 128:
+            raise SystemExit("--kernel pair takes a 16-bit head-dimension-128 forward workload")
+        plan = forward_plan(fa, torch, w, dev, stream, pair=True)
+    else:
+        plan = make(fa, torch, w, dev, stream)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
 
     t = time_steps(fa, torch, plan, stream, dev, flush, args.steps, args.warmup, world,
@@ -633,7 +644,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic (seeded SplitMix64 + Box-Muller, N(0,1)), resident in HBM",
-        "config": {**workload_config(w), "pass": args.pass_,
+        "config": {**workload_config(w), "pass": args.pass_, "kernel": plan.kernel,
                    "parallelism": f"replicas x{world}",
                    "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)",
                    **plan.launch_cfg},
