@@ -213,8 +213,9 @@ extern "C" {
 
 namespace {
 
+
 // fa_fwd, fa_fwd_strided and fa_fwd_pair: checks, tensor maps, plan, launch
-// (pair: the CTA-pair kernel, head dimension 128 only).
+// (the pair kernels take head dimension 128 only).
 fa_status fwd_call(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                    int N, int d, const fa_strides* s, int causal, float scale, fa_dtype dtype,
                    void* stream, bool pair = false) {
@@ -248,7 +249,11 @@ fa_status fwd_call(const void* q, const void* k, const void* v, void* o, float* 
   a.scale_log2 = scale * 1.4426950408889634f;
   int grid = 0;
   fa::plan_fwd(d, N, H, BH, st->sm_count, &a, &grid);
-  if (pair) grid = fa::fwd_grid_pair(a.n_units, st->sm_count);
+  if (pair) {  // units of 512 rows, two CTAs per unit
+    a.n_mblk = (N + 511) / 512;
+    a.n_units = static_cast<int>(BH * a.n_mblk);
+    grid = fa::fwd_grid_pair(a.n_units, st->sm_count);
+  }
 
   (void)cudaGetLastError();  // do not report an earlier, unrelated error as ours
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);

@@ -357,27 +357,6 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[2][32]) 
       : "r"(taddr));
 }
 
-// Waits for this thread's outstanding TMEM load into r (one 64-column load),
-// with the registers tied to the wait.
-__device__ __forceinline__ void tmem_ld_wait64(uint32_t (&r)[2][32]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : "+r"(r[0][0]), "+r"(r[0][1]), "+r"(r[0][2]), "+r"(r[0][3]), "+r"(r[0][4]),
-                 "+r"(r[0][5]), "+r"(r[0][6]), "+r"(r[0][7]), "+r"(r[0][8]), "+r"(r[0][9]),
-                 "+r"(r[0][10]), "+r"(r[0][11]), "+r"(r[0][12]), "+r"(r[0][13]), "+r"(r[0][14]),
-                 "+r"(r[0][15]), "+r"(r[0][16]), "+r"(r[0][17]), "+r"(r[0][18]), "+r"(r[0][19]),
-                 "+r"(r[0][20]), "+r"(r[0][21]), "+r"(r[0][22]), "+r"(r[0][23]), "+r"(r[0][24]),
-                 "+r"(r[0][25]), "+r"(r[0][26]), "+r"(r[0][27]), "+r"(r[0][28]), "+r"(r[0][29]),
-                 "+r"(r[0][30]), "+r"(r[0][31]), "+r"(r[1][0]), "+r"(r[1][1]), "+r"(r[1][2]),
-                 "+r"(r[1][3]), "+r"(r[1][4]), "+r"(r[1][5]), "+r"(r[1][6]), "+r"(r[1][7]),
-                 "+r"(r[1][8]), "+r"(r[1][9]), "+r"(r[1][10]), "+r"(r[1][11]), "+r"(r[1][12]),
-                 "+r"(r[1][13]), "+r"(r[1][14]), "+r"(r[1][15]), "+r"(r[1][16]), "+r"(r[1][17]),
-                 "+r"(r[1][18]), "+r"(r[1][19]), "+r"(r[1][20]), "+r"(r[1][21]), "+r"(r[1][22]),
-                 "+r"(r[1][23]), "+r"(r[1][24]), "+r"(r[1][25]), "+r"(r[1][26]), "+r"(r[1][27]),
-                 "+r"(r[1][28]), "+r"(r[1][29]), "+r"(r[1][30]), "+r"(r[1][31])
-               :
-               : "memory");
-}
-
 // Waits for this thread's outstanding TMEM loads into a and b (two 64-column
 // loads): the registers are tied to the wait so no use moves above it.
 __device__ __forceinline__ void tmem_ld_wait64x2(uint32_t (&a)[2][32], uint32_t (&b)[2][32]) {

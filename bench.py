@@ -94,7 +94,10 @@ def measured_peaks() -> dict:
 
 # the files fa_fwd_kernel (16-bit) is built and launched from
 FWD_SOURCES = ("ptx.cuh", "fa_common.cuh", "fa_kernel.cuh", "fa_launch.cuh", "fa_fwd_d64.cu",
-               "fa_fwd_d128.cu", "fa_host.cu", "fa_pair.cuh", "fa_fwd_pair.cu")
+               "fa_fwd_d128.cu", "fa_host.cu")
+# the files fa_fwd_pair_kernel is built and launched from
+PAIR_SOURCES = ("ptx.cuh", "fa_common.cuh", "fa_kernel.cuh", "fa_pair.cuh", "fa_fwd_pair.cu",
+                "fa_host.cu")
 
 
 def _code_only(text: str) -> str:
@@ -108,12 +111,13 @@ def _code_only(text: str) -> str:
     return "\n".join(lines)
 
 
-def kernel_source_sha256() -> str:
-    """Hash of the forward kernel's source code: a recorded DRAM traffic
-    figure holds only for the code it was measured on."""
+def kernel_source_sha256(pair: bool = False) -> str:
+    """Hash of a forward kernel's source code (the one-CTA kernel, or the
+    CTA-pair kernel): a recorded DRAM traffic figure holds only for the code
+    it was measured on."""
     from attention_forward_flashattention_gb300 import build as fabuild
     h = hashlib.sha256()
-    for name in sorted(FWD_SOURCES):
+    for name in sorted(PAIR_SOURCES if pair else FWD_SOURCES):
         with open(os.path.join(fabuild.CSRC, name), encoding="utf-8") as f:
             h.update(name.encode() + b"\0" + _code_only(f.read()).encode())
     return h.hexdigest()
@@ -121,22 +125,27 @@ def kernel_source_sha256() -> str:
 
 def recorded_traffic(workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources; else None."""
+    on the current sources of the kernel that runs `workload` (entries named
+    cta_pair:<workload> are the CTA-pair kernel's); else None. The file holds
+    blocks: a kernel_source_sha256 line, then workload / dram_bytes_per_launch
+    line pairs measured on those sources."""
     path = os.path.join(ROOT, "profiles", "fa_fwd_traffic.txt")
     try:
         lines = open(path).read().splitlines()
     except OSError:
         return None
-    kv = {}
+    want = kernel_source_sha256(pair=workload.startswith("cta_pair:"))
+    cur_hash, cur_wl = None, None
     for ln in lines:
-        if ":" in ln and not ln.lstrip().startswith("#"):
-            k, v = ln.split(":", 1)
-            kv.setdefault(k.strip(), []).append(v.strip())
-    if kv.get("kernel_source_sha256", [None])[0] != kernel_source_sha256():
-        return None
-    for wl, b in zip(kv.get("workload", []), kv.get("dram_bytes_per_launch", [])):
-        if wl == workload:
-            return int(float(b))
+        if ":" not in ln or ln.lstrip().startswith("#"):
+            continue
+        k, v = (x.strip() for x in ln.split(":", 1))
+        if k == "kernel_source_sha256":
+            cur_hash = v
+        elif k == "workload":
+            cur_wl = v
+        elif k == "dram_bytes_per_launch" and cur_wl == workload and cur_hash == want:
+            return int(float(v))
     return None
 
 
@@ -353,6 +362,7 @@ def forward_plan(fa, torch, w, dev, stream, x=None, pair=False) -> Plan:
     lh = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
     launch = fa.fa_query_launch(w.B, w.H, w.N, w.d, w.causal)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    pair_units = w.B * w.H * ((w.N + 511) // 512)   # the pair kernel's 512-row units
 
     def run(ins):
         if fp8:
@@ -392,8 +402,8 @@ def forward_plan(fa, torch, w, dev, stream, x=None, pair=False) -> Plan:
         d2h=o.numel() * o.element_size() + lse.numel() * 4,
         launches=1, peak_mult=2.0 if fp8 else 1.0, peak_note=peak_note,
         kernel="fa_fwd_pair_kernel" if pair else "fa_fwd_kernel",
-        launch_cfg=({"grid": 2 * min(launch["units"], sms // 2), "threads": launch["threads"],
-                     "cluster": 2, "units": launch["units"]} if pair else
+        launch_cfg=({"grid": 2 * min(pair_units, sms // 2), "threads": launch["threads"],
+                     "cluster": 2, "units": pair_units} if pair else
                     {"grid": launch["grid"], "threads": launch["threads"],
                      "smem_bytes": None if fp8 else launch["smem_bytes"],
                      "units": launch["units"]}),

@@ -87,15 +87,13 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
  * fa_fwd_pair - fa_fwd computed by pairs of CTAs on neighbouring SMs that
  * share each tensor-core product (tcgen05.mma cta_group::2, M = 256 query
  * rows): the CTA pair of "TMA + Warp Specialization" (CUDA book ch. 17),
- * section 17.9, item 3. Each SM holds 128 query rows and half of every K and
- * V tile; its tensor memory then has room for two S buffers and two P
- * buffers, so scores, weights and output products overlap without waiting
- * for one another's columns.
+ * section 17.9, item 3. Each SM holds two 128-row query tiles and loads and
+ * keeps only half of every K and V tile (64 keys of K, 64 columns of V); the
+ * per-tile arithmetic is fa_fwd's, and so are the results, bit for bit.
  *
  * Same arguments, layout, errors, asynchrony and status word as fa_fwd, but
- * d must be 128 (else FA_ERR_UNSUPPORTED). The result matches the same
- * tolerances as fa_fwd's (not bit for bit: the row sums are formed in
- * another order). Launches clusters of 2 CTAs, one per pair of SMs.
+ * d must be 128 (else FA_ERR_UNSUPPORTED). Launches clusters of 2 CTAs, one
+ * per pair of SMs, each unit 512 query rows of one (batch, head).
  */
 fa_status fa_fwd_pair(const void* q, const void* k, const void* v, void* o, float* lse,
                       int B, int H, int N, int d, int causal, float scale,
