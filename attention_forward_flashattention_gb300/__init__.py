@@ -95,7 +95,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                                          ctypes.POINTER(ctypes.c_ulonglong)]
         lib.fa_sm_clock_read.restype = i
         ip = ctypes.POINTER(ctypes.c_int)
-        lib.fa_query_launch.argtypes = [i, i, i, i, i, ip, ip, ip, ip]
+        lib.fa_query_launch.argtypes = [i, i, i, i, i, ip, ip, ip, ip, ip]
         lib.fa_query_launch.restype = i
         lib.fa_sm_clock_probe.argtypes = [vp, ctypes.c_longlong, vp]
         lib.fa_sm_clock_probe.restype = i
@@ -203,12 +203,14 @@ def fa_sm_clock_read(stream: int = 0) -> tuple[float, int]:
 
 
 def fa_query_launch(B: int, H: int, N: int, d: int, causal: bool = False) -> dict:
-    g, t, s, u = (ctypes.c_int(0) for _ in range(4))
+    g, t, s, u, c = (ctypes.c_int(0) for _ in range(5))
     rc = load_library().fa_query_launch(B, H, N, d, int(bool(causal)), ctypes.byref(g),
-                                        ctypes.byref(t), ctypes.byref(s), ctypes.byref(u))
+                                        ctypes.byref(t), ctypes.byref(s), ctypes.byref(u),
+                                        ctypes.byref(c))
     if rc != FA_OK:
         raise FaError(rc, "fa_query_launch")
-    return {"grid": g.value, "threads": t.value, "smem_bytes": s.value, "units": u.value}
+    return {"grid": g.value, "threads": t.value, "smem_bytes": s.value, "units": u.value,
+            "cluster": c.value}
 
 
 def fa_sm_clock_probe(out_ptr: int, cycles: int, stream: int = 0) -> int:

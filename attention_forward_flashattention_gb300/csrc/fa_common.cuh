@@ -169,6 +169,15 @@ __device__ __forceinline__ bool wait_cluster_warp(uint32_t bar, uint32_t parity,
   }
 }
 
+// Warp-uniform cluster-scope wait whose lanes suspend in hardware while the
+// phase is incomplete (for warps that share an SM sub-partition with busy
+// warps and usually wait long: polling would take their issue slots).
+__device__ __forceinline__ bool wait_cluster_warp_sleep(uint32_t bar, uint32_t parity,
+                                                        const AbortCtx& ab, uint32_t code) {
+  const bool ok = wait_cluster<true>(bar, parity, ab, code);
+  return __all_sync(0xffffffffu, ok) != 0;
+}
+
 // Warp-uniform variant: every lane polls; the warp proceeds only if all
 // lanes saw the phase complete.
 __device__ __forceinline__ bool wait_bounded_warp(uint32_t bar, uint32_t parity,

@@ -214,11 +214,16 @@ extern "C" {
 namespace {
 
 
+// Which forward kernel a call runs: fa_fwd and fa_fwd_strided choose (kAuto),
+// fa_fwd_pair asks for the CTA-pair kernel.
+enum class FwdChoice { kAuto, kPair };
+
 // fa_fwd, fa_fwd_strided and fa_fwd_pair: checks, tensor maps, plan, launch
-// (the pair kernels take head dimension 128 only).
+// (the pair kernel takes head dimension 128 only).
 fa_status fwd_call(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                    int N, int d, const fa_strides* s, int causal, float scale, fa_dtype dtype,
-                   void* stream, bool pair = false) {
+                   void* stream, FwdChoice choice = FwdChoice::kAuto) {
+  const bool want_pair = choice == FwdChoice::kPair;
   if (!q || !k || !v || !o || !lse || !s) return FA_ERR_INVALID_ARG;
   if (!fa::aligned16(q) || !fa::aligned16(k) || !fa::aligned16(v) || !fa::aligned16(o) ||
       !fa::aligned16(lse))
@@ -227,7 +232,7 @@ fa_status fwd_call(const void* q, const void* k, const void* v, void* o, float* 
   if (dtype != FA_DTYPE_FP16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
   const fa_status sz = fa::check_sizes(B, H, N, d);
   if (sz != FA_OK) return sz;
-  if (pair && d != 128) return FA_ERR_UNSUPPORTED;
+  if (want_pair && d != 128) return FA_ERR_UNSUPPORTED;
   const fa_status ss = fa::check_strides(s, d);
   if (ss != FA_OK) return ss;
 
@@ -238,6 +243,7 @@ fa_status fwd_call(const void* q, const void* k, const void* v, void* o, float* 
 
   const bool bf16 = dtype == FA_DTYPE_BF16;
   const long long BH = static_cast<long long>(B) * H;
+  const bool pair = want_pair || fa::fwd_prefers_pair(d, causal != 0, BH, N, st->sm_count);
   CUtensorMap maps[4];
   if (!fa::encode_fwd_maps(maps, q, k, v, o, s, bf16, B, H, N, d, pair ? 64 : 0))
     return FA_ERR_CUDA;
@@ -279,7 +285,8 @@ fa_status fa_fwd_pair(const void* q, const void* k, const void* v, void* o, floa
   if (d != 128) return FA_ERR_UNSUPPORTED;
   const fa_strides c = fa::contiguous_strides(H, N, d);
   const fa_strides s[4] = {c, c, c, c};
-  return fwd_call(q, k, v, o, lse, B, H, N, d, s, causal, scale, dtype, stream, true);
+  return fwd_call(q, k, v, o, lse, B, H, N, d, s, causal, scale, dtype, stream,
+                  FwdChoice::kPair);
 }
 
 fa_status fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B,
@@ -443,21 +450,27 @@ fa_status fa_sm_clock_read(void* stream, double* sm_mhz, unsigned long long* cta
 }
 
 fa_status fa_query_launch(int B, int H, int N, int d, int causal, int* grid, int* threads,
-                          int* smem_bytes, int* units) {
-  (void)causal;
+                          int* smem_bytes, int* units, int* cluster) {
   const fa_status sz = fa::check_sizes(B, H, N, d);
   if (sz != FA_OK) return sz;
   int dev = 0;
   fa::DeviceState* st = nullptr;
   const fa_status ds = fa::current_device(&dev, &st, false);
   if (ds != FA_OK) return ds;
+  const long long BH = static_cast<long long>(B) * H;
   fa::FwdArgs a{};
   int g = 0;
-  fa::plan_fwd(d, N, H, static_cast<long long>(B) * H, st->sm_count, &a, &g);
+  fa::plan_fwd(d, N, H, BH, st->sm_count, &a, &g);
+  const bool pair = fa::fwd_prefers_pair(d, causal != 0, BH, N, st->sm_count);
+  if (pair) {
+    a.n_units = static_cast<int>(BH * ((N + 511) / 512));
+    g = fa::fwd_grid_pair(a.n_units, st->sm_count);
+  }
   if (grid) *grid = g;
   if (threads) *threads = fa::kFwdThreads;
-  if (smem_bytes) *smem_bytes = fa::fwd_smem_bytes(d);
+  if (smem_bytes) *smem_bytes = pair ? fa::fwd_smem_bytes_pair() : fa::fwd_smem_bytes(d);
   if (units) *units = a.n_units;
+  if (cluster) *cluster = pair ? 2 : 1;
   return FA_OK;
 }
 

@@ -3,7 +3,8 @@
 //
 // fa_fwd keeps its status word (the scratch its kernel writes when a bounded
 // wait gives up) in device memory it allocates on its first call on a device.
-// This entry point runs the same kernel with that scratch taken from a
+// This entry point runs the one-CTA forward kernel (whose results fa_fwd's
+// kernels all reproduce bit for bit) with that scratch taken from a
 // statically sized device array of this library instead, so no call ever
 // allocates: no cudaMalloc, no cudaFree, no allocating library routine.
 #include <cuda.h>

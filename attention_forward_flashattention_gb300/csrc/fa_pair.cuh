@@ -64,33 +64,42 @@ __device__ __forceinline__ bool next_pair_unit(int& round, const FwdArgs& a, int
 }
 
 struct PairLayout {
-  static constexpr int kTileBytes = 2 * kPanelBytes;            // a Q tile (128 x 128)
+  static constexpr int kTileBytes = 2 * kPanelBytes;            // a Q or P tile (128 x 128)
   static constexpr int kSlotBytes = kPanelBytes;                // a K half or a V half
-  static constexpr int kStages = 8;
+  static constexpr int kKSlots = 2;                             // K ring (K_j, K_{j+1})
+  static constexpr int kVSlots = 3;                             // V ring
   static constexpr int kOffQ = 0;                               // Q0, Q1
-  static constexpr int kOffKV = 2 * kTileBytes;
-  static constexpr int kOffStats = kOffKV + kStages * kSlotBytes;  // [2 tiles][128] row sums
+  static constexpr int kOffP = 2 * kTileBytes;                  // P0, P1 (K-major SW128)
+  static constexpr int kOffK = 4 * kTileBytes;
+  static constexpr int kOffV = kOffK + kKSlots * kSlotBytes;
+  static constexpr int kOffStats = kOffV + kVSlots * kSlotBytes;  // [2 tiles][128] row sums
   static constexpr int kOffOut = kOffStats + 1024;
   static constexpr int kOutSliceBytes = 32 * 128;
   static constexpr int kOffBar = kOffOut + 4 * kOutSliceBytes;
   static constexpr int kSmemBytes = kOffBar + 512 + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  static_assert(kOffBar % 8 == 0, "barrier block alignment");
-  static constexpr uint32_t kColS = 0;    // S_i at 128 i (P_i over its first 64 columns)
+  static_assert(kOffBar % 8 == 0 && kOffOut % 1024 == 0, "alignment");
+  static constexpr uint32_t kColS = 0;    // S_i at 128 i
   static constexpr uint32_t kColO = 256;  // O_i at 256 + 128 i
 };
 
 enum PairBar : int {
   kQbQFull = 0,       // [2] even CTA: both CTAs' Q tile i landed
-  kQbQEmpty = 2,      // both: the unit's last S products done (multicast commit)
-  kQbSFull = 3,       // [2] both: S_i ready, O_i holds every earlier PV_i (multicast commit)
-  kQbPFull = 5,       // [2] even CTA: P_i written by the 8 softmax warps of tile i (pair)
-  kQbOFull = 7,       // [2] both: the unit's last PV_i done (multicast commit)
-  kQbOFree = 9,       // [2] even CTA: O_i read by the 8 epilogue warps of the pair
-  kQbStatsFull = 11,  // [2] local: 128 softmax threads wrote tile i's row sums
-  kQbStatsFree = 13,  // [2] local: 128 epilogue threads read them
-  kQbDrain = 15,      // even CTA: every product completed
-  kQbKVFull = 16,     // [stages] even CTA: both halves landed; then [stages] slot free (both)
+  kQbQEmpty = 2,      // both: the unit's last S products done (a commit per S warp)
+  kQbSFull = 3,       // [2] both: S_i ready (multicast commit)
+  kQbSFree = 5,       // [2] even CTA: S_i read by the 8 softmax warps of tile i (pair)
+  kQbPFull = 7,       // [2] even CTA: P_i in shared memory, O_i rescaled (8 warps, pair)
+  kQbPFree = 9,       // [2] both: PV_i done: P_i reusable, O_i updated (multicast commit)
+  kQbOFull = 11,      // [2] both: the unit's last PV_i done (multicast commit)
+  kQbOFree = 13,      // [2] even CTA: O_i read by the 8 epilogue warps of the pair
+  kQbStatsFull = 15,  // [2] local: 128 softmax threads wrote tile i's row sums
+  kQbStatsFree = 17,  // [2] local: 128 epilogue threads read them
+  kQbDrain = 19,      // [2] even CTA: every product of S warp w completed
+  kQbDrainPV = 21,    // even CTA: every PV product completed
+  kQbKFull = 22,      // [K slots] even CTA: both K halves landed
+  kQbKEmpty = 24,     // [K slots] both: K slot free (a commit per S warp)
+  kQbVFull = 26,      // [V slots] even CTA: both V halves landed
+  kQbVEmpty = 29,     // [V slots] both: V slot free (multicast commit)
 };
 
 // Units of 512 rows per pair (n_mblk = ceil(N / 512)): causal units visit KV
@@ -100,19 +109,21 @@ __device__ __forceinline__ int pair_kv_tiles(const FwdArgs& a, int mblk) {
   return CAUSAL ? min(4 * mblk + 4, a.n_kv) : a.n_kv;
 }
 
+// Loads, per unit: both Q tiles, then K_0, then K_{j+1} before V_j (the S
+// products of a tile need the next K while its softmax runs; V_j is needed
+// only when P_j is written), from two rings that release slots independently.
 template <bool CAUSAL>
 __device__ __forceinline__ void pair_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
-                                               const CUtensorMap* tm_v, const FwdArgs& a,
-                                               uint32_t sbase, uint32_t bars, uint32_t rank,
-                                               const AbortCtx& ab) {
+                                              const CUtensorMap* tm_v, const FwdArgs& a,
+                                              uint32_t sbase, uint32_t bars, uint32_t rank,
+                                              const AbortCtx& ab) {
   using L = PairLayout;
-  constexpr int S = L::kStages;
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
   auto lead = [&](int i) { return ptx::mapa_shared(bar(i), 0); };
   ptx::prefetch_tmap(tm_q);
   ptx::prefetch_tmap(tm_k);
   ptx::prefetch_tmap(tm_v);
-  uint32_t ring = 0, units = 0;
+  uint32_t kcnt = 0, vcnt = 0, units = 0;
   int round = 0, bh = 0, mblk = 0;
   bool ok = true;
   while (ok && next_pair_unit<CAUSAL>(round, a, bh, mblk)) {
@@ -127,29 +138,36 @@ __device__ __forceinline__ void pair_producer(const CUtensorMap* tm_q, const CUt
                               mblk * 512 + 256 * i + 128 * static_cast<int>(rank), hh, bb);
     }
     ++units;
-    for (int j = 0; j < nkv && ok; ++j) {
-      for (int t = 0; t < 2; ++t) {
-        const uint32_t s = ring % S, ph = (ring / S) & 1u;
-        if (!(ok = wait_cluster<false>(bar(kQbKVFull + S + s), ph ^ 1u, ab, kStatusProducer)))
-          break;
-        if (rank == 0) ptx::mbar_arrive_expect_tx(bar(kQbKVFull + s), 2 * L::kSlotBytes);
-        const uint32_t dst = sbase + L::kOffKV + s * L::kSlotBytes;
-        if (t == 0) {
-          for (int p = 0; p < 2; ++p)
-            ptx::tma_load_4d_pair(dst + p * (kPanelBytes / 2), tm_k, lead(kQbKVFull + s), 64 * p,
-                                  128 * j + 64 * static_cast<int>(rank), hh, bb);
-        } else {
-          ptx::tma_load_4d_pair(dst, tm_v, lead(kQbKVFull + s), 64 * static_cast<int>(rank),
-                                128 * j, hh, bb);
-        }
-        ++ring;
+    for (int j = 0; j <= nkv && ok; ++j) {
+      if (j < nkv) {  // K_j: keys 128 j + 64 rank .. +63
+        const uint32_t s = kcnt % L::kKSlots, ph = (kcnt / L::kKSlots) & 1u;
+        if (!(ok = wait_cluster<false>(bar(kQbKEmpty + s), ph ^ 1u, ab, kStatusProducer))) break;
+        if (rank == 0) ptx::mbar_arrive_expect_tx(bar(kQbKFull + s), 2 * L::kSlotBytes);
+        const uint32_t dst = sbase + L::kOffK + s * L::kSlotBytes;
+        for (int p = 0; p < 2; ++p)
+          ptx::tma_load_4d_pair(dst + p * (kPanelBytes / 2), tm_k, lead(kQbKFull + s), 64 * p,
+                                128 * j + 64 * static_cast<int>(rank), hh, bb);
+        ++kcnt;
+      }
+      if (j >= 1) {   // V_{j-1}: keys 128 (j - 1) .. +127, columns 64 rank .. +63
+        const uint32_t s = vcnt % L::kVSlots, ph = (vcnt / L::kVSlots) & 1u;
+        if (!(ok = wait_cluster<false>(bar(kQbVEmpty + s), ph ^ 1u, ab, kStatusProducer))) break;
+        if (rank == 0) ptx::mbar_arrive_expect_tx(bar(kQbVFull + s), 2 * L::kSlotBytes);
+        ptx::tma_load_4d_pair(sbase + L::kOffV + s * L::kSlotBytes, tm_v, lead(kQbVFull + s),
+                              64 * static_cast<int>(rank), 128 * (j - 1), hh, bb);
+        ++vcnt;
       }
     }
   }
   if (!ok && rank == 0) {
-    for (uint32_t s = 0; s < static_cast<uint32_t>(S) && s < ring; ++s) {
-      const uint32_t last = ring - 1 - ((ring - 1 - s) % S);
-      wait_drain(bar(kQbKVFull + s), (last / S) & 1u, ab, kStatusDrain);
+    // let the copies already issued (both CTAs' halves) land before exit
+    for (uint32_t s = 0; s < static_cast<uint32_t>(L::kKSlots) && s < kcnt; ++s) {
+      const uint32_t last = kcnt - 1 - ((kcnt - 1 - s) % L::kKSlots);
+      wait_drain(bar(kQbKFull + s), (last / L::kKSlots) & 1u, ab, kStatusDrain);
+    }
+    for (uint32_t s = 0; s < static_cast<uint32_t>(L::kVSlots) && s < vcnt; ++s) {
+      const uint32_t last = vcnt - 1 - ((vcnt - 1 - s) % L::kVSlots);
+      wait_drain(bar(kQbVFull + s), (last / L::kVSlots) & 1u, ab, kStatusDrain);
     }
     if (units > 0) {
       wait_drain(bar(kQbQFull + 0), (units - 1) & 1u, ab, kStatusDrain);
@@ -158,121 +176,125 @@ __device__ __forceinline__ void pair_producer(const CUtensorMap* tm_q, const CUt
   }
 }
 
-// Even CTA, whole warp: the one-CTA issue order with pair products:
-// S0(0), S1(0), then per KV tile j: PV0(j), S0(j+1), PV1(j), S1(j+1).
-template <bool BF16, bool CAUSAL>
-__device__ __forceinline__ void pair_mma(const FwdArgs& a, uint32_t sbase, uint32_t bars,
-                                          uint32_t tmem, const AbortCtx& ab) {
+// Even CTA: the products are issued by three warps (elected lane of each),
+// which need no ordering between them: S products write S_i, PV products read
+// P_i from shared memory and write O_i.
+//   S warp(s): S_i(j) = Q_i K_j^T once the softmax has read S_i(j - 1).
+//            Non-causal: one warp per tile, on different SM sub-partitions
+//            (each MMA issue takes issue slots from the softmax warps beside
+//            it, and the slowest softmax warp sets when P is complete);
+//            causal: one warp for both tiles (measured faster there).
+//   PV warp: O_i += P_i(j) V_j once P_i(j) is written (and the epilogue has
+//            drained O_i, at a unit's first tile).
+// K_j and V_j come from their own rings (global counters of the tiles loaded).
+// S warps of a kernel instance (each issues the tiles i0 .. i1 - 1).
+template <bool CAUSAL>
+__host__ __device__ constexpr int pair_s_warps() { return CAUSAL ? 1 : 2; }
+
+template <bool BF16, bool CAUSAL, int I0, int I1, int W>
+__device__ __forceinline__ void pair_mma_s(const FwdArgs& a, uint32_t sbase, uint32_t bars,
+                                           uint32_t tmem, const AbortCtx& ab) {
   using L = PairLayout;
-  constexpr int S = L::kStages;
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
   constexpr uint32_t kIdS = ptx::idesc_f16(BF16, false, 256, 128);
-  constexpr uint32_t kIdPV = ptx::idesc_f16(BF16, true, 256, 128);
-  const uint64_t dQ[2] = {desc_kmajor(sbase + L::kOffQ),
-                          desc_kmajor(sbase + L::kOffQ + L::kTileBytes)};
-  const uint64_t dK0 = desc_kmajor(sbase + L::kOffKV);
-  const uint64_t dV0 = desc_v(sbase + L::kOffKV);
-  const uint32_t tS[2] = {tmem + L::kColS, tmem + L::kColS + 128};
-  const uint32_t tO[2] = {tmem + L::kColO, tmem + L::kColO + 128};
-  auto slot_off = [](uint32_t idx) { return (idx % S) * static_cast<uint32_t>(L::kSlotBytes); };
-  auto kv_wait = [&](uint32_t idx) {
-    return wait_cluster_warp(bar(kQbKVFull + idx % S), (idx / S) & 1u, ab, kStatusMma);
-  };
-  auto qk = [&](int i, uint64_t dk) {
-    uint64_t q = dQ[i], k = dk;
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      ptx::umma_f16_ss_pair_elect(tS[i], q, k, kIdS, kk > 0 ? 1u : 0u);
-      const bool next_panel = (kk & 3) == 3;
-      q = desc_add(q, next_panel ? static_cast<uint32_t>(kPanelBytes - 96) : 32u);
-      k = desc_add(k, next_panel ? static_cast<uint32_t>(kPanelBytes / 2 - 96) : 32u);
-      asm volatile("" : "+l"(q), "+l"(k));
-    }
-  };
-  auto pv = [&](int i, uint64_t dv, bool acc) {
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      ptx::umma_f16_ts_pair_elect(tO[i], tS[i] + 8u * kk, dv, kIdPV, (acc || kk > 0) ? 1u : 0u);
-      dv = desc_add(dv, 2048u);
-      asm volatile("" : "+l"(dv));
-    }
-  };
-  uint32_t ring = 0, units = 0, pcnt[2] = {0u, 0u};
+  const uint64_t dQ0 = desc_kmajor(sbase + L::kOffQ);
+  const uint64_t dK0 = desc_kmajor(sbase + L::kOffK);
+  uint32_t units = 0, scnt = 0;  // scnt: K tiles used so far = S_i products issued (each tile)
   int round = 0, bh = 0, mblk = 0;
   bool ok = true;
   while (ok && next_pair_unit<CAUSAL>(round, a, bh, mblk)) {
     const int nkv = pair_kv_tiles<CAUSAL>(a, mblk);
-    ok = wait_cluster_warp(bar(kQbQFull + 0), units & 1u, ab, kStatusMma) &&
-         wait_cluster_warp(bar(kQbQFull + 1), units & 1u, ab, kStatusMma);
-    if (!ok) break;
-    const uint32_t k0 = ring++;
-    if (!(ok = kv_wait(k0))) break;
-    ptx::tc_fence_after();
-    {
-      const uint64_t dk = desc_add(dK0, slot_off(k0));
-      qk(0, dk);
-      ptx::umma_commit_pair_elect(bar(kQbSFull + 0), 3);
-      qk(1, dk);
-      ptx::umma_commit_pair_elect(bar(kQbSFull + 1), 3);
-      ptx::umma_commit_pair_elect(bar(kQbKVFull + S + k0 % S), 3);
-      if (nkv == 1) ptx::umma_commit_pair_elect(bar(kQbQEmpty), 3);
+#pragma unroll
+    for (int i = I0; i < I1; ++i)
+      ok = ok && wait_cluster_warp(bar(kQbQFull + i), units & 1u, ab, kStatusMma);
+    for (int j = 0; j < nkv && ok; ++j, ++scnt) {
+      const uint32_t ks = scnt % L::kKSlots;
+      if (!(ok = wait_cluster_warp(bar(kQbKFull + ks), (scnt / L::kKSlots) & 1u, ab, kStatusMma)))
+        break;
+#pragma unroll
+      for (int i = I0; i < I1; ++i) {
+        if (!ok) break;
+        // S_i(scnt) overwrites S_i(scnt - 1): read by the softmax?
+        if (scnt > 0 &&
+            !(ok = wait_cluster_warp(bar(kQbSFree + i), (scnt - 1) & 1u, ab, kStatusMma)))
+          break;
+        ptx::tc_fence_after();
+        uint64_t q = desc_add(dQ0, static_cast<uint32_t>(i) * L::kTileBytes);
+        uint64_t k = desc_add(dK0, ks * static_cast<uint32_t>(L::kSlotBytes));
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          ptx::umma_f16_ss_pair_elect(tmem + L::kColS + 128u * i, q, k, kIdS, kk > 0 ? 1u : 0u);
+          const bool next_panel = (kk & 3) == 3;
+          q = desc_add(q, next_panel ? static_cast<uint32_t>(kPanelBytes - 96) : 32u);
+          k = desc_add(k, next_panel ? static_cast<uint32_t>(kPanelBytes / 2 - 96) : 32u);
+          asm volatile("" : "+l"(q), "+l"(k));
+        }
+        ptx::umma_commit_pair_elect(bar(kQbSFull + i), 3);
+      }
+      if (!ok) break;
+      ptx::umma_commit_pair_elect(bar(kQbKEmpty + ks), 3);  // K_j consumed (by this warp's tiles)
+      if (j + 1 == nkv) ptx::umma_commit_pair_elect(bar(kQbQEmpty), 3);
     }
-    uint32_t rel_v = 0, rel_k = 0;
-    bool rel_pending = false;
-    for (int j = 0; j < nkv; ++j) {
-      const uint32_t vj = ring++;
-      if (!(ok = kv_wait(vj))) break;
-      const bool more = j + 1 < nkv;
-      const uint32_t kn = ring;
-      const uint64_t dv = desc_add(dV0, slot_off(vj));
-      const uint64_t dk = desc_add(dK0, slot_off(kn));
-      for (int i = 0; i < 2; ++i) {
-        if (!(ok = wait_cluster_warp(bar(kQbPFull + i), (pcnt[i]++) & 1u, ab, kStatusMma))) break;
+    ++units;
+  }
+  ptx::umma_commit_pair_elect(bar(kQbDrain + W), 1);
+  wait_drain(bar(kQbDrain + W), 0u, ab, kStatusDrain);
+}
+
+template <bool BF16, bool CAUSAL>
+__device__ __forceinline__ void pair_mma_pv(const FwdArgs& a, uint32_t sbase, uint32_t bars,
+                                            uint32_t tmem, const AbortCtx& ab) {
+  using L = PairLayout;
+  auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
+  constexpr uint32_t kIdPV = ptx::idesc_f16(BF16, true, 256, 128);
+  const uint64_t dP[2] = {desc_kmajor(sbase + L::kOffP),
+                          desc_kmajor(sbase + L::kOffP + L::kTileBytes)};
+  const uint64_t dV0 = desc_v(sbase + L::kOffV);
+  uint32_t units = 0, pcnt = 0;  // pcnt: V tiles used so far = P_i tiles consumed (each tile)
+  int round = 0, bh = 0, mblk = 0;
+  bool ok = true;
+  while (ok && next_pair_unit<CAUSAL>(round, a, bh, mblk)) {
+    const int nkv = pair_kv_tiles<CAUSAL>(a, mblk);
+    for (int j = 0; j < nkv && ok; ++j, ++pcnt) {
+      const uint32_t vs = pcnt % L::kVSlots;
+      if (!(ok = wait_cluster_warp(bar(kQbVFull + vs), (pcnt / L::kVSlots) & 1u, ab, kStatusMma)))
+        break;
+      for (int i = 0; i < 2 && ok; ++i) {
+        if (!(ok = wait_cluster_warp(bar(kQbPFull + i), pcnt & 1u, ab, kStatusMma))) break;
         if (j == 0 && units > 0 &&
             !(ok = wait_cluster_warp(bar(kQbOFree + i), (units - 1) & 1u, ab, kStatusMma)))
           break;
         ptx::tc_fence_after();
-        pv(i, dv, j > 0);
-        if (i == 0 && rel_pending) {
-          ptx::umma_commit_pair_elect(bar(kQbKVFull + S + rel_v % S), 3);
-          ptx::umma_commit_pair_elect(bar(kQbKVFull + S + rel_k % S), 3);
-          rel_pending = false;
+        uint64_t pd = dP[i], v = desc_add(dV0, vs * static_cast<uint32_t>(L::kSlotBytes));
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          ptx::umma_f16_ss_pair_elect(tmem + L::kColO + 128u * i, pd, v, kIdPV,
+                                      (j > 0 || kk > 0) ? 1u : 0u);
+          pd = desc_add(pd, (kk & 3) == 3 ? static_cast<uint32_t>(kPanelBytes - 96) : 32u);
+          v = desc_add(v, 2048u);
+          asm volatile("" : "+l"(pd), "+l"(v));
         }
-        if (!more) {
-          if (i == 1) ptx::umma_commit_pair_elect(bar(kQbKVFull + S + vj % S), 3);
-          ptx::umma_commit_pair_elect(bar(kQbOFull + i), 3);
-          continue;
-        }
-        if (i == 0 && !(ok = kv_wait(kn))) break;
-        qk(i, dk);
-        ptx::umma_commit_pair_elect(bar(kQbSFull + i), 3);
-        if (i == 1) {
-          rel_v = vj;
-          rel_k = kn;
-          rel_pending = true;
-          if (j + 2 == nkv) ptx::umma_commit_pair_elect(bar(kQbQEmpty), 3);
-        }
+        ptx::umma_commit_pair_elect(bar(kQbPFree + i), 3);
+        if (j + 1 == nkv) ptx::umma_commit_pair_elect(bar(kQbOFull + i), 3);
       }
       if (!ok) break;
-      if (more) ++ring;
-    }
-    if (rel_pending) {
-      ptx::umma_commit_pair_elect(bar(kQbKVFull + S + rel_v % S), 3);
-      ptx::umma_commit_pair_elect(bar(kQbKVFull + S + rel_k % S), 3);
+      ptx::umma_commit_pair_elect(bar(kQbVEmpty + vs), 3);  // V_j consumed
     }
     ++units;
   }
-  ptx::umma_commit_pair_elect(bar(kQbDrain), 1);
-  wait_drain(bar(kQbDrain), 0u, ab, kStatusDrain);
+  ptx::umma_commit_pair_elect(bar(kQbDrainPV), 1);
+  wait_drain(bar(kQbDrainPV), 0u, ab, kStatusDrain);
 }
 
 // Softmax of tile i (warpgroup 1 + i) of this CTA: the one-CTA kernel's
-// per-tile softmax (d = 128, 16-bit), with the P-full arrival sent to the
+// per-tile softmax (d = 128, 16-bit), with S released as soon as it is in
+// registers, P written to shared memory (K-major, 128-byte swizzle: the A
+// operand of the PV product), and the S-read / P-written arrivals sent to the
 // even CTA (one per warp).
 template <bool BF16, bool CAUSAL>
-__device__ __forceinline__ void pair_softmax(const FwdArgs& a, uint32_t bars, uint32_t tmem,
-                                              float* stats, uint32_t rank, const AbortCtx& ab,
-                                              int warp, int lane) {
+__device__ __forceinline__ void pair_softmax(const FwdArgs& a, uint32_t sbase, uint32_t bars,
+                                             uint32_t tmem, float* stats, uint32_t rank,
+                                             const AbortCtx& ab, int warp, int lane) {
   using L = PairLayout;
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
   const int wg = (warp >> 2) - 1;
@@ -281,6 +303,8 @@ __device__ __forceinline__ void pair_softmax(const FwdArgs& a, uint32_t bars, ui
   const uint32_t tS = tl + L::kColS + 128u * wg;
   const uint32_t tO = tl + L::kColO + 128u * wg;
   const uint32_t lead_pfull = ptx::mapa_shared(bar(kQbPFull + wg), 0);
+  const uint32_t lead_sfree = ptx::mapa_shared(bar(kQbSFree + wg), 0);
+  const uint32_t sP = sbase + L::kOffP + static_cast<uint32_t>(wg) * L::kTileBytes;
   const float cl2 = a.scale_log2;
   const float2 c2 = make_float2(cl2, cl2);
   uint32_t scnt = 0, units = 0;
@@ -300,6 +324,9 @@ __device__ __forceinline__ void pair_softmax(const FwdArgs& a, uint32_t bars, ui
       ptx::tmem_ld64(tS, sr[0]);
       ptx::tmem_ld64(tS + 64u, sr[1]);
       ptx::tmem_ld_wait64x2(sr[0], sr[1]);
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(lead_sfree);  // S_i may be overwritten
       float s[128];
 #pragma unroll
       for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 6][(c >> 5) & 1][c & 31]);
@@ -333,21 +360,25 @@ __device__ __forceinline__ void pair_softmax(const FwdArgs& a, uint32_t bars, ui
       float2 ls[4], lr[4];
 #pragma unroll
       for (int t = 0; t < 4; ++t) ls[t] = lr[t] = make_float2(0.f, 0.f);
-      uint32_t pk[2][32];
+      uint32_t pk[64];
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
         const float2 t = ptx::ffma2(make_float2(s[2 * c], s[2 * c + 1]), c2, neg2);
         const float p0 = ptx::ex2(t.x), p1 = ptx::ex2(t.y);
         const uint32_t w = pack2<BF16>(p0, p1);
-        pk[c >> 5][c & 31] = w;
+        pk[c] = w;
         ls[c & 3] = ptx::fadd2(ls[c & 3], make_float2(p0, p1));
         if constexpr (BF16) {
           lr[c & 3].x = ptx::add_f32_bf16_lo(lr[c & 3].x, w);
           lr[c & 3].y = ptx::add_f32_bf16_hi(lr[c & 3].y, w);
         }
       }
-      ptx::tmem_st32(tS, pk[0]);
-      ptx::tmem_st32(tS + 32u, pk[1]);
+      // PV_i of the previous tile done: P_i reusable, O_i updated
+      if (scnt > 1 &&
+          !(ok = wait_cluster_warp(bar(kQbPFree + wg), (scnt - 2) & 1u, ab, kStatusSoftmax)))
+        break;
+      ptx::tc_fence_after();
+      store_row128_sw128(sP, r, pk);
       const float2 s01 = ptx::fadd2(ptx::fadd2(ls[0], ls[1]), ptx::fadd2(ls[2], ls[3]));
       const float lsum = s01.x + s01.y;
       float lsum_p = lsum;
@@ -355,7 +386,7 @@ __device__ __forceinline__ void pair_softmax(const FwdArgs& a, uint32_t bars, ui
         const float2 r01 = ptx::fadd2(ptx::fadd2(lr[0], lr[1]), ptx::fadd2(lr[2], lr[3]));
         lsum_p = r01.x + r01.y;
       }
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {  // O_i holds PV_i(j - 1)
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {  // O_i holds PV_i(j - 1) (P-free)
         const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -372,6 +403,7 @@ __device__ __forceinline__ void pair_softmax(const FwdArgs& a, uint32_t bars, ui
           ptx::tmem_st32(tO + 32u * c, o);
         }
       }
+      ptx::fence_proxy_async_smem();  // P visible to the tensor core's reads
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       __syncwarp();
@@ -485,17 +517,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFwdThreads, 1)
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(bar(kQbQFull + i), 1);
       ptx::mbar_init(bar(kQbSFull + i), 1);
-      ptx::mbar_init(bar(kQbPFull + i), 8);      // 4 softmax warps of tile i in each CTA
+      ptx::mbar_init(bar(kQbSFree + i), 8);      // 4 softmax warps of tile i in each CTA
+      ptx::mbar_init(bar(kQbPFull + i), 8);
+      ptx::mbar_init(bar(kQbPFree + i), 1);
       ptx::mbar_init(bar(kQbOFull + i), 1);
       ptx::mbar_init(bar(kQbOFree + i), 8);      // 4 epilogue warps in each CTA
       ptx::mbar_init(bar(kQbStatsFull + i), 128);
       ptx::mbar_init(bar(kQbStatsFree + i), 128);
     }
-    ptx::mbar_init(bar(kQbQEmpty), 1);
-    ptx::mbar_init(bar(kQbDrain), 1);
-    for (int s = 0; s < L::kStages; ++s) {
-      ptx::mbar_init(bar(kQbKVFull + s), 1);
-      ptx::mbar_init(bar(kQbKVFull + L::kStages + s), 1);
+    ptx::mbar_init(bar(kQbQEmpty), pair_s_warps<CAUSAL>());
+    ptx::mbar_init(bar(kQbDrain + 0), 1);
+    ptx::mbar_init(bar(kQbDrain + 1), 1);
+    ptx::mbar_init(bar(kQbDrainPV), 1);
+    for (int s = 0; s < L::kKSlots; ++s) {
+      ptx::mbar_init(bar(kQbKFull + s), 1);
+      ptx::mbar_init(bar(kQbKEmpty + s), pair_s_warps<CAUSAL>());
+    }
+    for (int s = 0; s < L::kVSlots; ++s) {
+      ptx::mbar_init(bar(kQbVFull + s), 1);
+      ptx::mbar_init(bar(kQbVEmpty + s), 1);
     }
     *abort_flag = 0u;
     ptx::fence_mbar_init();
@@ -513,12 +553,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFwdThreads, 1)
     ptx::setmaxnreg_dec<kRegsWG0>();
     if (warp == 0) {
       if (lane == 0) pair_producer<CAUSAL>(&tm_q, &tm_k, &tm_v, a, sbase, bars, rank, ab);
-    } else if (warp == 1 && rank == 0) {
-      pair_mma<BF16, CAUSAL>(a, sbase, bars, tmem, ab);
+    } else if (warp == 2 && rank == 0) {
+      if constexpr (pair_s_warps<CAUSAL>() == 2)  // tile 1 (tile 0: warp 1)
+        pair_mma_s<BF16, CAUSAL, 1, 2, 1>(a, sbase, bars, tmem, ab);
+      else  // both tiles
+        pair_mma_s<BF16, CAUSAL, 0, 2, 0>(a, sbase, bars, tmem, ab);
+    } else if (warp == 1 && rank == 0 && pair_s_warps<CAUSAL>() == 2) {
+      pair_mma_s<BF16, CAUSAL, 0, 1, 0>(a, sbase, bars, tmem, ab);
+    } else if (warp == 3 && rank == 0) {
+      pair_mma_pv<BF16, CAUSAL>(a, sbase, bars, tmem, ab);
     }
   } else if (wgrp < 3) {
     ptx::setmaxnreg_inc<kRegsSoftmax>();
-    pair_softmax<BF16, CAUSAL>(a, bars, tmem, stats, rank, ab, warp, lane);
+    pair_softmax<BF16, CAUSAL>(a, sbase, bars, tmem, stats, rank, ab, warp, lane);
   } else {
     ptx::setmaxnreg_dec<kRegsEpilogue>();
     pair_epilogue<BF16, CAUSAL>(&tm_o, a, sbase, bars, tmem, stats, rank, ab, warp, lane);
@@ -537,6 +584,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFwdThreads, 1)
 cudaError_t launch_fwd_pair(bool bf16, bool causal, const CUtensorMap* maps, const FwdArgs& a,
                             int grid, cudaStream_t stream);
 int fwd_smem_bytes_pair();
+// Whether fa_fwd / fa_fwd_strided run the pair kernel: head dimension 128,
+// non-causal, and enough 512-row units to give every SM pair one. (Same-box
+// measurements: non-causal B4 H16 N4096 ~6 % faster than the one-CTA kernel;
+// causal shapes as fast or slower, their 512-row units masking more KV tiles.)
+// The two kernels' results are identical bit for bit.
+inline bool fwd_prefers_pair(int d, bool causal, long long BH, int N, int sm_count) {
+  return d == 128 && !causal && BH * ((static_cast<long long>(N) + 511) / 512) >= sm_count / 2;
+}
+
 // Grid of the pair kernel for n_units units: two CTAs per pair, one pair per
 // two SMs at most.
 inline int fwd_grid_pair(int n_units, int sm_count) {

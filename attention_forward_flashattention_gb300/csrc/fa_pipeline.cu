@@ -106,7 +106,7 @@ fa_status fa_fwd_host(const void* q, const void* k, const void* v, void* o, floa
   if (workspace_size < need) return FA_ERR_INVALID_ARG;
   // the per-chunk forwards see B = 1, H = heads of the chunk: check the whole
   // problem once here, with the forward's own rules, before enqueuing anything
-  fa_status st = fa_query_launch(B, H, N, d, causal, nullptr, nullptr, nullptr, nullptr);
+  fa_status st = fa_query_launch(B, H, N, d, causal, nullptr, nullptr, nullptr, nullptr, nullptr);
   if (st != FA_OK) return st;
 
   int dev = 0, sms = 0;

@@ -343,8 +343,10 @@ class Plan:
         self.__dict__.update(kw)
 
 
-def forward_plan(fa, torch, w, dev, stream, x=None, pair=False) -> Plan:
-    """pair: time the CTA-pair kernel (fa_fwd_pair) instead of fa_fwd."""
+def forward_plan(fa, torch, w, dev, stream, x=None, kernel="auto") -> Plan:
+    """kernel: "auto" times fa_fwd (which picks the one-CTA or the CTA-pair
+    kernel), "pair" fa_fwd_pair, "one_cta" the one-CTA kernel alone (through
+    fa_fwd_noalloc, which always runs it)."""
     fp8 = w.dtype == "e4m3"
     x = workload_inputs(w) if x is None else x
     if fp8:
@@ -363,14 +365,25 @@ def forward_plan(fa, torch, w, dev, stream, x=None, pair=False) -> Plan:
     launch = fa.fa_query_launch(w.B, w.H, w.N, w.d, w.causal)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     pair_units = w.B * w.H * ((w.N + 511) // 512)   # the pair kernel's 512-row units
+    one_units = w.B * w.H * ((w.N + 255) // 256)    # the one-CTA kernel's 256-row units
+    pair = kernel == "pair" or (kernel == "auto" and not fp8 and launch["cluster"] == 2)
+
+    code = fa.FA_DTYPE_BF16 if w.dtype == "bf16" else fa.FA_DTYPE_FP16
+    sh = int(stream.cuda_stream)
 
     def run(ins):
         if fp8:
             fa.attention_forward_fp8_into(ins[0], ins[1], ins[2], o, lse, x.q_scale, ins[3],
                                           x.v_scale, w.causal, w.scale, stream)
-        elif pair:
+        elif kernel == "pair":
             fa.attention_forward_pair_into(ins[0], ins[1], ins[2], o, lse, w.causal, w.scale,
                                            stream)
+        elif kernel == "one_cta":
+            rc = fa.fa_fwd_noalloc(ins[0].data_ptr(), ins[1].data_ptr(), ins[2].data_ptr(),
+                                   o.data_ptr(), lse.data_ptr(), w.B, w.H, w.N, w.d, w.causal,
+                                   w.scale, code, sh)
+            if rc != fa.FA_OK:
+                raise fa.FaError(rc, "fa_fwd_noalloc")
         else:
             fa.attention_forward_into(ins[0], ins[1], ins[2], o, lse, w.causal, w.scale, stream)
 
@@ -401,9 +414,12 @@ def forward_plan(fa, torch, w, dev, stream, x=None, pair=False) -> Plan:
         h2d=sum(h.numel() * h.element_size() for h in host),
         d2h=o.numel() * o.element_size() + lse.numel() * 4,
         launches=1, peak_mult=2.0 if fp8 else 1.0, peak_note=peak_note,
-        kernel="fa_fwd_pair_kernel" if pair else "fa_fwd_kernel",
+        kernel=("fa_fwd_pair_kernel" if pair else "fa_fwd_kernel")
+               + (" (fa_fwd's choice)" if kernel == "auto" and not fp8 else ""),
         launch_cfg=({"grid": 2 * min(pair_units, sms // 2), "threads": launch["threads"],
                      "cluster": 2, "units": pair_units} if pair else
+                    {"grid": min(one_units, sms), "threads": launch["threads"],
+                     "units": one_units} if launch["cluster"] == 2 else
                     {"grid": launch["grid"], "threads": launch["threads"],
                      "smem_bytes": None if fp8 else launch["smem_bytes"],
                      "units": launch["units"]}),
@@ -528,18 +544,26 @@ def clock_corrected_frac(tflops: float, dtype: str, sms: int, mhz) -> float | No
     return tflops * 1e12 / (sms * TENSOR_FLOP_PER_CLK_SM[dtype] * mhz * 1e6)
 
 
-PAIR_PREFIX = "cta_pair:"   # other_workloads key of the CTA-pair kernel on a workload
+PAIR_PREFIX = "cta_pair:"   # other_workloads key: the CTA-pair kernel on a workload
+ONE_PREFIX = "one_cta:"     # other_workloads key: the one-CTA kernel on a workload
 
 
 def other_workload_names(headline: str, pass_: str) -> list[str]:
-    """Every other named workload; in the forward pass also the 8-bit shapes and
-    the CTA-pair kernel on every head-dimension-128 16-bit workload (the
-    headline's included), so the two kernels are timed in the same run."""
+    """Every other named workload; in the forward pass also the 8-bit shapes
+    and, on every head-dimension-128 16-bit workload (the headline's
+    included), the kernel fa_fwd does not pick there (the CTA-pair kernel on
+    causal ones, the one-CTA kernel on the others), so both kernels are timed
+    in the same run."""
     names = [n for n in I.WORKLOAD_ORDER if n != headline]
     if pass_ == "forward":
         names += [n for n in I.FP8_WORKLOADS if n != headline]
-        names += [PAIR_PREFIX + n for n in I.WORKLOAD_ORDER if I.WORKLOADS[n].d == 128]
+        names += [(PAIR_PREFIX if I.WORKLOADS[n].causal else ONE_PREFIX) + n
+                  for n in I.WORKLOAD_ORDER if I.WORKLOADS[n].d == 128]
     return names
+
+
+def _base_name(name: str) -> str:
+    return name.removeprefix(PAIR_PREFIX).removeprefix(ONE_PREFIX)
 
 
 def run_ours(args, rank: int, world: int, local_rank: int):
@@ -555,8 +579,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     if others:
         pool = cf.ProcessPoolExecutor(max_workers=min(len(others), max(1, os.cpu_count() or 1)),
                                       mp_context=mp.get_context("spawn"))
-        futures = {n: pool.submit(_gen_inputs, n.removeprefix(PAIR_PREFIX)) for n in others
-                   if not (n.startswith(PAIR_PREFIX) and n.removeprefix(PAIR_PREFIX) == args.workload)}
+        futures = {n: pool.submit(_gen_inputs, _base_name(n)) for n in others
+                   if _base_name(n) != args.workload}
 
     import torch
 
@@ -574,7 +598,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     if args.kernel == "pair":
         if args.pass_ != "forward" or w.dtype == "e4m3" or w.d != 128:
             raise SystemExit("--kernel pair takes a 16-bit head-dimension-128 forward workload")
-        plan = forward_plan(fa, torch, w, dev, stream, pair=True)
+        plan = forward_plan(fa, torch, w, dev, stream, kernel="pair")
     else:
         plan = make(fa, torch, w, dev, stream)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
@@ -613,7 +637,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     other = {}
     head_inputs = None
     for name in others:
-        base = name.removeprefix(PAIR_PREFIX)
+        base = _base_name(name)
         ow = get_workload(base)
         if name in futures:
             x = futures[name].result()
@@ -621,7 +645,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             head_inputs = head_inputs if head_inputs is not None else workload_inputs(ow)
             x = head_inputs
         if name.startswith(PAIR_PREFIX):
-            oplan = forward_plan(fa, torch, ow, dev, stream, x=x, pair=True)
+            oplan = forward_plan(fa, torch, ow, dev, stream, x=x, kernel="pair")
+        elif name.startswith(ONE_PREFIX):
+            oplan = forward_plan(fa, torch, ow, dev, stream, x=x, kernel="one_cta")
         else:
             oplan = make(fa, torch, ow, dev, stream, x=x)
         ot = time_steps(fa, torch, oplan, stream, dev, flush, args.steps, args.warmup, world)

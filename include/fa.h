@@ -74,6 +74,8 @@ typedef struct fa_strides {
  * Asynchronous: returns after the launch is enqueued; O and LSE are valid
  * once the stream reaches that point. Arguments are checked before anything
  * is enqueued; on any error nothing is launched and nothing is written.
+ * Head dimension 128 without a causal mask runs on CTA pairs when the problem
+ * fills the GPU (see fa_query_launch); the results do not depend on it.
  * The first call on a device allocates a small device status word for that
  * device (kept until process exit); later calls allocate nothing.
  * A kernel whose internal waits run past their limit stops early and records
@@ -202,7 +204,8 @@ fa_status fa_bwd_workspace_size(int B, int H, int N, int d, size_t* bytes);
  * not call cudaMalloc / cudaFree at all once running (both can synchronise the
  * device). fa_fwd allocates a small status word on its first call on a
  * device; this entry point never allocates: it takes the same arguments and
- * runs the same kernel, with its scratch (one status word per launch) in a
+ * always runs the one-CTA kernel (fa_fwd's results bit for bit, whichever
+ * kernel fa_fwd picks), with its scratch (one status word per launch) in a
  * fixed 256-byte array inside this library that every device loading the
  * library holds until process exit. The scratch need does not grow with the
  * problem, so the size limits are fa_fwd's: larger sizes return
@@ -291,11 +294,15 @@ fa_status fa_sm_clock_read(void* stream, double* sm_mhz, unsigned long long* cta
 /*
  * fa_query_launch - launch shape fa_fwd would use on the current device for
  * these sizes: grid (persistent CTAs), threads per CTA, dynamic shared memory
- * bytes per CTA, and the number of 256-row work units. Any output pointer may
- * be NULL. Host memory only; enqueues nothing.
+ * bytes per CTA, the number of work units (256 query rows of one head, or 512
+ * for the CTA-pair kernel) and the cluster size (1: one CTA per unit; 2: the
+ * CTA-pair kernel, which fa_fwd runs for head dimension 128 without a causal
+ * mask when there are at least as many 512-row units as SM pairs; its results
+ * are the one-CTA kernel's bit for bit). Any output pointer may be NULL. Host
+ * memory only; enqueues nothing.
  */
 fa_status fa_query_launch(int B, int H, int N, int d, int causal, int* grid, int* threads,
-                          int* smem_bytes, int* units);
+                          int* smem_bytes, int* units, int* cluster);
 
 /*
  * fa_sm_clock_probe - measure the SM clock: one CTA spins for `cycles`

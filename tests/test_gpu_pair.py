@@ -1,8 +1,9 @@
 """Parity of the CTA-pair forward (fa_fwd_pair: tcgen05.mma cta_group::2,
 M = 256 rows shared by two SMs, head dimension 128) with the fp64 oracle,
 under the same bounds as the one-CTA kernel (parity_util.compare), and with
-fa_fwd bit for bit (the per-tile arithmetic is the same; a pair product gives
-the fp32 sums of two one-CTA products):
+the one-CTA kernel bit for bit (the per-tile arithmetic is the same; a pair
+product gives the fp32 sums of two one-CTA products; fa_fwd itself runs the
+pair kernel for large non-causal head-dimension-128 problems):
 
 * small problems: ragged N (1, 17, 129, 300, 1000), causal and not, fp16 and
   bf16, more units than pairs, a second row block past N; every element;
@@ -149,9 +150,16 @@ def test_pair_bitwise_equal_to_one_cta_kernel(B, H, N, dtype, causal):
     o1, l1 = run_pair(q, k, v, w.dtype, causal, w.scale)
     o2, l2 = run_pair(q, k, v, w.dtype, causal, w.scale)
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)          # deterministic
+    # the one-CTA kernel (fa_fwd_noalloc always runs it; fa_fwd may pick the pair)
     qd, kd, vd = (to_device(x, w.dtype) for x in (q, k, v))
-    o, lse = fa.attention_forward(qd, kd, vd, causal=causal, scale=w.scale)
+    o = torch.full_like(qd, float("nan"))
+    lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device="cuda:0")
+    code = fa.FA_DTYPE_BF16 if dtype == "bf16" else fa.FA_DTYPE_FP16
+    assert fa.fa_fwd_noalloc(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(),
+                             lse.data_ptr(), B, H, N, 128, causal, w.scale, code,
+                             int(torch.cuda.current_stream().cuda_stream)) == fa.FA_OK
     torch.cuda.synchronize()
+    assert fa.fa_check(0) == fa.FA_OK
     assert np.array_equal(to_bits(o), o1)
     assert np.array_equal(lse.cpu().numpy().view(np.uint32), l1.view(np.uint32))
 

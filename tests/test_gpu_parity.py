@@ -233,11 +233,19 @@ def test_rejects_unsupported_head_dim_on_gpu():
 def test_query_launch_is_persistent():
     import torch
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    for (B, H, N, d) in ((4, 16, 4096, 128), (2, 32, 8192, 64), (1, 1, 300, 128)):
-        info = fa.fa_query_launch(B, H, N, d)
-        assert info["units"] == B * H * ((N + 255) // 256)
-        assert info["grid"] == min(sms, info["units"])
+    for (B, H, N, d, causal) in ((4, 16, 4096, 128, True), (2, 32, 8192, 64, False),
+                                 (1, 1, 300, 128, False), (4, 16, 4096, 128, False)):
+        info = fa.fa_query_launch(B, H, N, d, causal)
+        pair = d == 128 and not causal and B * H * ((N + 511) // 512) >= sms // 2
+        assert info["cluster"] == (2 if pair else 1)
+        if pair:   # CTA pairs over 512-row units
+            assert info["units"] == B * H * ((N + 511) // 512)
+            assert info["grid"] == 2 * min(sms // 2, info["units"])
+        else:
+            assert info["units"] == B * H * ((N + 255) // 256)
+            assert info["grid"] == min(sms, info["units"])
         assert info["threads"] == 512 and info["smem_bytes"] <= 232448
+    assert fa.fa_query_launch(4, 16, 4096, 128, False)["cluster"] == 2
 
 
 # ------------------------------------------------------------ strided views (fa_fwd_strided)
