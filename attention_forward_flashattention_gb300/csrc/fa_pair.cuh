@@ -6,25 +6,33 @@
 // Work unit: 512 query rows of one (batch, head). Each CTA of the pair holds
 // two 128-row Q tiles (tile i of CTA r: rows 512 m + 256 i + 128 r), and tile
 // i of both CTAs forms one M = 256 product: each CTA supplies its own 128 rows
-// of the A operand (Q, or P from its tensor memory) and HALF of the B operand
-// (64 of the 128 keys of a K tile, 64 of the 128 columns of a V tile), and
-// receives its 128 rows of the result in its own tensor memory. So each SM
-// loads and holds only half of every K / V tile (16 KB ring slots), while the
-// per-SM schedule is the one-CTA kernel's: tensor memory S0, S1, O0, O1 with
-// P_i over the first 64 columns of S_i, the two tiles ping-ponging on the
-// tensor core (softmax of one tile while the other's products run).
+// of the A operand (Q, or P) and HALF of the B operand (64 of the 128 keys of
+// a K tile, 64 of the 128 columns of a V tile), and receives its 128 rows of
+// the result in its own tensor memory. So each SM loads and holds only half of
+// every K / V tile (16 KB ring slots: a K ring and a V ring of their own, so a
+// K half is refilled while the previous V half is still in use), and the two
+// tiles ping-pong on the tensor core as in the one-CTA kernel: the softmax of
+// one tile runs while the other's products run. Tensor memory holds S0, S1
+// (columns 0-255) and O0, O1 (256-511); the softmax writes P_i as bf16/fp16 to
+// shared memory in the layout the products read (128-byte swizzled, K-major),
+// and the PV products take both operands from shared memory.
 //
 // Warp roles (16 warps), the same in both CTAs unless noted:
-//   warp 0 (one lane): TMA producer: its two Q tiles, then per KV tile its K
-//           half and V half, the bytes counted on the EVEN CTA's barriers;
-//   warp 1: TMEM owner; in the even CTA the MMA issuer (whole warp, elected
-//           lane) of every pair product and commit;
+//   warp 0 (one lane): TMA producer: its two Q tiles, then per KV step its K
+//           half of tile j and its V half of tile j-1, the bytes counted on the
+//           EVEN CTA's barriers;
+//   warps 1-3, even CTA only (whole warp, elected lane): the S products
+//           (non-causal: warp 1 tile 0, warp 2 tile 1; causal: warp 2 both) and
+//           the PV products (warp 3), with their commits; warp 1 also owns the
+//           tensor memory in both CTAs;
 //   warps 4-7 / 8-11: softmax of tile 0 / tile 1 of this CTA (one thread per
 //           row; the one-CTA kernel's per-tile softmax);
 //   warps 12-15: epilogue (O / l by TMA store of the CTA's rows).
-// Barriers that collect arrivals from both CTAs (TMA bytes, P written, O
-// drained) live in the even CTA; products signal both CTAs by multicast
-// commits. Every wait is bounded (1 s), as in the one-CTA kernel.
+// Barriers that collect arrivals from both CTAs (TMA bytes, S read, P written,
+// O drained) live in the even CTA; products signal both CTAs by multicast
+// commits. Every wait is bounded (1 s), as in the one-CTA kernel. The
+// arithmetic of every output element is the one-CTA kernel's, so the two
+// kernels' results are identical bit for bit.
 #pragma once
 
 #include <cuda.h>

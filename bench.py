@@ -76,9 +76,10 @@ def parse_args():
                    help="untimed loaded seconds before the timed steps (clock samples)")
     p.add_argument("--other-workloads", default="all", choices=["all", "none"],
                    help="also time every other named workload (same steps, warm-up, flush)")
-    p.add_argument("--kernel", default="one-cta", choices=["one-cta", "pair"],
-                   help="forward kernel of the headline: fa_fwd (one CTA per tile pair) or "
-                        "fa_fwd_pair (CTA pairs, head dimension 128)")
+    p.add_argument("--kernel", default="auto", choices=["auto", "one-cta", "pair"],
+                   help="forward kernel of the headline: fa_fwd's own choice (auto), the "
+                        "one-CTA kernel alone (through fa_fwd_noalloc) or fa_fwd_pair "
+                        "(CTA pairs, head dimension 128)")
     return p.parse_args()
 
 
@@ -98,6 +99,10 @@ FWD_SOURCES = ("ptx.cuh", "fa_common.cuh", "fa_kernel.cuh", "fa_launch.cuh", "fa
 # the files fa_fwd_pair_kernel is built and launched from
 PAIR_SOURCES = ("ptx.cuh", "fa_common.cuh", "fa_kernel.cuh", "fa_pair.cuh", "fa_fwd_pair.cu",
                 "fa_host.cu")
+# the files the e4m3 instance of fa_fwd_kernel is built and launched from
+FP8_SOURCES = ("ptx.cuh", "fa_common.cuh", "fa_kernel.cuh", "fa_launch.cuh", "fa_fwd_fp8.cu",
+               "fa_host.cu")
+KERNEL_SOURCES = {"one_cta": FWD_SOURCES, "pair": PAIR_SOURCES, "fp8": FP8_SOURCES}
 
 
 def _code_only(text: str) -> str:
@@ -111,13 +116,13 @@ def _code_only(text: str) -> str:
     return "\n".join(lines)
 
 
-def kernel_source_sha256(pair: bool = False) -> str:
-    """Hash of a forward kernel's source code (the one-CTA kernel, or the
-    CTA-pair kernel): a recorded DRAM traffic figure holds only for the code
-    it was measured on."""
+def kernel_source_sha256(kind: str = "one_cta") -> str:
+    """Hash of a forward kernel's source code (kind: the 16-bit one-CTA
+    kernel, the CTA-pair kernel or the e4m3 kernel): a recorded DRAM traffic
+    figure holds only for the code it was measured on."""
     from attention_forward_flashattention_gb300 import build as fabuild
     h = hashlib.sha256()
-    for name in sorted(PAIR_SOURCES if pair else FWD_SOURCES):
+    for name in sorted(KERNEL_SOURCES[kind]):
         with open(os.path.join(fabuild.CSRC, name), encoding="utf-8") as f:
             h.update(name.encode() + b"\0" + _code_only(f.read()).encode())
     return h.hexdigest()
@@ -126,15 +131,18 @@ def kernel_source_sha256(pair: bool = False) -> str:
 def recorded_traffic(workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current sources of the kernel that runs `workload` (entries named
-    cta_pair:<workload> are the CTA-pair kernel's); else None. The file holds
-    blocks: a kernel_source_sha256 line, then workload / dram_bytes_per_launch
-    line pairs measured on those sources."""
+    cta_pair:<workload> are the CTA-pair kernel's, *_e4m3 the 8-bit
+    kernel's); else None. The file holds blocks: a kernel_source_sha256 line,
+    then workload / dram_bytes_per_launch line pairs measured on those
+    sources."""
     path = os.path.join(ROOT, "profiles", "fa_fwd_traffic.txt")
     try:
         lines = open(path).read().splitlines()
     except OSError:
         return None
-    want = kernel_source_sha256(pair=workload.startswith("cta_pair:"))
+    kind = ("pair" if workload.startswith(PAIR_PREFIX) else
+            "fp8" if workload.endswith("_e4m3") else "one_cta")
+    want = kernel_source_sha256(kind)
     cur_hash, cur_wl = None, None
     for ln in lines:
         if ":" not in ln or ln.lstrip().startswith("#"):
@@ -599,6 +607,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         if args.pass_ != "forward" or w.dtype == "e4m3" or w.d != 128:
             raise SystemExit("--kernel pair takes a 16-bit head-dimension-128 forward workload")
         plan = forward_plan(fa, torch, w, dev, stream, kernel="pair")
+    elif args.kernel == "one-cta":
+        if args.pass_ != "forward" or w.dtype == "e4m3":
+            raise SystemExit("--kernel one-cta takes a 16-bit forward workload")
+        plan = forward_plan(fa, torch, w, dev, stream, kernel="one_cta")
     else:
         plan = make(fa, torch, w, dev, stream)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
@@ -664,6 +676,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             "config": {k: v for k, v in workload_config(ow).items()
                        if k not in ("global_batch", "seq_len")},
             "kernel": oplan.kernel,
+            "traffic": oplan.traffic,
         }
         del oplan
         torch.cuda.empty_cache()
