@@ -98,6 +98,7 @@ struct Layout {
   // values per column), so S_i(j+1) can be computed while softmax(j) runs.
   static constexpr bool kSepP = D == 64 && !FP8;
   static constexpr uint32_t kColP = 256 + 2 * D;  // P_i at kColP + i*64 (kSepP)
+  static_assert(!kSepP || kStages % 2 == 0, "kSepP: K tiles in even ring slots, V in odd");
   static_assert(!kSepP || kColP + 128 <= kTmemCols, "TMEM columns");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kOffBar % 8 == 0, "barrier block alignment");
@@ -117,7 +118,7 @@ enum BarSlot : int {
   kBarSFree = 16,     // [2] 128 softmax threads: S_i read (kSepP)
   kBarPFree = 18,     // [2] MMA: O_i += P_i V done, P_i reusable (kSepP)
   kBarKVFull = 20,    // [stages] TMA: ring slot loaded; then [stages] ring slot free
-  kBarDrainPV = 36,   // PV-issuing warp (kSepP): every tcgen05 op it issued completed
+  kBarDrainPV = 36,   // [2] PV-issuing warps (kSepP): every tcgen05 op each issued completed
 };
 constexpr int kSlotTmem = 480;   // byte offset of the TMEM base address
 constexpr int kSlotAbort = 484;  // byte offset of the abort flag
@@ -325,18 +326,23 @@ __device__ __forceinline__ void mma_role(const FwdArgs& a, uint32_t sbase, uint3
   wait_drain(bar(kBarDrain), 0u, ab, kStatusDrain);
 }
 
-// MMA issue when P_i has TMEM columns of its own (d = 64), split over two
-// warps on different SM sub-partitions (each tcgen05.mma takes issue cycles
-// from the softmax warps sharing its sub-partition, and those hold the rows
-// the MMAs wait for). S products never touch the P or O columns, so the two
-// need no ordering between them beyond the softmax's own barriers:
-//   S warp:  S_i(j+1) = Q_i K_{j+1}^T once softmax i has read S_i(j);
-//   PV warp: O_i += P_i(j) V_j once P_i(j) is written, then P-free (O_i
-//            updated, P_i reusable), and O-full after a unit's last one.
+// MMA issue when P_i has TMEM columns of its own (d = 64), split over three
+// warps on three SM sub-partitions: each tcgen05.mma takes issue cycles from
+// the softmax warps sharing its sub-partition, and a softmax warp slowed that
+// way delays its whole tile (P-full waits for all four). Per KV step the S
+// warp issues 8 products and each PV warp 8; with one PV warp for both tiles
+// (16 products) the two softmax warps beside it finished ~1700 cycles after
+// their siblings on every step. S products never touch the P or O columns,
+// so the warps need no ordering beyond the softmax's own barriers:
+//   S warp:   S_i(j+1) = Q_i K_{j+1}^T once softmax i has read S_i(j);
+//   PV warps: O_i += P_i(j) V_j once P_i(j) is written (one warp per tile),
+//             then P-free (O_i updated, P_i reusable), and O-full after a
+//             unit's last one.
 // The softmax of tile j+1 never waits for PV(j): only its P store and O
-// rescale do. Both walk the same K, V ring: K_j at index 2j, V_j at 2j+1 of
-// the unit's tiles.
-template <int D, bool BF16, bool CAUSAL>
+// rescale do. All walk the same K, V ring: K_j at index 2j, V_j at 2j+1 of
+// the unit's tiles (so with an even slot count K lands in even slots, V in
+// odd ones, and a V slot is free once both PV warps have released it).
+template <int D, bool BF16, bool CAUSAL, int I0, int I1, int DRAIN>
 __device__ __forceinline__ void mma_s_role(const FwdArgs& a, uint32_t sbase, uint32_t bars,
                                            uint32_t tmem, const AbortCtx& ab) {
   using L = Layout<D, false>;
@@ -361,7 +367,8 @@ __device__ __forceinline__ void mma_s_role(const FwdArgs& a, uint32_t sbase, uin
       // S_i(j+1) = Q_i K_{j+1}^T (the first one of all waits for nothing)
       const uint32_t kn = ring + 2u * static_cast<uint32_t>(j + 1);
       if (!(ok = kv_wait(kn))) break;
-      for (int i = 0; i < 2 && ok; ++i) {
+#pragma unroll
+      for (int i = I0; i < I1 && ok; ++i) {
         if (units > 0 || j >= 0)
           ok = wait_spin_warp(bar(kBarSFree + i), (scnt[i]++) & 1u, ab, kStatusMma);
         if (!ok) break;
@@ -377,11 +384,11 @@ __device__ __forceinline__ void mma_s_role(const FwdArgs& a, uint32_t sbase, uin
     ++units;
   }
   // Every tcgen05 op this warp issued must finish before TMEM is freed.
-  ptx::umma_commit_elect(bar(kBarDrain));
-  wait_drain(bar(kBarDrain), 0u, ab, kStatusDrain);
+  ptx::umma_commit_elect(bar(DRAIN));
+  wait_drain(bar(DRAIN), 0u, ab, kStatusDrain);
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, int I0, int I1, int DRAIN>
 __device__ __forceinline__ void mma_pv_role(const FwdArgs& a, uint32_t sbase, uint32_t bars,
                                             uint32_t tmem, const AbortCtx& ab) {
   using L = Layout<D, false>;
@@ -403,7 +410,8 @@ __device__ __forceinline__ void mma_pv_role(const FwdArgs& a, uint32_t sbase, ui
       // O_i += P_i(j) V_j
       const uint32_t vj = ring + 2u * static_cast<uint32_t>(j) + 1u;
       if (!(ok = kv_wait(vj))) break;
-      for (int i = 0; i < 2 && ok; ++i) {
+#pragma unroll
+      for (int i = I0; i < I1 && ok; ++i) {
         if (!(ok = wait_spin_warp(bar(kBarPFull + i), (pcnt[i]++) & 1u, ab, kStatusMma))) break;
         if (j == 0 && units > 0 &&
             !(ok = wait_spin_warp(bar(kBarOFree + i), (units - 1) & 1u, ab, kStatusMma)))
@@ -419,8 +427,8 @@ __device__ __forceinline__ void mma_pv_role(const FwdArgs& a, uint32_t sbase, ui
     ring += 2u * static_cast<uint32_t>(nkv);
     ++units;
   }
-  ptx::umma_commit_elect(bar(kBarDrainPV));
-  wait_drain(bar(kBarDrainPV), 0u, ab, kStatusDrain);
+  ptx::umma_commit_elect(bar(DRAIN));
+  wait_drain(bar(DRAIN), 0u, ab, kStatusDrain);
 }
 
 template <int D, bool BF16, bool CAUSAL, bool FP8>
@@ -710,10 +718,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     ptx::mbar_init(bar(kBarQEmpty), 1);
     ptx::mbar_init(bar(kBarDrain), 1);
-    ptx::mbar_init(bar(kBarDrainPV), 1);
+    ptx::mbar_init(bar(kBarDrainPV + 0), 1);
+    ptx::mbar_init(bar(kBarDrainPV + 1), 1);
     for (int s = 0; s < L::kStages; ++s) {
       ptx::mbar_init(bar(kBarKVFull + s), 1);
-      ptx::mbar_init(bar(kBarKVFull + L::kStages + s), 1);
+      // kSepP: a V slot (odd) is released by both PV warps, a K slot by the S warp
+      ptx::mbar_init(bar(kBarKVFull + L::kStages + s), (L::kSepP && (s & 1)) ? 2 : 1);
     }
     *abort_flag = 0u;
     ptx::fence_mbar_init();
@@ -732,9 +742,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     ptx::setmaxnreg_dec<kRegsWG0>();
     if (warp == 0) {
       if (lane == 0) producer_role<D, BF16, CAUSAL, FP8>(&tm_q, &tm_k, &tm_v, a, sbase, bars, ab);
-    } else if constexpr (L::kSepP) {  // MMA issue split over warps 2 and 3
-      if (warp == 2) mma_s_role<D, BF16, CAUSAL>(a, sbase, bars, tmem, ab);
-      else if (warp == 3) mma_pv_role<D, BF16, CAUSAL>(a, sbase, bars, tmem, ab);
+    } else if constexpr (L::kSepP) {  // MMA issue split over warps 1, 2 and 3
+      if (warp == 2) mma_s_role<D, BF16, CAUSAL, 0, 2, kBarDrain>(a, sbase, bars, tmem, ab);
+      else if (warp == 3) mma_pv_role<D, BF16, CAUSAL, 0, 1, kBarDrainPV>(a, sbase, bars, tmem, ab);
+      else if (warp == 1) mma_pv_role<D, BF16, CAUSAL, 1, 2, kBarDrainPV + 1>(a, sbase, bars, tmem, ab);
     } else if (warp == 1) {
       mma_role<D, BF16, CAUSAL, FP8>(a, sbase, bars, tmem, ab);  // the whole warp
     }
