@@ -342,6 +342,7 @@ __device__ __forceinline__ void mma_role(const FwdArgs& a, uint32_t sbase, uint3
 // rescale do. All walk the same K, V ring: K_j at index 2j, V_j at 2j+1 of
 // the unit's tiles (so with an even slot count K lands in even slots, V in
 // odd ones, and a V slot is free once both PV warps have released it).
+// (Both roles serve the Q tiles I0 .. I1-1 and drain on barrier DRAIN.)
 template <int D, bool BF16, bool CAUSAL, int I0, int I1, int DRAIN>
 __device__ __forceinline__ void mma_s_role(const FwdArgs& a, uint32_t sbase, uint32_t bars,
                                            uint32_t tmem, const AbortCtx& ab) {
@@ -422,7 +423,7 @@ __device__ __forceinline__ void mma_pv_role(const FwdArgs& a, uint32_t sbase, ui
         if (j + 1 == nkv) ptx::umma_commit_elect(bar(kBarOFull + i));
       }
       if (!ok) break;
-      ptx::umma_commit_elect(bar(kBarKVFull + S + vj % S));  // V_j consumed
+      ptx::umma_commit_elect(bar(kBarKVFull + S + vj % S));  // V_j consumed by these tiles
     }
     ring += 2u * static_cast<uint32_t>(nkv);
     ++units;
