@@ -72,9 +72,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             lib.fa_fwd_strided.argtypes = [vp, vp, vp, vp, vp, i, i, i, i,
                                            ctypes.POINTER(FaStrides), i, f, i, vp]
             lib.fa_fwd_strided.restype = i
-        if hasattr(lib, "fa_fwd_fp8"):
-            lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, f, i, f, vp]
-            lib.fa_fwd_fp8.restype = i
+        for fn in ("fa_fwd_fp8", "fa_fwd_fp8_pair"):
+            if hasattr(lib, fn):
+                getattr(lib, fn).argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, f, i, f, vp]
+                getattr(lib, fn).restype = i
         if hasattr(lib, "fa_bwd"):
             lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
             lib.fa_bwd.restype = i
@@ -145,6 +146,15 @@ def fa_fwd_fp8(q: int, k: int, vt: int, o: int, lse: int, B: int, H: int, N: int
     """Same arguments as the C function (device pointers as ints); returns the status."""
     return load_library().fa_fwd_fp8(q, k, vt, o, lse, B, H, N, d, ldv, float(q_scale), k_scales,
                                      float(v_scale), int(bool(causal)), float(scale), stream)
+
+
+def fa_fwd_fp8_pair(q: int, k: int, vt: int, o: int, lse: int, B: int, H: int, N: int, d: int,
+                    ldv: int, q_scale: float, k_scales: int, v_scale: float, causal: bool,
+                    scale: float, stream: int = 0) -> int:
+    """fa_fwd_fp8 on CTA pairs; same arguments (device pointers as ints)."""
+    return load_library().fa_fwd_fp8_pair(q, k, vt, o, lse, B, H, N, d, ldv, float(q_scale),
+                                          k_scales, float(v_scale), int(bool(causal)),
+                                          float(scale), stream)
 
 
 def fa_bwd(q: int, k: int, v: int, o: int, dout: int, lse: int, dq: int, dk: int, dv: int,
@@ -341,12 +351,12 @@ def attention_forward_host(q, k, v, causal: bool = False, scale: float | None = 
 
 def attention_forward_fp8_into(q8, k8, vt8, o, lse, q_scale: float, k_scales, v_scale: float,
                                causal: bool = False, scale: float | None = None,
-                               stream=None) -> None:
-    """Enqueues fa_fwd_fp8: q8, k8 [B, H, N, 128] and vt8 [B, H, 128, ldv] (V
-    transposed) contiguous CUDA tensors of e4m3 codes (uint8 or float8_e4m3fn),
-    k_scales a contiguous float32 [B, H, ceil(N / 128)] CUDA tensor, o a
-    contiguous bfloat16 [B, H, N, 128] tensor, lse a contiguous float32
-    [B, H, N] tensor."""
+                               stream=None, pair: bool = False) -> None:
+    """Enqueues fa_fwd_fp8 (fa_fwd_fp8_pair if `pair`): q8, k8 [B, H, N, 128]
+    and vt8 [B, H, 128, ldv] (V transposed) contiguous CUDA tensors of e4m3
+    codes (uint8 or float8_e4m3fn), k_scales a contiguous float32
+    [B, H, ceil(N / 128)] CUDA tensor, o a contiguous bfloat16 [B, H, N, 128]
+    tensor, lse a contiguous float32 [B, H, N] tensor."""
     import torch
     B, H, N, d = q8.shape
     ldv = vt8.shape[-1]
@@ -361,11 +371,12 @@ def attention_forward_fp8_into(q8, k8, vt8, o, lse, q_scale: float, k_scales, v_
         raise ValueError("fa_fwd_fp8: bad shapes, dtypes or layouts")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    rc = fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), vt8.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                    B, H, N, d, ldv, q_scale, k_scales.data_ptr(), v_scale, causal, scale,
-                    _stream_handle(stream))
+    fn = fa_fwd_fp8_pair if pair else fa_fwd_fp8
+    rc = fn(q8.data_ptr(), k8.data_ptr(), vt8.data_ptr(), o.data_ptr(), lse.data_ptr(),
+            B, H, N, d, ldv, q_scale, k_scales.data_ptr(), v_scale, causal, scale,
+            _stream_handle(stream))
     if rc != FA_OK:
-        raise FaError(rc, "fa_fwd_fp8")
+        raise FaError(rc, fn.__name__)
 
 
 def attention_forward_fp8(q8, k8, vt8, q_scale: float, k_scales, v_scale: float,

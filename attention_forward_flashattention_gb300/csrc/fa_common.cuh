@@ -236,6 +236,18 @@ __device__ __forceinline__ void store_row128_sw128(uint32_t tile, int r, const u
   }
 }
 
+// Writes one 128-byte row (32 words: 128 8-bit elements) as row r of a
+// one-panel SW128 tile.
+__device__ __forceinline__ void store_row_panel_sw128(uint32_t tile, int r,
+                                                      const uint32_t (&pk)[32]) {
+  const uint32_t row = tile + static_cast<uint32_t>(r) * 128u;
+  const uint32_t x = static_cast<uint32_t>(r & 7);
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    ptx::st_shared_v4(row + ((static_cast<uint32_t>(q) ^ x) << 4), pk[4 * q], pk[4 * q + 1],
+                      pk[4 * q + 2], pk[4 * q + 3]);
+}
+
 // Writes 32 consecutive elements (16 packed pairs) starting at column
 // `col0` (a multiple of 32) of row r of an SW128 tile.
 __device__ __forceinline__ void store_row32_sw128(uint32_t tile, int r, int col0,

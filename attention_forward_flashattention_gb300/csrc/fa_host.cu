@@ -117,10 +117,10 @@ bool encode_qkv(CUtensorMap* m, const void* ptr, const fa_strides& st, bool bf16
 // dims[3]} with byte strides for dims 1..3; box = 128 x 128 x 1 x 1 bytes,
 // 128-byte swizzle. Elements past dims[0] / dims[1] read as zero.
 bool encode_bytes4(CUtensorMap* m, const void* ptr, const cuuint64_t (&dims)[4],
-                   const cuuint64_t (&strides)[3]) {
+                   const cuuint64_t (&strides)[3], cuuint32_t box_rows = 128u) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
-  const cuuint32_t box[4] = {128u, 128u, 1u, 1u};
+  const cuuint32_t box[4] = {128u, box_rows, 1u, 1u};
   const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(ptr), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -295,9 +295,13 @@ fa_status fa_fwd_strided(const void* q, const void* k, const void* v, void* o, f
   return fwd_call(q, k, v, o, lse, B, H, N, d, strides, causal, scale, dtype, stream);
 }
 
-fa_status fa_fwd_fp8(const void* q, const void* k, const void* vt, void* o, float* lse, int B,
-                     int H, int N, int d, int ldv, float q_scale, const float* k_scales,
-                     float v_scale, int causal, float scale, void* stream) {
+namespace {
+
+// The 8-bit forward of fa_fwd_fp8 (kAuto: the one-CTA kernel or, where it
+// is faster, the CTA pair) and fa_fwd_fp8_pair (kPair).
+fa_status fwd_fp8_call(const void* q, const void* k, const void* vt, void* o, float* lse, int B,
+                       int H, int N, int d, int ldv, float q_scale, const float* k_scales,
+                       float v_scale, int causal, float scale, void* stream, FwdChoice choice) {
   if (!q || !k || !vt || !o || !lse || !k_scales) return FA_ERR_INVALID_ARG;
   if (!fa::aligned16(q) || !fa::aligned16(k) || !fa::aligned16(vt) || !fa::aligned16(o) ||
       !fa::aligned16(lse) || (reinterpret_cast<uintptr_t>(k_scales) & 3u) != 0)
@@ -314,6 +318,9 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* vt, void* o, floa
   const fa_status ds = fa::current_device(&dev, &st, true);
   if (ds != FA_OK) return ds;
 
+  const long long BH = static_cast<long long>(B) * H;
+  const bool pair = choice == FwdChoice::kPair ||
+                    fa::fwd_fp8_prefers_pair(causal != 0, BH, N, st->sm_count);
   const cuuint64_t n = static_cast<cuuint64_t>(N), h = static_cast<cuuint64_t>(H),
                    b = static_cast<cuuint64_t>(B), lv = static_cast<cuuint64_t>(ldv);
   CUtensorMap maps[4];
@@ -321,9 +328,10 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* vt, void* o, floa
   const cuuint64_t qk_strides[3] = {128u, 128u * n, 128u * n * h};
   const cuuint64_t vt_dims[4] = {n, 128u, h, b};
   const cuuint64_t vt_strides[3] = {lv, 128u * lv, 128u * lv * h};
+  const cuuint32_t half_rows = pair ? 64u : 128u;  // the pair loads K / V^T halves
   if (!fa::encode_bytes4(&maps[0], q, qk_dims, qk_strides) ||
-      !fa::encode_bytes4(&maps[1], k, qk_dims, qk_strides) ||
-      !fa::encode_bytes4(&maps[2], vt, vt_dims, vt_strides) ||
+      !fa::encode_bytes4(&maps[1], k, qk_dims, qk_strides, half_rows) ||
+      !fa::encode_bytes4(&maps[2], vt, vt_dims, vt_strides, half_rows) ||
       !fa::encode_qkv(&maps[3], o, fa::contiguous_strides(H, N, d), true, B, H, N, d,
                       fa::kFwdOutBoxRows))
     return FA_ERR_CUDA;
@@ -336,12 +344,35 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* vt, void* o, floa
   a.v_scale = v_scale;
   a.clk = fa::clock_record(*st);
   int grid = 0;
-  fa::plan_fwd(d, N, H, static_cast<long long>(B) * H, st->sm_count, &a, &grid);
+  fa::plan_fwd(d, N, H, BH, st->sm_count, &a, &grid);
+  if (pair) {  // units of 512 rows, two CTAs per unit
+    a.n_mblk = (N + 511) / 512;
+    a.n_units = static_cast<int>(BH * a.n_mblk);
+    grid = fa::fwd_grid_pair(a.n_units, st->sm_count);
+  }
 
   (void)cudaGetLastError();
-  const cudaError_t e =
-      fa::launch_fwd_fp8(causal != 0, maps, a, grid, static_cast<cudaStream_t>(stream));
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = pair ? fa::launch_fwd_pair_fp8(causal != 0, maps, a, grid, cs)
+                             : fa::launch_fwd_fp8(causal != 0, maps, a, grid, cs);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+fa_status fa_fwd_fp8(const void* q, const void* k, const void* vt, void* o, float* lse, int B,
+                     int H, int N, int d, int ldv, float q_scale, const float* k_scales,
+                     float v_scale, int causal, float scale, void* stream) {
+  return fwd_fp8_call(q, k, vt, o, lse, B, H, N, d, ldv, q_scale, k_scales, v_scale, causal,
+                      scale, stream, FwdChoice::kAuto);
+}
+
+fa_status fa_fwd_fp8_pair(const void* q, const void* k, const void* vt, void* o, float* lse,
+                          int B, int H, int N, int d, int ldv, float q_scale,
+                          const float* k_scales, float v_scale, int causal, float scale,
+                          void* stream) {
+  return fwd_fp8_call(q, k, vt, o, lse, B, H, N, d, ldv, q_scale, k_scales, v_scale, causal,
+                      scale, stream, FwdChoice::kPair);
 }
 
 fa_status fa_bwd_workspace_size(int B, int H, int N, int d, size_t* bytes) {

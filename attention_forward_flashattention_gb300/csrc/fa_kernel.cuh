@@ -471,10 +471,13 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t bars, ui
       float cj = cl2;
       if constexpr (FP8) cj = cl2 * __ldg(a.k_scales + static_cast<size_t>(bh) * a.n_kv + j);
       const float2 c2j = make_float2(cj, cj);
-      uint32_t sr[2][2][32];  // columns 0-63, 64-127
-      ptx::tmem_ld64(tS, sr[0]);
-      ptx::tmem_ld64(tS + 64u, sr[1]);
+      // columns 0-63, 64-127, and the row maximum of each half formed by the loads
+      uint32_t sr[2][2][32];
+      float mx_lo, mx_hi;
+      ptx::tmem_ld64_max(tS, sr[0], mx_lo);
+      ptx::tmem_ld64_max(tS + 64u, sr[1], mx_hi);
       ptx::tmem_ld_wait64x2(sr[0], sr[1]);
+      ptx::tmem_ld_wait_f2(mx_lo, mx_hi);
       if constexpr (L::kSepP) {  // S_i is in registers: S_i(j+1) may overwrite it
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(kBarSFree + wg));
@@ -485,24 +488,26 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t bars, ui
       // Mask keys past the end of the sequence and (causal) past the row.
       const int k0 = j * kTileRows;
       const bool need_mask = (k0 + kTileRows > a.N) || (CAUSAL && k0 + kTileRows - 1 > tile_row0);
+      float m_raw = fmaxf(mx_lo, mx_hi);
       if (need_mask) {
         int lim = a.N - k0;
         if (CAUSAL) lim = min(lim, grow - k0 + 1);
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
+        // Row max over the visible keys: eight independent chains, elements
+        // 2t and 2t + 1 of each 16-element group in chain t.
+        float mx[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) mx[t] = fmaxf(s[2 * t], s[2 * t + 1]);
+#pragma unroll
+        for (int c = 16; c < 128; c += 16) {
+#pragma unroll
+          for (int t = 0; t < 8; ++t) mx[t] = ptx::fmax3(mx[t], s[c + 2 * t], s[c + 2 * t + 1]);
+        }
+        m_raw = fmaxf(ptx::fmax3(mx[0], mx[1], mx[2]),
+                      ptx::fmax3(ptx::fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
       }
-      // Row max over exactly s[0..127]: eight independent chains, elements
-      // 2t and 2t + 1 of each 16-element group in chain t.
-      float mx[8];
-#pragma unroll
-      for (int t = 0; t < 8; ++t) mx[t] = fmaxf(s[2 * t], s[2 * t + 1]);
-#pragma unroll
-      for (int c = 16; c < 128; c += 16) {
-#pragma unroll
-        for (int t = 0; t < 8; ++t) mx[t] = ptx::fmax3(mx[t], s[c + 2 * t], s[c + 2 * t + 1]);
-      }
-      const float m_tile = fmaxf(ptx::fmax3(mx[0], mx[1], mx[2]),
-                                 ptx::fmax3(ptx::fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7])) * cj;
+      const float m_tile = m_raw * cj;
       const float m_new = fmaxf(m_ref, m_tile);
       float alpha = 1.f;
       if (j == 0) {

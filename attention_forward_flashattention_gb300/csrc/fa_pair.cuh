@@ -71,11 +71,14 @@ __device__ __forceinline__ bool next_pair_unit(int& round, const FwdArgs& a, int
   }
 }
 
+// FP8: e4m3 Q, K and V^T, whose 128-element rows are one 128-byte panel, so
+// every tile and ring slot is half as large (and the rings are deeper).
+template <bool FP8 = false>
 struct PairLayout {
-  static constexpr int kTileBytes = 2 * kPanelBytes;            // a Q or P tile (128 x 128)
-  static constexpr int kSlotBytes = kPanelBytes;                // a K half or a V half
-  static constexpr int kKSlots = 2;                             // K ring (K_j, K_{j+1})
-  static constexpr int kVSlots = 3;                             // V ring
+  static constexpr int kTileBytes = (FP8 ? 1 : 2) * kPanelBytes;  // a Q or P tile (128 x 128)
+  static constexpr int kSlotBytes = FP8 ? kPanelBytes / 2 : kPanelBytes;  // a K / V half
+  static constexpr int kKSlots = FP8 ? 4 : 2;                   // K ring (K_j, K_{j+1}, ...)
+  static constexpr int kVSlots = FP8 ? 4 : 3;                   // V ring
   static constexpr int kOffQ = 0;                               // Q0, Q1
   static constexpr int kOffP = 2 * kTileBytes;                  // P0, P1 (K-major SW128)
   static constexpr int kOffK = 4 * kTileBytes;
@@ -89,6 +92,12 @@ struct PairLayout {
   static_assert(kOffBar % 8 == 0 && kOffOut % 1024 == 0, "alignment");
   static constexpr uint32_t kColS = 0;    // S_i at 128 i
   static constexpr uint32_t kColO = 256;  // O_i at 256 + 128 i
+  // barrier slots of the K and V rings (PairBar below)
+  static constexpr int kBarKFull = 22;
+  static constexpr int kBarKEmpty = kBarKFull + kKSlots;
+  static constexpr int kBarVFull = kBarKEmpty + kKSlots;
+  static constexpr int kBarVEmpty = kBarVFull + kVSlots;
+  static_assert(8 * (kBarVEmpty + kVSlots) <= kPairSlotTmem, "barrier block");
 };
 
 enum PairBar : int {
@@ -104,10 +113,9 @@ enum PairBar : int {
   kQbStatsFree = 17,  // [2] local: 128 epilogue threads read them
   kQbDrain = 19,      // [2] even CTA: every product of S warp w completed
   kQbDrainPV = 21,    // even CTA: every PV product completed
-  kQbKFull = 22,      // [K slots] even CTA: both K halves landed
-  kQbKEmpty = 24,     // [K slots] both: K slot free (a commit per S warp)
-  kQbVFull = 26,      // [V slots] even CTA: both V halves landed
-  kQbVEmpty = 29,     // [V slots] both: V slot free (multicast commit)
+  // then, from slot 22 (PairLayout::kBarKFull ...): [K slots] even CTA: both K
+  // halves landed; [K slots] both: K slot free (a commit per S warp); [V slots]
+  // even CTA: both V halves landed; [V slots] both: V slot free
 };
 
 // Units of 512 rows per pair (n_mblk = ceil(N / 512)): causal units visit KV
@@ -120,12 +128,15 @@ __device__ __forceinline__ int pair_kv_tiles(const FwdArgs& a, int mblk) {
 // Loads, per unit: both Q tiles, then K_0, then K_{j+1} before V_j (the S
 // products of a tile need the next K while its softmax runs; V_j is needed
 // only when P_j is written), from two rings that release slots independently.
-template <bool CAUSAL>
+template <bool CAUSAL, bool FP8>
 __device__ __forceinline__ void pair_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                               const CUtensorMap* tm_v, const FwdArgs& a,
                                               uint32_t sbase, uint32_t bars, uint32_t rank,
                                               const AbortCtx& ab) {
-  using L = PairLayout;
+  using L = PairLayout<FP8>;
+  constexpr int kQbKFull = L::kBarKFull, kQbKEmpty = L::kBarKEmpty;
+  constexpr int kQbVFull = L::kBarVFull, kQbVEmpty = L::kBarVEmpty;
+  constexpr int kPanels = FP8 ? 1 : 2;  // 128-byte panels per Q / K row
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
   auto lead = [&](int i) { return ptx::mapa_shared(bar(i), 0); };
   ptx::prefetch_tmap(tm_q);
@@ -140,7 +151,7 @@ __device__ __forceinline__ void pair_producer(const CUtensorMap* tm_q, const CUt
     const int hh = bh % a.H, bb = bh / a.H;
     for (int i = 0; i < 2; ++i) {
       if (rank == 0) ptx::mbar_arrive_expect_tx(bar(kQbQFull + i), 2 * L::kTileBytes);
-      for (int p = 0; p < 2; ++p)
+      for (int p = 0; p < kPanels; ++p)
         ptx::tma_load_4d_pair(sbase + L::kOffQ + i * L::kTileBytes + p * kPanelBytes, tm_q,
                               lead(kQbQFull + i), 64 * p,
                               mblk * 512 + 256 * i + 128 * static_cast<int>(rank), hh, bb);
@@ -152,7 +163,7 @@ __device__ __forceinline__ void pair_producer(const CUtensorMap* tm_q, const CUt
         if (!(ok = wait_cluster<false>(bar(kQbKEmpty + s), ph ^ 1u, ab, kStatusProducer))) break;
         if (rank == 0) ptx::mbar_arrive_expect_tx(bar(kQbKFull + s), 2 * L::kSlotBytes);
         const uint32_t dst = sbase + L::kOffK + s * L::kSlotBytes;
-        for (int p = 0; p < 2; ++p)
+        for (int p = 0; p < kPanels; ++p)
           ptx::tma_load_4d_pair(dst + p * (kPanelBytes / 2), tm_k, lead(kQbKFull + s), 64 * p,
                                 128 * j + 64 * static_cast<int>(rank), hh, bb);
         ++kcnt;
@@ -161,8 +172,12 @@ __device__ __forceinline__ void pair_producer(const CUtensorMap* tm_q, const CUt
         const uint32_t s = vcnt % L::kVSlots, ph = (vcnt / L::kVSlots) & 1u;
         if (!(ok = wait_cluster<false>(bar(kQbVEmpty + s), ph ^ 1u, ab, kStatusProducer))) break;
         if (rank == 0) ptx::mbar_arrive_expect_tx(bar(kQbVFull + s), 2 * L::kSlotBytes);
-        ptx::tma_load_4d_pair(sbase + L::kOffV + s * L::kSlotBytes, tm_v, lead(kQbVFull + s),
-                              64 * static_cast<int>(rank), 128 * (j - 1), hh, bb);
+        if constexpr (FP8)  // V^T {keys, d, h, b}: those keys of d rows 64 rank .. +63
+          ptx::tma_load_4d_pair(sbase + L::kOffV + s * L::kSlotBytes, tm_v, lead(kQbVFull + s),
+                                128 * (j - 1), 64 * static_cast<int>(rank), hh, bb);
+        else
+          ptx::tma_load_4d_pair(sbase + L::kOffV + s * L::kSlotBytes, tm_v, lead(kQbVFull + s),
+                                64 * static_cast<int>(rank), 128 * (j - 1), hh, bb);
         ++vcnt;
       }
     }
@@ -199,12 +214,13 @@ __device__ __forceinline__ void pair_producer(const CUtensorMap* tm_q, const CUt
 template <bool CAUSAL>
 __host__ __device__ constexpr int pair_s_warps() { return CAUSAL ? 1 : 2; }
 
-template <bool BF16, bool CAUSAL, int I0, int I1, int W>
+template <bool BF16, bool CAUSAL, bool FP8, int I0, int I1, int W>
 __device__ __forceinline__ void pair_mma_s(const FwdArgs& a, uint32_t sbase, uint32_t bars,
                                            uint32_t tmem, const AbortCtx& ab) {
-  using L = PairLayout;
+  using L = PairLayout<FP8>;
+  constexpr int kQbKFull = L::kBarKFull, kQbKEmpty = L::kBarKEmpty;
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
-  constexpr uint32_t kIdS = ptx::idesc_f16(BF16, false, 256, 128);
+  constexpr uint32_t kIdS = FP8 ? ptx::idesc_f8(256, 128) : ptx::idesc_f16(BF16, false, 256, 128);
   const uint64_t dQ0 = desc_kmajor(sbase + L::kOffQ);
   const uint64_t dK0 = desc_kmajor(sbase + L::kOffK);
   uint32_t units = 0, scnt = 0;  // scnt: K tiles used so far = S_i products issued (each tile)
@@ -229,13 +245,23 @@ __device__ __forceinline__ void pair_mma_s(const FwdArgs& a, uint32_t sbase, uin
         ptx::tc_fence_after();
         uint64_t q = desc_add(dQ0, static_cast<uint32_t>(i) * L::kTileBytes);
         uint64_t k = desc_add(dK0, ks * static_cast<uint32_t>(L::kSlotBytes));
+        if constexpr (FP8) {  // K = 32 per product, one panel: +32 bytes per step
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          ptx::umma_f16_ss_pair_elect(tmem + L::kColS + 128u * i, q, k, kIdS, kk > 0 ? 1u : 0u);
-          const bool next_panel = (kk & 3) == 3;
-          q = desc_add(q, next_panel ? static_cast<uint32_t>(kPanelBytes - 96) : 32u);
-          k = desc_add(k, next_panel ? static_cast<uint32_t>(kPanelBytes / 2 - 96) : 32u);
-          asm volatile("" : "+l"(q), "+l"(k));
+          for (int kk = 0; kk < 4; ++kk) {
+            ptx::umma_f8_ss_pair_elect(tmem + L::kColS + 128u * i, q, k, kIdS, kk > 0 ? 1u : 0u);
+            q = desc_add(q, 32u);
+            k = desc_add(k, 32u);
+            asm volatile("" : "+l"(q), "+l"(k));
+          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            ptx::umma_f16_ss_pair_elect(tmem + L::kColS + 128u * i, q, k, kIdS, kk > 0 ? 1u : 0u);
+            const bool next_panel = (kk & 3) == 3;
+            q = desc_add(q, next_panel ? static_cast<uint32_t>(kPanelBytes - 96) : 32u);
+            k = desc_add(k, next_panel ? static_cast<uint32_t>(kPanelBytes / 2 - 96) : 32u);
+            asm volatile("" : "+l"(q), "+l"(k));
+          }
         }
         ptx::umma_commit_pair_elect(bar(kQbSFull + i), 3);
       }
@@ -249,15 +275,17 @@ __device__ __forceinline__ void pair_mma_s(const FwdArgs& a, uint32_t sbase, uin
   wait_drain(bar(kQbDrain + W), 0u, ab, kStatusDrain);
 }
 
-template <bool BF16, bool CAUSAL>
+template <bool BF16, bool CAUSAL, bool FP8>
 __device__ __forceinline__ void pair_mma_pv(const FwdArgs& a, uint32_t sbase, uint32_t bars,
                                             uint32_t tmem, const AbortCtx& ab) {
-  using L = PairLayout;
+  using L = PairLayout<FP8>;
+  constexpr int kQbVFull = L::kBarVFull, kQbVEmpty = L::kBarVEmpty;
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
-  constexpr uint32_t kIdPV = ptx::idesc_f16(BF16, true, 256, 128);
+  // 16-bit: V as stored ([key][d], MN-major B); FP8: V^T ([d][key], K-major B)
+  constexpr uint32_t kIdPV = FP8 ? ptx::idesc_f8(256, 128) : ptx::idesc_f16(BF16, true, 256, 128);
   const uint64_t dP[2] = {desc_kmajor(sbase + L::kOffP),
                           desc_kmajor(sbase + L::kOffP + L::kTileBytes)};
-  const uint64_t dV0 = desc_v(sbase + L::kOffV);
+  const uint64_t dV0 = FP8 ? desc_kmajor(sbase + L::kOffV) : desc_v(sbase + L::kOffV);
   uint32_t units = 0, pcnt = 0;  // pcnt: V tiles used so far = P_i tiles consumed (each tile)
   int round = 0, bh = 0, mblk = 0;
   bool ok = true;
@@ -274,13 +302,24 @@ __device__ __forceinline__ void pair_mma_pv(const FwdArgs& a, uint32_t sbase, ui
           break;
         ptx::tc_fence_after();
         uint64_t pd = dP[i], v = desc_add(dV0, vs * static_cast<uint32_t>(L::kSlotBytes));
+        if constexpr (FP8) {  // K = 32 keys per product: +32 bytes in P and V^T
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          ptx::umma_f16_ss_pair_elect(tmem + L::kColO + 128u * i, pd, v, kIdPV,
-                                      (j > 0 || kk > 0) ? 1u : 0u);
-          pd = desc_add(pd, (kk & 3) == 3 ? static_cast<uint32_t>(kPanelBytes - 96) : 32u);
-          v = desc_add(v, 2048u);
-          asm volatile("" : "+l"(pd), "+l"(v));
+          for (int kk = 0; kk < 4; ++kk) {
+            ptx::umma_f8_ss_pair_elect(tmem + L::kColO + 128u * i, pd, v, kIdPV,
+                                       (j > 0 || kk > 0) ? 1u : 0u);
+            pd = desc_add(pd, 32u);
+            v = desc_add(v, 32u);
+            asm volatile("" : "+l"(pd), "+l"(v));
+          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            ptx::umma_f16_ss_pair_elect(tmem + L::kColO + 128u * i, pd, v, kIdPV,
+                                        (j > 0 || kk > 0) ? 1u : 0u);
+            pd = desc_add(pd, (kk & 3) == 3 ? static_cast<uint32_t>(kPanelBytes - 96) : 32u);
+            v = desc_add(v, 2048u);
+            asm volatile("" : "+l"(pd), "+l"(v));
+          }
         }
         ptx::umma_commit_pair_elect(bar(kQbPFree + i), 3);
         if (j + 1 == nkv) ptx::umma_commit_pair_elect(bar(kQbOFull + i), 3);
@@ -299,11 +338,11 @@ __device__ __forceinline__ void pair_mma_pv(const FwdArgs& a, uint32_t sbase, ui
 // registers, P written to shared memory (K-major, 128-byte swizzle: the A
 // operand of the PV product), and the S-read / P-written arrivals sent to the
 // even CTA (one per warp).
-template <bool BF16, bool CAUSAL>
+template <bool BF16, bool CAUSAL, bool FP8>
 __device__ __forceinline__ void pair_softmax(const FwdArgs& a, uint32_t sbase, uint32_t bars,
                                              uint32_t tmem, float* stats, uint32_t rank,
                                              const AbortCtx& ab, int warp, int lane) {
-  using L = PairLayout;
+  using L = PairLayout<FP8>;
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
   const int wg = (warp >> 2) - 1;
   const int r = (warp & 3) * 32 + lane;
@@ -314,7 +353,6 @@ __device__ __forceinline__ void pair_softmax(const FwdArgs& a, uint32_t sbase, u
   const uint32_t lead_sfree = ptx::mapa_shared(bar(kQbSFree + wg), 0);
   const uint32_t sP = sbase + L::kOffP + static_cast<uint32_t>(wg) * L::kTileBytes;
   const float cl2 = a.scale_log2;
-  const float2 c2 = make_float2(cl2, cl2);
   uint32_t scnt = 0, units = 0;
   int round = 0, bh = 0, mblk = 0;
   bool ok = true;
@@ -328,34 +366,43 @@ __device__ __forceinline__ void pair_softmax(const FwdArgs& a, uint32_t sbase, u
       if (!(ok = __all_sync(0xffffffffu, ok) != 0)) break;
       ++scnt;
       ptx::tc_fence_after();
+      // S with its row maximum over each 64-column half formed by the loads
       uint32_t sr[2][2][32];
-      ptx::tmem_ld64(tS, sr[0]);
-      ptx::tmem_ld64(tS + 64u, sr[1]);
+      float mx_lo, mx_hi;
+      ptx::tmem_ld64_max(tS, sr[0], mx_lo);
+      ptx::tmem_ld64_max(tS + 64u, sr[1], mx_hi);
       ptx::tmem_ld_wait64x2(sr[0], sr[1]);
+      ptx::tmem_ld_wait_f2(mx_lo, mx_hi);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive_cluster(lead_sfree);  // S_i may be overwritten
+      // base-2 score scale of this tile (8-bit inputs: times its K block's scale)
+      float cj = cl2;
+      if constexpr (FP8) cj = cl2 * __ldg(a.k_scales + static_cast<size_t>(bh) * a.n_kv + j);
+      const float2 c2 = make_float2(cj, cj);
       float s[128];
 #pragma unroll
       for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 6][(c >> 5) & 1][c & 31]);
       const int k0 = j * kTileRows;
       const bool need_mask = (k0 + kTileRows > a.N) || (CAUSAL && k0 + kTileRows - 1 > tile_row0);
-      if (need_mask) {
+      float m_raw = fmaxf(mx_lo, mx_hi);
+      if (need_mask) {  // masked keys: the maximum over the visible ones only
         int lim = a.N - k0;
         if (CAUSAL) lim = min(lim, grow - k0 + 1);
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
+        float mx[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) mx[t] = fmaxf(s[2 * t], s[2 * t + 1]);
+#pragma unroll
+        for (int c = 16; c < 128; c += 16) {
+#pragma unroll
+          for (int t = 0; t < 8; ++t) mx[t] = ptx::fmax3(mx[t], s[c + 2 * t], s[c + 2 * t + 1]);
+        }
+        m_raw = fmaxf(ptx::fmax3(mx[0], mx[1], mx[2]),
+                      ptx::fmax3(ptx::fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
       }
-      float mx[8];
-#pragma unroll
-      for (int t = 0; t < 8; ++t) mx[t] = fmaxf(s[2 * t], s[2 * t + 1]);
-#pragma unroll
-      for (int c = 16; c < 128; c += 16) {
-#pragma unroll
-        for (int t = 0; t < 8; ++t) mx[t] = ptx::fmax3(mx[t], s[c + 2 * t], s[c + 2 * t + 1]);
-      }
-      const float m_tile = fmaxf(ptx::fmax3(mx[0], mx[1], mx[2]),
-                                 ptx::fmax3(ptx::fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7])) * cl2;
+      const float m_tile = m_raw * cj;
       const float m_new = fmaxf(m_ref, m_tile);
       float alpha = 1.f;
       if (j == 0) {
@@ -368,17 +415,31 @@ __device__ __forceinline__ void pair_softmax(const FwdArgs& a, uint32_t sbase, u
       float2 ls[4], lr[4];
 #pragma unroll
       for (int t = 0; t < 4; ++t) ls[t] = lr[t] = make_float2(0.f, 0.f);
-      uint32_t pk[64];
+      uint32_t pk[FP8 ? 32 : 64];
+      if constexpr (FP8) {
+        // P as e4m3, four keys per word (O is normalised by the unrounded sum)
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float2 t = ptx::ffma2(make_float2(s[2 * c], s[2 * c + 1]), c2, neg2);
-        const float p0 = ptx::ex2(t.x), p1 = ptx::ex2(t.y);
-        const uint32_t w = pack2<BF16>(p0, p1);
-        pk[c] = w;
-        ls[c & 3] = ptx::fadd2(ls[c & 3], make_float2(p0, p1));
-        if constexpr (BF16) {
-          lr[c & 3].x = ptx::add_f32_bf16_lo(lr[c & 3].x, w);
-          lr[c & 3].y = ptx::add_f32_bf16_hi(lr[c & 3].y, w);
+        for (int c = 0; c < 32; ++c) {
+          const float2 t0 = ptx::ffma2(make_float2(s[4 * c], s[4 * c + 1]), c2, neg2);
+          const float2 t1 = ptx::ffma2(make_float2(s[4 * c + 2], s[4 * c + 3]), c2, neg2);
+          const float p0 = ptx::ex2(t0.x), p1 = ptx::ex2(t0.y);
+          const float p2 = ptx::ex2(t1.x), p3 = ptx::ex2(t1.y);
+          pk[c] = ptx::pack4_e4m3(p0, p1, p2, p3);
+          ls[(2 * c) & 3] = ptx::fadd2(ls[(2 * c) & 3], make_float2(p0, p1));
+          ls[(2 * c + 1) & 3] = ptx::fadd2(ls[(2 * c + 1) & 3], make_float2(p2, p3));
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const float2 t = ptx::ffma2(make_float2(s[2 * c], s[2 * c + 1]), c2, neg2);
+          const float p0 = ptx::ex2(t.x), p1 = ptx::ex2(t.y);
+          const uint32_t w = pack2<BF16>(p0, p1);
+          pk[c] = w;
+          ls[c & 3] = ptx::fadd2(ls[c & 3], make_float2(p0, p1));
+          if constexpr (BF16) {
+            lr[c & 3].x = ptx::add_f32_bf16_lo(lr[c & 3].x, w);
+            lr[c & 3].y = ptx::add_f32_bf16_hi(lr[c & 3].y, w);
+          }
         }
       }
       // PV_i of the previous tile done: P_i reusable, O_i updated
@@ -386,11 +447,12 @@ __device__ __forceinline__ void pair_softmax(const FwdArgs& a, uint32_t sbase, u
           !(ok = wait_cluster_warp(bar(kQbPFree + wg), (scnt - 2) & 1u, ab, kStatusSoftmax)))
         break;
       ptx::tc_fence_after();
-      store_row128_sw128(sP, r, pk);
+      if constexpr (FP8) store_row_panel_sw128(sP, r, pk);
+      else store_row128_sw128(sP, r, pk);
       const float2 s01 = ptx::fadd2(ptx::fadd2(ls[0], ls[1]), ptx::fadd2(ls[2], ls[3]));
       const float lsum = s01.x + s01.y;
       float lsum_p = lsum;
-      if constexpr (BF16) {
+      if constexpr (BF16 && !FP8) {
         const float2 r01 = ptx::fadd2(ptx::fadd2(lr[0], lr[1]), ptx::fadd2(lr[2], lr[3]));
         lsum_p = r01.x + r01.y;
       }
@@ -431,12 +493,12 @@ __device__ __forceinline__ void pair_softmax(const FwdArgs& a, uint32_t sbase, u
   }
 }
 
-template <bool BF16, bool CAUSAL>
+template <bool BF16, bool CAUSAL, bool FP8>
 __device__ __forceinline__ void pair_epilogue(const CUtensorMap* tm_o, const FwdArgs& a,
                                                uint32_t sbase, uint32_t bars, uint32_t tmem,
                                                const float* stats, uint32_t rank,
                                                const AbortCtx& ab, int warp, int lane) {
-  using L = PairLayout;
+  using L = PairLayout<FP8>;
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
   const int w = warp & 3;
   const int r = w * 32 + lane;
@@ -457,7 +519,7 @@ __device__ __forceinline__ void pair_epilogue(const CUtensorMap* tm_o, const Fwd
            wait_bounded_warp(bar(kQbStatsFull + i), units & 1u, ab, kStatusEpilogue);
       if (!ok) break;
       ptx::tc_fence_after();
-      const float inv_l = 1.f / stats[i * 128 + r];
+      const float inv_l = (FP8 ? a.v_scale : 1.f) / stats[i * 128 + r];
       ptx::mbar_arrive(bar(kQbStatsFree + i));
       const float2 il2 = make_float2(inv_l, inv_l);
       const int row0 = mblk * 512 + 256 * i + 128 * static_cast<int>(rank) + 32 * w;
@@ -499,13 +561,16 @@ __device__ __forceinline__ void pair_epilogue(const CUtensorMap* tm_o, const Fwd
   if (lane == 0 && pending) ptx::bulk_wait_all();
 }
 
-template <bool BF16, bool CAUSAL>
+// FP8: e4m3 Q, K, V^T (instantiate with BF16 = true: bf16 O).
+template <bool BF16, bool CAUSAL, bool FP8 = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFwdThreads, 1)
     fa_fwd_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v,
                         const __grid_constant__ CUtensorMap tm_o, const FwdArgs a) {
-  using L = PairLayout;
+  using L = PairLayout<FP8>;
+  constexpr int kQbKFull = L::kBarKFull, kQbKEmpty = L::kBarKEmpty;
+  constexpr int kQbVFull = L::kBarVFull, kQbVEmpty = L::kBarVEmpty;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -560,23 +625,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFwdThreads, 1)
   if (wgrp == 0) {
     ptx::setmaxnreg_dec<kRegsWG0>();
     if (warp == 0) {
-      if (lane == 0) pair_producer<CAUSAL>(&tm_q, &tm_k, &tm_v, a, sbase, bars, rank, ab);
+      if (lane == 0) pair_producer<CAUSAL, FP8>(&tm_q, &tm_k, &tm_v, a, sbase, bars, rank, ab);
     } else if (warp == 2 && rank == 0) {
       if constexpr (pair_s_warps<CAUSAL>() == 2)  // tile 1 (tile 0: warp 1)
-        pair_mma_s<BF16, CAUSAL, 1, 2, 1>(a, sbase, bars, tmem, ab);
+        pair_mma_s<BF16, CAUSAL, FP8, 1, 2, 1>(a, sbase, bars, tmem, ab);
       else  // both tiles
-        pair_mma_s<BF16, CAUSAL, 0, 2, 0>(a, sbase, bars, tmem, ab);
+        pair_mma_s<BF16, CAUSAL, FP8, 0, 2, 0>(a, sbase, bars, tmem, ab);
     } else if (warp == 1 && rank == 0 && pair_s_warps<CAUSAL>() == 2) {
-      pair_mma_s<BF16, CAUSAL, 0, 1, 0>(a, sbase, bars, tmem, ab);
+      pair_mma_s<BF16, CAUSAL, FP8, 0, 1, 0>(a, sbase, bars, tmem, ab);
     } else if (warp == 3 && rank == 0) {
-      pair_mma_pv<BF16, CAUSAL>(a, sbase, bars, tmem, ab);
+      pair_mma_pv<BF16, CAUSAL, FP8>(a, sbase, bars, tmem, ab);
     }
   } else if (wgrp < 3) {
     ptx::setmaxnreg_inc<kRegsSoftmax>();
-    pair_softmax<BF16, CAUSAL>(a, sbase, bars, tmem, stats, rank, ab, warp, lane);
+    pair_softmax<BF16, CAUSAL, FP8>(a, sbase, bars, tmem, stats, rank, ab, warp, lane);
   } else {
     ptx::setmaxnreg_dec<kRegsEpilogue>();
-    pair_epilogue<BF16, CAUSAL>(&tm_o, a, sbase, bars, tmem, stats, rank, ab, warp, lane);
+    pair_epilogue<BF16, CAUSAL, FP8>(&tm_o, a, sbase, bars, tmem, stats, rank, ab, warp, lane);
   }
   __syncwarp();
   ptx::tc_fence_before();
@@ -591,7 +656,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFwdThreads, 1)
 // (a.n_mblk = ceil(N / 512)); grid = 2 x pairs.
 cudaError_t launch_fwd_pair(bool bf16, bool causal, const CUtensorMap* maps, const FwdArgs& a,
                             int grid, cudaStream_t stream);
-int fwd_smem_bytes_pair();
+// 8-bit inputs: maps = Q, K ({128 bytes, N, H, B}: 128- / 64-row boxes), V^T
+// ({keys, 128, H, B}: 128 keys x 64 rows), O as above.
+cudaError_t launch_fwd_pair_fp8(bool causal, const CUtensorMap* maps, const FwdArgs& a, int grid,
+                                cudaStream_t stream);
+int fwd_smem_bytes_pair(bool fp8 = false);
 // Whether fa_fwd / fa_fwd_strided run the pair kernel: head dimension 128,
 // non-causal, and enough 512-row units to give every SM pair one. (Same-box
 // measurements: non-causal B4 H16 N4096 ~6 % faster than the one-CTA kernel;
@@ -599,6 +668,16 @@ int fwd_smem_bytes_pair();
 // The two kernels' results are identical bit for bit.
 inline bool fwd_prefers_pair(int d, bool causal, long long BH, int N, int sm_count) {
   return d == 128 && !causal && BH * ((static_cast<long long>(N) + 511) / 512) >= sm_count / 2;
+}
+
+// Whether fa_fwd_fp8 runs the pair kernel (8-bit inputs are always head
+// dimension 128). Kept to the one-CTA kernel until measured otherwise.
+inline bool fwd_fp8_prefers_pair(bool causal, long long BH, int N, int sm_count) {
+  (void)causal;
+  (void)BH;
+  (void)N;
+  (void)sm_count;
+  return false;
 }
 
 // Grid of the pair kernel for n_units units: two CTAs per pair, one pair per

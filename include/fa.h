@@ -160,6 +160,19 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* vt, void* o, floa
                      void* stream);
 
 /*
+ * fa_fwd_fp8_pair - fa_fwd_fp8 computed by pairs of CTAs sharing each
+ * tensor-core product (tcgen05.mma cta_group::2, M = 256 query rows), as
+ * fa_fwd_pair does for 16-bit inputs: each SM keeps half of every K and V^T
+ * tile, and the 8-bit weights P go through shared memory to the P V product.
+ * Same arguments, layout, precision, errors, asynchrony and status word as
+ * fa_fwd_fp8, whose results it reproduces bit for bit.
+ */
+fa_status fa_fwd_fp8_pair(const void* q, const void* k, const void* vt, void* o, float* lse,
+                          int B, int H, int N, int d, int ldv, float q_scale,
+                          const float* k_scales, float v_scale, int causal, float scale,
+                          void* stream);
+
+/*
  * fa_bwd - enqueue the backward pass of fa_fwd: gradients dq, dk, dv of a
  * loss whose gradient at O is dout. The backward recomputes the scores
  * instead of storing them ("TCA 51%, MFU below 8%", section "MFU is always a

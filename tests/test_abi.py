@@ -19,7 +19,8 @@ def lib():
 
 def test_header_declares_expected_entry_points():
     names = fa.header_functions()
-    assert names == ["fa_fwd", "fa_fwd_pair", "fa_fwd_strided", "fa_fwd_fp8", "fa_bwd", "fa_bwd_workspace_size",
+    assert names == ["fa_fwd", "fa_fwd_pair", "fa_fwd_strided", "fa_fwd_fp8", "fa_fwd_fp8_pair",
+                     "fa_bwd", "fa_bwd_workspace_size",
                      "fa_fwd_noalloc", "fa_fwd_host", "fa_fwd_host_workspace_size", "fa_check",
                      "fa_sm_clock_read", "fa_query_launch",
                      "fa_sm_clock_probe", "fa_status_string", "fa_version"]
@@ -138,33 +139,39 @@ def test_strided_valid_layouts_reach_the_device(lib):
                                                                            fa.FA_ERR_ARCH)
 
 
-def _fp8(**kw):
+FP8_ENTRIES = ["fa_fwd_fp8", "fa_fwd_fp8_pair"]
+
+
+def _fp8(fn="fa_fwd_fp8", **kw):
     a = dict(q=GOOD, k=GOOD, vt=GOOD, o=GOOD, lse=GOOD, B=1, H=2, N=300, d=128, ldv=304,
              q_scale=0.01, k_scales=GOOD, v_scale=0.01, causal=0, scale=0.088)
     a.update(kw)
-    return fa.fa_fwd_fp8(a["q"], a["k"], a["vt"], a["o"], a["lse"], a["B"], a["H"], a["N"],
-                         a["d"], a["ldv"], a["q_scale"], a["k_scales"], a["v_scale"], a["causal"],
-                         a["scale"], 0)
+    return getattr(fa, fn)(a["q"], a["k"], a["vt"], a["o"], a["lse"], a["B"], a["H"], a["N"],
+                           a["d"], a["ldv"], a["q_scale"], a["k_scales"], a["v_scale"],
+                           a["causal"], a["scale"], 0)
 
 
+@pytest.mark.parametrize("fn", FP8_ENTRIES)
 @pytest.mark.parametrize("kw", [dict(q=0), dict(vt=0), dict(k_scales=0), dict(vt=GOOD + 8),
                                 dict(k_scales=GOOD + 2), dict(ldv=296), dict(ldv=300),
                                 dict(q_scale=0.0), dict(v_scale=float("nan")),
                                 dict(scale=-1.0), dict(N=0)])
-def test_fp8_bad_arguments_rejected(lib, kw):
-    assert _fp8(**kw) == fa.FA_ERR_INVALID_ARG
+def test_fp8_bad_arguments_rejected(lib, kw, fn):
+    assert _fp8(fn, **kw) == fa.FA_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("fn", FP8_ENTRIES)
 @pytest.mark.parametrize("kw", [dict(d=64), dict(d=96)])
-def test_fp8_head_dim_must_be_128(lib, kw):
-    assert _fp8(**kw) == fa.FA_ERR_UNSUPPORTED
+def test_fp8_head_dim_must_be_128(lib, kw, fn):
+    assert _fp8(fn, **kw) == fa.FA_ERR_UNSUPPORTED
 
 
-def test_fp8_valid_arguments_reach_the_device(lib):
+@pytest.mark.parametrize("fn", FP8_ENTRIES)
+def test_fp8_valid_arguments_reach_the_device(lib, fn):
     import torch
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
-    assert _fp8() in (fa.FA_ERR_CUDA, fa.FA_ERR_ARCH)
+    assert _fp8(fn) in (fa.FA_ERR_CUDA, fa.FA_ERR_ARCH)
 
 
 def _bwd(**kw):
@@ -241,7 +248,8 @@ C_PROGRAM = r"""
 int main(void) {
   /* every entry point is a plain C function */
   typedef void (*fn_t)(void);
-  fn_t fns[] = {(fn_t)fa_fwd, (fn_t)fa_fwd_pair, (fn_t)fa_fwd_strided, (fn_t)fa_fwd_fp8, (fn_t)fa_bwd,
+  fn_t fns[] = {(fn_t)fa_fwd, (fn_t)fa_fwd_pair, (fn_t)fa_fwd_strided, (fn_t)fa_fwd_fp8,
+                (fn_t)fa_fwd_fp8_pair, (fn_t)fa_bwd,
                 (fn_t)fa_bwd_workspace_size, (fn_t)fa_fwd_noalloc, (fn_t)fa_fwd_host,
                 (fn_t)fa_fwd_host_workspace_size, (fn_t)fa_check, (fn_t)fa_sm_clock_read,
                 (fn_t)fa_query_launch,

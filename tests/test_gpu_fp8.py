@@ -110,14 +110,15 @@ def test_pack_e4m3_matches_host_encoder(slib):
 
 # ------------------------------------------------------------ forward parity
 
-def _run_fp8(f, w):
+def _run_fp8(f, w, pair=False):
+    """fa_fwd_fp8 (or fa_fwd_fp8_pair) on the inputs; O bits and LSE."""
     import torch
     q8, k8, vt8 = (_dev_u8(t) for t in (f.q, f.k, f.vt))
     ks = torch.from_numpy(np.ascontiguousarray(f.k_scales)).to("cuda:0")
     o = torch.full((w.B, w.H, w.N, w.d), float("nan"), dtype=torch.bfloat16, device="cuda:0")
     lse = torch.full((w.B, w.H, w.N), float("nan"), dtype=torch.float32, device="cuda:0")
     fa.attention_forward_fp8_into(q8, k8, vt8, o, lse, f.q_scale, ks, f.v_scale, w.causal,
-                                  w.scale)
+                                  w.scale, pair=pair)
     torch.cuda.synchronize()
     assert fa.fa_check(0) == fa.FA_OK
     return to_bits(o), lse.cpu().numpy()
@@ -151,14 +152,38 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("pair", [False, True], ids=["auto", "cta_pair"])
 @pytest.mark.parametrize("B,H,N,causal,q_mult", SMALL)
-def test_fp8_small_every_element(slib, oracle_mod, B, H, N, causal, q_mult):
+def test_fp8_small_every_element(slib, oracle_mod, B, H, N, causal, q_mult, pair):
     w = I.custom("fp8small", B, H, N, 128, "e4m3", causal, 400 + N, q_mult)
     f = I.fp8_inputs(w)
-    o, lse = _run_fp8(f, w)
+    o, lse = _run_fp8(f, w, pair)
     o_ref, l_ref, bound = oracle_mod.attn_fp8(f.q, f.k, f.vt, f.q_scale, f.k_scales, f.v_scale,
                                               causal, w.scale)
-    _check(o.reshape(-1, 128), lse.reshape(-1), o_ref, l_ref, bound, f"fp8 B{B} H{H} N{N}")
+    _check(o.reshape(-1, 128), lse.reshape(-1), o_ref, l_ref, bound,
+           f"fp8{' pair' if pair else ''} B{B} H{H} N{N}")
+
+
+# Problems small enough (at most 32 units of 512 rows) or causal, which
+# fa_fwd_fp8 runs on the one-CTA kernel: the CTA pair must reproduce its bits.
+ONE_CTA_SHAPES = [
+    # B, H, N, causal, q_mult
+    (1, 4, 2048, False, 1.0),
+    (2, 3, 1000, False, 1.0),
+    (1, 2, 777, False, 3.0),
+    (2, 4, 1536, True, 1.0),
+    (1, 3, 1000, True, 3.0),
+    (4, 16, 4096, True, 1.0),
+]
+
+
+@pytest.mark.parametrize("B,H,N,causal,q_mult", ONE_CTA_SHAPES)
+def test_fp8_pair_matches_one_cta_bitwise(slib, B, H, N, causal, q_mult):
+    w = I.custom("fp8pairbits", B, H, N, 128, "e4m3", causal, 500 + N, q_mult)
+    f = I.fp8_inputs(w)
+    o1, l1 = _run_fp8(f, w)
+    o2, l2 = _run_fp8(f, w, pair=True)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2), (B, H, N, causal)
 
 
 @functools.lru_cache(maxsize=1)
