@@ -13,8 +13,10 @@ of the backward; halved for causal).
 
 Prints ONE JSON line (rank 0). Besides the headline workload it times every
 other named workload (the other 16-bit configurations and the two 8-bit
-shapes) in the same process, with the same steps, warm-up and L2 flush, under
-"other_workloads". The SM clock of each timed region is read from the kernels
+shapes) in the same process, with the same steps, warm-up, L2 flush and
+untimed soak before the timed steps (--soak-s: every figure is taken at the
+clock the board sustains under that load, which a 1.4 kW power cap sets),
+under "other_workloads". The SM clock of each timed region is read from the kernels
 themselves (clock64 / %globaltimer per CTA, fa_sm_clock_read), and the
 clock-corrected tensor fraction FLOPs / (t x SMs x 8192 x f_clock) is reported
 beside the fraction of the measured peak.
@@ -645,7 +647,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     else:
         peak16, peak_src = FALLBACK_PEAK_TFLOPS, "fallback"
 
-    # every other workload: same steps, warm-up and flush, one after another
+    # every other workload: same steps, warm-up, flush and untimed soak (so every
+    # figure is taken at the clock the board sustains), one after another
     other = {}
     head_inputs = None
     for name in others:
@@ -662,7 +665,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             oplan = forward_plan(fa, torch, ow, dev, stream, x=x, kernel="one_cta")
         else:
             oplan = make(fa, torch, ow, dev, stream, x=x)
-        ot = time_steps(fa, torch, oplan, stream, dev, flush, args.steps, args.warmup, world)
+        ot = time_steps(fa, torch, oplan, stream, dev, flush, args.steps, args.warmup, world,
+                        soak_s=args.soak_s)
         oms = ot["total_ms"] / args.steps
         otf = job_throughput(oplan.flops, ot["total_ms"], args.steps, world) / world
         opeak = oplan.peak_mult * peak16
