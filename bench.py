@@ -558,16 +558,18 @@ PAIR_PREFIX = "cta_pair:"   # other_workloads key: the CTA-pair kernel on a work
 ONE_PREFIX = "one_cta:"     # other_workloads key: the one-CTA kernel on a workload
 
 
-def other_workload_names(headline: str, pass_: str) -> list[str]:
+def other_workload_names(headline: str, pass_: str, picks_pair=None) -> list[str]:
     """Every other named workload; in the forward pass also the 8-bit shapes
     and, on every head-dimension-128 16-bit workload (the headline's
-    included), the kernel fa_fwd does not pick there (the CTA-pair kernel on
-    causal ones, the one-CTA kernel on the others), so both kernels are timed
-    in the same run."""
+    included), the kernel fa_fwd does not pick there, so both kernels are
+    timed in the same run. picks_pair(name) says whether fa_fwd runs the
+    CTA-pair kernel on a workload (default: on the non-causal ones)."""
+    if picks_pair is None:
+        picks_pair = lambda n: not I.WORKLOADS[n].causal  # noqa: E731
     names = [n for n in I.WORKLOAD_ORDER if n != headline]
     if pass_ == "forward":
         names += [n for n in I.FP8_WORKLOADS if n != headline]
-        names += [(PAIR_PREFIX if I.WORKLOADS[n].causal else ONE_PREFIX) + n
+        names += [(ONE_PREFIX if picks_pair(n) else PAIR_PREFIX) + n
                   for n in I.WORKLOAD_ORDER if I.WORKLOADS[n].d == 128]
     return names
 
@@ -589,8 +591,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     if others:
         pool = cf.ProcessPoolExecutor(max_workers=min(len(others), max(1, os.cpu_count() or 1)),
                                       mp_context=mp.get_context("spawn"))
-        futures = {n: pool.submit(_gen_inputs, _base_name(n)) for n in others
-                   if _base_name(n) != args.workload}
+        futures = {b: pool.submit(_gen_inputs, b)
+                   for b in sorted({_base_name(n) for n in others}) if b != args.workload}
 
     import torch
 
@@ -602,6 +604,11 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     fabuild.build()
     fa.load_library()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    if others:  # the other kernel of each head-dimension-128 workload, by fa_fwd's own choice
+        others = other_workload_names(
+            args.workload, args.pass_,
+            picks_pair=lambda n: fa.fa_query_launch(*(getattr(I.WORKLOADS[n], k) for k in
+                                                      ("B", "H", "N", "d", "causal")))["cluster"] == 2)
     w = get_workload(args.workload)
     stream = torch.cuda.current_stream(dev)
     make = backward_plan if args.pass_ == "backward" else forward_plan
@@ -654,8 +661,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     for name in others:
         base = _base_name(name)
         ow = get_workload(base)
-        if name in futures:
-            x = futures[name].result()
+        if base in futures:
+            x = futures[base].result()
         else:  # the headline workload on the pair kernel: its own inputs
             head_inputs = head_inputs if head_inputs is not None else workload_inputs(ow)
             x = head_inputs

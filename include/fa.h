@@ -74,8 +74,9 @@ typedef struct fa_strides {
  * Asynchronous: returns after the launch is enqueued; O and LSE are valid
  * once the stream reaches that point. Arguments are checked before anything
  * is enqueued; on any error nothing is launched and nothing is written.
- * Head dimension 128 without a causal mask runs on CTA pairs when the problem
- * fills the GPU (see fa_query_launch); the results do not depend on it.
+ * Head dimension 128 runs on CTA pairs (fa_fwd_pair) when the problem fills
+ * the GPU and is not causal, or causal with N >= 16384 (see fa_query_launch);
+ * the results do not depend on it.
  * The first call on a device allocates a small device status word for that
  * device (kept until process exit); later calls allocate nothing.
  * A kernel whose internal waits run past their limit stops early and records
@@ -310,8 +311,8 @@ fa_status fa_sm_clock_read(void* stream, double* sm_mhz, unsigned long long* cta
  * bytes per CTA, the number of work units (256 query rows of one head, or 512
  * for the CTA-pair kernel) and the cluster size (1: one CTA per unit; 2: the
  * CTA-pair kernel, which fa_fwd runs for head dimension 128 without a causal
- * mask when there are at least as many 512-row units as SM pairs; its results
- * are the one-CTA kernel's bit for bit). Any output pointer may be NULL. Host
+ * mask, or with one when N >= 16384, when there are at least as many 512-row
+ * units as SM pairs; its results are the one-CTA kernel's bit for bit). Any output pointer may be NULL. Host
  * memory only; enqueues nothing.
  */
 fa_status fa_query_launch(int B, int H, int N, int d, int causal, int* grid, int* threads,

@@ -141,7 +141,7 @@ def test_pair_named_workload(oracle_named, name):
 
 @pytest.mark.parametrize("B,H,N,dtype,causal", [
     (2, 4, 1500, "bf16", True), (1, 3, 700, "fp16", False), (2, 200, 128, "bf16", True),
-    (4, 16, 4096, "bf16", True), (4, 16, 4096, "fp16", False),
+    (4, 16, 4096, "bf16", True), (4, 16, 4096, "fp16", False), (1, 32, 16384, "bf16", True),
 ])
 def test_pair_bitwise_equal_to_one_cta_kernel(B, H, N, dtype, causal):
     import torch

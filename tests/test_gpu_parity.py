@@ -234,9 +234,11 @@ def test_query_launch_is_persistent():
     import torch
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     for (B, H, N, d, causal) in ((4, 16, 4096, 128, True), (2, 32, 8192, 64, False),
-                                 (1, 1, 300, 128, False), (4, 16, 4096, 128, False)):
+                                 (1, 1, 300, 128, False), (4, 16, 4096, 128, False),
+                                 (1, 32, 16384, 128, True), (2, 32, 8192, 128, True)):
         info = fa.fa_query_launch(B, H, N, d, causal)
-        pair = d == 128 and not causal and B * H * ((N + 511) // 512) >= sms // 2
+        pair = (d == 128 and (not causal or N >= 16384)
+                and B * H * ((N + 511) // 512) >= sms // 2)
         assert info["cluster"] == (2 if pair else 1)
         if pair:   # CTA pairs over 512-row units
             assert info["units"] == B * H * ((N + 511) // 512)
