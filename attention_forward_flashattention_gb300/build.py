@@ -26,7 +26,7 @@ LIB_UNITS = ["fa_host.cu", "fa_fwd_d64.cu", "fa_fwd_d128.cu", "fa_fwd_fp8.cu", "
              "fa_bwd_d64.cu", "fa_bwd_d128.cu", "fa_noalloc.cu", "fa_pipeline.cu"]
 SELFTEST_UNITS = ["selftest.cu"]
 HEADERS = ["ptx.cuh", "fa_common.cuh", "fa_kernel.cuh", "fa_launch.cuh", "fa_pair.cuh", "fa_bwd.cuh",
-           "fa_bwd_launch.cuh"]
+           "fa_bwd_launch.cuh", "fa_dispatch.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -17,6 +17,7 @@
 #include "fa.h"
 #include "fa_bwd.cuh"
 #include "fa_kernel.cuh"
+#include "fa_dispatch.h"
 #include "fa_pair.cuh"
 
 namespace fa {

@@ -661,29 +661,6 @@ cudaError_t launch_fwd_pair(bool bf16, bool causal, const CUtensorMap* maps, con
 cudaError_t launch_fwd_pair_fp8(bool causal, const CUtensorMap* maps, const FwdArgs& a, int grid,
                                 cudaStream_t stream);
 int fwd_smem_bytes_pair(bool fp8 = false);
-// Whether fa_fwd / fa_fwd_strided run the pair kernel: head dimension 128,
-// enough 512-row units to give every SM pair one, and non-causal or long
-// causal rows. Same-box measurements (row maximum from the S loads):
-// non-causal B4 H16 N4096 ~5 % faster than the one-CTA kernel (~15 % in a
-// power-capped sustained run); causal N = 4096 ~5 % slower (a 512-row unit
-// visits up to two more wholly masked KV tiles than two 256-row units, a
-// larger share of short rows' work), N = 8192 / 12288 even, N = 16384 and
-// 32768 1-2 % faster. The two kernels' results are identical bit for bit.
-inline bool fwd_prefers_pair(int d, bool causal, long long BH, int N, int sm_count) {
-  return d == 128 && (!causal || N >= 16384) &&
-         BH * ((static_cast<long long>(N) + 511) / 512) >= sm_count / 2;
-}
-
-// Whether fa_fwd_fp8 runs the pair kernel (8-bit inputs are always head
-// dimension 128). Kept to the one-CTA kernel until measured otherwise.
-inline bool fwd_fp8_prefers_pair(bool causal, long long BH, int N, int sm_count) {
-  (void)causal;
-  (void)BH;
-  (void)N;
-  (void)sm_count;
-  return false;
-}
-
 // Grid of the pair kernel for n_units units: two CTAs per pair, one pair per
 // two SMs at most.
 inline int fwd_grid_pair(int n_units, int sm_count) {
