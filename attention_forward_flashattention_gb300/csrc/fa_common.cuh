@@ -372,6 +372,23 @@ __device__ __forceinline__ void issue_pv_fp8(uint32_t d_tmem, uint32_t p_tmem, u
   }
 }
 
+// O[tmem] (+)= P V with both operands in shared memory: P[128 x 128 keys]
+// (e4m3, K-major SW128, one panel) and V^T[128 columns of O][128 keys].
+template <bool kElect = false>
+__device__ __forceinline__ void issue_pv_fp8_ss(uint32_t d_tmem, uint64_t dp, uint64_t dvt,
+                                                bool accumulate) {
+  constexpr uint32_t id = ptx::idesc_f8(128, 128);
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    const uint32_t acc = (accumulate || kk > 0) ? 1u : 0u;
+    if constexpr (kElect) ptx::umma_f8_ss_elect(d_tmem, dp, dvt, id, acc);
+    else ptx::umma_f8_ss(d_tmem, dp, dvt, id, acc);
+    dp = desc_add(dp, 32u);
+    dvt = desc_add(dvt, 32u);
+    asm volatile("" : "+l"(dp), "+l"(dvt));
+  }
+}
+
 // Pair MMAs for head dimension 128 (M = 256: 128 query rows in each CTA).
 // S = Q K^T: each CTA holds its 128 Q rows (two 16 KB panels) and 64 of the
 // 128 keys (two 8 KB panels of 64 rows); the pair's S has all 128 keys.

@@ -84,7 +84,13 @@ struct Layout {
   static constexpr int kStages = (D == 128 && !FP8) ? 4 : 8;  // K / V ring slots
   static constexpr int kOffQ = 0;                           // Q0, Q1
   static constexpr int kOffKV = 2 * kTileBytes;             // ring
-  static constexpr int kOffStats = kOffKV + kStages * kTileBytes;  // [2 tiles][128] row sums l
+  // 8-bit inputs: P_i goes through shared memory (one 128 x 128-byte panel
+  // each; tensor memory holds S0, S1, O0, O1 and has no room for it), so
+  // S_i(j+1) can be computed while softmax(j) runs and the PV products read
+  // both operands from shared memory.
+  static constexpr bool kPSmem = FP8;
+  static constexpr int kOffP = kOffKV + kStages * kTileBytes;  // P0, P1 (kPSmem)
+  static constexpr int kOffStats = kOffP + (kPSmem ? 2 * kTileBytes : 0);  // [2][128] row sums l
   // O staging for the TMA-store epilogue: one 32-row x 128-byte slice per
   // epilogue warp (1024-byte aligned, as the 128-byte swizzle requires)
   static constexpr int kOffOut = kOffStats + 1024;
@@ -98,7 +104,10 @@ struct Layout {
   // values per column), so S_i(j+1) can be computed while softmax(j) runs.
   static constexpr bool kSepP = D == 64 && !FP8;
   static constexpr uint32_t kColP = 256 + 2 * D;  // P_i at kColP + i*64 (kSepP)
-  static_assert(!kSepP || kStages % 2 == 0, "kSepP: K tiles in even ring slots, V in odd");
+  // P_i apart from S_i (TMEM columns of its own, or shared memory): S and PV
+  // products are issued by separate warps, with S-free / P-free barriers
+  static constexpr bool kSplit = kSepP || kPSmem;
+  static_assert(!kSplit || kStages % 2 == 0, "kSplit: K tiles in even ring slots, V in odd");
   static_assert(!kSepP || kColP + 128 <= kTmemCols, "TMEM columns");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kOffBar % 8 == 0, "barrier block alignment");
@@ -343,10 +352,10 @@ __device__ __forceinline__ void mma_role(const FwdArgs& a, uint32_t sbase, uint3
 // the unit's tiles (so with an even slot count K lands in even slots, V in
 // odd ones, and a V slot is free once both PV warps have released it).
 // (Both roles serve the Q tiles I0 .. I1-1 and drain on barrier DRAIN.)
-template <int D, bool BF16, bool CAUSAL, int I0, int I1, int DRAIN>
+template <int D, bool BF16, bool CAUSAL, bool FP8, int I0, int I1, int DRAIN>
 __device__ __forceinline__ void mma_s_role(const FwdArgs& a, uint32_t sbase, uint32_t bars,
                                            uint32_t tmem, const AbortCtx& ab) {
-  using L = Layout<D, false>;
+  using L = Layout<D, FP8>;
   constexpr int S = L::kStages;
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
   const uint64_t dQ[2] = {desc_kmajor(sbase + L::kOffQ),
@@ -374,7 +383,8 @@ __device__ __forceinline__ void mma_s_role(const FwdArgs& a, uint32_t sbase, uin
           ok = wait_spin_warp(bar(kBarSFree + i), (scnt[i]++) & 1u, ab, kStatusMma);
         if (!ok) break;
         ptx::tc_fence_after();
-        issue_qk_desc<D, BF16, true>(tS[i], dQ[i], desc_add(dK0, slot_off(kn)));
+        if constexpr (FP8) issue_qk_fp8<true>(tS[i], dQ[i], desc_add(dK0, slot_off(kn)));
+        else issue_qk_desc<D, BF16, true>(tS[i], dQ[i], desc_add(dK0, slot_off(kn)));
         ptx::umma_commit_elect(bar(kBarSFull + i));
       }
       if (!ok) break;
@@ -389,13 +399,16 @@ __device__ __forceinline__ void mma_s_role(const FwdArgs& a, uint32_t sbase, uin
   wait_drain(bar(DRAIN), 0u, ab, kStatusDrain);
 }
 
-template <int D, bool BF16, bool CAUSAL, int I0, int I1, int DRAIN>
+template <int D, bool BF16, bool CAUSAL, bool FP8, int I0, int I1, int DRAIN>
 __device__ __forceinline__ void mma_pv_role(const FwdArgs& a, uint32_t sbase, uint32_t bars,
                                             uint32_t tmem, const AbortCtx& ab) {
-  using L = Layout<D, false>;
+  using L = Layout<D, FP8>;
   constexpr int S = L::kStages;
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
-  const uint64_t dV0 = desc_v(sbase + L::kOffKV);
+  // V as stored ([key][d], MN-major B), or V^T for 8-bit (K-major)
+  const uint64_t dV0 = FP8 ? desc_kmajor(sbase + L::kOffKV) : desc_v(sbase + L::kOffKV);
+  const uint64_t dP[2] = {desc_kmajor(sbase + L::kOffP),  // (kPSmem)
+                          desc_kmajor(sbase + L::kOffP + L::kTileBytes)};
   const uint32_t tO[2] = {tmem + L::kColO, tmem + L::kColO + D};
   const uint32_t tP[2] = {tmem + L::kColP, tmem + L::kColP + 64};
   auto slot_off = [](uint32_t idx) { return (idx % S) * static_cast<uint32_t>(L::kTileBytes); };
@@ -418,7 +431,8 @@ __device__ __forceinline__ void mma_pv_role(const FwdArgs& a, uint32_t sbase, ui
             !(ok = wait_spin_warp(bar(kBarOFree + i), (units - 1) & 1u, ab, kStatusMma)))
           break;
         ptx::tc_fence_after();
-        issue_pv_ts_desc<D, BF16, true>(tO[i], tP[i], desc_add(dV0, slot_off(vj)), j > 0);
+        if constexpr (FP8) issue_pv_fp8_ss<true>(tO[i], dP[i], desc_add(dV0, slot_off(vj)), j > 0);
+        else issue_pv_ts_desc<D, BF16, true>(tO[i], tP[i], desc_add(dV0, slot_off(vj)), j > 0);
         ptx::umma_commit_elect(bar(kBarPFree + i));
         if (j + 1 == nkv) ptx::umma_commit_elect(bar(kBarOFull + i));
       }
@@ -433,9 +447,9 @@ __device__ __forceinline__ void mma_pv_role(const FwdArgs& a, uint32_t sbase, ui
 }
 
 template <int D, bool BF16, bool CAUSAL, bool FP8>
-__device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t bars, uint32_t tmem,
-                                             float* stats, const AbortCtx& ab, int warp,
-                                             int lane) {
+__device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t sbase, uint32_t bars,
+                                             uint32_t tmem, float* stats, const AbortCtx& ab,
+                                             int warp, int lane) {
   using L = Layout<D, FP8>;
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
   const int wg = (warp >> 2) - 1;           // which Q tile
@@ -444,7 +458,9 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t bars, ui
   const uint32_t tS = tl + L::kColS + 128u * wg;  // S_i; P_i over its first 64 columns
   // or in columns of its own (kSepP)
   const uint32_t tP = L::kSepP ? tl + L::kColP + 64u * wg : tS;
-  uint32_t pstores = 0;  // P_i stores so far (kSepP: each but the first waits for P-free)
+  // or in shared memory (kPSmem: the A operand of the PV product, K-major)
+  const uint32_t sP = sbase + L::kOffP + static_cast<uint32_t>(wg * L::kTileBytes);
+  uint32_t pstores = 0;  // P_i stores so far (kSplit: each but the first waits for P-free)
   const uint32_t tO = tl + L::kColO + static_cast<uint32_t>(D) * wg;
   const float cl2 = a.scale_log2;
   uint32_t scnt = 0, units = 0;
@@ -458,10 +474,10 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t bars, ui
     // exponentials, for the LSE. They differ only for bf16 (see below).
     float m_ref = -INFINITY, l = 0.f, l_exp = 0.f;
     for (int j = 0; j < nkv; ++j) {
-      // d = 64 computes S_i(j+1) during softmax(j), so S is usually ready: poll
-      // (resumes sooner); otherwise suspend, leaving issue slots to the other
-      // tile's softmax on the same sub-partition
-      if (!(ok = L::kSepP
+      // with P apart from S, S_i(j+1) is computed during softmax(j), so S is
+      // usually ready: poll (resumes sooner); otherwise suspend, leaving issue
+      // slots to the other tile's softmax on the same sub-partition
+      if (!(ok = L::kSplit
                      ? wait_spin_warp(bar(kBarSFull + wg), scnt & 1u, ab, kStatusSoftmax)
                      : wait_bounded_warp(bar(kBarSFull + wg), scnt & 1u, ab, kStatusSoftmax)))
         break;
@@ -478,7 +494,7 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t bars, ui
       ptx::tmem_ld64_max(tS + 64u, sr[1], mx_hi);
       ptx::tmem_ld_wait64x2(sr[0], sr[1]);
       ptx::tmem_ld_wait_f2(mx_lo, mx_hi);
-      if constexpr (L::kSepP) {  // S_i is in registers: S_i(j+1) may overwrite it
+      if constexpr (L::kSplit) {  // S_i is in registers: S_i(j+1) may overwrite it
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(kBarSFree + wg));
       }
@@ -521,8 +537,9 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t bars, ui
 #pragma unroll
       for (int t = 0; t < 4; ++t) ls[t] = lr[t] = make_float2(0.f, 0.f);
       if constexpr (FP8) {
-        // P as e4m3, four keys per TMEM column over the first 32 S_i columns
-        // (O is normalised by the unrounded sum).
+        // P as e4m3, four keys per 32-bit word (O is normalised by the
+        // unrounded sum), into shared memory (kPSmem) or over the first 32
+        // S_i columns.
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
@@ -534,7 +551,20 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t bars, ui
           ls[(2 * c) & 3] = ptx::fadd2(ls[(2 * c) & 3], make_float2(p0, p1));
           ls[(2 * c + 1) & 3] = ptx::fadd2(ls[(2 * c + 1) & 3], make_float2(p2, p3));
         }
-        ptx::tmem_st32(tS, pk);
+        if constexpr (L::kPSmem) {
+          // P_i(j-1) read and O_i updated by its PV before P_i is rewritten
+          // (and before the O rescale below)
+          if (pstores > 0 &&
+              !(ok = wait_spin_warp(bar(kBarPFree + wg), (pstores - 1) & 1u, ab,
+                                    kStatusSoftmax)))
+            break;
+          ptx::tc_fence_after();
+          ++pstores;
+          store_row_panel_sw128(sP, r, pk);
+          ptx::fence_proxy_async_smem();  // visible to the tensor core's reads
+        } else {
+          ptx::tmem_st32(tS, pk);
+        }
       } else {
         uint32_t pk[2][32];
 #pragma unroll
@@ -728,8 +758,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     ptx::mbar_init(bar(kBarDrainPV + 1), 1);
     for (int s = 0; s < L::kStages; ++s) {
       ptx::mbar_init(bar(kBarKVFull + s), 1);
-      // kSepP: a V slot (odd) is released by both PV warps, a K slot by the S warp
-      ptx::mbar_init(bar(kBarKVFull + L::kStages + s), (L::kSepP && (s & 1)) ? 2 : 1);
+      // kSplit: a V slot (odd) is released by both PV warps, a K slot by the S warp
+      ptx::mbar_init(bar(kBarKVFull + L::kStages + s), (L::kSplit && (s & 1)) ? 2 : 1);
     }
     *abort_flag = 0u;
     ptx::fence_mbar_init();
@@ -748,16 +778,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     ptx::setmaxnreg_dec<kRegsWG0>();
     if (warp == 0) {
       if (lane == 0) producer_role<D, BF16, CAUSAL, FP8>(&tm_q, &tm_k, &tm_v, a, sbase, bars, ab);
-    } else if constexpr (L::kSepP) {  // MMA issue split over warps 1, 2 and 3
-      if (warp == 2) mma_s_role<D, BF16, CAUSAL, 0, 2, kBarDrain>(a, sbase, bars, tmem, ab);
-      else if (warp == 3) mma_pv_role<D, BF16, CAUSAL, 0, 1, kBarDrainPV>(a, sbase, bars, tmem, ab);
-      else if (warp == 1) mma_pv_role<D, BF16, CAUSAL, 1, 2, kBarDrainPV + 1>(a, sbase, bars, tmem, ab);
+    } else if constexpr (L::kSplit) {  // MMA issue split over warps 1, 2 and 3
+      if (warp == 2) mma_s_role<D, BF16, CAUSAL, FP8, 0, 2, kBarDrain>(a, sbase, bars, tmem, ab);
+      else if (warp == 3)
+        mma_pv_role<D, BF16, CAUSAL, FP8, 0, 1, kBarDrainPV>(a, sbase, bars, tmem, ab);
+      else if (warp == 1)
+        mma_pv_role<D, BF16, CAUSAL, FP8, 1, 2, kBarDrainPV + 1>(a, sbase, bars, tmem, ab);
     } else if (warp == 1) {
       mma_role<D, BF16, CAUSAL, FP8>(a, sbase, bars, tmem, ab);  // the whole warp
     }
   } else if (wgrp < 3) {
     ptx::setmaxnreg_inc<kRegsSoftmax>();
-    softmax_role<D, BF16, CAUSAL, FP8>(a, bars, tmem, stats, ab, warp, lane);
+    softmax_role<D, BF16, CAUSAL, FP8>(a, sbase, bars, tmem, stats, ab, warp, lane);
   } else {
     ptx::setmaxnreg_dec<kRegsEpilogue>();
     epilogue_role<D, BF16, CAUSAL, FP8>(&tm_o, a, sbase, bars, tmem, stats, ab, warp, lane);
