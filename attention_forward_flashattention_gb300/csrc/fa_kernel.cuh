@@ -14,8 +14,9 @@
 //                issued by one thread, "TCA 51%, MFU below 8%", B200 section).
 //        warps 2-3 idle, except where P is kept apart from S (d = 64: TMEM
 //                columns of its own; 8-bit inputs: shared memory): there
-//                the S products come from warp 2 and the PV products of
-//                tile 0 / tile 1 from warp 3 / warp 1 (see mma_s_role).
+//                the S products come from warp 2 and the PV products from
+//                warp 3 (d = 64: tile 0's from warp 3, tile 1's from
+//                warp 1; see mma_s_role).
 //   WG1  softmax of Q tile 0, one thread per row = TMEM lane (the B300
 //        walkthrough, V14 item d);
 //   WG2  softmax of Q tile 1;
@@ -114,6 +115,10 @@ struct Layout {
   // P_i apart from S_i (TMEM columns of its own, or shared memory): S and PV
   // products are issued by separate warps, with S-free / P-free barriers
   static constexpr bool kSplit = kSepP || kPSmem;
+  // PV products of the two tiles from two warps (d = 64) or from one (8-bit):
+  // same-box A/B with the row maximum from the S loads, d = 64 1179 -> 1198
+  // TFLOPS (causal 921 -> 989), 8-bit 1998 -> 1969 (causal 1713 -> 1671)
+  static constexpr bool kPvPerTile = kSepP;
   static_assert(!kSplit || kStages % 2 == 0, "kSplit: K tiles in even ring slots, V in odd");
   static_assert(!kSepP || kColP + 128 <= kTmemCols, "TMEM columns");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -342,22 +347,25 @@ __device__ __forceinline__ void mma_role(const FwdArgs& a, uint32_t sbase, uint3
   wait_drain(bar(kBarDrain), 0u, ab, kStatusDrain);
 }
 
-// MMA issue when P_i has TMEM columns of its own (d = 64), split over three
-// warps on three SM sub-partitions: each tcgen05.mma takes issue cycles from
-// the softmax warps sharing its sub-partition, and a softmax warp slowed that
-// way delays its whole tile (P-full waits for all four). Per KV step the S
-// warp issues 8 products and each PV warp 8; with one PV warp for both tiles
-// (16 products) the two softmax warps beside it finished ~1700 cycles after
-// their siblings on every step. S products never touch the P or O columns,
-// so the warps need no ordering beyond the softmax's own barriers:
+// MMA issue when P_i is kept apart from S_i (d = 64: TMEM columns of its
+// own; 8-bit: shared memory), split over separate warps on separate SM
+// sub-partitions: each tcgen05.mma takes issue cycles from the softmax warps
+// sharing its sub-partition, and a softmax warp slowed that way delays its
+// whole tile (P-full waits for all four). At d = 64 the S warp issues 8
+// products per KV step and each of two PV warps (one per tile) 8; with one
+// PV warp for both tiles (16 products) the two softmax warps beside it
+// finished ~1700 cycles after their siblings on every step. The 8-bit kernel
+// measured faster with one PV warp (kPvPerTile). S products never touch the
+// P or O columns, so the warps need no ordering beyond the softmax's own
+// barriers:
 //   S warp:   S_i(j+1) = Q_i K_{j+1}^T once softmax i has read S_i(j);
-//   PV warps: O_i += P_i(j) V_j once P_i(j) is written (one warp per tile),
-//             then P-free (O_i updated, P_i reusable), and O-full after a
-//             unit's last one.
+//   PV warp(s): O_i += P_i(j) V_j once P_i(j) is written, then P-free (O_i
+//             updated, P_i reusable), and O-full after a unit's last one.
 // The softmax of tile j+1 never waits for PV(j): only its P store and O
 // rescale do. All walk the same K, V ring: K_j at index 2j, V_j at 2j+1 of
 // the unit's tiles (so with an even slot count K lands in even slots, V in
-// odd ones, and a V slot is free once both PV warps have released it).
+// odd ones, and at d = 64 a V slot is free once both PV warps have released
+// it).
 // (Both roles serve the Q tiles I0 .. I1-1 and drain on barrier DRAIN.)
 template <int D, bool BF16, bool CAUSAL, bool FP8, int I0, int I1, int DRAIN>
 __device__ __forceinline__ void mma_s_role(const FwdArgs& a, uint32_t sbase, uint32_t bars,
@@ -765,8 +773,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     ptx::mbar_init(bar(kBarDrainPV + 1), 1);
     for (int s = 0; s < L::kStages; ++s) {
       ptx::mbar_init(bar(kBarKVFull + s), 1);
-      // kSplit: a V slot (odd) is released by both PV warps, a K slot by the S warp
-      ptx::mbar_init(bar(kBarKVFull + L::kStages + s), (L::kSplit && (s & 1)) ? 2 : 1);
+      // kPvPerTile: a V slot (odd) is released by both PV warps, a K slot by the S warp
+      ptx::mbar_init(bar(kBarKVFull + L::kStages + s), (L::kPvPerTile && (s & 1)) ? 2 : 1);
     }
     *abort_flag = 0u;
     ptx::fence_mbar_init();
@@ -785,12 +793,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     ptx::setmaxnreg_dec<kRegsWG0>();
     if (warp == 0) {
       if (lane == 0) producer_role<D, BF16, CAUSAL, FP8>(&tm_q, &tm_k, &tm_v, a, sbase, bars, ab);
-    } else if constexpr (L::kSplit) {  // MMA issue split over warps 1, 2 and 3
+    } else if constexpr (L::kSplit) {  // MMA issue split over warps 2, 3 (and 1)
       if (warp == 2) mma_s_role<D, BF16, CAUSAL, FP8, 0, 2, kBarDrain>(a, sbase, bars, tmem, ab);
-      else if (warp == 3)
-        mma_pv_role<D, BF16, CAUSAL, FP8, 0, 1, kBarDrainPV>(a, sbase, bars, tmem, ab);
-      else if (warp == 1)
-        mma_pv_role<D, BF16, CAUSAL, FP8, 1, 2, kBarDrainPV + 1>(a, sbase, bars, tmem, ab);
+      else if constexpr (L::kPvPerTile) {
+        if (warp == 3)
+          mma_pv_role<D, BF16, CAUSAL, FP8, 0, 1, kBarDrainPV>(a, sbase, bars, tmem, ab);
+        else if (warp == 1)
+          mma_pv_role<D, BF16, CAUSAL, FP8, 1, 2, kBarDrainPV + 1>(a, sbase, bars, tmem, ab);
+      } else if (warp == 3) {
+        mma_pv_role<D, BF16, CAUSAL, FP8, 0, 2, kBarDrainPV>(a, sbase, bars, tmem, ab);
+      }
     } else if (warp == 1) {
       mma_role<D, BF16, CAUSAL, FP8>(a, sbase, bars, tmem, ab);  // the whole warp
     }
