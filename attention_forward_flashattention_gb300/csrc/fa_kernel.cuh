@@ -249,24 +249,22 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* tm_q, const CUt
 // everything else minimal: descriptors are built once and advanced in place,
 // waits are warp-uniform try_waits, commits are elected (a few cycles each,
 // against ~47 from a lone thread), and each step commits only what a waiter
-// needs.
-template <int D, bool BF16, bool CAUSAL, bool FP8>
+// needs. (16-bit, P over S: head dimension 128; the other paths issue from
+// mma_s_role / mma_pv_role.)
+template <int D, bool BF16, bool CAUSAL>
 __device__ __forceinline__ void mma_role(const FwdArgs& a, uint32_t sbase, uint32_t bars,
                                          uint32_t tmem, const AbortCtx& ab) {
-  using L = Layout<D, FP8>;
+  using L = Layout<D, false>;
+  static_assert(!L::kSplit, "P over S only");
   constexpr int S = L::kStages;
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
   const uint64_t dQ[2] = {desc_kmajor(sbase + L::kOffQ),
                           desc_kmajor(sbase + L::kOffQ + L::kTileBytes)};
   const uint64_t dK0 = desc_kmajor(sbase + L::kOffKV);  // ring slot s: + s * kTileBytes
-  // V as stored ([key][d], MN-major B operand), or V^T for 8-bit (K-major)
-  const uint64_t dV0 = FP8 ? desc_kmajor(sbase + L::kOffKV) : desc_v(sbase + L::kOffKV);
+  const uint64_t dV0 = desc_v(sbase + L::kOffKV);  // V as stored ([key][d], MN-major B)
   const uint32_t tS[2] = {tmem + L::kColS, tmem + L::kColS + 128};
   const uint32_t tO[2] = {tmem + L::kColO, tmem + L::kColO + D};
-  auto qk = [&](int i, uint64_t dk) {
-    if constexpr (FP8) issue_qk_fp8<true>(tS[i], dQ[i], dk);
-    else issue_qk_desc<D, BF16, true>(tS[i], dQ[i], dk);
-  };
+  auto qk = [&](int i, uint64_t dk) { issue_qk_desc<D, BF16, true>(tS[i], dQ[i], dk); };
   auto slot_off = [](uint32_t idx) { return (idx % S) * static_cast<uint32_t>(L::kTileBytes); };
   auto kv_wait = [&](uint32_t idx) {
     return wait_spin_warp(bar(kBarKVFull + idx % S), (idx / S) & 1u, ab, kStatusMma);
@@ -310,8 +308,7 @@ __device__ __forceinline__ void mma_role(const FwdArgs& a, uint32_t sbase, uint3
             !(ok = wait_spin_warp(bar(kBarOFree + i), (units - 1) & 1u, ab, kStatusMma)))
           break;
         ptx::tc_fence_after();
-        if constexpr (FP8) issue_pv_fp8<true>(tO[i], tS[i], dv, j > 0);
-        else issue_pv_ts_desc<D, BF16, true>(tO[i], tS[i], dv, j > 0);
+        issue_pv_ts_desc<D, BF16, true>(tO[i], tS[i], dv, j > 0);
         if (i == 0 && rel_pending) {
           ptx::umma_commit_elect(bar(kBarKVFull + S + rel_v % S));
           ptx::umma_commit_elect(bar(kBarKVFull + S + rel_k % S));
@@ -553,8 +550,8 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t sbase, u
       for (int t = 0; t < 4; ++t) ls[t] = lr[t] = make_float2(0.f, 0.f);
       if constexpr (FP8) {
         // P as e4m3, four keys per 32-bit word (O is normalised by the
-        // unrounded sum), into shared memory (kPSmem) or over the first 32
-        // S_i columns.
+        // unrounded sum), into shared memory.
+        static_assert(L::kPSmem, "8-bit P goes through shared memory");
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
@@ -566,20 +563,15 @@ __device__ __forceinline__ void softmax_role(const FwdArgs& a, uint32_t sbase, u
           ls[(2 * c) & 3] = ptx::fadd2(ls[(2 * c) & 3], make_float2(p0, p1));
           ls[(2 * c + 1) & 3] = ptx::fadd2(ls[(2 * c + 1) & 3], make_float2(p2, p3));
         }
-        if constexpr (L::kPSmem) {
-          // P_i(j-1) read and O_i updated by its PV before P_i is rewritten
-          // (and before the O rescale below)
-          if (pstores > 0 &&
-              !(ok = wait_spin_warp(bar(kBarPFree + wg), (pstores - 1) & 1u, ab,
-                                    kStatusSoftmax)))
-            break;
-          ptx::tc_fence_after();
-          ++pstores;
-          store_row_panel_sw128(sP, r, pk);
-          ptx::fence_proxy_async_smem();  // visible to the tensor core's reads
-        } else {
-          ptx::tmem_st32(tS, pk);
-        }
+        // P_i(j-1) read and O_i updated by its PV before P_i is rewritten
+        // (and before the O rescale below)
+        if (pstores > 0 &&
+            !(ok = wait_spin_warp(bar(kBarPFree + wg), (pstores - 1) & 1u, ab, kStatusSoftmax)))
+          break;
+        ptx::tc_fence_after();
+        ++pstores;
+        store_row_panel_sw128(sP, r, pk);
+        ptx::fence_proxy_async_smem();  // visible to the tensor core's reads
       } else {
         uint32_t pk[2][32];
 #pragma unroll
@@ -804,7 +796,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mma_pv_role<D, BF16, CAUSAL, FP8, 0, 2, kBarDrainPV>(a, sbase, bars, tmem, ab);
       }
     } else if (warp == 1) {
-      mma_role<D, BF16, CAUSAL, FP8>(a, sbase, bars, tmem, ab);  // the whole warp
+      mma_role<D, BF16, CAUSAL>(a, sbase, bars, tmem, ab);  // the whole warp
     }
   } else if (wgrp < 3) {
     ptx::setmaxnreg_inc<kRegsSoftmax>();
