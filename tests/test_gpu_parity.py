@@ -278,6 +278,9 @@ STRIDED = [
     (2, 2, 300, 128, "bf16", True, ("pad", "pad", "pad", "pad")),
     (1, 3, 1000, 64, "fp16", False, ("bnhd", "bhnd", "pad", "pad")),
     (3, 2, 129, 128, "fp16", True, ("bhnd", "bnhd", "bhnd", "bnhd")),
+    # large enough for fa_fwd's CTA-pair kernel (checked below), ragged N
+    (1, 16, 2500, 128, "fp16", False, ("bnhd", "pad", "bnhd", "pad")),
+    (1, 3, 16400, 128, "bf16", True, ("pad", "bnhd", "bnhd", "bnhd")),
 ]
 
 
@@ -292,6 +295,8 @@ def test_strided_views_every_element(oracle_mod, B, H, N, d, dtype, causal, layo
                    layouts[3], pad_value=sentinel)
     lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device="cuda:0")
     assert any(not t.is_contiguous() for t in (qd, kd, vd, o))
+    if N >= 2500:  # these cases exist to put strided views through the CTA-pair kernel
+        assert fa.fa_query_launch(B, H, N, d, causal)["cluster"] == 2
     fa.attention_forward_into(qd, kd, vd, o, lse, causal=causal, scale=w.scale)
     torch.cuda.synchronize()
     assert fa.fa_check(0) == fa.FA_OK
