@@ -575,17 +575,6 @@ __device__ __forceinline__ void bwd_mma_dq_chain(const BwdArgs& a, uint32_t sbas
   wait_drain(bar(SQ ? kBbDrain : kBbDrainB), 0u, ab, kStatusDrain);
 }
 
-// Unpacks the 16-bit pair w to two floats.
-template <bool BF16>
-__device__ __forceinline__ float2 unpack2(uint32_t w) {
-  if constexpr (BF16) {
-    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-  } else {
-    const __half2 h = *reinterpret_cast<const __half2*>(&w);
-    return __half22float2(h);
-  }
-}
-
 // Element-wise softmax gradient, one thread per TMEM lane (row r of the
 // 128-row scratch tiles) and 64 columns per warpgroup (half h). KEYS (dK/dV):
 // the row is key k = 128 t + r, the columns are queries of the streamed tile,

@@ -169,15 +169,6 @@ __device__ __forceinline__ bool wait_cluster_warp(uint32_t bar, uint32_t parity,
   }
 }
 
-// Warp-uniform cluster-scope wait whose lanes suspend in hardware while the
-// phase is incomplete (for warps that share an SM sub-partition with busy
-// warps and usually wait long: polling would take their issue slots).
-__device__ __forceinline__ bool wait_cluster_warp_sleep(uint32_t bar, uint32_t parity,
-                                                        const AbortCtx& ab, uint32_t code) {
-  const bool ok = wait_cluster<true>(bar, parity, ab, code);
-  return __all_sync(0xffffffffu, ok) != 0;
-}
-
 // Warp-uniform variant: every lane polls; the warp proceeds only if all
 // lanes saw the phase complete.
 __device__ __forceinline__ bool wait_bounded_warp(uint32_t bar, uint32_t parity,
@@ -246,21 +237,6 @@ __device__ __forceinline__ void store_row_panel_sw128(uint32_t tile, int r,
   for (int q = 0; q < 8; ++q)
     ptx::st_shared_v4(row + ((static_cast<uint32_t>(q) ^ x) << 4), pk[4 * q], pk[4 * q + 1],
                       pk[4 * q + 2], pk[4 * q + 3]);
-}
-
-// Writes 32 consecutive elements (16 packed pairs) starting at column
-// `col0` (a multiple of 32) of row r of an SW128 tile.
-__device__ __forceinline__ void store_row32_sw128(uint32_t tile, int r, int col0,
-                                                  const uint32_t (&pk)[16]) {
-  const uint32_t row = tile + static_cast<uint32_t>(col0 >> 6) * kPanelBytes +
-                       static_cast<uint32_t>(r) * 128u;
-  const uint32_t x = static_cast<uint32_t>(r & 7);
-  const uint32_t q0 = static_cast<uint32_t>((col0 & 63) >> 3);
-#pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    ptx::st_shared_v4(row + (((q0 + t) ^ x) << 4), pk[4 * t], pk[4 * t + 1], pk[4 * t + 2],
-                      pk[4 * t + 3]);
-  }
 }
 
 // Shared-memory descriptor of a K-major SW128 tile (8-row groups 1024 B apart).

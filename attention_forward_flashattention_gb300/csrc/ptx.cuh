@@ -114,15 +114,6 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, uint
       : "memory");
 }
 
-// 3-D tiled store from shared memory (bulk-group completion).
-__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int c0, int c1, int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(tmap)),
-      "r"(src), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-
 // 4-D tiled store from shared memory (bulk-group completion); the box is
 // clipped at the tensor's bounds, and no coordinate may be negative.
 __device__ __forceinline__ void tma_store_4d(const void* tmap, uint32_t src, int c0, int c1,
@@ -603,17 +594,6 @@ __device__ __forceinline__ void umma_f8_ss_pair_elect(uint32_t d_tmem, uint64_t 
       "setp.ne.b32 p, %4, 0;\n\t"
       "@e tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void umma_f16_ts_pair_elect(uint32_t d_tmem, uint32_t a_tmem,
-                                                       uint64_t bdesc, uint32_t idesc,
-                                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred e, p;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 __device__ __forceinline__ void umma_commit_pair_elect(uint32_t bar, uint16_t cta_mask) {
