@@ -634,6 +634,11 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     # end to end through the public API: pinned host in, pinned host out
     e2e = None
     if not args.no_e2e:
+        # the host-link figure is taken with the host quiet: the workers that
+        # generate the other workloads' inputs (numpy, gigabytes written) finish
+        # first, since they compete for host memory bandwidth and cores
+        if futures:
+            cf.wait(list(futures.values()))
         plan.e2e_step()
         torch.cuda.synchronize(dev)
         n_e2e = max(3, min(args.steps, 10))
