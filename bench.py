@@ -55,6 +55,7 @@ NOMINAL_DENSE_FP16_TFLOPS = 2250.0
 # (2 * 128 * 128 * 16 FLOPs) takes 64 cycles; 8-bit products run at twice that
 TENSOR_FLOP_PER_CLK_SM = {"fp16": 8192.0, "bf16": 8192.0, "e4m3": 16384.0}
 FALLBACK_PEAK_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
 SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -86,6 +87,18 @@ def parse_args():
 
 
 # ------------------------------------------------------------ helpers
+
+def hbm_figure(plan, ms: float, peaks: dict) -> dict:
+    """The step's algorithmic HBM bytes (inputs read once, outputs written
+    once: the bytes the host path copies) over its time, against the measured
+    copy bandwidth: the roofline of the small, latency-bound workloads, and
+    context for the others."""
+    nbytes = plan.h2d + plan.d2h
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    return {"bytes": nbytes, "gbs": gbs, "peak_gbs": peak, "frac": gbs / peak,
+            "peak_source": "measured copy" if "hbm_gbs" in peaks else "fallback"}
+
 
 def measured_peaks() -> dict:
     try:
@@ -693,6 +706,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                        if k not in ("global_batch", "seq_len")},
             "kernel": oplan.kernel,
             "traffic": oplan.traffic,
+            "hbm": hbm_figure(oplan, oms, peaks),
         }
         del oplan
         torch.cuda.empty_cache()
@@ -726,6 +740,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "clocks": {**t["clocks"], "clk64_mhz": t["clk64_mhz"], "clk64_ctas": t["ctas"],
                    "window": "nvidia-smi: soak + timed steps; clk64: the timed kernels' CTAs "
                              "(clock64 / %globaltimer)"},
+        "hbm": hbm_figure(plan, ms_per_step, peaks),
         "gpu_launches": args.steps * plan.launches,
         "e2e": e2e,
         "cpu_baseline": cpu,

@@ -80,3 +80,13 @@ def test_clock_corrected_fraction():
     assert f16 == pytest.approx(1e15 / (152 * 8192 * 2e9))
     assert bench.clock_corrected_frac(1000.0, "e4m3", 152, 2000.0) == pytest.approx(f16 / 2)
     assert bench.clock_corrected_frac(1000.0, "bf16", 152, None) is None
+
+
+def test_hbm_figure():
+    # C1: Q, K, V, O of B1 H2 N256 d64 fp16 (4 x 65536 bytes) and the fp32 LSE (2048 bytes)
+    plan = bench.Plan(h2d=3 * 65536, d2h=65536 + 2048)
+    f = bench.hbm_figure(plan, 0.0106, {"hbm_gbs": 6789.0})
+    assert f["bytes"] == 264192
+    assert f["gbs"] == pytest.approx(264192 / 10.6e-6 / 1e9)
+    assert f["frac"] == pytest.approx(f["gbs"] / 6789.0) and f["peak_source"] == "measured copy"
+    assert bench.hbm_figure(plan, 1.0, {})["peak_gbs"] == bench.FALLBACK_HBM_GBS
