@@ -242,6 +242,16 @@ def _dtype_code(t) -> int:
     raise TypeError(f"unsupported dtype {t.dtype} (fp16 or bf16)")
 
 
+def _allocating_on(stream):
+    """Context for the tensors a call creates (outputs, workspace): with an
+    explicit stream they are allocated on it, so PyTorch's caching allocator
+    reuses their memory only in that stream's order, never while the call's
+    kernels may still be running."""
+    import contextlib
+    import torch
+    return torch.cuda.stream(stream) if stream is not None else contextlib.nullcontext()
+
+
 def _stream_handle(stream) -> int:
     import torch
     if stream is None:
@@ -299,8 +309,9 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
     """Returns (O [B, H, N, d] in q's dtype, LSE [B, H, N] float32)."""
     import torch
     B, H, N, d = q.shape
-    o = torch.empty_like(q)
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    with _allocating_on(stream):
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     attention_forward_into(q, k, v, o, lse, causal, scale, stream)
     return o, lse
 
@@ -384,8 +395,9 @@ def attention_forward_fp8(q8, k8, vt8, q_scale: float, k_scales, v_scale: float,
     """Returns (O bfloat16 [B, H, N, 128], LSE float32 [B, H, N]) of the 8-bit forward."""
     import torch
     B, H, N, d = q8.shape
-    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device)
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    with _allocating_on(stream):
+        o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
     attention_forward_fp8_into(q8, k8, vt8, o, lse, q_scale, k_scales, v_scale, causal, scale,
                                stream)
     return o, lse
@@ -406,9 +418,12 @@ def attention_backward(q, k, v, o, lse, dout, causal: bool = False, scale: float
             raise ValueError("tensors must be contiguous CUDA tensors")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    ws = torch.empty(fa_bwd_workspace_size(B, H, N, d) // 4, dtype=torch.float32,
-                     device=q.device)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    # the workspace is freed when this returns, possibly before the kernels
+    # that use it have run: allocated on their stream, it is reused only after
+    with _allocating_on(stream):
+        ws = torch.empty(fa_bwd_workspace_size(B, H, N, d) // 4, dtype=torch.float32,
+                         device=q.device)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     rc = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
                 lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws.data_ptr(),
                 B, H, N, d, causal, scale, _dtype_code(q), _stream_handle(stream))
