@@ -96,3 +96,58 @@ def test_side_stream_backward_keeps_its_workspace():
     assert _same(got, ref)
     assert all(bool(torch.isnan(j).all()) for j in junk)
     assert fa.fa_check(0) == fa.FA_OK
+
+
+_THREADS_SCRIPT = r"""
+import sys, threading
+import torch
+sys.path.insert(0, sys.argv[1])
+import attention_forward_flashattention_gb300 as fa
+fa.load_library()
+torch.cuda.init()
+# 8 host threads make their first calls at the same moment (the per-device
+# setup of every entry point runs under its lock), each on a stream of its own
+shapes = [(1, 4, 300 + 97 * i, 64 if i % 2 else 128, torch.float16 if i % 3 else torch.bfloat16,
+           bool(i % 2)) for i in range(8)]
+ins = []
+for i, (B, H, N, d, dt, c) in enumerate(shapes):
+    g = torch.Generator(device="cuda:0").manual_seed(100 + i)
+    ins.append([torch.randn(B, H, N, d, device="cuda:0", generator=g).to(dt) for _ in range(3)])
+torch.cuda.synchronize()
+start = threading.Barrier(8)
+got, errs = [None] * 8, []
+def work(i):
+    try:
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.default_stream())
+        start.wait()
+        for _ in range(4):
+            o, lse = fa.attention_forward(*ins[i], causal=shapes[i][5], stream=s)
+        s.synchronize()
+        got[i] = (o, lse)
+    except Exception as e:  # reported below
+        errs.append(repr(e))
+ts = [threading.Thread(target=work, args=(i,)) for i in range(8)]
+[t.start() for t in ts]
+[t.join() for t in ts]
+assert not errs, errs
+for i in range(8):
+    o, lse = fa.attention_forward(*ins[i], causal=shapes[i][5])
+    torch.cuda.synchronize()
+    assert torch.equal(o, got[i][0]) and torch.equal(lse, got[i][1]), i
+assert fa.fa_check(0) == fa.FA_OK
+print("threads ok")
+"""
+
+
+def test_first_calls_from_many_host_threads():
+    """A fresh process whose first calls come from 8 host threads at once,
+    each on its own stream: no error, and every result equals the same call
+    made afterwards alone."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _THREADS_SCRIPT, root], capture_output=True,
+                       text=True, timeout=300)
+    assert r.returncode == 0 and "threads ok" in r.stdout, r.stdout + r.stderr
