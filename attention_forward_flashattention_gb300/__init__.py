@@ -430,3 +430,43 @@ def attention_backward(q, k, v, o, lse, dout, causal: bool = False, scale: float
     if rc != FA_OK:
         raise FaError(rc, "fa_bwd")
     return dq, dk, dv
+
+
+_autograd_fn = None
+
+
+def _attention_function():
+    """The torch.autograd.Function behind `attention` (built on first use, so
+    importing this module does not import torch)."""
+    global _autograd_fn
+    if _autograd_fn is None:
+        import torch
+
+        class _Attention(torch.autograd.Function):
+            @staticmethod
+            def forward(ctx, q, k, v, causal, scale):
+                o, lse = attention_forward(q, k, v, causal=causal, scale=scale)
+                ctx.save_for_backward(q, k, v, o, lse)
+                ctx.causal, ctx.scale = causal, scale
+                return o
+
+            @staticmethod
+            def backward(ctx, do):
+                q, k, v, o, lse = ctx.saved_tensors
+                dq, dk, dv = attention_backward(*(t.contiguous() for t in (q, k, v, o)), lse,
+                                                do.contiguous(), causal=ctx.causal,
+                                                scale=ctx.scale)
+                return dq, dk, dv, None, None
+
+        _autograd_fn = _Attention
+    return _autograd_fn
+
+
+def attention(q, k, v, causal: bool = False, scale: float | None = None):
+    """O = softmax(scale q k^T [+ causal mask]) v for [B, H, N, d] fp16 / bf16
+    CUDA tensors (d = 64 or 128), differentiable: autograd runs fa_bwd on the
+    saved q, k, v, O and LSE. Returns O only (attention_forward also returns
+    the LSE)."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    return _attention_function().apply(q, k, v, bool(causal), float(scale))
